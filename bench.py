@@ -1,0 +1,454 @@
+#!/usr/bin/env python
+"""Benchmark of the SPRINT block-decode step on B300.
+
+One bench step decodes one block: the step-0 prefix pass (LM-head
+confidences of every prefix row, key-norm scoring and per-modality
+selection, KV compaction), then every denoising step (block attention over
+the full prefix at step 0 and the pruned prefix afterwards, block LM head,
+adaptive unmasking) until the block is unmasked.  The metric is decode
+steps per second (tokens per second alongside), whole job, inputs resident
+in HBM; `e2e` repeats it through the same public API with the inputs coming
+from pinned host memory each block.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...    # the CPU oracle, timed on a sample
+
+Multi-GPU (torchrun, one rank per GPU): every rank decodes its own
+independent sequence; there is no data-path collective (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-decode steps/s and tokens/s at 32K prefix; % tensor peak / % HBM BW"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40, help="timed blocks")
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="prefix-32k")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- ranks
+def rank_info():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend)
+    return dist
+
+
+def barrier(world):
+    import torch.distributed as dist
+    if world > 1:
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """Largest value of x over all ranks (the job's wall time)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device="cpu") -> float:
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of one GPU while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.f = None
+
+    def __enter__(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 8:
+                    rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        pw = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- inputs
+def build_inputs(w, seqs, device):
+    """Seeded prefix and per-step inputs of sequences `seqs` (CSR layout)."""
+    import torch
+
+    from workload import lm_head_weight, prefix_inputs, step_inputs
+    pres = [prefix_inputs(w, seq=s, device="cpu") for s in seqs]
+    prefix = {
+        "K": torch.cat([p["K"].reshape(-1) for p in pres]),
+        "V": torch.cat([p["V"].reshape(-1) for p in pres]),
+        "H": torch.cat([p["H"] for p in pres]),
+        "theta": torch.cat([p["theta"] for p in pres]),
+        "modality": torch.cat([p["modality"] for p in pres]),
+    }
+    counts = [(int((p["modality"] == 0).sum()), int((p["modality"] != 0).sum())) for p in pres]
+    steps = []
+    for t in range(w.T):
+        xs = [step_inputs(w, s, 0, t, device="cpu") for s in seqs]
+        steps.append({
+            "Q": torch.stack([x["Q"] for x in xs]).contiguous(),
+            "Kb": torch.stack([x["Kb"] for x in xs]).contiguous(),
+            "Vb": torch.stack([x["Vb"] for x in xs]).contiguous(),
+            "h": torch.cat([x["h"] for x in xs]).contiguous(),
+            "theta": torch.cat([x["theta"] for x in xs]).contiguous(),
+        })
+    W = lm_head_weight(w, device="cpu")
+    return prefix, steps, W, counts, pres
+
+
+def to_device(d, device, non_blocking=False):
+    return {k: v.to(device, non_blocking=non_blocking) for k, v in d.items()}
+
+
+def nbytes(d):
+    return sum(v.numel() * v.element_size() for v in d.values())
+
+
+# ---------------------------------------------------------------- oracle timing
+def cpu_baseline(w, pres, steps_host, W, steps_per_block, sample_rows=128):
+    """The oracle, as it stands, on a bounded sample of one block.
+
+    Measured: key-norm importance, selection and compaction of the whole
+    prefix; prefix confidences of `sample_rows` rows (scaled to all rows);
+    block attention of layer 0 at the full and at the pruned prefix (scaled
+    to all layers); the block LM head and unmask of one step (whole)."""
+    import numpy as np
+
+    from oracle import sprint_oracle as orc
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:  # noqa: BLE001
+        cores = os.cpu_count()
+    p = pres[0]
+    n = p["modality"].numel()
+    t0 = time.perf_counter()
+    imp = orc.key_norm_importance(p["K"])
+    t_imp = time.perf_counter() - t0
+    rows = np.linspace(0, n - 1, min(sample_rows, n)).astype(np.int64)
+    t0 = time.perf_counter()
+    c_s, _, _ = orc.lm_confidence(p["H"], W, p["theta"], rows=rows)
+    t_conf = (time.perf_counter() - t0) * n / len(rows)
+    conf_all = np.full(n, float(np.mean(c_s)))
+    conf_all[rows] = c_s
+    t0 = time.perf_counter()
+    score = orc.composite_score(imp, conf_all, w.alpha)
+    kept = orc.select_kept(score, p["modality"].numpy(), w.r_text, w.r_img)
+    Kp = orc.compact(p["K"], kept)
+    Vp = orc.compact(p["V"], kept)
+    t_sel = time.perf_counter() - t0
+    x = steps_host[0]
+    one = lambda a: a[0]  # noqa: E731  (first sequence of the stacked inputs)
+    t0 = time.perf_counter()
+    orc.block_attention(one(x["Q"]), p["K"], p["V"], one(x["Kb"]), one(x["Vb"]), layers=[0])
+    t_attn_full = (time.perf_counter() - t0) * w.NL
+    t0 = time.perf_counter()
+    orc.block_attention(one(x["Q"]), Kp, Vp, one(x["Kb"]), one(x["Vb"]), layers=[0])
+    t_attn_pruned = (time.perf_counter() - t0) * w.NL
+    t0 = time.perf_counter()
+    c_b, am_b, _ = orc.lm_confidence(x["h"][:w.LB], W, x["theta"][:w.LB])
+    orc.unmask_step(c_b, am_b, np.ones(w.LB, bool), np.full(w.LB, -1), 0, w.T, w.tau)
+    t_step_head = time.perf_counter() - t0
+    extra = max(steps_per_block - 1, 0)
+    t_block = (t_imp + t_conf + t_sel + t_attn_full + t_step_head
+               + extra * (t_attn_pruned + t_step_head))
+    measured = t_imp + t_conf * len(rows) / n + t_sel + (t_attn_full + t_attn_pruned) / w.NL \
+        + t_step_head
+    return {
+        "value": steps_per_block / t_block,
+        "unit": "steps/s",
+        "cores": cores,
+        "kind": "oracle",
+        "tokens_per_s": w.LB / t_block,
+        "block_s_extrapolated": t_block,
+        "measured_s": measured,
+        "sample": (f"one block of sequence 0 ({n}-row prefix): key norms, selection and "
+                   f"compaction of the whole prefix; LM-head confidences of {len(rows)} of "
+                   f"{n} prefix rows scaled x{n / len(rows):.0f}; attention of layer 0 of "
+                   f"{w.NL} scaled x{w.NL} (full prefix, then pruned); one step's block LM "
+                   f"head and unmask; block = step 0 + {extra} pruned steps"),
+    }
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+
+    from kv_cache_pruning_step_b300 import BlockDecoder
+    from kv_cache_pruning_step_b300 import sprint as sp
+    from workload import WORKLOADS
+
+    rank, world, local = rank_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    w = WORKLOADS[args.workload]
+    seqs = [rank * w.S + s for s in range(w.S)]
+    prefix_h, steps_h, W_h, counts, pres = build_inputs(w, seqs, "cpu")
+    W = W_h.to(dev)
+    prefix = to_device(prefix_h, dev)
+    steps = [to_device(x, dev) for x in steps_h]
+    dec = BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
+                       r_text=w.r_text, r_img=w.r_img, alpha=w.alpha, modality_counts=counts)
+    step_fn = lambda t: steps[t]  # noqa: E731
+
+    for _ in range(args.warmup):
+        dec.decode(prefix, step_fn)
+    torch.cuda.synchronize()
+    assert dec.status.item() == 0, f"device status {dec.status.item()}"
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local)
+    dec.timing = {}
+    n_steps = 0
+    hist = {}
+    launches0 = sp.sprint_kernel_launches()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_id) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record()
+        for _ in range(args.steps):
+            res = dec.decode(prefix, step_fn)
+            n_steps += res.steps
+            for a in res.accepted_per_step:
+                for v in a:
+                    hist[v] = hist.get(v, 0) + 1
+        end.record()
+        torch.cuda.synchronize()
+        barrier(world)
+    launches = sp.sprint_kernel_launches() - launches0
+    elapsed = start.elapsed_time(end) / 1e3
+    stage_ms = {k: statistics.mean(a.elapsed_time(b) for a, b in v) for k, v in dec.timing.items()}
+    stage_launches = {k: len(v) for k, v in dec.timing.items()}
+    dec.timing = None
+    assert dec.status.item() == 0, f"device status {dec.status.item()}"
+
+    t_job = max_over_ranks(elapsed, world, dev)
+    total_steps = sum_over_ranks(n_steps, world, dev)
+    blocks = args.steps * world
+    value = total_steps / t_job
+    tokens_per_s = blocks * w.S * w.LB / t_job
+
+    # e2e: the same decode with this block's inputs copied from pinned host
+    # memory every block and the decoded tokens read back.
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda d: {k: v.pin_memory() for k, v in d.items()}  # noqa: E731
+        prefix_p = pin(prefix_h)
+        steps_p = [pin(x) for x in steps_h]
+        tok_host = torch.empty((w.S, w.LB), dtype=torch.int32, pin_memory=True)
+        h2d = nbytes(prefix_h) + sum(nbytes(x) for x in steps_h)
+        d2h = tok_host.numel() * 4
+        dev_prefix = {k: torch.empty_like(v, device=dev) for k, v in prefix_h.items()}
+        dev_steps = [{k: torch.empty_like(v, device=dev) for k, v in x.items()} for x in steps_h]
+        e_steps = 0
+        barrier(world)
+        torch.cuda.synchronize()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record()
+        for _ in range(args.steps):
+            for k, v in prefix_p.items():
+                dev_prefix[k].copy_(v, non_blocking=True)
+            for xd, xp in zip(dev_steps, steps_p):
+                for k, v in xp.items():
+                    xd[k].copy_(v, non_blocking=True)
+            res = dec.decode(dev_prefix, lambda t: dev_steps[t])
+            tok_host.copy_(res.tokens, non_blocking=True)
+            e_steps += res.steps
+        e2.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        t_e2e = max_over_ranks(s2.elapsed_time(e2) / 1e3, world, dev)
+        e2e = {"value": sum_over_ranks(e_steps, world, dev) / t_e2e, "unit": "steps/s",
+               "tokens_per_s": blocks * w.S * w.LB / t_e2e,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h + 4 * w.S * w.T}
+
+    peaks, peak_kind = load_peaks()
+    n_rows = dec.total_rows
+    kept = dec.total_kept
+    row_b = w.NL * w.Hkv * w.d * 2
+    work = {  # algorithmic work per launch of each stage
+        "lmhead_prefix": ("tensor", 2.0 * n_rows * w.D * w.V),
+        "score_prune": ("hbm", n_rows * row_b),
+        "compact": ("hbm", 2 * 2 * kept * row_b),
+        "attn_full": ("hbm", 2 * (n_rows + w.S * w.LB) * row_b),
+        "attn_pruned": ("hbm", 2 * (kept + w.S * w.LB) * row_b),
+        "lmhead_block": ("hbm", w.V * w.D * 2),
+    }
+    kernels = {}
+    for k, (bound, amount) in work.items():
+        if k not in stage_ms:
+            continue
+        sec = stage_ms[k] / 1e3
+        if bound == "tensor":
+            ach = amount / sec / 1e12
+            pk = peaks["bf16_tflops_sustained"]
+            kernels[k] = {"bound": "tensor", "achieved": ach, "peak": pk, "unit": "TFLOP/s",
+                          "frac": ach / pk, "ms": stage_ms[k]}
+        else:
+            ach = amount / sec / 1e9
+            pk = peaks["hbm_gbs"]
+            kernels[k] = {"bound": "hbm", "achieved": ach, "peak": pk, "unit": "GB/s",
+                          "frac": ach / pk, "ms": stage_ms[k]}
+    dom = max(stage_ms, key=lambda k: stage_ms[k] * stage_launches[k])
+    r = kernels.get(dom, {})
+    roofline = {"kernel": dom, "bound": r.get("bound"), "achieved": r.get("achieved"),
+                "peak": r.get("peak"), "unit": r.get("unit"), "frac": r.get("frac"),
+                "traffic": None,
+                "peak_source": f"{peak_kind} ({'sustained bf16, kernel timed inside a long step loop' if r.get('bound') == 'tensor' else 'copy bandwidth'})"}
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "tokens_per_s": tokens_per_s,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t_job / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded; shapes and modality layout of the workload)",
+        "config": {"workload": w.name, "description": w.description,
+                   "prefix_rows": n_rows, "kept_rows": kept, "sequences": w.S,
+                   "LB": w.LB, "T": w.T, "tau": w.tau, "r_text": w.r_text, "r_img": w.r_img,
+                   "alpha": w.alpha, "NL": w.NL, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "D": w.D,
+                   "V": w.V, "bench_step": "one block decoded to completion",
+                   "l2": "inputs larger than L2 (K+V+W+H well above 126 MB)",
+                   "parallelism": f"replicas x{world}, one sequence set per GPU"},
+        "decode_steps_per_block": n_steps / args.steps,
+        "accepted_per_step_hist": {str(k): v for k, v in sorted(hist.items())},
+        "stages_ms": stage_ms, "stage_launches": stage_launches, "kernels": kernels,
+        "roofline": roofline, "gpu_launches": launches, "clocks": clk.summary(),
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, pres, steps_h, W_h, n_steps / args.steps)
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    """The CPU oracle as the reference arm: each bench step is one bounded
+    sample of a block (see cpu_baseline), timed on the host cores."""
+    rank, world, local = rank_info()
+    if rank != 0:
+        return
+    from workload import WORKLOADS
+    w = WORKLOADS[args.workload]
+    prefix_h, steps_h, W_h, counts, pres = build_inputs(w, [0], "cpu")
+    for _ in range(args.warmup):
+        cpu_baseline(w, pres, steps_h, W_h, w.T, sample_rows=32)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(w, pres, steps_h, W_h, w.T, sample_rows=32))
+    wall = time.perf_counter() - t0
+    block_s = statistics.mean(v["block_s_extrapolated"] for v in vals)
+    value = w.T / block_s
+    cb = dict(vals[-1])
+    cb["value"] = value
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
+        "tokens_per_s": w.LB / block_s, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * block_s, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description,
+                   "bench_step": "one block, oracle on a bounded sample, extrapolated"},
+        "cpu_baseline": cb, "wall_s": wall,
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

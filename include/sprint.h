@@ -1,0 +1,245 @@
+/*
+ * sprint.h -- C ABI of the SPRINT block-decode step on NVIDIA B300 (sm_103a).
+ *
+ * SPRINT ("Sparse Prefix Retention with Inference-time Non-uniform Token
+ * Unmasking") is the training-free decode accelerator of LLaDA2.0-Uni
+ * (arXiv 2604.20796, Inference section).  A block of LB masked tokens is
+ * decoded in at most T steps.  On the block's first step every prefix
+ * position is scored, the prefix KV cache is pruned per modality, and every
+ * step attends, predicts and unmasks:
+ *
+ *   sprint_lmhead_confidence  top-1 softmax confidence c and greedy token of
+ *                             LM-head rows (prefix rows on step 0, the block's
+ *                             rows on every step); optional logits
+ *   sprint_score_prune        key-norm importance, composite score, and the
+ *                             per-modality top-floor(r n) kept set
+ *   sprint_compact_kv         gather of the kept rows of K and V
+ *   sprint_block_attn         bidirectional block attention over
+ *                             [pruned prefix ; block]
+ *   sprint_unmask             confidence-adaptive (or fixed) unmasking
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.    Every tensor pointer is a DEVICE pointer owned by the caller.
+ *            The library allocates nothing and frees nothing.  Scratch
+ *            memory is a caller-provided workspace of at least the size the
+ *            matching *_workspace_bytes() function returns (16-byte aligned).
+ * Streams.   Every call enqueues work on the caller's stream and returns
+ *            without synchronising.  Calls on one stream run in order.
+ * Layouts.   Dense, row-major, no padding.  Tensors of several sequences are
+ *            concatenated; sequence s starts at the row offset given by a
+ *            CSR offset array (int32 [S+1], device, off[0] = 0).
+ *              K, V        per sequence [NL][n_s][Hkv][d]
+ *              Kb, Vb      [S][NL][LB][Hkv][d]
+ *              Q, O        [S][NL][LB][Hq][d]
+ *              W           [V][D]  (nn.Linear weight layout)
+ *              h           [M][D]
+ * dtype.     SPRINT_F32: fp32 storage and arithmetic.
+ *            SPRINT_BF16: bf16 storage, fp32 accumulation; the LM head and
+ *            attention run on the tcgen05 tensor cores.
+ * Errors.    Return value: SPRINT_OK, or a negative SPRINT_ERR_* code when
+ *            the host-side checks reject the call (nothing is launched) or a
+ *            launch fails.  Data-dependent errors found on the device (bad
+ *            offsets or indices, a wait that timed out) are OR-ed into the
+ *            caller's int32 device word `status` as SPRINT_STATUS_* bits;
+ *            the caller zeroes it and reads it when convenient.
+ */
+#ifndef SPRINT_H
+#define SPRINT_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPRINT_VERSION 100 /* 1.0.0 */
+
+/* Return codes. */
+#define SPRINT_OK 0
+#define SPRINT_ERR_INVALID_ARG (-1) /* null pointer, bad size, misaligned  */
+#define SPRINT_ERR_UNSUPPORTED (-2) /* valid but not implemented (e.g. d)   */
+#define SPRINT_ERR_CUDA (-3)        /* a CUDA call or launch failed         */
+#define SPRINT_ERR_WORKSPACE (-5)   /* workspace smaller than required      */
+
+/* Bits of the device status word. */
+#define SPRINT_STATUS_BAD_OFFSETS 1u   /* CSR offsets not monotone / too big */
+#define SPRINT_STATUS_KEPT_MISMATCH 2u /* kept_off disagrees with floor(r n) */
+#define SPRINT_STATUS_TIMEOUT 4u       /* a bounded device wait expired      */
+#define SPRINT_STATUS_BAD_INDEX 8u     /* kept index outside its prefix      */
+#define SPRINT_STATUS_BAD_TEMPERATURE 16u /* temperature <= 0 or not finite  */
+
+/* Storage types. */
+#define SPRINT_F32 0
+#define SPRINT_BF16 1
+
+/* Unmask schedules. */
+#define SPRINT_UNMASK_ADAPTIVE 0
+#define SPRINT_UNMASK_FIXED 1
+
+int sprint_version(void);
+const char *sprint_strerror(int code);
+
+/* Kernels this library has launched in this process (a diagnostic counter;
+ * every successful launch adds one). */
+unsigned long long sprint_kernel_launches(void);
+
+/*
+ * floor(r * n) keep count of one modality.  LLaDA2.0-Uni paper, Sparse
+ * Prefix Retention paragraph: within each modality the top floor(r n)
+ * positions are retained.  Computed in double as floor(r n + 1e-9), which
+ * is the exact floor for decimal ratios with up to 6 digits and n < 2^31.
+ * Returns -1 when n < 0 or r is outside [0, 1].  Host function.
+ */
+int sprint_keep_count(int n, double r);
+
+/*
+ * sprint_lmhead_confidence -- LM-head logits reduced to the top-1 softmax
+ * confidence and the greedy token, without materialising probabilities.
+ *
+ * LLaDA2.0-Uni paper, Sparse Prefix Retention paragraph: c_i = max_v
+ * p(v | x_t), the top-1 softmax confidence of prefix position i; and
+ * Non-uniform Token Unmasking paragraph: c_n = p(x0_hat^n | x_t) of the
+ * predicted token x0_hat^n.  Logits are z[i][v] = (h[i] . W[v]) / temp[i].
+ *
+ *   h          [M][D]  hidden states (dtype)
+ *   W          [V][D]  LM-head weight (dtype)
+ *   temp       [M] fp32 per-row logit temperature, > 0; NULL means 1
+ *   logits_out [M][V]  (dtype) temperature-scaled logits, or NULL
+ *   conf_out   [M] fp32  c = 1 / sum_v exp(z_v - max_v z)
+ *   argmax_out [M] int32 smallest v attaining max_v z
+ *   ws         workspace of sprint_lmhead_workspace_bytes(M, D, V, dtype)
+ *
+ * M >= 0, D >= 1, V >= 1; bf16 needs D % 8 == 0 and 16-byte aligned h, W.
+ * Device status: SPRINT_STATUS_BAD_TEMPERATURE, SPRINT_STATUS_TIMEOUT.
+ */
+size_t sprint_lmhead_workspace_bytes(int M, int D, int V, int dtype);
+int sprint_lmhead_confidence(const void *h, const void *W, const float *temp,
+                             int M, int D, int V, int dtype, void *logits_out,
+                             float *conf_out, int32_t *argmax_out, void *ws,
+                             size_t ws_bytes, int32_t *status,
+                             cudaStream_t stream);
+
+/*
+ * sprint_score_prune -- per-modality kept set of every sequence's prefix.
+ *
+ * LLaDA2.0-Uni paper, Sparse Prefix Retention paragraph:
+ *   key-norm importance  I_i = ||k_i|| / ((1/L) sum_j ||k_j||), where ||k_i||
+ *                        is the L2 norm of position i's keys concatenated
+ *                        over the KV heads, averaged over the NL layers, and
+ *                        the mean runs over all L = n_s prefix positions;
+ *   composite score      s_i = alpha I_i + (1 - alpha) c_i  (the paper's
+ *                        equation is not reproduced; this blend is the
+ *                        convention, alpha = 0.5 in the paper);
+ *   modality-aware keep  within each modality mu the top floor(r_mu n_mu)
+ *                        positions by (s descending, index ascending).
+ *
+ *   K            keys, per sequence [NL][n_s][Hkv][d] (dtype)
+ *   prefix_off   int32 [S+1] device CSR offsets of the prefixes
+ *   total_rows   prefix_off[S] (host copy; sizes the launch)
+ *   conf         fp32 [total_rows] top-1 confidence of every prefix row
+ *   modality     uint8 [total_rows], 0 = text, any other value = image
+ *   kept_off     int32 [S+1] device CSR offsets of the kept sets; sequence
+ *                s must have kept_off[s+1]-kept_off[s] = k_text + k_img
+ *                with k = sprint_keep_count(n_mu, r_mu)
+ *   kept_idx     int32 [kept_off[S]] OUT: kept positions of each sequence,
+ *                ascending, as indices local to the sequence's prefix
+ *   score_out    fp32 [total_rows] OUT composite scores, or NULL
+ *   ws           workspace of sprint_score_prune_workspace_bytes(...)
+ *
+ * Device status: SPRINT_STATUS_BAD_OFFSETS, SPRINT_STATUS_KEPT_MISMATCH
+ * (that sequence's kept_idx range is left unwritten).
+ */
+size_t sprint_score_prune_workspace_bytes(int S, int total_rows);
+int sprint_score_prune(const void *K, int S, const int32_t *prefix_off,
+                       int total_rows, int NL, int Hkv, int d, int dtype,
+                       const float *conf, const uint8_t *modality, float alpha,
+                       double r_text, double r_img, int32_t *kept_idx,
+                       const int32_t *kept_off, float *score_out, void *ws,
+                       size_t ws_bytes, int32_t *status, cudaStream_t stream);
+
+/*
+ * sprint_compact_kv -- pruned prefix cache: Kp[l][j] = K[l][kept_idx[j]],
+ * the same for V, every layer, per sequence.  LLaDA2.0-Uni paper, Sparse
+ * Prefix Retention paragraph: a pruned prefix KV cache is constructed once
+ * per block; evicted positions are dropped.
+ *
+ *   K, V         per sequence [NL][n_s][Hkv][d] (dtype), offsets prefix_off
+ *   total_rows   prefix_off[S] (host copy; bounds the reads)
+ *   kept_idx     int32, per sequence local ascending indices, offsets kept_off
+ *   Kp, Vp       OUT per sequence [NL][k_s][Hkv][d] (dtype), offsets kept_off
+ *   total_kept   kept_off[S] (host copy; sizes the launch)
+ *
+ * Rows are copied bit for bit.  Device status: SPRINT_STATUS_BAD_OFFSETS,
+ * SPRINT_STATUS_BAD_INDEX (that row is skipped).
+ */
+int sprint_compact_kv(const void *K, const void *V, int S,
+                      const int32_t *prefix_off, int total_rows, int NL,
+                      int Hkv, int d,
+                      int dtype, const int32_t *kept_idx,
+                      const int32_t *kept_off, int total_kept, void *Kp,
+                      void *Vp, int32_t *status, cudaStream_t stream);
+
+/*
+ * sprint_block_attn -- bidirectional in-block attention of the block's
+ * queries over [prefix keys ; block keys], every layer and query head.
+ * LLaDA2.0-Uni paper, Sparse Prefix Retention paragraph: the block's first
+ * step attends to the full prefix, every later step to the much shorter
+ * pruned prefix.  Block diffusion gives no causal mask inside the block.
+ *
+ *   O[l][j][h] = sum_i softmax_i(Q[l][j][h] . key_i / sqrt(d)) value_i over
+ *   key_i in [Kp[l][0..k_s) ; Kb[l][0..LB)] of KV head g = floor(h Hkv / Hq).
+ *
+ *   Q            [S][NL][LB][Hq][d] (dtype)
+ *   Kp, Vp       prefix keys/values, per sequence [NL][k_s][Hkv][d], located
+ *                by kv_off (int32 [S+1], device); the full prefix on step 0
+ *   max_kv_rows  max_s k_s (host; sizes the launch)
+ *   total_kv_rows kv_off[S] (host; bounds the reads)
+ *   Kb, Vb       [S][NL][LB][Hkv][d] the block's own keys/values
+ *   O            OUT [S][NL][LB][Hq][d] (dtype)
+ *   ws           workspace of sprint_block_attn_workspace_bytes(...)
+ *
+ * d in {64, 128}; Hq % Hkv == 0; LB * Hq / Hkv <= 128 for bf16.
+ * Device status: SPRINT_STATUS_BAD_OFFSETS, SPRINT_STATUS_TIMEOUT.
+ */
+size_t sprint_block_attn_workspace_bytes(int S, int NL, int LB, int Hq, int Hkv,
+                                         int d, int max_kv_rows, int dtype);
+int sprint_block_attn(const void *Q, const void *Kp, const void *Vp,
+                      const int32_t *kv_off, int max_kv_rows,
+                      int total_kv_rows, const void *Kb,
+                      const void *Vb, int S, int NL, int LB, int Hq, int Hkv,
+                      int d, int dtype, void *O, void *ws, size_t ws_bytes,
+                      int32_t *status, cudaStream_t stream);
+
+/*
+ * sprint_unmask -- one unmask decision per sequence.  LLaDA2.0-Uni paper,
+ * Non-uniform Token Unmasking paragraph:
+ *   ADAPTIVE  accept every masked position whose confidence exceeds tau
+ *             (strictly); if fewer than ceil(m / (T - t)) qualify, accept
+ *             the ceil(m / (T - t)) most confident instead (m = positions
+ *             still masked, t = 0-based step; t >= T - 1 accepts all);
+ *   FIXED     accept the min(m, ceil(LB / T)) most confident (a block
+ *             starts fully masked, so LB is its initial masked count).
+ * Ranking is by (confidence descending, position ascending), in fp32.
+ * Accepted positions take their argmax token and are never re-masked.
+ *
+ *   conf, argmax   [S][LB] fp32 / int32 (from sprint_lmhead_confidence)
+ *   mask           [S][LB] uint8 IN/OUT, nonzero = still masked
+ *   tokens         [S][LB] int32 IN/OUT
+ *   m_out          [S] int32 OUT positions still masked after this step
+ *   accepted_out   [S][LB] uint8 OUT 1 where accepted this step, or NULL
+ *
+ * 1 <= LB <= 1024, T >= 1, 0 <= t.
+ */
+int sprint_unmask(const float *conf, const int32_t *argmax, uint8_t *mask,
+                  int32_t *tokens, int32_t *m_out, int S, int LB, int t, int T,
+                  float tau, int mode, uint8_t *accepted_out, int32_t *status,
+                  cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPRINT_H */

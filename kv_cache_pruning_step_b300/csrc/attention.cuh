@@ -1,0 +1,39 @@
+// Internal interface between the attention entry point and its chunk kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace sprint {
+
+// Split-KV partials: unit u = ((s * NL + l) * Hkv + g) * chunks + chunk holds
+// R = LB * Hq / Hkv rows of (unnormalised O row [d], row max in log2 units,
+// row sum of exp2(score - max)).
+struct AttnWs {
+  float *o;        // [units][R][d]
+  float *ml;       // [units][R][2]
+  int chunks;      // key chunks per (sequence, layer, KV head)
+  int chunk_keys;  // keys per chunk
+  size_t bytes;    // workspace bytes of this layout
+};
+
+AttnWs attn_ws_layout(void *ws, int S, int NL, int LB, int Hq, int Hkv, int d, int max_kv_rows,
+                      int chunk_keys);
+int attn_chunk_keys(int S, int NL, int Hkv, int LB, int max_kv_rows, int target_units);
+
+// Chunk length the bf16 tensor-core kernel is launched with.
+int attn_tc_chunk_keys(int S, int NL, int Hkv, int LB, int max_kv_rows);
+
+int attn_tc_chunks(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 *Vp,
+                   const int32_t *kv_off, int total_kv_rows, const __nv_bfloat16 *Kb,
+                   const __nv_bfloat16 *Vb, int S, int NL, int LB, int Hq, int Hkv, int d,
+                   const AttnWs &w, int32_t *status, cudaStream_t stream);
+
+int attn_simt_chunks_bf16(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp,
+                          const __nv_bfloat16 *Vp, const int32_t *kv_off, int total_kv_rows,
+                          const __nv_bfloat16 *Kb, const __nv_bfloat16 *Vb, int S, int NL,
+                          int LB, int Hq, int Hkv, int d, const AttnWs &w, int32_t *status,
+                          cudaStream_t stream);
+
+}  // namespace sprint

@@ -1,0 +1,27 @@
+// Internal interface between the LM-head entry point and its tile kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace sprint {
+
+// Vocabulary columns folded into one (max, sum-exp, argmax) partial per row.
+constexpr int kPartCols = 256;
+
+struct LmheadWs {
+  float *pmax;    // [strips][M] max of the raw fp32 dot products in the strip
+  float *psum;    // [strips][M] sum of exp(z - z_stripmax) over the strip
+  int32_t *parg;  // [strips][M] first column attaining the strip max
+  int strips;     // ceil(V / kPartCols)
+};
+
+LmheadWs lmhead_ws_layout(void *ws, int M, int V);
+
+// bf16 tiles on the tcgen05 tensor cores; writes the strip partials (and
+// the temperature-scaled logits when `logits` is not null).
+int lmhead_tc_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *temp, int M,
+                    int D, int V, __nv_bfloat16 *logits, const LmheadWs &p, int32_t *status,
+                    cudaStream_t stream);
+
+}  // namespace sprint

@@ -1,0 +1,317 @@
+// bf16 LM-head tiles on the tcgen05 tensor cores with the vocabulary
+// softmax reduction fused into the epilogue.
+//
+// LLaDA2.0-Uni paper (arXiv 2604.20796): the block's first step scores every
+// prefix position by its top-1 softmax confidence c_i ("Sparse Prefix
+// Retention" paragraph) and every step ranks the block's predictions by
+// c_n ("Non-uniform Token Unmasking" paragraph).  Both are max_v softmax
+// of z = (h . W_v) / theta; the probability vector is never formed.
+//
+// Design (one persistent CTA per SM, 192 threads, 1 CTA/SM):
+//   warp 0      TMA producer: 128x64 tiles of h and 256x64 tiles of W (bf16,
+//               128-byte swizzle) into a 4-stage shared-memory ring;
+//   warp 1      allocates 512 TMEM columns; one lane issues
+//               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=256, K=16) into
+//               one of two 256-column fp32 accumulators;
+//   warps 2-5   epilogue: each thread owns one accumulator row (TMEM lane),
+//               reads its 256 columns 32 at a time with tcgen05.ld, and folds
+//               them into (max of raw dot products, first column reaching it,
+//               sum of exp2((acc - max) * log2(e) / theta)); optional logits
+//               (acc / theta in bf16).  The second accumulator lets the MMA of
+//               the next tile overlap this epilogue.
+// Output tiles are visited in bands of 32 column tiles so that a band of W
+// (32 x 256 rows) stays in L2 while all row tiles stream past it.
+#include <cuda.h>
+#include <math.h>
+#include <stdlib.h>
+
+#include "common.cuh"
+#include "lmhead.cuh"
+#include "tc_ptx.cuh"
+
+namespace sprint {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, BAND = 32;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int THREADS = 192;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &m, int &n) {
+  const int per_band = BAND * num_m;
+  const int band = t / per_band;
+  const int idx = t - band * per_band;
+  const int bw = min(BAND, num_n - band * BAND);
+  m = idx / bw;
+  n = band * BAND + idx % bw;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
+                 const float *__restrict__ temp, int M, int D, int V,
+                 __nv_bfloat16 *__restrict__ logits, float *__restrict__ pmax,
+                 float *__restrict__ psum, int32_t *__restrict__ parg, int32_t *status,
+                 unsigned long long cap_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  uint64_t *full = bars, *empty = bars + STAGES;
+  uint64_t *tfull = bars + 2 * STAGES, *tempty = tfull + 2, *drain = tempty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_m = (M + BM - 1) / BM, num_n = (V + BN - 1) / BN;
+  const int tiles = num_m * num_n, nk = (D + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(tc::smem_u32(full + s), 1);
+      tc::mbar_init(tc::smem_u32(empty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(tc::smem_u32(tfull + b), 1);
+      tc::mbar_init(tc::smem_u32(tempty + b), 4);
+    }
+    tc::mbar_init(tc::smem_u32(drain), 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tmap(&tm_h);
+    tc::prefetch_tmap(&tm_w);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, last_parity = 0;  // bit s: stage s has a load issued
+      for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+        int m, n;
+        tile_coords(t, num_m, num_n, m, n);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!tc::mbar_wait(tc::smem_u32(empty + stage), phase ^ 1, cap_ns, abort_flag))
+            goto producer_done;
+          const uint32_t fb = tc::smem_u32(full + stage);
+          tc::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t sa = tc::smem_u32(smem + stage * STAGE_BYTES);
+          tc::tma_load_2d(sa, &tm_h, fb, kb * BK, m * BM);
+          tc::tma_load_2d(sa + A_BYTES, &tm_w, fb, kb * BK, n * BN);
+          issued |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+    producer_done:
+      // Never leave with a copy in flight: wait (bounded) for the last load
+      // issued into every stage.
+      for (int s = 0; s < STAGES; ++s)
+        if (issued >> s & 1u) {
+          volatile int no_abort = 0;
+          tc::mbar_wait(tc::smem_u32(full + s), last_parity >> s & 1u, cap_ns, &no_abort);
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN, false, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+        const int buf = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1);
+        if (!tc::mbar_wait(tc::smem_u32(tempty + buf), (use & 1u) ^ 1u, cap_ns, abort_flag))
+          break;
+        tc::fence_after_sync();
+        const uint32_t d = tmem + (uint32_t)(buf * BN);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!tc::mbar_wait(tc::smem_u32(full + stage), phase, cap_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t sa = tc::smem_u32(smem + stage * STAGE_BYTES);
+          const uint64_t adesc = tc::desc_kmajor_sw128(sa);
+          const uint64_t bdesc = tc::desc_kmajor_sw128(sa + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)  // +32 bytes along K per step
+            tc::mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+          tc::mma_commit(tc::smem_u32(empty + stage));
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc::mma_commit(tc::smem_u32(tfull + buf));
+      }
+      // Every MMA this thread issued has finished once `drain` completes.
+      tc::mma_commit(tc::smem_u32(drain));
+      volatile int no_abort = 0;
+      tc::mbar_wait(tc::smem_u32(drain), 0, cap_ns, &no_abort);
+    }
+  } else {
+    // ---------------- epilogue: one accumulator row per thread
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int r_tile = q * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+      const int buf = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      int m, n;
+      tile_coords(t, num_m, num_n, m, n);
+      if (!tc::mbar_wait(tc::smem_u32(tfull + buf), use & 1u, cap_ns, abort_flag)) break;
+      tc::fence_after_sync();
+      const int row = m * BM + r_tile;
+      const bool vrow = row < M;
+      float th = 1.0f;
+      if (temp && vrow) {
+        th = temp[row];
+        if (!(th > 0.0f) || !isfinite(th)) {
+          report(status, SPRINT_STATUS_BAD_TEMPERATURE);
+          th = 1.0f;
+        }
+      }
+      const float sc = kLog2e / th, inv = 1.0f / th;
+      float run_max = -INFINITY, run_sum = 0.f;
+      int arg = 0;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      const int col0 = n * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int cb = col0 + c * 32;
+        const int ncol = min(32, V - cb);
+        if (ncol <= 0) break;  // uniform across the warp
+        float v[32];
+        tc::tmem_ld32(taddr + (uint32_t)(c * 32), v);
+        tc::tmem_wait_ld();
+        float cm = v[0];
+        int ca = 0;
+#pragma unroll
+        for (int i = 1; i < 32; ++i)
+          if (i < ncol && v[i] > cm) { cm = v[i]; ca = i; }
+        if (cm > run_max) {
+          run_sum *= exp2f((run_max - cm) * sc);
+          run_max = cm;
+          arg = cb + ca;
+        }
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < ncol) sum += exp2f((v[i] - run_max) * sc);
+        run_sum += sum;
+        if (logits && vrow) {
+          __nv_bfloat16 *dst = logits + (size_t)row * V + cb;
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < ncol) dst[i] = __float2bfloat16_rn(v[i] * inv);
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(tempty + buf));
+      if (vrow) {
+        const size_t at = (size_t)n * M + row;
+        pmax[at] = run_max;
+        psum[at] = run_sum;
+        parg[at] = arg;
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (threadIdx.x == 0 && *abort_flag) report(status, SPRINT_STATUS_TIMEOUT);
+  if (warp == 1) tc::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+}  // namespace
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// bf16 row-major [rows][inner] tensor map with a (box_inner x box_rows) box
+// in the 128-byte swizzle; out-of-range elements read as zero.
+bool make_tmap_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
+                       uint64_t row_stride_elems, uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_stride_elems * 2};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+unsigned long long wait_cap_ns() {
+  static unsigned long long cap = 0;
+  if (!cap) {
+    const char *e = getenv("SPRINT_WAIT_CAP_NS");
+    cap = e ? strtoull(e, nullptr, 10) : 2000000000ull;
+    if (!cap) cap = 1;
+  }
+  return cap;
+}
+
+int sm_count() {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
+int lmhead_tc_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *temp, int M,
+                    int D, int V, __nv_bfloat16 *logits, const LmheadWs &p, int32_t *status,
+                    cudaStream_t stream) {
+  CUtensorMap tm_h, tm_w;
+  if (!make_tmap_bf16_2d(&tm_h, h, D, M, D, BK, BM) ||
+      !make_tmap_bf16_2d(&tm_w, W, D, V, D, BK, BN))
+    return SPRINT_ERR_CUDA;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(lmhead_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess)
+      return SPRINT_ERR_CUDA;
+    attr_set = true;
+  }
+  const int tiles = ((M + BM - 1) / BM) * ((V + BN - 1) / BN);
+  const int grid = tiles < sm_count() ? tiles : sm_count();
+  lmhead_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tm_h, tm_w, temp, M, D, V, logits,
+                                                          p.pmax, p.psum, p.parg, status,
+                                                          wait_cap_ns());
+  return launch_status();
+}
+
+}  // namespace sprint

@@ -1,0 +1,188 @@
+"""Block-decode driver of the SPRINT step: the host loop over denoising steps.
+
+LLaDA2.0-Uni paper (arXiv 2604.20796), Inference section.  A block of LB
+masked tokens is decoded in at most T steps.  Step 0 is the full forward
+pass: the prefix rows' confidences are computed, every prefix position is
+scored, the per-modality kept set is chosen and the pruned KV cache is
+gathered; step 0 itself attends to the full prefix.  Every later step
+attends to the pruned prefix.  Every step predicts the block's tokens and
+unmasks a confidence-adaptive number of them.
+
+The driver only sequences library calls and sizes buffers.  All buffers are
+allocated once per decoder, so a decode call launches kernels and nothing
+else; the only device-to-host traffic is the per-step read of the masked
+counts that decides whether the block is finished.
+"""
+from __future__ import annotations
+
+import contextlib
+from dataclasses import dataclass
+
+import torch
+
+from . import sprint as sp
+
+
+@dataclass
+class BlockResult:
+    steps: int                 # denoising steps executed (step 0 included)
+    tokens: torch.Tensor       # [S][LB] int32 decoded tokens
+    accepted_per_step: list    # per step: [S] accepted counts (host ints)
+
+
+class BlockDecoder:
+    """Buffers and call sequence for decoding blocks of S sequences.
+
+    prefix_lens[s] and modality_counts[s] = (n_text, n_image) describe the
+    prefixes the decoder will see; they fix every buffer size.
+    """
+
+    def __init__(self, W, *, NL, Hq, Hkv, d, LB, T, tau, r_text, r_img, alpha=0.5,
+                 mode=sp.UNMASK_ADAPTIVE, modality_counts, want_logits=False):
+        self.W = W
+        self.dev = W.device
+        self.dtype = W.dtype
+        self.NL, self.Hq, self.Hkv, self.d = NL, Hq, Hkv, d
+        self.LB, self.T, self.tau, self.mode = LB, T, tau, mode
+        self.r_text, self.r_img, self.alpha = r_text, r_img, alpha
+        self.V, self.D = W.shape
+        self.S = S = len(modality_counts)
+        lens = [nt + ni for nt, ni in modality_counts]
+        kept = [sp.sprint_keep_count(nt, r_text) + sp.sprint_keep_count(ni, r_img)
+                for nt, ni in modality_counts]
+        self.prefix_off_host = [0]
+        self.kept_off_host = [0]
+        for n, k in zip(lens, kept):
+            self.prefix_off_host.append(self.prefix_off_host[-1] + n)
+            self.kept_off_host.append(self.kept_off_host[-1] + k)
+        self.total_rows = self.prefix_off_host[-1]
+        self.total_kept = self.kept_off_host[-1]
+        self.max_rows = max(lens) if lens else 0
+        self.max_kept = max(kept) if kept else 0
+        i32 = dict(dtype=torch.int32, device=self.dev)
+        self.prefix_off = torch.tensor(self.prefix_off_host, **i32)
+        self.kept_off = torch.tensor(self.kept_off_host, **i32)
+        f32 = dict(dtype=torch.float32, device=self.dev)
+        dt = sp.BF16 if self.dtype == torch.bfloat16 else sp.F32
+        self.status = sp.new_status(self.dev)
+        # step-0 prefix pass
+        self.conf_prefix = torch.empty(self.total_rows, **f32)
+        self.argmax_prefix = torch.empty(self.total_rows, **i32)
+        self.ws_lm_prefix = torch.empty(
+            max(16, sp.sprint_lmhead_workspace_bytes(self.total_rows, self.D, self.V, dt)),
+            dtype=torch.uint8, device=self.dev)
+        self.kept_idx = torch.empty(self.total_kept, **i32)
+        self.score = torch.empty(self.total_rows, **f32)
+        self.ws_score = torch.empty(
+            max(16, sp.sprint_score_prune_workspace_bytes(S, self.total_rows)),
+            dtype=torch.uint8, device=self.dev)
+        row = NL * Hkv * d
+        self.Kp = torch.empty(self.total_kept * row, dtype=self.dtype, device=self.dev)
+        self.Vp = torch.empty(self.total_kept * row, dtype=self.dtype, device=self.dev)
+        # per-step buffers
+        self.O = torch.empty((S, NL, LB, Hq, d), dtype=self.dtype, device=self.dev)
+        self.ws_attn = torch.empty(
+            max(16, sp.sprint_block_attn_workspace_bytes(S, NL, LB, Hq, Hkv, d,
+                                                         self.max_rows, dt)),
+            dtype=torch.uint8, device=self.dev)
+        self.conf_blk = torch.empty(S * LB, **f32)
+        self.argmax_blk = torch.empty(S * LB, **i32)
+        self.logits = (torch.empty((S * LB, self.V), dtype=self.dtype, device=self.dev)
+                       if want_logits else None)
+        self.want_logits = want_logits
+        self.ws_lm_blk = torch.empty(
+            max(16, sp.sprint_lmhead_workspace_bytes(S * LB, self.D, self.V, dt)),
+            dtype=torch.uint8, device=self.dev)
+        self.mask = torch.empty((S, LB), dtype=torch.uint8, device=self.dev)
+        self.tokens = torch.empty((S, LB), **i32)
+        self.m_out = torch.empty(S, **i32)
+        self.accepted = torch.empty((S, LB), dtype=torch.uint8, device=self.dev)
+        self.m_host = torch.empty(S, dtype=torch.int32, pin_memory=True)
+        self.ev = torch.cuda.Event()
+        # When a dict, every stage records (start, end) CUDA events under its
+        # name on the current stream (used by the benchmark).
+        self.timing = None
+
+    @contextlib.contextmanager
+    def _stage(self, name):
+        if self.timing is None:
+            yield
+            return
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        yield
+        b.record()
+        self.timing.setdefault(name, []).append((a, b))
+
+    # -- the individual stages (each is one or two library calls) --------
+    def prefix_pass(self, K, V, H, theta, modality):
+        """Step-0 scoring and pruning: confidences of every prefix row, the
+        kept set, and the pruned cache (self.Kp / self.Vp)."""
+        with self._stage("lmhead_prefix"):
+            sp.sprint_lmhead_confidence(H, self.W, theta, conf=self.conf_prefix,
+                                        argmax=self.argmax_prefix, ws=self.ws_lm_prefix,
+                                        status=self.status)
+        with self._stage("score_prune"):
+            sp.sprint_score_prune(K, self.prefix_off, self.total_rows, self.NL, self.Hkv,
+                                  self.d, self.conf_prefix, modality, self.alpha, self.r_text,
+                                  self.r_img, self.kept_off, self.total_kept,
+                                  kept_idx=self.kept_idx, score=self.score, ws=self.ws_score,
+                                  status=self.status)
+        with self._stage("compact"):
+            sp.sprint_compact_kv(K, V, self.prefix_off, self.total_rows, self.NL, self.Hkv,
+                                 self.d, self.kept_idx, self.kept_off, self.total_kept,
+                                 Kp=self.Kp, Vp=self.Vp, status=self.status)
+
+    def step(self, t, x, K=None, V=None):
+        """One denoising step; K/V given = attend to the full prefix."""
+        if K is not None:
+            with self._stage("attn_full"):
+                sp.sprint_block_attn(x["Q"], K, V, self.prefix_off, self.max_rows,
+                                     self.total_rows, x["Kb"], x["Vb"], O=self.O,
+                                     ws=self.ws_attn, status=self.status)
+        else:
+            with self._stage("attn_pruned"):
+                sp.sprint_block_attn(x["Q"], self.Kp, self.Vp, self.kept_off, self.max_kept,
+                                     self.total_kept, x["Kb"], x["Vb"], O=self.O,
+                                     ws=self.ws_attn, status=self.status)
+        with self._stage("lmhead_block"):
+            sp.sprint_lmhead_confidence(x["h"], self.W, x["theta"], conf=self.conf_blk,
+                                        argmax=self.argmax_blk, logits=self.logits,
+                                        ws=self.ws_lm_blk, status=self.status)
+        with self._stage("unmask"):
+            sp.sprint_unmask(self.conf_blk, self.argmax_blk, self.mask, self.tokens, t, self.T,
+                             self.tau, self.mode, m_out=self.m_out, accepted=self.accepted,
+                             status=self.status)
+
+    def masked_left(self):
+        self.m_host.copy_(self.m_out, non_blocking=True)
+        self.ev.record()
+        self.ev.synchronize()
+        return self.m_host.tolist()
+
+    def decode(self, prefix, steps, on_step=None) -> BlockResult:
+        """Decode one block.  prefix: dict K, V, H, theta, modality (device,
+        sequences concatenated).  steps(t) -> dict Q, Kb, Vb, h, theta."""
+        self.mask.fill_(1)
+        self.tokens.fill_(-1)
+        self.prefix_pass(prefix["K"], prefix["V"], prefix["H"], prefix["theta"],
+                         prefix["modality"])
+        accepted = []
+        prev = [self.LB] * self.S
+        n_steps = 0
+        for t in range(self.T):
+            x = steps(t)
+            if t == 0:
+                self.step(0, x, prefix["K"], prefix["V"])
+            else:
+                self.step(t, x)
+            n_steps += 1
+            if on_step is not None:
+                on_step(t, self)
+            left = self.masked_left()
+            accepted.append([p - q for p, q in zip(prev, left)])
+            prev = left
+            if not any(left):
+                break
+        return BlockResult(n_steps, self.tokens, accepted)

@@ -1,0 +1,243 @@
+"""Python binding of libsprint.so, the SPRINT C ABI (include/sprint.h).
+
+Argument marshalling only: each function has the name of the C entry point
+it calls, checks that tensors are contiguous CUDA tensors of the right
+dtype, allocates outputs and the workspace with torch when the caller gives
+none, passes raw pointers and the current CUDA stream, and raises
+SprintError on a negative return code.  Every step of the computation runs
+in the library's CUDA kernels; there is no other implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsprint.so")
+
+F32 = 0
+BF16 = 1
+UNMASK_ADAPTIVE = 0
+UNMASK_FIXED = 1
+
+STATUS_BAD_OFFSETS = 1
+STATUS_KEPT_MISMATCH = 2
+STATUS_TIMEOUT = 4
+STATUS_BAD_INDEX = 8
+STATUS_BAD_TEMPERATURE = 16
+
+# Every symbol include/sprint.h declares, with (restype, argtypes).
+_P, _I, _Z, _F, _D = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float, ctypes.c_double
+SIGNATURES = {
+    "sprint_version": (_I, []),
+    "sprint_strerror": (ctypes.c_char_p, [_I]),
+    "sprint_kernel_launches": (ctypes.c_ulonglong, []),
+    "sprint_keep_count": (_I, [_I, _D]),
+    "sprint_lmhead_workspace_bytes": (_Z, [_I, _I, _I, _I]),
+    "sprint_lmhead_confidence": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P, _P]),
+    "sprint_score_prune_workspace_bytes": (_Z, [_I, _I]),
+    "sprint_score_prune": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _F, _D, _D, _P, _P,
+                                _P, _P, _Z, _P, _P]),
+    "sprint_compact_kv": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P]),
+    "sprint_block_attn_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I]),
+    "sprint_block_attn": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
+                               _P, _Z, _P, _P]),
+    "sprint_unmask": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
+}
+
+
+class SprintError(RuntimeError):
+    pass
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is not built; run `python -m kv_cache_pruning_step_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise SprintError(f"{what}: {lib.sprint_strerror(rc).decode()} (code {rc})")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise SprintError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise SprintError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise SprintError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise SprintError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr() if t.numel() else None
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ws(ws, nbytes, device):
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+    return ws
+
+
+def new_status(device) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def sprint_version() -> int:
+    return lib.sprint_version()
+
+
+def sprint_strerror(code: int) -> str:
+    return lib.sprint_strerror(code).decode()
+
+
+def sprint_kernel_launches() -> int:
+    return lib.sprint_kernel_launches()
+
+
+def sprint_keep_count(n: int, r: float) -> int:
+    return lib.sprint_keep_count(int(n), float(r))
+
+
+def sprint_lmhead_workspace_bytes(M, D, V, dtype) -> int:
+    return lib.sprint_lmhead_workspace_bytes(M, D, V, dtype)
+
+
+def sprint_lmhead_confidence(h, W, temp=None, *, want_logits=False, conf=None, argmax=None,
+                             logits=None, ws=None, status=None, stream=None):
+    """c = top-1 softmax confidence and argmax token of every row of h @ W^T / temp.
+
+    Returns (conf fp32 [M], argmax int32 [M], logits [M][V] or None)."""
+    M, D = h.shape
+    V = W.shape[0]
+    dt = _dtype_code(h)
+    dev = h.device
+    conf = torch.empty(M, dtype=torch.float32, device=dev) if conf is None else conf
+    argmax = torch.empty(M, dtype=torch.int32, device=dev) if argmax is None else argmax
+    if want_logits and logits is None:
+        logits = torch.empty((M, V), dtype=h.dtype, device=dev)
+    status = new_status(dev) if status is None else status
+    nb = sprint_lmhead_workspace_bytes(M, D, V, dt)
+    ws = _ws(ws, nb, dev)
+    rc = lib.sprint_lmhead_confidence(
+        _ptr(h, h.dtype, "h"), _ptr(W, h.dtype, "W"), _ptr(temp, torch.float32, "temp"),
+        M, D, V, dt, _ptr(logits, h.dtype, "logits"), _ptr(conf, torch.float32, "conf"),
+        _ptr(argmax, torch.int32, "argmax"), _ptr(ws), ws.numel(),
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "sprint_lmhead_confidence")
+    return conf, argmax, logits
+
+
+def sprint_score_prune_workspace_bytes(S, total_rows) -> int:
+    return lib.sprint_score_prune_workspace_bytes(S, total_rows)
+
+
+def sprint_score_prune(K, prefix_off, total_rows, NL, Hkv, d, conf, modality, alpha,
+                       r_text, r_img, kept_off, total_kept, *, kept_idx=None,
+                       want_score=False, score=None, ws=None, status=None, stream=None):
+    """Kept positions of every sequence (int32, local indices, ascending).
+
+    Returns (kept_idx int32 [total_kept], score fp32 [total_rows] or None)."""
+    S = prefix_off.numel() - 1
+    dev = K.device
+    dt = _dtype_code(K)
+    kept_idx = (torch.empty(total_kept, dtype=torch.int32, device=dev)
+                if kept_idx is None else kept_idx)
+    if want_score and score is None:
+        score = torch.empty(total_rows, dtype=torch.float32, device=dev)
+    status = new_status(dev) if status is None else status
+    ws = _ws(ws, sprint_score_prune_workspace_bytes(S, total_rows), dev)
+    rc = lib.sprint_score_prune(
+        _ptr(K, K.dtype, "K"), S, _ptr(prefix_off, torch.int32, "prefix_off"), int(total_rows),
+        NL, Hkv, d, dt, _ptr(conf, torch.float32, "conf"),
+        _ptr(modality, torch.uint8, "modality"), float(alpha), float(r_text), float(r_img),
+        _ptr(kept_idx, torch.int32, "kept_idx"), _ptr(kept_off, torch.int32, "kept_off"),
+        _ptr(score, torch.float32, "score"), _ptr(ws), ws.numel(),
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "sprint_score_prune")
+    return kept_idx, score
+
+
+def sprint_compact_kv(K, V, prefix_off, total_rows, NL, Hkv, d, kept_idx, kept_off,
+                      total_kept, *, Kp=None, Vp=None, status=None, stream=None):
+    """Gather of the kept rows: returns (Kp, Vp), flat [total_kept*NL*Hkv*d]."""
+    S = prefix_off.numel() - 1
+    dev = K.device
+    n = int(total_kept) * NL * Hkv * d
+    Kp = torch.empty(n, dtype=K.dtype, device=dev) if Kp is None else Kp
+    Vp = torch.empty(n, dtype=K.dtype, device=dev) if Vp is None else Vp
+    status = new_status(dev) if status is None else status
+    rc = lib.sprint_compact_kv(
+        _ptr(K, K.dtype, "K"), _ptr(V, K.dtype, "V"), S,
+        _ptr(prefix_off, torch.int32, "prefix_off"), int(total_rows), NL, Hkv, d,
+        _dtype_code(K), _ptr(kept_idx, torch.int32, "kept_idx"),
+        _ptr(kept_off, torch.int32, "kept_off"), int(total_kept), _ptr(Kp, K.dtype, "Kp"),
+        _ptr(Vp, K.dtype, "Vp"), _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "sprint_compact_kv")
+    return Kp, Vp
+
+
+def sprint_block_attn_workspace_bytes(S, NL, LB, Hq, Hkv, d, max_kv_rows, dtype) -> int:
+    return lib.sprint_block_attn_workspace_bytes(S, NL, LB, Hq, Hkv, d, max_kv_rows, dtype)
+
+
+def sprint_block_attn(Q, Kp, Vp, kv_off, max_kv_rows, total_kv_rows, Kb, Vb, *, O=None,
+                      ws=None, status=None, stream=None):
+    """Block attention; Q [S][NL][LB][Hq][d], Kb/Vb [S][NL][LB][Hkv][d]."""
+    S, NL, LB, Hq, d = Q.shape
+    Hkv = Kb.shape[3]
+    dev = Q.device
+    dt = _dtype_code(Q)
+    O = torch.empty_like(Q) if O is None else O
+    status = new_status(dev) if status is None else status
+    ws = _ws(ws, sprint_block_attn_workspace_bytes(S, NL, LB, Hq, Hkv, d, int(max_kv_rows), dt),
+             dev)
+    rc = lib.sprint_block_attn(
+        _ptr(Q, Q.dtype, "Q"), _ptr(Kp, Q.dtype, "Kp"), _ptr(Vp, Q.dtype, "Vp"),
+        _ptr(kv_off, torch.int32, "kv_off"), int(max_kv_rows), int(total_kv_rows),
+        _ptr(Kb, Q.dtype, "Kb"), _ptr(Vb, Q.dtype, "Vb"), S, NL, LB, Hq, Hkv, d, dt,
+        _ptr(O, Q.dtype, "O"), _ptr(ws), ws.numel(), _ptr(status, torch.int32, "status"),
+        _stream(stream))
+    _check(rc, "sprint_block_attn")
+    return O
+
+
+def sprint_unmask(conf, argmax, mask, tokens, t, T, tau, mode=UNMASK_ADAPTIVE, *, m_out=None,
+                  accepted=None, status=None, stream=None):
+    """One unmask step in place on mask/tokens ([S][LB]); returns (m_out, accepted)."""
+    S, LB = mask.shape
+    dev = mask.device
+    m_out = torch.empty(S, dtype=torch.int32, device=dev) if m_out is None else m_out
+    accepted = torch.empty((S, LB), dtype=torch.uint8, device=dev) if accepted is None else accepted
+    status = new_status(dev) if status is None else status
+    rc = lib.sprint_unmask(
+        _ptr(conf, torch.float32, "conf"), _ptr(argmax, torch.int32, "argmax"),
+        _ptr(mask, torch.uint8, "mask"), _ptr(tokens, torch.int32, "tokens"),
+        _ptr(m_out, torch.int32, "m_out"), S, LB, int(t), int(T), float(tau), int(mode),
+        _ptr(accepted, torch.uint8, "accepted"), _ptr(status, torch.int32, "status"),
+        _stream(stream))
+    _check(rc, "sprint_unmask")
+    return m_out, accepted

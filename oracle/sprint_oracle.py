@@ -46,14 +46,19 @@ UNMASK_ADAPTIVE = 0
 UNMASK_FIXED = 1
 
 
-def _f64(x):
-    """Exact fp64 copy of a numpy array or a CPU torch tensor (bf16 ok)."""
+def _np(x):
+    """numpy view of a numpy array, list or torch tensor (copied to host)."""
     if hasattr(x, "detach"):
         x = x.detach().cpu()
         if str(x.dtype) in ("torch.bfloat16", "torch.float16"):
             x = x.float()
         x = x.numpy()
-    return np.asarray(x, dtype=np.float64)
+    return np.asarray(x)
+
+
+def _f64(x):
+    """Exact fp64 copy of a numpy array or a torch tensor (bf16 ok)."""
+    return np.asarray(_np(x), dtype=np.float64)
 
 
 # --------------------------------------------------------------------------
@@ -144,7 +149,7 @@ def select_kept(score, modality, r_text, r_img):
     retained and the rest evicted.
     """
     s = _f64(score)
-    mod = np.asarray(modality).astype(np.int64)
+    mod = _np(modality).astype(np.int64)
     kept = []
     for tag, r in ((TEXT, r_text), (IMAGE, r_img)):
         pos = [int(i) for i in np.nonzero(mod == tag)[0]]
@@ -160,7 +165,7 @@ def compact(K, kept):
     K: [NL, L, Hkv, d]; kept: ascending indices.  Returns [NL, k, Hkv, d]
     (fp64, exact copies of the stored values).
     """
-    return _f64(K)[:, np.asarray(kept, dtype=np.int64)]
+    return _f64(K)[:, _np(kept).astype(np.int64)]
 
 
 # --------------------------------------------------------------------------
@@ -211,10 +216,11 @@ def unmask_step(conf, argmax, mask, tokens, t, T, tau, mode=UNMASK_ADAPTIVE):
 
     Returns (mask', tokens', accepted [LB] bool).
     """
-    conf32 = np.asarray(conf, dtype=np.float64).astype(np.float32)
+    conf32 = _f64(conf).astype(np.float32)
     tau32 = np.float32(tau)
-    mask = np.asarray(mask).astype(bool).copy()
-    tokens = np.asarray(tokens).astype(np.int64).copy()
+    mask = _np(mask).astype(bool).copy()
+    tokens = _np(tokens).astype(np.int64).copy()
+    argmax = _np(argmax)
     LB = mask.shape[0]
     masked = [j for j in range(LB) if mask[j]]
     m = len(masked)

@@ -1,0 +1,113 @@
+"""Shared helpers of the GPU parity tests: device inputs from the seeded
+workload generator, host copies for the oracle, and the comparison rules.
+
+Comparison rules (written here once, used by every parity test):
+  * kept sets, unmask decisions, compaction: exact, except positions whose
+    oracle score lies within SCORE_EXCUSE of their modality's threshold
+    (the k-th largest score); kept counts must match exactly;
+  * top-1 confidence c: |gpu - oracle| <= CONF_ATOL (absolute);
+  * argmax: the GPU's token must have an oracle logit within ARGMAX_EXCUSE
+    of the oracle's maximum logit (exact unless two logits nearly tie);
+  * bf16 attention outputs and logits: |g - o| <= 2e-2 + 1e-2 |o|;
+  * fp32 attention outputs and logits: |g - o| <= 1e-4 + 1e-4 |o|.
+"""
+import numpy as np
+import torch
+
+from oracle import sprint_oracle as orc
+
+SCORE_EXCUSE = 1e-6
+CONF_ATOL = 1e-5
+# fp32 dot products of D <= 2048 terms of size O(0.1) carry an absolute
+# error of order 1e-5 (relative 2^-24 per add, sqrt(D) growth); 5e-4 in
+# logit units leaves a wide margin and is still a near-tie.
+ARGMAX_EXCUSE = 5e-4
+BF16_TOL = (2e-2, 1e-2)
+F32_TOL = (1e-4, 1e-4)
+
+
+def tol_for(dtype):
+    return BF16_TOL if dtype == torch.bfloat16 else F32_TOL
+
+
+def assert_close(got, want, dtype, what=""):
+    atol, rtol = tol_for(dtype)
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    err = np.abs(got - want)
+    bad = err > atol + rtol * np.abs(want)
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} outside atol={atol} rtol={rtol}; "
+                           f"max err {err.max():.3e}")
+
+
+def host(t):
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        t = t.float()
+    return t.numpy()
+
+
+def check_confidence(c_gpu, am_gpu, h, W, theta, rows, what=""):
+    """c within CONF_ATOL; argmax exact or a near-tie in the oracle."""
+    c_o, am_o, z = orc.lm_confidence(h, W, theta, rows=rows, want_logits=True)
+    c_gpu = np.asarray(c_gpu, dtype=np.float64)
+    am_gpu = np.asarray(am_gpu).astype(np.int64)
+    err = np.abs(c_gpu - c_o)
+    assert err.max() <= CONF_ATOL, f"{what}: conf max err {err.max():.3e}"
+    mism = np.nonzero(am_gpu != am_o)[0]
+    for i in mism:
+        gap = z[i, am_o[i]] - z[i, am_gpu[i]]
+        assert gap <= ARGMAX_EXCUSE, f"{what}: row {rows[i]} argmax {am_gpu[i]} vs {am_o[i]} gap {gap}"
+    return z, len(mism)
+
+
+def check_kept(kept_gpu, score_o, modality, r_text, r_img, what=""):
+    """Compare a GPU kept set with the oracle's under the excuse rule."""
+    kept_o = orc.select_kept(score_o, modality, r_text, r_img)
+    kept_gpu = np.asarray(kept_gpu).astype(np.int64)
+    assert np.all(np.diff(kept_gpu) > 0), f"{what}: kept indices not strictly ascending"
+    mod = np.asarray(modality).astype(np.int64) != 0
+    for tag, r in ((False, r_text), (True, r_img)):
+        n_mu = int((mod == tag).sum())
+        k = orc.keep_count(n_mu, r)
+        assert int((mod[kept_gpu] == tag).sum()) == k, f"{what}: count mismatch"
+    diff = set(kept_gpu.tolist()) ^ set(kept_o.tolist())
+    if diff:
+        for i in diff:
+            tag = mod[i]
+            pool = np.nonzero(mod == tag)[0]
+            k = orc.keep_count(len(pool), r_img if tag else r_text)
+            ranked = sorted(pool.tolist(), key=lambda j: (-score_o[j], j))
+            thr = score_o[ranked[k - 1]] if k > 0 else np.inf
+            assert abs(score_o[i] - thr) <= SCORE_EXCUSE, (
+                f"{what}: position {i} differs, score {score_o[i]} threshold {thr}")
+    return kept_o, len(diff)
+
+
+def concat_prefixes(prefixes):
+    """Concatenate per-sequence prefix dicts into the library's CSR layout."""
+    out = {
+        "K": torch.cat([p["K"].reshape(-1) for p in prefixes]),
+        "V": torch.cat([p["V"].reshape(-1) for p in prefixes]),
+        "H": torch.cat([p["H"] for p in prefixes]),
+        "theta": torch.cat([p["theta"] for p in prefixes]),
+        "modality": torch.cat([p["modality"] for p in prefixes]),
+    }
+    lens = [p["modality"].numel() for p in prefixes]
+    off = [0]
+    for n in lens:
+        off.append(off[-1] + n)
+    out["off_host"] = off
+    out["off"] = torch.tensor(off, dtype=torch.int32, device=prefixes[0]["K"].device)
+    return out
+
+
+def kept_offsets(modalities, r_text, r_img, device):
+    """CSR offsets of the kept sets, from the library's own keep count."""
+    from kv_cache_pruning_step_b300 import sprint as sp
+    off = [0]
+    for mod in modalities:
+        mod = np.asarray(mod.cpu()) != 0
+        off.append(off[-1] + sp.sprint_keep_count(int((~mod).sum()), r_text)
+                   + sp.sprint_keep_count(int(mod.sum()), r_img))
+    return off, torch.tensor(off, dtype=torch.int32, device=device)

@@ -1,0 +1,101 @@
+"""GPU parity of sprint_block_attn against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import sprint_oracle as orc
+from tests import gpu_cases as gc
+from workload import WORKLOADS, prefix_inputs, step_inputs, small_workload
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def sp():
+    from kv_cache_pruning_step_b300 import sprint
+    return sprint
+
+
+def run_attn(sp, w, prefixes, steps):
+    cat = gc.concat_prefixes(prefixes)
+    lens = [p["modality"].numel() for p in prefixes]
+    Q = torch.stack([x["Q"] for x in steps]).contiguous()
+    Kb = torch.stack([x["Kb"] for x in steps]).contiguous()
+    Vb = torch.stack([x["Vb"] for x in steps]).contiguous()
+    status = sp.new_status(DEV)
+    O = sp.sprint_block_attn(Q, cat["K"], cat["V"], cat["off"], max(lens), sum(lens), Kb, Vb,
+                             status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    return O
+
+
+def check(w, prefixes, steps, O, layers=None, what=""):
+    for s, (p, x) in enumerate(zip(prefixes, steps)):
+        want = orc.block_attention(x["Q"], p["K"], p["V"], x["Kb"], x["Vb"], layers=layers)
+        got = gc.host(O[s])
+        sel = list(range(w.NL)) if layers is None else layers
+        gc.assert_close(got[sel], want[sel], w.torch_dtype, f"{what} seq {s}")
+
+
+def test_tiny_fp32_full_prefix(sp):
+    w = WORKLOADS["tiny-256"]
+    pre = prefix_inputs(w, device=DEV)
+    x = step_inputs(w, 0, 0, 1, device=DEV)
+    O = run_attn(sp, w, [pre], [x])
+    check(w, [pre], [x], O, what="tiny")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("Hq,Hkv,d,LB", [(4, 2, 64, 32), (16, 4, 128, 32), (8, 8, 64, 16),
+                                         (6, 2, 128, 7), (2, 1, 64, 1)])
+def test_fuzz_ragged(sp, dtype, Hq, Hkv, d, LB):
+    lens = [0, 1, 129, 700, 2051]
+    prefixes, steps = [], []
+    for s, n in enumerate(lens):
+        w = small_workload(dtype=dtype, NL=2, Hq=Hq, Hkv=Hkv, d=d, LB=LB, n=n, n_img=n // 3,
+                           seed=40 + s)
+        prefixes.append(prefix_inputs(w, seq=s, device=DEV))
+        steps.append(step_inputs(w, s, 0, 3, device=DEV))
+    O = run_attn(sp, w, prefixes, steps)
+    check(w, prefixes, steps, O, what=f"{dtype} {Hq}/{Hkv}/{d}/{LB}")
+
+
+def test_identical_keys_average_values(sp):
+    w = small_workload(dtype="f32", NL=1, Hq=4, Hkv=2, d=64, LB=8, n=50, n_img=0)
+    pre = prefix_inputs(w, device=DEV)
+    x = step_inputs(w, 0, 0, 0, device=DEV)
+    pre["K"][:] = 0.25
+    x["Kb"][:] = 0.25
+    O = run_attn(sp, w, [pre], [x])
+    vals = torch.cat([pre["V"][0], x["Vb"][0]], dim=0)  # [n+LB][Hkv][d]
+    mean = vals.double().mean(dim=0)                      # [Hkv][d]
+    for h in range(4):
+        g = h * 2 // 4
+        want = mean[g].expand(8, 64).cpu().numpy()
+        gc.assert_close(gc.host(O[0, 0, :, h]), want, torch.float32, "mean of values")
+
+
+@pytest.mark.parametrize("name", ["prefix-4k", "prefix-32k"])
+def test_full_size_sampled_layers(sp, name):
+    w = WORKLOADS[name]
+    pre = prefix_inputs(w, device=DEV)
+    x = step_inputs(w, 0, 0, 2, device=DEV)
+    O = run_attn(sp, w, [pre], [x])
+    check(w, [pre], [x], O, layers=[0, w.NL - 1], what=name)
+    assert torch.isfinite(O.float()).all()
+
+
+def test_batched_ragged_full_size(sp):
+    w = WORKLOADS["batch-16x8k"]
+    prefixes = [prefix_inputs(w, seq=s, device=DEV) for s in range(4)]
+    # ragged: cut each prefix to a different length
+    cuts = [8192, 5000, 1, 7777]
+    for p, n in zip(prefixes, cuts):
+        p["K"] = p["K"][:, :n].contiguous()
+        p["V"] = p["V"][:, :n].contiguous()
+        p["modality"] = p["modality"][:n]
+    steps = [step_inputs(w, s, 0, 1, device=DEV) for s in range(4)]
+    O = run_attn(sp, w, prefixes, steps)
+    check(w, prefixes, steps, O, layers=[3], what="batch")

@@ -1,0 +1,110 @@
+"""GPU parity of sprint_unmask and of whole-block decoding against the oracle."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import sprint_oracle as orc
+from tests import gpu_cases as gc
+from workload import WORKLOADS, lm_head_weight, prefix_inputs, step_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def sp():
+    from kv_cache_pruning_step_b300 import sprint
+    return sprint
+
+
+def test_golden_cases(sp):
+    cases = json.load(open(os.path.join(GOLD, "unmask_hand.json")))["cases"]
+    for case in cases:
+        mode = sp.UNMASK_FIXED if case["mode"] == "fixed" else sp.UNMASK_ADAPTIVE
+        LB = len(case["conf"])
+        conf = torch.tensor([case["conf"]], dtype=torch.float32, device=DEV)
+        am = torch.arange(100, 100 + LB, dtype=torch.int32, device=DEV)[None]
+        mask = torch.tensor([case["mask"]], dtype=torch.uint8, device=DEV)
+        tokens = torch.full((1, LB), -1, dtype=torch.int32, device=DEV)
+        m, acc = sp.sprint_unmask(conf, am, mask, tokens, case["t"], case["T"], case["tau"], mode)
+        got = torch.nonzero(acc[0]).flatten().tolist()
+        assert got == case["expected_accepted"], case
+        assert m.item() == sum(case["mask"]) - len(got)
+        for j in got:
+            assert tokens[0, j].item() == 100 + j and mask[0, j].item() == 0
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("LB,T", [(32, 8), (32, 4), (7, 3), (1, 1), (100, 5), (1024, 9)])
+def test_random_trajectories_match_oracle(sp, mode, LB, T):
+    S = 6
+    g = torch.Generator().manual_seed(LB * 31 + T)
+    mask = torch.ones((S, LB), dtype=torch.uint8, device=DEV)
+    tokens = torch.full((S, LB), -1, dtype=torch.int32, device=DEV)
+    o_mask = [np.ones(LB, bool) for _ in range(S)]
+    o_tok = [np.full(LB, -1) for _ in range(S)]
+    for t in range(T):
+        # coarse confidences: ties and values at tau are frequent
+        conf = (torch.randint(0, 21, (S, LB), generator=g).float() / 20).to(DEV)
+        am = torch.randint(0, 50000, (S, LB), generator=g, dtype=torch.int32).to(DEV)
+        tau = [0.9, 0.95, 0.5, 1.0][t % 4]
+        m, acc = sp.sprint_unmask(conf, am, mask, tokens, t, T, tau, mode)
+        for s in range(S):
+            o_mask[s], o_tok[s], o_acc = orc.unmask_step(conf[s].cpu().numpy(), am[s].cpu().numpy(),
+                                                         o_mask[s], o_tok[s], t, T, tau, mode)
+            assert acc[s].cpu().numpy().astype(bool).tolist() == o_acc.tolist()
+            assert mask[s].cpu().numpy().astype(bool).tolist() == o_mask[s].tolist()
+            assert tokens[s].cpu().numpy().tolist() == o_tok[s].tolist()
+            assert m[s].item() == int(o_mask[s].sum())
+    if mode == 0:
+        assert int(mask.sum()) == 0  # terminates within T
+
+
+def test_tiny_block_end_to_end(sp):
+    """Whole block on the fp32 tiny workload, every step compared."""
+    from kv_cache_pruning_step_b300 import BlockDecoder
+    w = WORKLOADS["tiny-256"]
+    W = lm_head_weight(w, device=DEV)
+    pre = prefix_inputs(w, device=DEV)
+    steps = [step_inputs(w, 0, 0, t, device=DEV) for t in range(w.T)]
+    mod = pre["modality"].cpu().numpy()
+    counts = [(int((mod == 0).sum()), int((mod == 1).sum()))]
+    dec = BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
+                       r_text=w.r_text, r_img=w.r_img, alpha=w.alpha, modality_counts=counts,
+                       want_logits=True)
+    seen = []
+
+    def on_step(t, d):
+        seen.append({"O": gc.host(d.O[0]), "conf": d.conf_blk.cpu().numpy(),
+                     "argmax": d.argmax_blk.cpu().numpy(), "acc": d.accepted[0].cpu().numpy(),
+                     "kept": d.kept_idx.cpu().numpy(), "score": d.score.cpu().numpy(),
+                     "conf_prefix": d.conf_prefix.cpu().numpy()})
+
+    def step_fn(t):
+        x = steps[t]
+        return {"Q": x["Q"][None].contiguous(), "Kb": x["Kb"][None].contiguous(),
+                "Vb": x["Vb"][None].contiguous(), "h": x["h"], "theta": x["theta"]}
+
+    res = dec.decode({**pre, "modality": pre["modality"]}, step_fn, on_step=on_step)
+    torch.cuda.synchronize()
+    assert dec.status.item() == 0
+    ref = orc.decode_block(pre, lambda t: steps[t], W, LB=w.LB, T=w.T, tau=w.tau,
+                           r_text=w.r_text, r_img=w.r_img, alpha=w.alpha)
+    # step-0 scoring: confidences, scores, kept set
+    assert np.abs(seen[0]["conf_prefix"] - ref["prefix_conf"]).max() <= gc.CONF_ATOL
+    assert np.abs(seen[0]["score"] - ref["score"]).max() <= gc.SCORE_EXCUSE
+    gc.check_kept(seen[0]["kept"], ref["score"], mod, w.r_text, w.r_img, "tiny kept")
+    assert res.steps == len(ref["steps"])
+    for t, (g, r) in enumerate(zip(seen, ref["steps"])):
+        gc.assert_close(g["O"], r["O"], torch.float32, f"step {t} O")
+        assert np.abs(g["conf"] - r["conf"]).max() <= gc.CONF_ATOL
+        # decisions: exact unless a confidence sits within CONF_ATOL of tau
+        if g["acc"].astype(bool).tolist() != r["accepted"].tolist():
+            near = np.abs(r["conf"] - w.tau) <= gc.CONF_ATOL
+            assert near.any(), f"step {t}: unmask decisions differ"
+            return
+    assert res.tokens[0].cpu().numpy().tolist() == ref["tokens"].tolist()

@@ -102,11 +102,12 @@ WORKLOADS = {
 
 def small_workload(name="fuzz", *, dtype="f32", NL=2, Hq=4, Hkv=2, d=64, D=128,
                    V=300, LB=32, T=4, tau=0.9, r_text=1.0, r_img=0.8,
-                   alpha=0.5, seed=7, S=1) -> Workload:
-    """A workload of arbitrary (small) shapes for parity fuzzing."""
+                   alpha=0.5, seed=7, S=1, n=96, n_img=32) -> Workload:
+    """A workload of arbitrary (small) shapes for parity fuzzing; its prefix
+    is n positions, the last n_img of them image."""
     return Workload(name=name, dtype=dtype, NL=NL, Hq=Hq, Hkv=Hkv, d=d, D=D, V=V,
                     LB=LB, T=T, tau=tau, r_text=r_text, r_img=r_img,
-                    alpha=alpha, seed=seed, S=S)
+                    alpha=alpha, seed=seed, S=S, extra={"n": n, "n_img": n_img})
 
 
 def _stream_seed(*key) -> int:
