@@ -11,7 +11,7 @@
 // an unnormalised partial (row max m in log2 units, row sum l, O row) to the
 // workspace; attn_combine_kernel merges the chunks in ascending order.
 // This file holds the CUDA-core (SIMT) chunk kernel used for fp32 and the
-// combine kernel and entry point; bf16 chunks run on tcgen05 (attention_tc.cu).
+// combine kernel and entry point; bf16 runs on tcgen05 (attention_tc.cu).
 #include <math.h>
 
 #include "attention.cuh"
@@ -189,11 +189,9 @@ AttnWs attn_ws_layout(void *ws, int S, int NL, int LB, int Hq, int Hkv, int d, i
 
 using namespace sprint;
 
-static int attn_chunk_policy(int S, int NL, int Hkv, int LB, int max_kv_rows, int dtype) {
-  // The SIMT kernel is arithmetic-bound: spread it over ~4 units per SM.
-  // The tensor-core kernel is HBM-bound: ~2 units per SM, long chunks.
-  return dtype == SPRINT_BF16 ? attn_tc_chunk_keys(S, NL, Hkv, LB, max_kv_rows)
-                              : attn_chunk_keys(S, NL, Hkv, LB, max_kv_rows, 4 * 148);
+// The fp32 SIMT kernel is arithmetic-bound: spread it over ~4 units per SM.
+static int attn_chunk_policy(int S, int NL, int Hkv, int LB, int max_kv_rows) {
+  return attn_chunk_keys(S, NL, Hkv, LB, max_kv_rows, 4 * 148);
 }
 
 extern "C" size_t sprint_block_attn_workspace_bytes(int S, int NL, int LB, int Hq, int Hkv,
@@ -201,7 +199,8 @@ extern "C" size_t sprint_block_attn_workspace_bytes(int S, int NL, int LB, int H
   if (S < 1 || NL < 1 || LB < 1 || Hq < 1 || Hkv < 1 || d < 1 || max_kv_rows < 0 ||
       Hq % Hkv != 0)
     return 0;
-  const int ck = attn_chunk_policy(S, NL, Hkv, LB, max_kv_rows, dtype);
+  if (dtype == SPRINT_BF16) return attn_tc_workspace_bytes(S, NL, Hkv, d);
+  const int ck = attn_chunk_policy(S, NL, Hkv, LB, max_kv_rows);
   return attn_ws_layout(nullptr, S, NL, LB, Hq, Hkv, d, max_kv_rows, ck).bytes;
 }
 
@@ -221,18 +220,21 @@ extern "C" int sprint_block_attn(const void *Q, const void *Kp, const void *Vp,
   if (total_kv_rows > 0 && (!Kp || !Vp)) return SPRINT_ERR_INVALID_ARG;
   if (ws_bytes < sprint_block_attn_workspace_bytes(S, NL, LB, Hq, Hkv, d, max_kv_rows, dtype))
     return SPRINT_ERR_WORKSPACE;
-  const int ck = attn_chunk_policy(S, NL, Hkv, LB, max_kv_rows, dtype);
+  if (dtype == SPRINT_BF16) {
+    if (!aligned16(Q) || !aligned16(Kb) || !aligned16(Vb) || (Kp && !aligned16(Kp)) ||
+        (Vp && !aligned16(Vp)))
+      return SPRINT_ERR_UNSUPPORTED;
+    return attn_tc_forward(static_cast<const __nv_bfloat16 *>(Q),
+                           static_cast<const __nv_bfloat16 *>(Kp),
+                           static_cast<const __nv_bfloat16 *>(Vp), kv_off, total_kv_rows,
+                           static_cast<const __nv_bfloat16 *>(Kb),
+                           static_cast<const __nv_bfloat16 *>(Vb), S, NL, LB, Hq, Hkv, d, O, ws,
+                           status, stream);
+  }
+  const int ck = attn_chunk_policy(S, NL, Hkv, LB, max_kv_rows);
   const AttnWs w = attn_ws_layout(ws, S, NL, LB, Hq, Hkv, d, max_kv_rows, ck);
   const int R = LB * (Hq / Hkv);
-  if (dtype == SPRINT_BF16) {
-    const int rc = attn_tc_chunks(static_cast<const __nv_bfloat16 *>(Q),
-                                  static_cast<const __nv_bfloat16 *>(Kp),
-                                  static_cast<const __nv_bfloat16 *>(Vp), kv_off, total_kv_rows,
-                                  static_cast<const __nv_bfloat16 *>(Kb),
-                                  static_cast<const __nv_bfloat16 *>(Vb), S, NL, LB, Hq, Hkv, d,
-                                  w, status, stream);
-    if (rc != SPRINT_OK) return rc;
-  } else {
+  {
     dim3 grid(w.chunks, NL * Hkv, S);
     const size_t sm = ((size_t)R * d + 32 * (d + 1) + 32 * d) * 4;
     if (d == 64) {
@@ -254,36 +256,7 @@ extern "C" int sprint_block_attn(const void *Q, const void *Kp, const void *Vp,
   }
   const long long rows = (long long)S * NL * Hkv * R;
   const int blocks = (int)((rows * 32 + 255) / 256);
-  if (dtype == SPRINT_BF16)
-    attn_combine_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
-        w, S, NL, LB, Hq, Hkv, d, static_cast<__nv_bfloat16 *>(O));
-  else
-    attn_combine_kernel<float><<<blocks, 256, 0, stream>>>(w, S, NL, LB, Hq, Hkv, d,
-                                                           static_cast<float *>(O));
-  return launch_status();
-}
-
-// Interim bf16 chunk producer on CUDA cores, used until the tensor-core
-// kernel is selected by attn_tc_chunks.
-int sprint::attn_simt_chunks_bf16(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp,
-                                  const __nv_bfloat16 *Vp, const int32_t *kv_off,
-                                  int total_kv_rows, const __nv_bfloat16 *Kb,
-                                  const __nv_bfloat16 *Vb, int S, int NL, int LB, int Hq,
-                                  int Hkv, int d, const AttnWs &w, int32_t *status,
-                                  cudaStream_t stream) {
-  const int R = LB * (Hq / Hkv);
-  dim3 grid(w.chunks, NL * Hkv, S);
-  const size_t sm = ((size_t)R * d + 32 * (d + 1) + 32 * d) * 4;
-  if (d == 64) {
-    cudaFuncSetAttribute(attn_simt_kernel<__nv_bfloat16, 64>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    attn_simt_kernel<__nv_bfloat16, 64><<<grid, 256, sm, stream>>>(
-        Q, Kp, Vp, kv_off, total_kv_rows, Kb, Vb, NL, LB, Hq, Hkv, w, status);
-  } else {
-    cudaFuncSetAttribute(attn_simt_kernel<__nv_bfloat16, 128>,
-                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    attn_simt_kernel<__nv_bfloat16, 128><<<grid, 256, sm, stream>>>(
-        Q, Kp, Vp, kv_off, total_kv_rows, Kb, Vb, NL, LB, Hq, Hkv, w, status);
-  }
+  attn_combine_kernel<float><<<blocks, 256, 0, stream>>>(w, S, NL, LB, Hq, Hkv, d,
+                                                         static_cast<float *>(O));
   return launch_status();
 }

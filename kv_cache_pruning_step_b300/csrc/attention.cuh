@@ -22,18 +22,12 @@ AttnWs attn_ws_layout(void *ws, int S, int NL, int LB, int Hq, int Hkv, int d, i
                       int chunk_keys);
 int attn_chunk_keys(int S, int NL, int Hkv, int LB, int max_kv_rows, int target_units);
 
-// Chunk length the bf16 tensor-core kernel is launched with.
-int attn_tc_chunk_keys(int S, int NL, int Hkv, int LB, int max_kv_rows);
-
-int attn_tc_chunks(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 *Vp,
-                   const int32_t *kv_off, int total_kv_rows, const __nv_bfloat16 *Kb,
-                   const __nv_bfloat16 *Vb, int S, int NL, int LB, int Hq, int Hkv, int d,
-                   const AttnWs &w, int32_t *status, cudaStream_t stream);
-
-int attn_simt_chunks_bf16(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp,
-                          const __nv_bfloat16 *Vp, const int32_t *kv_off, int total_kv_rows,
-                          const __nv_bfloat16 *Kb, const __nv_bfloat16 *Vb, int S, int NL,
-                          int LB, int Hq, int Hkv, int d, const AttnWs &w, int32_t *status,
-                          cudaStream_t stream);
+// bf16 path on the tcgen05 tensor cores (attention_tc.cu): workspace size
+// and the whole call (chunk kernel and combine).
+size_t attn_tc_workspace_bytes(int S, int NL, int Hkv, int d);
+int attn_tc_forward(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 *Vp,
+                    const int32_t *kv_off, int total_kv_rows, const __nv_bfloat16 *Kb,
+                    const __nv_bfloat16 *Vb, int S, int NL, int LB, int Hq, int Hkv, int d,
+                    void *O, void *ws, int32_t *status, cudaStream_t stream);
 
 }  // namespace sprint

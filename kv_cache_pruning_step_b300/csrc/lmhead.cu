@@ -127,6 +127,7 @@ __global__ void lmhead_combine_kernel(const float *__restrict__ pmax,
   const float sc = kLog2e / th;
   float best = -INFINITY, sum = 0.f;
   int arg = 0;
+#pragma unroll 8
   for (int t = 0; t < strips; ++t) {
     const float mx = pmax[(size_t)t * M + row];
     const float sm = psum[(size_t)t * M + row];
@@ -140,6 +141,55 @@ __global__ void lmhead_combine_kernel(const float *__restrict__ pmax,
   }
   conf[row] = 1.0f / sum;
   argmax[row] = arg;
+}
+
+struct Part {
+  float m, s;
+  int a;
+};
+
+// Fold of two partials of one row: max, rescaled sum, lowest column on ties.
+__device__ __forceinline__ Part fold(Part x, Part y, float sc) {
+  if (x.m == -INFINITY) return y;
+  if (y.m == -INFINITY) return x;
+  const float m = fmaxf(x.m, y.m);
+  Part r;
+  r.m = m;
+  r.s = x.s * exp2f((x.m - m) * sc) + y.s * exp2f((y.m - m) * sc);
+  r.a = x.m > y.m ? x.a : (y.m > x.m ? y.a : min(x.a, y.a));
+  return r;
+}
+
+// Few rows: one CTA per row, threads stride over the strips, then a fixed
+// shuffle/shared-memory tree (deterministic).
+__global__ void __launch_bounds__(128)
+lmhead_combine_rows_kernel(const float *__restrict__ pmax, const float *__restrict__ psum,
+                           const int32_t *__restrict__ parg, const float *__restrict__ temp,
+                           int M, int strips, float *__restrict__ conf,
+                           int32_t *__restrict__ argmax) {
+  __shared__ Part sh[4];
+  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float th = temp ? temp[row] : 1.0f;
+  if (!(th > 0.0f) || !isfinite(th)) th = 1.0f;
+  const float sc = kLog2e / th;
+  Part acc{-INFINITY, 0.f, 0};
+  for (int t = tid; t < strips; t += 128) {
+    const size_t at = (size_t)t * M + row;
+    acc = fold(acc, Part{pmax[at], psum[at], parg[at]}, sc);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Part y{__shfl_xor_sync(0xffffffffu, acc.m, o), __shfl_xor_sync(0xffffffffu, acc.s, o),
+           __shfl_xor_sync(0xffffffffu, acc.a, o)};
+    acc = (lane & o) ? fold(y, acc, sc) : fold(acc, y, sc);
+  }
+  if (lane == 0) sh[warp] = acc;
+  __syncthreads();
+  if (tid == 0) {
+    Part r = fold(fold(sh[0], sh[1], sc), fold(sh[2], sh[3], sc), sc);
+    conf[row] = 1.0f / r.s;
+    argmax[row] = r.a;
+  }
 }
 
 LmheadWs lmhead_ws_layout(void *ws, int M, int V) {
@@ -186,7 +236,11 @@ extern "C" int sprint_lmhead_confidence(const void *h, const void *W, const floa
         static_cast<float *>(logits_out), p.pmax, p.psum, p.parg, status);
     if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   }
-  lmhead_combine_kernel<<<(M + 255) / 256, 256, 0, stream>>>(p.pmax, p.psum, p.parg, temp, M,
-                                                             p.strips, conf_out, argmax_out);
+  if (M < 4096)
+    lmhead_combine_rows_kernel<<<M, 128, 0, stream>>>(p.pmax, p.psum, p.parg, temp, M, p.strips,
+                                                      conf_out, argmax_out);
+  else
+    lmhead_combine_kernel<<<(M + 255) / 256, 256, 0, stream>>>(p.pmax, p.psum, p.parg, temp, M,
+                                                               p.strips, conf_out, argmax_out);
   return launch_status();
 }
