@@ -63,6 +63,7 @@ extern "C" {
 #define SPRINT_ERR_UNSUPPORTED (-2) /* valid but not implemented (e.g. d)   */
 #define SPRINT_ERR_CUDA (-3)        /* a CUDA call or launch failed         */
 #define SPRINT_ERR_WORKSPACE (-5)   /* workspace smaller than required      */
+#define SPRINT_ERR_TOO_LARGE (-6)   /* beyond a fixed-size internal buffer  */
 
 /* Bits of the device status word. */
 #define SPRINT_STATUS_BAD_OFFSETS 1u   /* CSR offsets not monotone / too big */
@@ -121,6 +122,32 @@ int sprint_lmhead_confidence(const void *h, const void *W, const float *temp,
                              float *conf_out, int32_t *argmax_out, void *ws,
                              size_t ws_bytes, int32_t *status,
                              cudaStream_t stream);
+
+/*
+ * sprint_lmhead_confidence_noalloc -- sprint_lmhead_confidence for callers
+ * that cannot allocate device memory (for example a serving host or plugin
+ * whose device memory all comes from a pool it may not bypass, or a
+ * latency-critical loop that must not call cudaMalloc).  It takes no
+ * workspace; the partials live in a fixed file-scope device array of
+ * SPRINT_NOALLOC_SCRATCH_BYTES that every GPU which loads this library holds
+ * until the process exits.  The LLaDA2.0-Uni paper has no counterpart to
+ * this entry point: it is a memory-management variant of the one above.
+ *
+ * Arguments, layouts and results are those of sprint_lmhead_confidence.
+ * Limit: sprint_lmhead_workspace_bytes(M, D, V, dtype) must not exceed
+ * SPRINT_NOALLOC_SCRATCH_BYTES (4 MiB: 3 x 4 bytes x M x ceil(V / 256), e.g.
+ * up to 512 rows at a 157,184-entry vocabulary); larger calls return
+ * SPRINT_ERR_TOO_LARGE and launch nothing.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  All
+ * calls share the array: calls whose kernels overlap on the GPU race and
+ * must be serialised by the caller.  Nothing in the array needs clearing.
+ */
+#define SPRINT_NOALLOC_SCRATCH_BYTES (4u << 20)
+int sprint_lmhead_confidence_noalloc(const void *h, const void *W, const float *temp,
+                                     int M, int D, int V, int dtype, void *logits_out,
+                                     float *conf_out, int32_t *argmax_out,
+                                     int32_t *status, cudaStream_t stream);
 
 /*
  * sprint_score_prune -- per-modality kept set of every sequence's prefix.

@@ -18,6 +18,7 @@ extern "C" const char *sprint_strerror(int code) {
     case SPRINT_ERR_UNSUPPORTED: return "unsupported shape or layout for this build";
     case SPRINT_ERR_CUDA: return "a CUDA call or kernel launch failed";
     case SPRINT_ERR_WORKSPACE: return "workspace smaller than the *_workspace_bytes() size";
+    case SPRINT_ERR_TOO_LARGE: return "request larger than the library's fixed scratch array";
     default: return "unknown sprint error code";
   }
 }

@@ -36,6 +36,7 @@ SIGNATURES = {
     "sprint_keep_count": (_I, [_I, _D]),
     "sprint_lmhead_workspace_bytes": (_Z, [_I, _I, _I, _I]),
     "sprint_lmhead_confidence": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P, _P]),
+    "sprint_lmhead_confidence_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "sprint_score_prune_workspace_bytes": (_Z, [_I, _I]),
     "sprint_score_prune": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _F, _D, _D, _P, _P,
                                 _P, _P, _Z, _P, _P]),
@@ -148,6 +149,29 @@ def sprint_lmhead_confidence(h, W, temp=None, *, want_logits=False, conf=None, a
         _ptr(argmax, torch.int32, "argmax"), _ptr(ws), ws.numel(),
         _ptr(status, torch.int32, "status"), _stream(stream))
     _check(rc, "sprint_lmhead_confidence")
+    return conf, argmax, logits
+
+
+def sprint_lmhead_confidence_noalloc(h, W, temp=None, *, want_logits=False, conf=None,
+                                     argmax=None, logits=None, status=None, stream=None):
+    """sprint_lmhead_confidence without a workspace: the library's fixed
+    device scratch array holds the partials (see include/sprint.h for its
+    size limit and for the sharing rules between calls)."""
+    M, D = h.shape
+    V = W.shape[0]
+    dt = _dtype_code(h)
+    dev = h.device
+    conf = torch.empty(M, dtype=torch.float32, device=dev) if conf is None else conf
+    argmax = torch.empty(M, dtype=torch.int32, device=dev) if argmax is None else argmax
+    if want_logits and logits is None:
+        logits = torch.empty((M, V), dtype=h.dtype, device=dev)
+    status = new_status(dev) if status is None else status
+    rc = lib.sprint_lmhead_confidence_noalloc(
+        _ptr(h, h.dtype, "h"), _ptr(W, h.dtype, "W"), _ptr(temp, torch.float32, "temp"),
+        M, D, V, dt, _ptr(logits, h.dtype, "logits"), _ptr(conf, torch.float32, "conf"),
+        _ptr(argmax, torch.int32, "argmax"), _ptr(status, torch.int32, "status"),
+        _stream(stream))
+    _check(rc, "sprint_lmhead_confidence_noalloc")
     return conf, argmax, logits
 
 
