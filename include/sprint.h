@@ -135,8 +135,9 @@ int sprint_lmhead_confidence(const void *h, const void *W, const float *temp,
  *
  * Arguments, layouts and results are those of sprint_lmhead_confidence.
  * Limit: sprint_lmhead_workspace_bytes(M, D, V, dtype) must not exceed
- * SPRINT_NOALLOC_SCRATCH_BYTES (4 MiB: 3 x 4 bytes x M x ceil(V / 256), e.g.
- * up to 512 rows at a 157,184-entry vocabulary); larger calls return
+ * SPRINT_NOALLOC_SCRATCH_BYTES (4 MiB: 3 x 4 bytes x M x ceil(V / 224) for
+ * bf16 below 4096 rows, e.g. up to 497 rows at a 157,184-entry vocabulary;
+ * ceil(V / 256) strips otherwise); larger calls return
  * SPRINT_ERR_TOO_LARGE and launch nothing.  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture.  All

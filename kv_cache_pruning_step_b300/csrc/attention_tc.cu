@@ -5,28 +5,37 @@
 // to the pruned prefix; attention inside the block is bidirectional.
 //
 // Work decomposition (stream-K).  For sequence s the keys of one (layer l,
-// KV head g) pair are ceil(k_s / 128) prefix tiles of 128 keys plus one tile
-// holding the block's LB keys.  All tiles of all pairs form one ordered list
-// of T tiles; CTA c (of G = #SMs, one per SM) takes tiles
+// KV head g) pair are ceil(k_s / 64) prefix tiles of 64 keys plus
+// ceil(LB / 64) tiles of the block's own keys.  All tiles of all pairs form
+// one ordered list of T tiles; CTA c (of G = #SMs, one per SM) takes tiles
 // [c T / G, (c+1) T / G).  A CTA's range splits into segments at pair
-// boundaries; each segment writes one unnormalised partial (O rows, row max,
-// row sum) into slot  pair(x) + min(G, ceil((x+1) G / T)) - 1  (x = the
-// segment's first tile), which is unique over all segments and below
-// #pairs + G.  attn_tc_combine_kernel enumerates the segments of every pair
-// the same way and merges them in tile order.
+// boundaries; each segment writes two unnormalised partials (O rows, row
+// max, row sum; one per softmax warpgroup) into slots 2 * slot + {0, 1} with
+// slot = pair(x) + min(G, ceil((x+1) G / T)) - 1 (x = the segment's first
+// tile), which is unique over all segments and below #pairs + G.
+// attn_tc_combine_kernel enumerates the segments of every pair the same way
+// and merges them in tile order.
 //
-// Per segment (192 threads):
+// Per segment (320 threads):
 //   warp 0      TMA: the pair's 128 query rows (LB block positions x G heads of
 //               the group, one 3-D box per 64 head-dim columns), then K and V
-//               tiles (128 keys x d) into a 2-stage ring (128-byte swizzle);
-//   warp 1      owns 512 TMEM columns: S double buffer (2 x 128) and O (d);
-//               one lane issues S = Q K^T (M=128, N=128) and O += P V
-//               (M=128, N=d, V read MN-major), QK of tile t+1 ahead of PV of t;
-//   warps 2-5   softmax, one query row per thread: tile max from S, lazy
-//               rescale of O and l only when the max grows by more than 2^8,
-//               P = exp2(S * log2e/sqrt(d) - m) written as bf16 into the
-//               swizzled shared-memory A operand of the PV MMA; at the end of
-//               the segment O, m, l go to the workspace.
+//               tiles (64 keys x d) into a 4-stage ring (128-byte swizzle);
+//   warp 1      owns 512 TMEM columns: two S buffers (64 columns each) and two
+//               O accumulators (d each); one lane issues S = Q K^T (M=128,
+//               N=64) for tile q into S[q & 1] and O[q & 1] += P V (M=128,
+//               N=d, K=64, V read MN-major), QK of tile q+1 ahead of PV of q;
+//   warps 2-9   softmax in two warpgroups that take alternate tiles:
+//               warpgroup h owns the tiles q with q & 1 == h, with its own S
+//               buffer, P buffer and O accumulator, and runs its own online
+//               softmax (row max m_h, row sum l_h), one query row per thread.
+//               S is read from TMEM once into registers; the reference max
+//               moves only when the tile max exceeds it by more than 2^8 (O_h
+//               is then rescaled in TMEM); P = exp2(S * log2e/sqrt(d) - m_h)
+//               goes as bf16 into the warpgroup's swizzled P buffer, the A
+//               operand of the PV MMA.  Writing P of tile q waits only for
+//               the PV of tile q-2, so the other warpgroup's tile hides the
+//               PV latency.  At the end of the segment each warpgroup writes
+//               its (O_h, m_h, l_h) partial.
 #include <cuda.h>
 #include <math.h>
 
@@ -39,13 +48,15 @@ namespace sprint {
 bool make_tmap_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
                        uint64_t row_stride_elems, uint32_t box_inner, uint32_t box_rows);
 unsigned long long wait_cap_ns();
+int stall_test_enabled();
 int sm_count();
 
 namespace {
 
-constexpr int TILE = 128;       // keys per tile
+constexpr int TILE = 64;        // keys per tile
+constexpr int STAGES = 4;       // K/V ring depth
 constexpr int ROWS = 128;       // query rows per MMA tile (LB x G <= 128)
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;
 constexpr int MAX_SEQ = 1024;   // sequences per call on this path
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
@@ -56,18 +67,19 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 template <int D> struct Layout {
-  static constexpr int BOX = ROWS * 128;           // one 128-row x 64-col box
-  static constexpr int Q_BYTES = (D / 64) * BOX;
-  static constexpr int K_BYTES = (D / 64) * BOX;   // 128 keys x d
+  static constexpr int QBOX = ROWS * 128;          // 128 query rows x 64 cols
+  static constexpr int KBOX = TILE * 128;          // 64 keys x 64 cols
+  static constexpr int Q_BYTES = (D / 64) * QBOX;
+  static constexpr int K_BYTES = (D / 64) * KBOX;  // 64 keys x d
   static constexpr int STAGE = 2 * K_BYTES;        // K then V
-  static constexpr int P_BYTES = 2 * BOX;          // 128 rows x 128 keys
+  static constexpr int P_BUF = ROWS * 128;         // 128 rows x 64 keys bf16
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = Q_BYTES;
-  static constexpr int OFF_P = OFF_KV + 2 * STAGE;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int OFF_P = OFF_KV + STAGES * STAGE;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BUF;
   static constexpr int OFF_SEQ = OFF_BAR + 256;
   static constexpr size_t SMEM = 1024 + OFF_SEQ + 4 * (MAX_SEQ + 1) * 4;
-  static constexpr uint32_t TMEM_O = 2 * TILE;     // S buffers at 0 and 128
+  static constexpr uint32_t TMEM_O = 2 * TILE;     // S[0], S[1] at 0, 64; O_0, O_1 after
 };
 
 struct Problem {
@@ -75,12 +87,14 @@ struct Problem {
   int total_kv_rows, S, NL, LB, Hq, Hkv;
   float *ws_o, *ws_ml;
   int32_t *status;
-  unsigned long long cap_ns;
+  unsigned long long cap_ns;    // limit of every pipeline wait
+  unsigned long long drain_ns;  // limit of the final waits for in-flight work
+  int stall_test;               // failure-path test: the MMA role stalls first
 };
 
 // Per-sequence tables: ts[s] = first global tile of sequence s; nt[s] =
-// tiles per (layer, KV head) pair = ceil(k_s/128) + 1; ks[s] = prefix keys
-// (0 when the offsets are invalid); k0[s] = kv_off[s].
+// tiles per (layer, KV head) pair = ceil(k_s/64) + ceil(LB/64); ks[s] =
+// prefix keys (0 when the offsets are invalid); k0[s] = kv_off[s].
 __device__ void build_seq_tables(const Problem &pb, int *ts, int *nt, int *ks, int *k0,
                                  int32_t *status) {
   if (threadIdx.x == 0) {
@@ -91,7 +105,7 @@ __device__ void build_seq_tables(const Problem &pb, int *ts, int *nt, int *ks, i
       int k = b - a;
       if (a < 0 || k < 0 || b > pb.total_kv_rows) { bad = true; k = 0; a = 0; }
       ts[s] = acc;
-      nt[s] = (k + TILE - 1) / TILE + 1;
+      nt[s] = (k + TILE - 1) / TILE + (pb.LB + TILE - 1) / TILE;
       ks[s] = k;
       k0[s] = a;
       acc += pb.NL * pb.Hkv * nt[s];
@@ -142,11 +156,38 @@ __device__ __forceinline__ Seg locate(const Problem &pb, const int *ts, const in
   return sg;
 }
 
-// Swizzled (128-byte) address of 16-byte chunk `ch` (0..15 over 128 keys) of
-// row r in the P operand: two 64-key column blocks of 128 rows x 128 bytes.
-__device__ __forceinline__ uint32_t p_chunk_addr(uint32_t p_base, int r, int ch) {
-  const int blk = ch >> 3, c = ch & 7;
-  return p_base + blk * (ROWS * 128) + r * 128 + ((c ^ (r & 7)) << 4);
+// Swizzled (128-byte) address of 16-byte chunk `c` (0..7 over 64 keys) of
+// row r in a P buffer (128 rows x 128 bytes).
+__device__ __forceinline__ uint32_t p_chunk_addr(uint32_t buf, int r, int c) {
+  return buf + r * 128 + ((c ^ (r & 7)) << 4);
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22);
+// results below 2^-126 flush to zero, as do probabilities that small.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+      "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+      "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
+      "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
+      "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
 }
 
 template <int D>
@@ -160,10 +201,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
-  uint64_t *q_full = bar + 0, *k_full = bar + 1, *v_full = bar + 3, *kv_empty = bar + 5;
-  uint64_t *s_full = bar + 7, *s_free = bar + 9, *p_ready = bar + 11, *pv_done = bar + 12;
-  uint64_t *o_full = bar + 13, *drain = bar + 14;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 15);
+  uint64_t *q_full = bar;                        // 1
+  uint64_t *k_full = bar + 1;                    // STAGES
+  uint64_t *v_full = k_full + STAGES;            // STAGES
+  uint64_t *kv_empty = v_full + STAGES;          // STAGES
+  uint64_t *s_full = kv_empty + STAGES;          // 2
+  uint64_t *s_free = s_full + 2;                 // 2
+  uint64_t *p_ready = s_free + 2;                // 2
+  uint64_t *pv_done = p_ready + 2;               // 2
+  uint64_t *o_full = pv_done + 2, *drain = o_full + 1;
+  uint64_t *never = drain + 1;  // no one arrives: the stall test waits on it
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(never + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *ts = reinterpret_cast<int *>(smem + L::OFF_SEQ);
   int *nt = ts + (MAX_SEQ + 1), *ks = nt + (MAX_SEQ + 1), *k0 = ks + (MAX_SEQ + 1);
@@ -171,6 +219,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
   const int GQ = pb.Hq / pb.Hkv, R = pb.LB * GQ;
+  const int BR = pb.LB < TILE ? pb.LB : TILE;  // rows of a block-key box
 
   // Zero every operand buffer once: rows TMA never writes (query rows >= R,
   // key rows past a short tile) then hold finite values.
@@ -180,17 +229,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   build_seq_tables(pb, ts, nt, ks, k0, pb.status);
   if (threadIdx.x == 0) {
     tc::mbar_init(tc::smem_u32(q_full), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < STAGES; ++i) {
       tc::mbar_init(tc::smem_u32(k_full + i), 1);
       tc::mbar_init(tc::smem_u32(v_full + i), 1);
       tc::mbar_init(tc::smem_u32(kv_empty + i), 1);
-      tc::mbar_init(tc::smem_u32(s_full + i), 1);
-      tc::mbar_init(tc::smem_u32(s_free + i), 4);
     }
-    tc::mbar_init(tc::smem_u32(p_ready), 4);
-    tc::mbar_init(tc::smem_u32(pv_done), 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(tc::smem_u32(s_full + i), 1);
+      tc::mbar_init(tc::smem_u32(s_free + i), 4);   // the 4 warps of warpgroup i
+      tc::mbar_init(tc::smem_u32(p_ready + i), 4);
+      tc::mbar_init(tc::smem_u32(pv_done + i), 1);
+    }
     tc::mbar_init(tc::smem_u32(o_full), 1);
     tc::mbar_init(tc::smem_u32(drain), 1);
+    tc::mbar_init(tc::smem_u32(never), 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -210,14 +262,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const uint32_t sP = tc::smem_u32(smem + L::OFF_P);
   const float qk_scale = kLog2e * rsqrtf((float)D);
 
-  // Counters shared in meaning by all roles (each role keeps its own copy).
-  uint32_t seg_no = 0, tile_no = 0, qk_no = 0, pv_no = 0;
+  // Global tile counter (same in every role) and segment counter.
+  uint32_t seg_no = 0, tile_no = 0;
   // Producer bookkeeping for the final drain.
-  uint32_t issued = 0, last_par = 0;
+  uint32_t issued = 0, last_par = 0, q_issued = 0, q_par = 0;
 
   for (int x = x_begin; x < x_end; ++seg_no) {
     const Seg sg = locate(pb, ts, nt, ks, k0, x, x_end, G, T);
     x += sg.ntile;
+    const int np = (sg.k_s + TILE - 1) / TILE;  // prefix tiles of the pair
     const bool run = !*abort_flag;
     if (warp == 0 && lane == 0 && run) {
       // ------------------------------------------------ producer
@@ -225,27 +278,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       tc::mbar_arrive_expect_tx(qb, (uint32_t)((D / 64) * R * 128));
       const int qrow = (sg.s * pb.NL + sg.l) * pb.LB;
       for (int b = 0; b < D / 64; ++b)
-        tc::tma_load_3d(sQ + b * L::BOX, &tm_q, qb, b * 64, sg.g * GQ, qrow);
+        tc::tma_load_3d(sQ + b * L::QBOX, &tm_q, qb, b * 64, sg.g * GQ, qrow);
+      q_issued = 1;
+      q_par = seg_no & 1;
       for (int t = 0; t < sg.ntile; ++t) {
-        const int stage = (tile_no + t) & 1;
-        const uint32_t ph = ((tile_no + t) >> 1) & 1;
+        const uint32_t q = tile_no + t;
+        const int stage = q % STAGES;
+        const uint32_t ph = (q / STAGES) & 1;
         if (!tc::mbar_wait(tc::smem_u32(kv_empty + stage), ph ^ 1, pb.cap_ns, abort_flag)) break;
         const int i = sg.first_tile + t;
         const uint32_t kdst = sKV + stage * L::STAGE, vdst = kdst + L::K_BYTES;
         const uint32_t kb = tc::smem_u32(k_full + stage), vb = tc::smem_u32(v_full + stage);
-        if (i < sg.n_pair - 1) {
+        if (i < np) {
           const int z = pb.NL * sg.kv0 + sg.l * sg.k_s + i * TILE;
           tc::mbar_arrive_expect_tx(kb, L::K_BYTES);
-          for (int b = 0; b < D / 64; ++b) tc::tma_load_3d(kdst + b * L::BOX, &tm_kp, kb, b * 64, sg.g, z);
+          for (int b = 0; b < D / 64; ++b) tc::tma_load_3d(kdst + b * L::KBOX, &tm_kp, kb, b * 64, sg.g, z);
           tc::mbar_arrive_expect_tx(vb, L::K_BYTES);
-          for (int b = 0; b < D / 64; ++b) tc::tma_load_3d(vdst + b * L::BOX, &tm_vp, vb, b * 64, sg.g, z);
+          for (int b = 0; b < D / 64; ++b) tc::tma_load_3d(vdst + b * L::KBOX, &tm_vp, vb, b * 64, sg.g, z);
         } else {
-          const int z = (sg.s * pb.NL + sg.l) * pb.LB;
-          const uint32_t bytes = (uint32_t)((D / 64) * pb.LB * 128);
+          const int z = (sg.s * pb.NL + sg.l) * pb.LB + (i - np) * TILE;
+          const uint32_t bytes = (uint32_t)((D / 64) * BR * 128);
           tc::mbar_arrive_expect_tx(kb, bytes);
-          for (int b = 0; b < D / 64; ++b) tc::tma_load_3d(kdst + b * L::BOX, &tm_kb, kb, b * 64, sg.g, z);
+          for (int b = 0; b < D / 64; ++b) tc::tma_load_3d(kdst + b * L::KBOX, &tm_kb, kb, b * 64, sg.g, z);
           tc::mbar_arrive_expect_tx(vb, bytes);
-          for (int b = 0; b < D / 64; ++b) tc::tma_load_3d(vdst + b * L::BOX, &tm_vb, vb, b * 64, sg.g, z);
+          for (int b = 0; b < D / 64; ++b) tc::tma_load_3d(vdst + b * L::KBOX, &tm_vb, vb, b * 64, sg.g, z);
         }
         issued |= 1u << stage;
         last_par = (last_par & ~(1u << stage)) | (ph << stage);
@@ -254,40 +310,59 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       // ------------------------------------------------ MMA issuer
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(ROWS, TILE, false, false);
       constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(ROWS, D, false, true);
-      bool ok = tc::mbar_wait(tc::smem_u32(q_full), seg_no & 1, pb.cap_ns, abort_flag);
+      // Failure-path test: wait on a barrier no one arrives on, so the
+      // bounded wait expires and the CTA takes its abort path.
+      if (pb.stall_test) tc::mbar_wait(tc::smem_u32(never), 0, pb.cap_ns, abort_flag);
+      bool ok = !*abort_flag &&
+                tc::mbar_wait(tc::smem_u32(q_full), seg_no & 1, pb.cap_ns, abort_flag);
+      // Shared-memory descriptors: built once, then advanced by constant
+      // offsets (the start-address field counts 16-byte units and never
+      // carries: every address is below 256 KB).  The issuing warp shares
+      // its SM sub-partition with softmax warps, so every instruction here
+      // is on the critical path.
+      const uint64_t qd = tc::desc_kmajor_sw128(sQ);
+      const uint64_t kd0 = tc::desc_kmajor_sw128(sKV);
+      const uint64_t vd0 = tc::desc_mnmajor_sw128(sKV + L::K_BYTES, L::KBOX);
+      const uint64_t pd0 = tc::desc_kmajor_sw128(sP);
+      constexpr uint64_t kStageD = L::STAGE >> 4, kPbufD = L::P_BUF >> 4;
+      // O[q & 1] += P[q & 1] V for segment tile u (global tile q).
       auto issue_pv = [&](int u) -> bool {
-        const int stage = (tile_no + u) & 1;
-        const uint32_t ph = ((tile_no + u) >> 1) & 1;
-        if (!tc::mbar_wait(tc::smem_u32(p_ready), (pv_no + u) & 1, pb.cap_ns, abort_flag)) return false;
-        if (!tc::mbar_wait(tc::smem_u32(v_full + stage), ph, pb.cap_ns, abort_flag)) return false;
+        const uint32_t q = tile_no + u;
+        const int stage = q % STAGES, h = q & 1;
+        const uint32_t ph = (q / STAGES) & 1;
+        if (!tc::mbar_wait(tc::smem_u32(p_ready + h), (q >> 1) & 1, pb.cap_ns, abort_flag) ||
+            !tc::mbar_wait(tc::smem_u32(v_full + stage), ph, pb.cap_ns, abort_flag))
+          return false;
         tc::fence_after_sync();
-        const uint32_t vbase = sKV + stage * L::STAGE + L::K_BYTES;
+        const uint64_t vd = vd0 + (uint64_t)stage * kStageD;
+        const uint64_t pd = pd0 + (uint64_t)h * kPbufD;
+        const uint32_t od = tmem + L::TMEM_O + h * D;
+        // A warpgroup's first tile of the segment (u < 2) starts its O.
+        tc::mma_bf16(od, pd, vd, idesc_pv, u >= 2 ? 1u : 0u);
 #pragma unroll
-        for (int k = 0; k < TILE / 16; ++k) {
-          const uint64_t a = tc::desc_kmajor_sw128(sP + (k >> 2) * L::BOX + (k & 3) * 32);
-          const uint64_t b = tc::desc_mnmajor_sw128(vbase + k * 16 * 128, L::BOX);
-          tc::mma_bf16(tmem + L::TMEM_O, a, b, idesc_pv, (u > 0 || k > 0) ? 1u : 0u);
-        }
-        tc::mma_commit(tc::smem_u32(pv_done));
+        for (int k = 1; k < TILE / 16; ++k)  // 16 keys: 32 B of P, 16 rows of V
+          tc::mma_bf16(od, pd + 2 * k, vd + (16 * 128 >> 4) * k, idesc_pv, 1u);
+        tc::mma_commit(tc::smem_u32(pv_done + h));
         tc::mma_commit(tc::smem_u32(kv_empty + stage));
         return true;
       };
       for (int t = 0; ok && t < sg.ntile; ++t) {
-        const int stage = (tile_no + t) & 1;
-        const uint32_t ph = ((tile_no + t) >> 1) & 1;
-        const uint32_t q = qk_no + t, sb = q & 1;
+        const uint32_t q = tile_no + t;
+        const int stage = q % STAGES, sb = q & 1;
+        const uint32_t ph = (q / STAGES) & 1;
         if (!tc::mbar_wait(tc::smem_u32(k_full + stage), ph, pb.cap_ns, abort_flag) ||
             !tc::mbar_wait(tc::smem_u32(s_free + sb), ((q >> 1) & 1) ^ 1, pb.cap_ns, abort_flag)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        const uint32_t kbase = sKV + stage * L::STAGE;
+        const uint64_t kd = kd0 + (uint64_t)stage * kStageD;
+        const uint32_t sd = tmem + sb * TILE;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * L::BOX + (k & 3) * 32;
-          tc::mma_bf16(tmem + sb * TILE, tc::desc_kmajor_sw128(sQ + off),
-                       tc::desc_kmajor_sw128(kbase + off), idesc_qk, k > 0 ? 1u : 0u);
+          constexpr int kQBoxD = L::QBOX >> 4, kKBoxD = L::KBOX >> 4;
+          tc::mma_bf16(sd, qd + (k >> 2) * kQBoxD + (k & 3) * 2, kd + (k >> 2) * kKBoxD + (k & 3) * 2,
+                       idesc_qk, k > 0 ? 1u : 0u);
         }
         tc::mma_commit(tc::smem_u32(s_full + sb));
         if (t > 0 && !issue_pv(t - 1)) { ok = false; break; }
@@ -295,148 +370,157 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       if (ok) ok = issue_pv(sg.ntile - 1);
       if (ok) tc::mma_commit(tc::smem_u32(o_full));
     } else if (warp >= 2 && run) {
-      // ------------------------------------------------ softmax
+      // ------------------------------------------------ softmax, warpgroup h
+      const int h = (warp - 2) >> 2;
       const int q4 = warp & 3, r = q4 * 32 + lane;
       const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+      const uint32_t o_addr = tmem + lane_off + L::TMEM_O + h * D;
+      const uint32_t s_addr = tmem + lane_off + h * TILE;
+      const uint32_t pbuf = sP + h * L::P_BUF;
       float m_used = -INFINITY, l_sum = 0.f;
-      bool ok = true;
+      bool ok = true, mine = false;
       for (int t = 0; t < sg.ntile; ++t) {
-        const uint32_t q = qk_no + t, sb = q & 1;
+        const uint32_t q = tile_no + t;
+        if ((int)(q & 1) != h) continue;
+        mine = true;
         const int i = sg.first_tile + t;
-        const int nvalid = i < sg.n_pair - 1 ? min(TILE, sg.k_s - i * TILE) : pb.LB;
-        if (!__all_sync(0xffffffffu,
-                        tc::mbar_wait(tc::smem_u32(s_full + sb), (q >> 1) & 1, pb.cap_ns, abort_flag))) {
+        const int nvalid = i < np ? min(TILE, sg.k_s - i * TILE)
+                                  : min(TILE, pb.LB - (i - np) * TILE);
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(tc::smem_u32(s_full + h), (q >> 1) & 1,
+                                                   pb.cap_ns, abort_flag))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        const uint32_t s_addr = tmem + lane_off + sb * TILE;
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int c = 0; c < TILE / 32; ++c) {
-          float v[32];
-          tc::tmem_ld32(s_addr + c * 32, v);
+        float v[64];
+        {
+          float (&v0)[32] = *reinterpret_cast<float (*)[32]>(&v[0]);
+          float (&v1)[32] = *reinterpret_cast<float (*)[32]>(&v[32]);
+          tc::tmem_ld32(s_addr, v0);
+          tc::tmem_ld32(s_addr + 32, v1);
           tc::tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c * 32 + j < nvalid) mx = fmaxf(mx, v[j] * qk_scale);
         }
-        // P buffer and O are free once the previous PV has completed.
-        if (t > 0 && !__all_sync(0xffffffffu, tc::mbar_wait(tc::smem_u32(pv_done),
-                                                            (pv_no + t - 1) & 1, pb.cap_ns,
-                                                            abort_flag))) {
+        // S of this tile is in registers: its TMEM columns may be reused.
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(s_free + h));
+        const bool full = nvalid == TILE;
+        if (!full) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (j >= nvalid) v[j] = -INFINITY;  // masked keys: exp2 gives 0
+        }
+        // Row max of the 64 raw scores: a tree of 3-input maxima.
+        float m1[22], m2[8];
+#pragma unroll
+        for (int j = 0; j < 21; ++j) m1[j] = max3(v[3 * j], v[3 * j + 1], v[3 * j + 2]);
+        m1[21] = v[63];
+#pragma unroll
+        for (int j = 0; j < 7; ++j) m2[j] = max3(m1[3 * j], m1[3 * j + 1], m1[3 * j + 2]);
+        m2[7] = m1[21];
+        const float mraw = max3(max3(m2[0], m2[1], m2[2]), max3(m2[3], m2[4], m2[5]),
+                                fmaxf(m2[6], m2[7]));
+        const float mx = mraw * qk_scale;
+        // This warpgroup's P buffer and O are free once the PV of its
+        // previous tile (q - 2) is done; within a segment only.
+        if (t >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(tc::smem_u32(pv_done + h),
+                                                             ((q >> 1) & 1) ^ 1, pb.cap_ns,
+                                                             abort_flag))) {
           ok = false;
           break;
         }
         // Lazy rescale: a row moves its reference max only when the tile max
-        // exceeds it by more than 2^8; O rows are rescaled in TMEM (the
-        // tcgen05.ld/st are warp-collective, the factor is per row).
+        // exceeds it by more than 2^8; O rows are then rescaled in TMEM.
         const bool need = mx > m_used + kRescaleLog2;
         const float alpha = need ? exp2f(m_used - mx) : 1.0f;
         if (need) {
           l_sum *= alpha;
           m_used = mx;
         }
-        if (t > 0 && __any_sync(0xffffffffu, need)) {
+        if (t >= 2 && __any_sync(0xffffffffu, need)) {
           tc::fence_after_sync();
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             float o[32];
-            tc::tmem_ld32(tmem + lane_off + L::TMEM_O + c * 32, o);
+            tc::tmem_ld32(o_addr + c * 32, o);
             tc::tmem_wait_ld();
-            uint32_t u[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(o[j] * alpha);
-            asm volatile(
-                "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-                "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-                "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
-                ::"r"(tmem + lane_off + L::TMEM_O + c * 32),
-                "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]),
-                "r"(u[7]), "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]),
-                "r"(u[13]), "r"(u[14]), "r"(u[15]), "r"(u[16]), "r"(u[17]), "r"(u[18]),
-                "r"(u[19]), "r"(u[20]), "r"(u[21]), "r"(u[22]), "r"(u[23]), "r"(u[24]),
-                "r"(u[25]), "r"(u[26]), "r"(u[27]), "r"(u[28]), "r"(u[29]), "r"(u[30]),
-                "r"(u[31])
-                : "memory");
+            for (int j = 0; j < 32; ++j) o[j] *= alpha;
+            tmem_st32(o_addr + c * 32, o);
           }
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
-        // P = exp2(S * scale - m) in bf16, written to the swizzled A operand.
-#pragma unroll 1
-        for (int c = 0; c < TILE / 32; ++c) {
-          float v[32];
-          tc::tmem_ld32(s_addr + c * 32, v);
-          tc::tmem_wait_ld();
-          uint32_t pk[16];
+        // P = exp2(S * scale - m) in bf16, written to the swizzled P buffer
+        // (masked keys hold -inf and give 0).
+        float lsum = 0.f;
+        const float nm = -m_used;
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float p0 = c * 32 + j < nvalid ? exp2f(fmaf(v[j], qk_scale, -m_used)) : 0.f;
-            const float p1 = c * 32 + j + 1 < nvalid ? exp2f(fmaf(v[j + 1], qk_scale, -m_used)) : 0.f;
-            l_sum += p0 + p1;
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-            pk[j >> 1] = *reinterpret_cast<uint32_t *>(&h2);
-          }
+        for (int c = 0; c < 8; ++c) {
+          uint32_t pk[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const uint32_t addr = p_chunk_addr(sP, r, c * 4 + u);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * u]),
-                         "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]), "r"(pk[4 * u + 3])
-                         : "memory");
+            const int j = c * 8 + 2 * u;
+            const float p0 = fast_exp2(fmaf(v[j], qk_scale, nm));
+            const float p1 = fast_exp2(fmaf(v[j + 1], qk_scale, nm));
+            lsum += p0 + p1;
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+            pk[u] = *reinterpret_cast<uint32_t *>(&h2);
           }
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(p_chunk_addr(pbuf, r, c)),
+                       "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
+                       : "memory");
         }
+        l_sum += lsum;
         tc::fence_before_sync();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) {
-          tc::mbar_arrive(tc::smem_u32(s_free + sb));
-          tc::mbar_arrive(tc::smem_u32(p_ready));
-        }
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(p_ready + h));
       }
       if (ok && __all_sync(0xffffffffu, tc::mbar_wait(tc::smem_u32(o_full), seg_no & 1,
                                                       pb.cap_ns, abort_flag))) {
         tc::fence_after_sync();
-        float *dst = pb.ws_o + ((size_t)sg.slot * ROWS + r) * D;
+        const size_t part = (size_t)(2 * sg.slot + h) * ROWS + r;
+        if (mine) {
+          float *dst = pb.ws_o + part * D;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          float o[32];
-          tc::tmem_ld32(tmem + lane_off + L::TMEM_O + c * 32, o);
-          tc::tmem_wait_ld();
-          if (r < R) {
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tc::tmem_ld32(o_addr + c * 32, o);
+            tc::tmem_wait_ld();
+            if (r < R) {
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4 *>(dst + c * 32 + j) =
-                  make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+              for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4 *>(dst + c * 32 + j) =
+                    make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+            }
           }
         }
-        if (r < R) {
-          pb.ws_ml[((size_t)sg.slot * ROWS + r) * 2] = m_used;
-          pb.ws_ml[((size_t)sg.slot * ROWS + r) * 2 + 1] = l_sum;
-        }
+        // A warpgroup with no tile in this segment leaves an empty partial.
+        if (r < R) *reinterpret_cast<float2 *>(pb.ws_ml + part * 2) = make_float2(m_used, l_sum);
         tc::fence_before_sync();
       }
     }
     tile_no += sg.ntile;
-    qk_no += sg.ntile;
-    pv_no += sg.ntile;
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
   }
 
-  // Drain: no copy or MMA of this CTA may be in flight when it exits.
+  // Drain: no copy or MMA of this CTA may be in flight when it exits.  These
+  // waits ignore the abort flag and use the longer drain limit.
   if (warp == 0 && lane == 0) {
-    for (int s = 0; s < 2; ++s)
+    volatile int no_abort = 0;
+    if (q_issued) tc::mbar_wait(tc::smem_u32(q_full), q_par, pb.drain_ns, &no_abort);
+    for (int s = 0; s < STAGES; ++s)
       if (issued >> s & 1u) {
-        volatile int no_abort = 0;
-        tc::mbar_wait(tc::smem_u32(k_full + s), last_par >> s & 1u, pb.cap_ns, &no_abort);
-        tc::mbar_wait(tc::smem_u32(v_full + s), last_par >> s & 1u, pb.cap_ns, &no_abort);
+        tc::mbar_wait(tc::smem_u32(k_full + s), last_par >> s & 1u, pb.drain_ns, &no_abort);
+        tc::mbar_wait(tc::smem_u32(v_full + s), last_par >> s & 1u, pb.drain_ns, &no_abort);
       }
   }
   if (warp == 1 && lane == 0) {
     tc::mma_commit(tc::smem_u32(drain));
     volatile int no_abort = 0;
-    tc::mbar_wait(tc::smem_u32(drain), 0, pb.cap_ns, &no_abort);
+    tc::mbar_wait(tc::smem_u32(drain), 0, pb.drain_ns, &no_abort);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -445,9 +529,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (warp == 1) tc::tmem_dealloc(tmem, 512);
 }
 
-// One warp per (pair, query row): merge the pair's segments in tile order.
+// One warp per (pair, query row): merge both warpgroup partials of every
+// segment of the pair in tile order with a running max (single pass).
 template <int D>
-__global__ void attn_tc_combine_kernel(Problem pb, int G, __nv_bfloat16 *__restrict__ O) {
+__global__ void __launch_bounds__(256)
+attn_tc_combine_kernel(Problem pb, int G, __nv_bfloat16 *__restrict__ O) {
   __shared__ int ts[MAX_SEQ + 1], nt[MAX_SEQ + 1], ks[MAX_SEQ + 1], k0[MAX_SEQ + 1];
   build_seq_tables(pb, ts, nt, ks, k0, nullptr);
   __syncthreads();
@@ -462,28 +548,33 @@ __global__ void attn_tc_combine_kernel(Problem pb, int G, __nv_bfloat16 *__restr
   const int l = pis / pb.Hkv, g = pis % pb.Hkv;
   const long long T = ts[pb.S];
   const int p0 = ts[s] + pis * nt[s], p1 = p0 + nt[s];
-  float mx = -INFINITY;
-  for (long long x = p0; x < p1;) {
-    const long long c = starts_le(x, G, T);
-    const long long nxt = c < G ? c * T / G : T;
-    const int slot = pair + (int)c - 1;
-    mx = fmaxf(mx, pb.ws_ml[((size_t)slot * ROWS + r) * 2]);
-    x = nxt < p1 ? nxt : p1;
-  }
-  float den = 0.f, acc[D / 32];
+  float mx = -INFINITY, den = 0.f, acc[D / 32];
 #pragma unroll
   for (int q = 0; q < D / 32; ++q) acc[q] = 0.f;
   for (long long x = p0; x < p1;) {
     const long long c = starts_le(x, G, T);
     const long long nxt = c < G ? c * T / G : T;
     const int slot = pair + (int)c - 1;
-    const float mc = pb.ws_ml[((size_t)slot * ROWS + r) * 2];
-    if (mc != -INFINITY) {
-      const float wgt = exp2f(mc - mx);
-      den = fmaf(wgt, pb.ws_ml[((size_t)slot * ROWS + r) * 2 + 1], den);
-      const float *oc = pb.ws_o + ((size_t)slot * ROWS + r) * D;
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) acc[q] = fmaf(wgt, oc[lane + 32 * q], acc[q]);
+    for (int h = 0; h < 2; ++h) {
+      const size_t part = (size_t)(2 * slot + h) * ROWS + r;
+      const float2 ml = *reinterpret_cast<const float2 *>(pb.ws_ml + part * 2);
+      if (ml.x == -INFINITY) continue;  // this warpgroup saw no key of the segment
+      const float *oc = pb.ws_o + part * D;
+      float oq[D / 32];
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) oq[q] = oc[lane + 32 * q];
+      if (ml.x > mx) {
+        const float sc = exp2f(mx - ml.x);  // 0 while mx is -inf
+        den *= sc;
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) acc[q] *= sc;
+        mx = ml.x;
+      }
+      const float wgt = exp2f(ml.x - mx);
+      den = fmaf(wgt, ml.y, den);
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) acc[q] = fmaf(wgt, oq[q], acc[q]);
     }
     x = nxt < p1 ? nxt : p1;
   }
@@ -531,8 +622,9 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
   const int GQ = Hq / Hkv;
   CUtensorMap tq, tkp, tvp, tkb, tvb;
   const uint64_t brows = (uint64_t)S * NL * LB;
-  if (!make_tmap_3d(&tq, Q, D, Hq, brows, GQ, LB) || !make_tmap_3d(&tkb, Kb, D, Hkv, brows, 1, LB) ||
-      !make_tmap_3d(&tvb, Vb, D, Hkv, brows, 1, LB))
+  const int BR = LB < TILE ? LB : TILE;
+  if (!make_tmap_3d(&tq, Q, D, Hq, brows, GQ, LB) || !make_tmap_3d(&tkb, Kb, D, Hkv, brows, 1, BR) ||
+      !make_tmap_3d(&tvb, Vb, D, Hkv, brows, 1, BR))
     return SPRINT_ERR_CUDA;
   if (total_kv_rows > 0) {
     if (!make_tmap_3d(&tkp, Kp, D, Hkv, (uint64_t)NL * total_kv_rows, 1, TILE) ||
@@ -557,9 +649,11 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
   pb.S = S; pb.NL = NL; pb.LB = LB; pb.Hq = Hq; pb.Hkv = Hkv;
   pb.ws_o = static_cast<float *>(ws);
   pb.ws_ml = reinterpret_cast<float *>(static_cast<char *>(ws) +
-                                       align_up((pairs + G) * ROWS * D * 4, 256));
+                                       align_up(2 * (pairs + G) * ROWS * D * 4, 256));
   pb.status = status;
   pb.cap_ns = wait_cap_ns();
+  pb.drain_ns = pb.cap_ns > 1000000000ull ? pb.cap_ns : 1000000000ull;
+  pb.stall_test = stall_test_enabled();
   attn_tc_kernel<D><<<G, THREADS, Lt::SMEM, stream>>>(tq, tkp, tvp, tkb, tvb, pb);
   if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   const long long warps = (long long)pairs * LB * GQ;
@@ -571,8 +665,8 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
 }  // namespace
 
 size_t attn_tc_workspace_bytes(int S, int NL, int Hkv, int d) {
-  const size_t slots = (size_t)S * NL * Hkv + (size_t)sm_count();
-  return align_up(slots * ROWS * d * 4, 256) + align_up(slots * ROWS * 2 * 4, 256);
+  const size_t parts = 2 * ((size_t)S * NL * Hkv + (size_t)sm_count());
+  return align_up(parts * ROWS * d * 4, 256) + align_up(parts * ROWS * 2 * 4, 256);
 }
 
 int attn_tc_forward(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 *Vp,

@@ -114,35 +114,6 @@ lmhead_simt_kernel(const T *__restrict__ h, const T *__restrict__ W,
   }
 }
 
-// Fold the column-strip partials of every row in ascending strip order.
-__global__ void lmhead_combine_kernel(const float *__restrict__ pmax,
-                                      const float *__restrict__ psum,
-                                      const int32_t *__restrict__ parg,
-                                      const float *__restrict__ temp, int M, int strips,
-                                      float *__restrict__ conf, int32_t *__restrict__ argmax) {
-  const int row = blockIdx.x * blockDim.x + threadIdx.x;
-  if (row >= M) return;
-  float th = temp ? temp[row] : 1.0f;
-  if (!(th > 0.0f) || !isfinite(th)) th = 1.0f;
-  const float sc = kLog2e / th;
-  float best = -INFINITY, sum = 0.f;
-  int arg = 0;
-#pragma unroll 8
-  for (int t = 0; t < strips; ++t) {
-    const float mx = pmax[(size_t)t * M + row];
-    const float sm = psum[(size_t)t * M + row];
-    if (mx > best) {
-      sum = sum * exp2f((best - mx) * sc) + sm;
-      best = mx;
-      arg = parg[(size_t)t * M + row];
-    } else {
-      sum += sm * exp2f((mx - best) * sc);
-    }
-  }
-  conf[row] = 1.0f / sum;
-  argmax[row] = arg;
-}
-
 struct Part {
   float m, s;
   int a;
@@ -158,6 +129,41 @@ __device__ __forceinline__ Part fold(Part x, Part y, float sc) {
   r.s = x.s * exp2f((x.m - m) * sc) + y.s * exp2f((y.m - m) * sc);
   r.a = x.m > y.m ? x.a : (y.m > x.m ? y.a : min(x.a, y.a));
   return r;
+}
+
+// Many rows: a CTA of 32 rows x 8 strip groups.  Thread (x, y) folds strips
+// y, y + 8, ... of row x (loads coalesced over x), then the 8 group partials
+// of each row are folded in ascending y.  Deterministic for given M, V.
+constexpr int kCombRows = 32, kCombGroups = 8;
+
+__global__ void __launch_bounds__(kCombRows * kCombGroups)
+lmhead_combine_kernel(const float *__restrict__ pmax, const float *__restrict__ psum,
+                      const int32_t *__restrict__ parg, const float *__restrict__ temp, int M,
+                      int strips, float *__restrict__ conf, int32_t *__restrict__ argmax) {
+  __shared__ Part sh[kCombGroups][kCombRows];
+  const int x = threadIdx.x, y = threadIdx.y;
+  const int row = blockIdx.x * kCombRows + x;
+  float th = 1.0f;
+  if (row < M && temp) th = temp[row];
+  if (!(th > 0.0f) || !isfinite(th)) th = 1.0f;
+  const float sc = kLog2e / th;
+  Part acc{-INFINITY, 0.f, 0};
+  if (row < M) {
+#pragma unroll 4
+    for (int t = y; t < strips; t += kCombGroups) {
+      const size_t at = (size_t)t * M + row;
+      acc = fold(acc, Part{pmax[at], psum[at], parg[at]}, sc);
+    }
+  }
+  sh[y][x] = acc;
+  __syncthreads();
+  if (y == 0 && row < M) {
+    Part r = sh[0][x];
+#pragma unroll
+    for (int g = 1; g < kCombGroups; ++g) r = fold(r, sh[g][x], sc);
+    conf[row] = 1.0f / r.s;
+    argmax[row] = r.a;
+  }
 }
 
 // Few rows: one CTA per row, threads stride over the strips, then a fixed
@@ -192,12 +198,12 @@ lmhead_combine_rows_kernel(const float *__restrict__ pmax, const float *__restri
   }
 }
 
-LmheadWs lmhead_ws_layout(void *ws, int M, int V) {
-  const int strips = (V + kPartCols - 1) / kPartCols;
+LmheadWs lmhead_ws_layout(void *ws, int M, int V, int cols) {
+  const int strips = (V + cols - 1) / cols;
   const size_t one = align_up((size_t)strips * M * 4, 256);
   char *p = static_cast<char *>(ws);
   return {reinterpret_cast<float *>(p), reinterpret_cast<float *>(p + one),
-          reinterpret_cast<int32_t *>(p + 2 * one), strips};
+          reinterpret_cast<int32_t *>(p + 2 * one), strips, cols};
 }
 
 }  // namespace sprint
@@ -206,9 +212,9 @@ using namespace sprint;
 
 extern "C" size_t sprint_lmhead_workspace_bytes(int M, int D, int V, int dtype) {
   (void)D;
-  (void)dtype;
   if (M < 0 || V < 1) return 0;
-  const int strips = (V + kPartCols - 1) / kPartCols;
+  const int cols = lmhead_strip_cols(M, dtype);
+  const int strips = (V + cols - 1) / cols;
   return 3 * align_up((size_t)strips * M * 4, 256);
 }
 
@@ -222,7 +228,7 @@ extern "C" int sprint_lmhead_confidence(const void *h, const void *W, const floa
   if (M == 0) return SPRINT_OK;
   if (!h || !W || !conf_out || !argmax_out || !ws || !status) return SPRINT_ERR_INVALID_ARG;
   if (ws_bytes < sprint_lmhead_workspace_bytes(M, D, V, dtype)) return SPRINT_ERR_WORKSPACE;
-  const LmheadWs p = lmhead_ws_layout(ws, M, V);
+  const LmheadWs p = lmhead_ws_layout(ws, M, V, lmhead_strip_cols(M, dtype));
   if (dtype == SPRINT_BF16) {
     if (D % 8 != 0 || !aligned16(h) || !aligned16(W)) return SPRINT_ERR_UNSUPPORTED;
     const int rc = lmhead_tc_tiles(static_cast<const __nv_bfloat16 *>(h),
@@ -240,7 +246,8 @@ extern "C" int sprint_lmhead_confidence(const void *h, const void *W, const floa
     lmhead_combine_rows_kernel<<<M, 128, 0, stream>>>(p.pmax, p.psum, p.parg, temp, M, p.strips,
                                                       conf_out, argmax_out);
   else
-    lmhead_combine_kernel<<<(M + 255) / 256, 256, 0, stream>>>(p.pmax, p.psum, p.parg, temp, M,
-                                                               p.strips, conf_out, argmax_out);
+    lmhead_combine_kernel<<<(M + kCombRows - 1) / kCombRows, dim3(kCombRows, kCombGroups), 0,
+                            stream>>>(p.pmax, p.psum, p.parg, temp, M, p.strips, conf_out,
+                                      argmax_out);
   return launch_status();
 }

@@ -4,19 +4,31 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "../../include/sprint.h"
+
 namespace sprint {
 
-// Vocabulary columns folded into one (max, sum-exp, argmax) partial per row.
+// Vocabulary columns folded into one (max, sum-exp, argmax) partial per row:
+// 256 by default; 224 for bf16 calls with few rows (block steps), where the
+// column tiles are the whole grid's work and 702 tiles of 224 divide over
+// 148 SMs better than 614 tiles of 256.
 constexpr int kPartCols = 256;
+constexpr int kPartColsNarrow = 224;
+constexpr int kNarrowMaxRows = 4096;
+
+inline int lmhead_strip_cols(int M, int dtype) {
+  return dtype == SPRINT_BF16 && M < kNarrowMaxRows ? kPartColsNarrow : kPartCols;
+}
 
 struct LmheadWs {
   float *pmax;    // [strips][M] max of the raw fp32 dot products in the strip
   float *psum;    // [strips][M] sum of exp(z - z_stripmax) over the strip
   int32_t *parg;  // [strips][M] first column attaining the strip max
-  int strips;     // ceil(V / kPartCols)
+  int strips;     // ceil(V / cols)
+  int cols;       // vocabulary columns per strip
 };
 
-LmheadWs lmhead_ws_layout(void *ws, int M, int V);
+LmheadWs lmhead_ws_layout(void *ws, int M, int V, int cols);
 
 // bf16 tiles on the tcgen05 tensor cores; writes the strip partials (and
 // the temperature-scaled logits when `logits` is not null).

@@ -8,13 +8,16 @@
 // of z = (h . W_v) / theta; the probability vector is never formed.
 //
 // Design (one persistent CTA per SM, 192 threads, 1 CTA/SM):
-//   warp 0      TMA producer: 128x64 tiles of h and 256x64 tiles of W (bf16,
-//               128-byte swizzle) into a 4-stage shared-memory ring;
+//   warp 0      TMA producer: 128x64 tiles of h and BNx64 tiles of W (bf16,
+//               128-byte swizzle) into a 4-stage shared-memory ring; BN =
+//               256, or 224 when the call has few rows (the column tiles are
+//               then all the work, and 702 of them spread over 148 SMs more
+//               evenly than 614);
 //   warp 1      allocates 512 TMEM columns; one lane issues
-//               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=256, K=16) into
-//               one of two 256-column fp32 accumulators;
+//               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16) into
+//               one of two fp32 accumulators (TMEM columns 0 and 256);
 //   warps 2-5   epilogue: each thread owns one accumulator row (TMEM lane),
-//               reads its 256 columns 32 at a time with tcgen05.ld, and folds
+//               reads its BN columns 32 at a time with tcgen05.ld, and folds
 //               them into (max of raw dot products, first column reaching it,
 //               sum of exp2((acc - max) * log2(e) / theta)); optional logits
 //               (acc / theta in bf16).  The second accumulator lets the MMA of
@@ -32,14 +35,21 @@
 namespace sprint {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, BAND = 32;
+constexpr int BM = 128, BK = 64, STAGES = 4, BAND = 32;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_STRIDE = 256;  // TMEM columns between the two accumulators
 constexpr int THREADS = 192;
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Tile shape per column width BN (256, or 224 for calls with few rows).
+template <int BN> struct Tiles {
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+  static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
+  static_assert(BN % 32 == 0 && BN <= 256, "epilogue reads 32 columns at a time");
+};
 
 __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &m, int &n) {
   const int per_band = BAND * num_m;
@@ -50,19 +60,25 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &m,
   n = band * BAND + idx % bw;
 }
 
+template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
 lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                  const float *__restrict__ temp, int M, int D, int V,
                  __nv_bfloat16 *__restrict__ logits, float *__restrict__ pmax,
                  float *__restrict__ psum, int32_t *__restrict__ parg, int32_t *status,
-                 unsigned long long cap_ns) {
+                 unsigned long long cap_ns, int stall_test) {
+  // The final waits for in-flight copies and MMAs ignore the abort flag and
+  // get at least one second.
+  const unsigned long long drain_ns = cap_ns > 1000000000ull ? cap_ns : 1000000000ull;
+  constexpr int STAGE_BYTES = Tiles<BN>::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
   uint64_t *full = bars, *empty = bars + STAGES;
   uint64_t *tfull = bars + 2 * STAGES, *tempty = tfull + 2, *drain = tempty + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *never = drain + 1;  // no one arrives: the stall test waits on it
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(never + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -79,6 +95,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       tc::mbar_init(tc::smem_u32(tempty + b), 4);
     }
     tc::mbar_init(tc::smem_u32(drain), 1);
+    tc::mbar_init(tc::smem_u32(never), 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -123,7 +140,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       for (int s = 0; s < STAGES; ++s)
         if (issued >> s & 1u) {
           volatile int no_abort = 0;
-          tc::mbar_wait(tc::smem_u32(full + s), last_parity >> s & 1u, cap_ns, &no_abort);
+          tc::mbar_wait(tc::smem_u32(full + s), last_parity >> s & 1u, drain_ns, &no_abort);
         }
     }
   } else if (warp == 1) {
@@ -133,13 +150,16 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+      // Failure-path test: wait on a barrier no one arrives on, so the
+      // bounded wait expires and the CTA takes its abort path.
+      if (stall_test) tc::mbar_wait(tc::smem_u32(never), 0, cap_ns, abort_flag);
+      for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x, ++it) {
         const int buf = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
         if (!tc::mbar_wait(tc::smem_u32(tempty + buf), (use & 1u) ^ 1u, cap_ns, abort_flag))
           break;
         tc::fence_after_sync();
-        const uint32_t d = tmem + (uint32_t)(buf * BN);
+        const uint32_t d = tmem + (uint32_t)buf * ACC_STRIDE;
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait(tc::smem_u32(full + stage), phase, cap_ns, abort_flag)) {
@@ -162,7 +182,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       // Every MMA this thread issued has finished once `drain` completes.
       tc::mma_commit(tc::smem_u32(drain));
       volatile int no_abort = 0;
-      tc::mbar_wait(tc::smem_u32(drain), 0, cap_ns, &no_abort);
+      tc::mbar_wait(tc::smem_u32(drain), 0, drain_ns, &no_abort);
     }
   } else {
     // ---------------- epilogue: one accumulator row per thread
@@ -189,7 +209,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       const float sc = kLog2e / th, inv = 1.0f / th;
       float run_max = -INFINITY, run_sum = 0.f;
       int arg = 0;
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)buf * ACC_STRIDE;
       const int col0 = n * BN;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
@@ -275,6 +295,15 @@ bool make_tmap_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int stall_test_enabled() {
+  static int v = -1;
+  if (v < 0) {
+    const char *e = getenv("SPRINT_TEST_STALL");
+    v = (e && e[0] == '1') ? 1 : 0;
+  }
+  return v;
+}
+
 unsigned long long wait_cap_ns() {
   static unsigned long long cap = 0;
   if (!cap) {
@@ -292,26 +321,38 @@ int sm_count() {
   return sms;
 }
 
-int lmhead_tc_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *temp, int M,
-                    int D, int V, __nv_bfloat16 *logits, const LmheadWs &p, int32_t *status,
-                    cudaStream_t stream) {
+template <int BN>
+int launch_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *temp, int M, int D,
+                 int V, __nv_bfloat16 *logits, const LmheadWs &p, int32_t *status,
+                 cudaStream_t stream) {
+  constexpr size_t SMEM_BYTES = Tiles<BN>::SMEM_BYTES;
   CUtensorMap tm_h, tm_w;
   if (!make_tmap_bf16_2d(&tm_h, h, D, M, D, BK, BM) ||
       !make_tmap_bf16_2d(&tm_w, W, D, V, D, BK, BN))
     return SPRINT_ERR_CUDA;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(lmhead_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(lmhead_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess)
       return SPRINT_ERR_CUDA;
     attr_set = true;
   }
   const int tiles = ((M + BM - 1) / BM) * ((V + BN - 1) / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  lmhead_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(tm_h, tm_w, temp, M, D, V, logits,
-                                                          p.pmax, p.psum, p.parg, status,
-                                                          wait_cap_ns());
+  lmhead_tc_kernel<BN><<<grid, THREADS, SMEM_BYTES, stream>>>(
+      tm_h, tm_w, temp, M, D, V, logits, p.pmax, p.psum, p.parg, status, wait_cap_ns(),
+      stall_test_enabled());
   return launch_status();
+}
+
+int lmhead_tc_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *temp, int M,
+                    int D, int V, __nv_bfloat16 *logits, const LmheadWs &p, int32_t *status,
+                    cudaStream_t stream) {
+  if (p.cols == kPartColsNarrow)
+    return launch_tiles<kPartColsNarrow>(h, W, temp, M, D, V, logits, p, status, stream);
+  if (p.cols == kPartCols)
+    return launch_tiles<kPartCols>(h, W, temp, M, D, V, logits, p, status, stream);
+  return SPRINT_ERR_UNSUPPORTED;
 }
 
 }  // namespace sprint

@@ -8,24 +8,63 @@
 // Two kernels:
 //   keynorm_kernel  HBM-bound: one warp per prefix position reads that
 //                   position's key rows of every layer (NL x Hkv*d elements,
-//                   1 KB per layer at Hkv*d = 512 bf16) with 16-byte loads
-//                   and writes u_i = mean over layers of the L2 norm of the
+//                   1 KB per layer at Hkv*d = 512 bf16) with 16-byte loads,
+//                   eight layers' loads in flight at once, and writes
+//                   u_i = mean over layers of the L2 norm of the
 //                   concatenated KV heads.
 //   select_kernel   latency-bound: one 1024-thread CTA per sequence.  Mean of
-//                   u (fp64 sum), composite score s_i in fp32, then a 4-pass
+//                   u (fp32 per thread, fp64 across threads), composite score
+//                   s_i in fp32, then a 4-pass
 //                   8-bit radix select on the orderable 32-bit key of s_i for
 //                   both modalities at once, ties at the threshold resolved
 //                   by ascending position with a block scan, and a stable
 //                   block-scan compaction writing kept indices in ascending
-//                   position order.
+//                   position order.  The sequence's keys and modality tags
+//                   are staged in shared memory (5 bytes per position) when
+//                   they fit, so global memory is read once and the six
+//                   passes run at shared-memory latency; longer sequences
+//                   keep them in the workspace.
 #include <math.h>
 
 #include "common.cuh"
 
 namespace sprint {
 
+// Eight consecutive elements as raw loaded bits, squared and summed in
+// element order after the load has landed.
+template <typename T> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> {
+  typedef uint4 type;
+  static __device__ __forceinline__ uint4 load(const __nv_bfloat16 *p) {
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+  }
+  static __device__ __forceinline__ float sum_sq(uint4 u, float acc) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float a = __uint_as_float(w[i] << 16), b = __uint_as_float(w[i] & 0xffff0000u);
+      acc = fmaf(a, a, acc);
+      acc = fmaf(b, b, acc);
+    }
+    return acc;
+  }
+};
+template <> struct Raw8<float> {
+  struct type { float4 a, b; };
+  static __device__ __forceinline__ type load(const float *p) {
+    return {__ldg(reinterpret_cast<const float4 *>(p)),
+            __ldg(reinterpret_cast<const float4 *>(p) + 1)};
+  }
+  static __device__ __forceinline__ float sum_sq(type v, float acc) {
+    const float x[8] = {v.a.x, v.a.y, v.a.z, v.a.w, v.b.x, v.b.y, v.b.z, v.b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc = fmaf(x[i], x[i], acc);
+    return acc;
+  }
+};
+
 template <typename T>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 keynorm_kernel(const T *__restrict__ K, const int32_t *__restrict__ prefix_off,
                int S, int total_rows, int NL, int row_elems,
                float *__restrict__ u, int32_t *status) {
@@ -43,31 +82,36 @@ keynorm_kernel(const T *__restrict__ K, const int32_t *__restrict__ prefix_off,
     const size_t layer_stride = (size_t)(p1 - p0) * row_elems;
     const T *base = K + ((size_t)NL * p0 + i) * row_elems;
     float acc = 0.f;
-    int l = 0;
-    // Four layers' loads in flight per step keep enough bytes outstanding.
-    for (; l + 4 <= NL; l += 4) {
-      float ss[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int e = lane * 8; e < row_elems; e += 256) {
-        float x[4][8];
+    // Up to LG layers x two 16-byte chunks per lane are loaded before any is
+    // used: 256 bytes per lane (8 KB per warp) in flight for bf16.
+    constexpr int LG = sizeof(T) == 2 ? 8 : 4;
+    for (int l0 = 0; l0 < NL; l0 += LG) {
+      const int nl = min(LG, NL - l0);
+      float ss[LG];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) Vec8<T>::load(base + (l + q) * layer_stride + e, x[q]);
+      for (int q = 0; q < LG; ++q) ss[q] = 0.f;
+      for (int e = lane * 8; e < row_elems; e += 512) {
+        const bool second = e + 256 < row_elems;
+        typename Raw8<T>::type x[LG], y[LG];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < LG; ++q) {
+          if (q < nl) {
+            const T *p = base + (size_t)(l0 + q) * layer_stride + e;
+            x[q] = Raw8<T>::load(p);
+            if (second) y[q] = Raw8<T>::load(p + 256);
+          }
+        }
 #pragma unroll
-          for (int k = 0; k < 8; ++k) ss[q] = fmaf(x[q][k], x[q][k], ss[q]);
+        for (int q = 0; q < LG; ++q) {
+          if (q < nl) {
+            ss[q] = Raw8<T>::sum_sq(x[q], ss[q]);
+            if (second) ss[q] = Raw8<T>::sum_sq(y[q], ss[q]);
+          }
+        }
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) acc += sqrtf(warp_sum(ss[q]));
-    }
-    for (; l < NL; ++l) {
-      float ss = 0.f;
-      for (int e = lane * 8; e < row_elems; e += 256) {
-        float x[8];
-        Vec8<T>::load(base + l * layer_stride + e, x);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) ss = fmaf(x[k], x[k], ss);
-      }
-      acc += sqrtf(warp_sum(ss));
+      for (int q = 0; q < LG; ++q)
+        if (q < nl) acc += sqrtf(warp_sum(ss[q]));
     }
     if (lane == 0) u[row] = acc / (float)NL;
   }
@@ -75,6 +119,9 @@ keynorm_kernel(const T *__restrict__ K, const int32_t *__restrict__ prefix_off,
 
 constexpr int kSelThreads = 1024;
 constexpr int kSelPer = 8;  // consecutive positions per thread per chunk
+// Longest sequence whose keys and tags are staged in shared memory:
+// 40,960 x 5 bytes = 200 KB of the 227 KB a CTA may hold.
+constexpr int kStageMax = 40960;
 
 __device__ __forceinline__ int keep_count_dev(int n, double r) {
   return (int)floor(r * (double)n + 1e-9);
@@ -86,8 +133,9 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
               const int32_t *__restrict__ prefix_off,
               const int32_t *__restrict__ kept_off, int S, int total_rows,
               float alpha, double r_text, double r_img,
-              uint32_t *__restrict__ keys, int32_t *__restrict__ kept_idx,
-              float *__restrict__ score_out, int32_t *status) {
+              uint32_t *__restrict__ keys_ws, int32_t *__restrict__ kept_idx,
+              float *__restrict__ score_out, int32_t *status, int stage_cap) {
+  extern __shared__ uint32_t stage_sh[];  // [stage_cap] keys, then [stage_cap] tags
   __shared__ uint32_t hist[2][256];
   __shared__ int scan_sh[33];
   __shared__ double dsum_sh[32];
@@ -104,15 +152,31 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
     return;
   }
   const int n = p1 - p0;
+  // Keys and modality tags of this sequence: staged in shared memory when
+  // they fit, else read from the workspace / the caller's array.
+  const bool staged = n <= stage_cap;
+  uint32_t *keys = staged ? stage_sh : keys_ws + p0;
+  uint8_t *mod_sh = reinterpret_cast<uint8_t *>(stage_sh + stage_cap);
+  const uint8_t *mods = staged ? mod_sh : modality + p0;
 
-  // Pass 1: sum of u (fp64, fixed order) and the image count.
-  double su = 0.0;
+  // Pass 1: sum of u and the image count; u is kept (as raw bits) where the
+  // keys will go.  Each thread sums its positions in fp32; the 1024 thread
+  // sums are added in fp64 (FP64 throughput is low on this GPU, so fp64 is
+  // kept off the per-position path).
+  float su_f = 0.f;
   int nimg = 0;
+#pragma unroll 8
   for (int i = tid; i < n; i += kSelThreads) {
-    su += (double)u[p0 + i];
-    nimg += modality[p0 + i] != 0;
+    const float ui = u[p0 + i];
+    const uint8_t mi = modality[p0 + i] != 0;
+    su_f += ui;
+    nimg += mi;
+    if (staged) {
+      keys[i] = __float_as_uint(ui);
+      mod_sh[i] = mi;
+    }
   }
-  su = warp_sum(su);
+  double su = warp_sum((double)su_f);
   nimg = warp_sum(nimg);
   if (lane == 0) { dsum_sh[warp] = su; cnt_sh[warp] = nimg; }
   __syncthreads();
@@ -132,12 +196,16 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
     return;
   }
 
-  // Pass 2: composite score s_i = alpha I_i + (1 - alpha) c_i in fp32.
+  // Pass 2: composite score s_i = alpha I_i + (1 - alpha) c_i in fp32
+  // (I_i = u_i / mean, an fp32 division by the fp32-rounded mean).
   const float one_m_alpha = 1.0f - alpha;
+  const float mean_f = (float)mean;
+#pragma unroll 8
   for (int i = tid; i < n; i += kSelThreads) {
-    const float imp = mean > 0.0 ? (float)((double)u[p0 + i] / mean) : 0.0f;
+    const float ui = staged ? __uint_as_float(keys[i]) : u[p0 + i];
+    const float imp = mean_f > 0.0f ? ui / mean_f : 0.0f;
     const float sc = fmaf(alpha, imp, one_m_alpha * conf[p0 + i]);
-    keys[p0 + i] = float_key(sc);
+    keys[i] = float_key(sc);
     if (score_out) score_out[p0 + i] = sc;
   }
   if (tid < 2) {
@@ -160,8 +228,8 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
       const int i = base + tid;
       int bin = -1;
       if (i < n) {
-        const uint32_t key = keys[p0 + i];
-        const int mu = modality[p0 + i] != 0;
+        const uint32_t key = keys[i];
+        const int mu = mods[i] != 0;
         const uint32_t pre = mu ? pre1 : pre0;
         const bool act = mu ? act1 : act0;
         if (act && ((key ^ pre) & hi_mask) == 0u) bin = mu * 256 + ((key >> shift) & 255u);
@@ -224,8 +292,8 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
       kk[q] = 0u;
       mm[q] = 0;
       if (i < n) {
-        kk[q] = keys[p0 + i];
-        mm[q] = modality[p0 + i] != 0;
+        kk[q] = keys[i];
+        mm[q] = mods[i] != 0;
         if (mm[q] == 0 && m0 == 2 && kk[q] == T0) ties += 1;
         if (mm[q] != 0 && m1 == 2 && kk[q] == T1) ties += 1 << 16;
       }
@@ -299,9 +367,10 @@ extern "C" int sprint_score_prune(const void *K, int S, const int32_t *prefix_of
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int warps_needed = total_rows;
-    int blocks = (warps_needed + 7) / 8;
-    blocks = blocks < sms * 8 ? blocks : sms * 8;
+    // One wave: two 256-thread CTAs per SM (register-limited), each warp
+    // striding over rows.
+    int blocks = (total_rows + 7) / 8;
+    blocks = blocks < sms * 2 ? blocks : sms * 2;
     if (dtype == SPRINT_BF16)
       keynorm_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
           static_cast<const __nv_bfloat16 *>(K), prefix_off, S, total_rows, NL, row_elems, u,
@@ -311,9 +380,21 @@ extern "C" int sprint_score_prune(const void *K, int S, const int32_t *prefix_of
           static_cast<const float *>(K), prefix_off, S, total_rows, NL, row_elems, u, status);
     if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   }
-  select_kernel<<<S, kSelThreads, 0, stream>>>(u, conf, modality, prefix_off, kept_off, S,
-                                               total_rows, alpha, r_text, r_img, keys,
-                                               kept_idx, score_out, status);
+  // Stage up to kStageMax positions per sequence in shared memory (5 bytes
+  // each); the capacity follows the longest sequence the call can hold.
+  const int stage_cap = total_rows < kStageMax ? total_rows : kStageMax;
+  const size_t stage_bytes = (size_t)stage_cap * 5 + 16;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)((size_t)kStageMax * 5 + 16)) != cudaSuccess)
+      return SPRINT_ERR_CUDA;
+    attr_set = true;
+  }
+  select_kernel<<<S, kSelThreads, stage_bytes, stream>>>(u, conf, modality, prefix_off,
+                                                         kept_off, S, total_rows, alpha, r_text,
+                                                         r_img, keys, kept_idx, score_out,
+                                                         status, stage_cap);
   return launch_status();
 }
 

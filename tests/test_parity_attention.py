@@ -99,3 +99,24 @@ def test_batched_ragged_full_size(sp):
     steps = [step_inputs(w, s, 0, 1, device=DEV) for s in range(4)]
     O = run_attn(sp, w, prefixes, steps)
     check(w, prefixes, steps, O, layers=[3], what="batch")
+
+
+def test_full_retention_pruned_cache_equals_full_prefix_bitwise(sp):
+    """r = 1 keeps every position: attention over the compacted cache must be
+    bit-identical to attention over the full prefix (same kernel, same keys)."""
+    w = WORKLOADS["prefix-4k"]
+    pre = prefix_inputs(w, device=DEV)
+    n = pre["modality"].numel()
+    x = step_inputs(w, 0, 0, 1, device=DEV)
+    off = torch.tensor([0, n], dtype=torch.int32, device=DEV)
+    kept = torch.arange(n, dtype=torch.int32, device=DEV)
+    status = sp.new_status(DEV)
+    Kp, Vp = sp.sprint_compact_kv(pre["K"], pre["V"], off, n, w.NL, w.Hkv, w.d, kept, off, n,
+                                  status=status)
+    O_full = run_attn(sp, w, [pre], [x])
+    O_pruned = sp.sprint_block_attn(x["Q"][None].contiguous(), Kp, Vp, off, n, n,
+                                    x["Kb"][None].contiguous(), x["Vb"][None].contiguous(),
+                                    status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.equal(O_full, O_pruned)
