@@ -266,6 +266,83 @@ int sprint_unmask(const float *conf, const int32_t *argmax, uint8_t *mask,
                   float tau, int mode, uint8_t *accepted_out, int32_t *status,
                   cudaStream_t stream);
 
+/*
+ * sprint_decode_steps -- every denoising step of one block, enqueued in one
+ * call (the library's native block driver).  LLaDA2.0-Uni paper, Sparse
+ * Prefix Retention and Non-uniform Token Unmasking paragraphs: step 0
+ * attends to the full prefix, steps t >= 1 to the pruned prefix; every step
+ * predicts the block's tokens and unmasks a confidence-adaptive number of
+ * them, at least ceil(m / (T - t)), so the block ends within T steps.
+ *
+ * For step t = 0 .. T-1 the call enqueues sprint_block_attn, then
+ * sprint_lmhead_confidence on the block rows, then sprint_unmask, on
+ * `stream`, without any device-to-host synchronisation.  Whether a step
+ * runs is decided on the device: the kernels of step t >= 1 read the
+ * still-masked counts m_hist[t-1][0..S) written by step t-1 and return at
+ * once when all are zero (the block finished earlier).  Before step 0 the
+ * call sets mask to 1 and tokens to -1 (cudaMemsetAsync).  The prefix pass
+ * (prefix confidences, sprint_score_prune, sprint_compact_kv) is not part
+ * of this call.
+ *
+ * Steps executed = 1 + the number of t in [1, T) with some m_hist[t-1][s]
+ * > 0; the caller reads m_hist after synchronising.
+ *
+ * Every step's inputs (Q, Kb, Vb, h, theta) are given up front: this
+ * driver suits step inputs that are already resident (for example produced
+ * by device work enqueued earlier on the same stream).
+ *
+ * Fields (all device pointers unless noted; layouts as for the five calls):
+ *   S, NL, LB, Hq, Hkv, d, D, vocab, dtype   shapes and storage type
+ *   T, tau, mode                             step budget and unmask rule
+ *   Kf, Vf, prefix_off, max_rows, total_rows the full prefix (step 0)
+ *   Kp, Vp, kept_off, max_kept, total_kept   the pruned prefix (t >= 1)
+ *   W                                        LM-head weight [vocab][D]
+ *   Q, Kb, Vb, h, theta                      HOST arrays of T device pointers
+ *                                            (theta entries may be NULL)
+ *   O                                        [S][NL][LB][Hq][d] attention out
+ *   logits                                   [S*LB][vocab] or NULL
+ *   conf, argmax                             [S*LB] last executed step's c
+ *   mask, tokens                             [S][LB] state, reset at step 0
+ *   m_hist                                   int32 [T][S] masked after step t
+ *   accepted                                 uint8 [T][S][LB] or NULL
+ *   ws_attn / ws_lm (+ bytes)                workspaces of the two calls
+ *   status                                   device status word
+ *   events                                   NULL or a HOST array of 6*T
+ *                                            cudaEvent_t: per step, start and
+ *                                            end of attention, LM head, unmask
+ * Returns the first non-zero code of the enqueued calls (nothing after it
+ * is enqueued), SPRINT_ERR_INVALID_ARG for a missing field.
+ */
+typedef struct sprint_steps_args {
+  int S, NL, LB, Hq, Hkv, d, D, vocab, dtype;
+  int T;
+  float tau;
+  int mode;
+  const void *Kf, *Vf;
+  const int32_t *prefix_off;
+  int max_rows, total_rows;
+  const void *Kp, *Vp;
+  const int32_t *kept_off;
+  int max_kept, total_kept;
+  const void *W;
+  const void *const *Q, *const *Kb, *const *Vb, *const *h;
+  const float *const *theta;
+  void *O, *logits;
+  float *conf;
+  int32_t *argmax;
+  uint8_t *mask;
+  int32_t *tokens, *m_hist;
+  uint8_t *accepted;
+  void *ws_attn;
+  size_t ws_attn_bytes;
+  void *ws_lm;
+  size_t ws_lm_bytes;
+  int32_t *status;
+  void *const *events;
+} sprint_steps_args;
+
+int sprint_decode_steps(const sprint_steps_args *args, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

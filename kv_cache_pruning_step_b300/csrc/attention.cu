@@ -26,8 +26,9 @@ __global__ void __launch_bounds__(256)
 attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ Kp, const T *__restrict__ Vp,
                  const int32_t *__restrict__ kv_off, int total_kv_rows,
                  const T *__restrict__ Kb, const T *__restrict__ Vb, int NL, int LB, int Hq,
-                 int Hkv, AttnWs ws, int32_t *status) {
+                 int Hkv, AttnWs ws, int32_t *status, Gate gate) {
   constexpr int TK = 32;
+  if (gate_closed(gate)) return;
   extern __shared__ float smem[];
   const int G = Hq / Hkv, R = LB * G;
   float *Qs = smem;                  // [R][D]
@@ -130,7 +131,8 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ Kp, const T *__r
 // chunk partials in ascending chunk order and normalise.
 template <typename T>
 __global__ void attn_combine_kernel(AttnWs ws, int S, int NL, int LB, int Hq, int Hkv, int D,
-                                    T *__restrict__ O) {
+                                    T *__restrict__ O, Gate gate) {
+  if (gate_closed(gate)) return;
   const int G = Hq / Hkv, R = LB * G;
   const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -204,11 +206,11 @@ extern "C" size_t sprint_block_attn_workspace_bytes(int S, int NL, int LB, int H
   return attn_ws_layout(nullptr, S, NL, LB, Hq, Hkv, d, max_kv_rows, ck).bytes;
 }
 
-extern "C" int sprint_block_attn(const void *Q, const void *Kp, const void *Vp,
-                                 const int32_t *kv_off, int max_kv_rows, int total_kv_rows,
-                                 const void *Kb, const void *Vb, int S, int NL, int LB, int Hq,
-                                 int Hkv, int d, int dtype, void *O, void *ws, size_t ws_bytes,
-                                 int32_t *status, cudaStream_t stream) {
+int sprint::block_attn_impl(const void *Q, const void *Kp, const void *Vp,
+                            const int32_t *kv_off, int max_kv_rows, int total_kv_rows,
+                            const void *Kb, const void *Vb, int S, int NL, int LB, int Hq,
+                            int Hkv, int d, int dtype, void *O, void *ws, size_t ws_bytes,
+                            int32_t *status, Gate gate, cudaStream_t stream) {
   if (S < 0 || NL < 1 || LB < 1 || Hq < 1 || Hkv < 1 || max_kv_rows < 0 || total_kv_rows < 0)
     return SPRINT_ERR_INVALID_ARG;
   if (dtype != SPRINT_F32 && dtype != SPRINT_BF16) return SPRINT_ERR_INVALID_ARG;
@@ -229,7 +231,7 @@ extern "C" int sprint_block_attn(const void *Q, const void *Kp, const void *Vp,
                            static_cast<const __nv_bfloat16 *>(Vp), kv_off, total_kv_rows,
                            static_cast<const __nv_bfloat16 *>(Kb),
                            static_cast<const __nv_bfloat16 *>(Vb), S, NL, LB, Hq, Hkv, d, O, ws,
-                           status, stream);
+                           status, gate, stream);
   }
   const int ck = attn_chunk_policy(S, NL, Hkv, LB, max_kv_rows);
   const AttnWs w = attn_ws_layout(ws, S, NL, LB, Hq, Hkv, d, max_kv_rows, ck);
@@ -243,20 +245,29 @@ extern "C" int sprint_block_attn(const void *Q, const void *Kp, const void *Vp,
       attn_simt_kernel<float, 64><<<grid, 256, sm, stream>>>(
           static_cast<const float *>(Q), static_cast<const float *>(Kp),
           static_cast<const float *>(Vp), kv_off, total_kv_rows, static_cast<const float *>(Kb),
-          static_cast<const float *>(Vb), NL, LB, Hq, Hkv, w, status);
+          static_cast<const float *>(Vb), NL, LB, Hq, Hkv, w, status, gate);
     } else {
       cudaFuncSetAttribute(attn_simt_kernel<float, 128>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
       attn_simt_kernel<float, 128><<<grid, 256, sm, stream>>>(
           static_cast<const float *>(Q), static_cast<const float *>(Kp),
           static_cast<const float *>(Vp), kv_off, total_kv_rows, static_cast<const float *>(Kb),
-          static_cast<const float *>(Vb), NL, LB, Hq, Hkv, w, status);
+          static_cast<const float *>(Vb), NL, LB, Hq, Hkv, w, status, gate);
     }
     if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   }
   const long long rows = (long long)S * NL * Hkv * R;
   const int blocks = (int)((rows * 32 + 255) / 256);
   attn_combine_kernel<float><<<blocks, 256, 0, stream>>>(w, S, NL, LB, Hq, Hkv, d,
-                                                         static_cast<float *>(O));
+                                                         static_cast<float *>(O), gate);
   return launch_status();
+}
+
+extern "C" int sprint_block_attn(const void *Q, const void *Kp, const void *Vp,
+                                 const int32_t *kv_off, int max_kv_rows, int total_kv_rows,
+                                 const void *Kb, const void *Vb, int S, int NL, int LB, int Hq,
+                                 int Hkv, int d, int dtype, void *O, void *ws, size_t ws_bytes,
+                                 int32_t *status, cudaStream_t stream) {
+  return block_attn_impl(Q, Kp, Vp, kv_off, max_kv_rows, total_kv_rows, Kb, Vb, S, NL, LB, Hq,
+                         Hkv, d, dtype, O, ws, ws_bytes, status, Gate{nullptr, 0}, stream);
 }

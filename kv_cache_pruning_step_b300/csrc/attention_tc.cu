@@ -90,6 +90,7 @@ struct Problem {
   unsigned long long cap_ns;    // limit of every pipeline wait
   unsigned long long drain_ns;  // limit of the final waits for in-flight work
   int stall_test;               // failure-path test: the MMA role stalls first
+  Gate gate;                    // step gate of the native block driver
 };
 
 // Per-sequence tables: ts[s] = first global tile of sequence s; nt[s] =
@@ -197,6 +198,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                const __grid_constant__ CUtensorMap tm_kb,
                const __grid_constant__ CUtensorMap tm_vb, Problem pb) {
   using L = Layout<D>;
+  if (gate_closed(pb.gate)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -534,6 +536,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 template <int D>
 __global__ void __launch_bounds__(256)
 attn_tc_combine_kernel(Problem pb, int G, __nv_bfloat16 *__restrict__ O) {
+  if (gate_closed(pb.gate)) return;
   __shared__ int ts[MAX_SEQ + 1], nt[MAX_SEQ + 1], ks[MAX_SEQ + 1], k0[MAX_SEQ + 1];
   build_seq_tables(pb, ts, nt, ks, k0, nullptr);
   __syncthreads();
@@ -617,7 +620,7 @@ template <int D>
 int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 *Vp,
            const int32_t *kv_off, int total_kv_rows, const __nv_bfloat16 *Kb,
            const __nv_bfloat16 *Vb, int S, int NL, int LB, int Hq, int Hkv, void *O, void *ws,
-           int32_t *status, cudaStream_t stream) {
+           int32_t *status, Gate gate, cudaStream_t stream) {
   using Lt = Layout<D>;
   const int GQ = Hq / Hkv;
   CUtensorMap tq, tkp, tvp, tkb, tvb;
@@ -654,6 +657,7 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
   pb.cap_ns = wait_cap_ns();
   pb.drain_ns = pb.cap_ns > 1000000000ull ? pb.cap_ns : 1000000000ull;
   pb.stall_test = stall_test_enabled();
+  pb.gate = gate;
   attn_tc_kernel<D><<<G, THREADS, Lt::SMEM, stream>>>(tq, tkp, tvp, tkb, tvb, pb);
   if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   const long long warps = (long long)pairs * LB * GQ;
@@ -672,12 +676,12 @@ size_t attn_tc_workspace_bytes(int S, int NL, int Hkv, int d) {
 int attn_tc_forward(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 *Vp,
                     const int32_t *kv_off, int total_kv_rows, const __nv_bfloat16 *Kb,
                     const __nv_bfloat16 *Vb, int S, int NL, int LB, int Hq, int Hkv, int d,
-                    void *O, void *ws, int32_t *status, cudaStream_t stream) {
+                    void *O, void *ws, int32_t *status, Gate gate, cudaStream_t stream) {
   if (S > MAX_SEQ) return SPRINT_ERR_UNSUPPORTED;
   return d == 64 ? launch<64>(Q, Kp, Vp, kv_off, total_kv_rows, Kb, Vb, S, NL, LB, Hq, Hkv, O,
-                              ws, status, stream)
+                              ws, status, gate, stream)
                  : launch<128>(Q, Kp, Vp, kv_off, total_kv_rows, Kb, Vb, S, NL, LB, Hq, Hkv, O,
-                               ws, status, stream);
+                               ws, status, gate, stream);
 }
 
 }  // namespace sprint

@@ -130,6 +130,43 @@ __device__ __forceinline__ int csr_owner(const int32_t *off, int S, int row) {
   return lo;
 }
 
+// Step gate of the native block driver (sprint_decode_steps): the kernels
+// of a step after the first do nothing once every sequence finished at an
+// earlier step, i.e. when the previous step's still-masked counts
+// m_prev[0..S) are all zero.  m_prev == nullptr: always open.
+struct Gate {
+  const int32_t *m_prev;
+  int S;
+};
+
+// Block-uniform test; every thread of the block must call it, before any
+// other barrier of the kernel.
+__device__ __forceinline__ bool gate_closed(const Gate &g) {
+  if (!g.m_prev) return false;
+  __shared__ int closed_sh;
+  if (threadIdx.x == 0 && threadIdx.y == 0) {
+    int any = 0;
+    for (int s = 0; s < g.S; ++s) any |= __ldg(g.m_prev + s);
+    closed_sh = any == 0;
+  }
+  __syncthreads();
+  return closed_sh != 0;
+}
+
+// Entry points with a step gate, shared by the C ABI (gate open) and the
+// native block driver.
+int lmhead_confidence_impl(const void *h, const void *W, const float *temp, int M, int D, int V,
+                           int dtype, void *logits_out, float *conf_out, int32_t *argmax_out,
+                           void *ws, size_t ws_bytes, int32_t *status, Gate gate,
+                           cudaStream_t stream);
+int block_attn_impl(const void *Q, const void *Kp, const void *Vp, const int32_t *kv_off,
+                    int max_kv_rows, int total_kv_rows, const void *Kb, const void *Vb, int S,
+                    int NL, int LB, int Hq, int Hkv, int d, int dtype, void *O, void *ws,
+                    size_t ws_bytes, int32_t *status, Gate gate, cudaStream_t stream);
+int unmask_impl(const float *conf, const int32_t *argmax, uint8_t *mask, int32_t *tokens,
+                int32_t *m_out, int S, int LB, int t, int T, float tau, int mode,
+                uint8_t *accepted_out, int32_t *status, Gate gate, cudaStream_t stream);
+
 // Orderable unsigned key of a float: a > b  <=>  key(a) > key(b); -0 == +0.
 __device__ __forceinline__ uint32_t float_key(float f) {
   if (f == 0.0f) f = 0.0f;

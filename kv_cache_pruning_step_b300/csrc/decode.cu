@@ -1,0 +1,65 @@
+// Native block driver: all denoising steps of one block enqueued at once.
+//
+// LLaDA2.0-Uni paper (arXiv 2604.20796), Sparse Prefix Retention and
+// Non-uniform Token Unmasking paragraphs: a block of LB masked tokens is
+// decoded in at most T steps; step 0 attends to the full prefix, later steps
+// to the pruned one; each step unmasks at least ceil(m / (T - t)) positions.
+//
+// The host enqueues the T steps back to back; whether a step runs is decided
+// on the GPU from the previous step's still-masked counts (the step gate in
+// every kernel), so no step waits for a host round trip.
+#include "common.cuh"
+
+using namespace sprint;
+
+namespace {
+
+int record(void *const *events, int i, cudaStream_t stream) {
+  if (!events) return SPRINT_OK;
+  return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) == cudaSuccess
+             ? SPRINT_OK
+             : SPRINT_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int sprint_decode_steps(const sprint_steps_args *a, cudaStream_t stream) {
+  if (!a) return SPRINT_ERR_INVALID_ARG;
+  if (a->S < 1 || a->LB < 1 || a->T < 1) return SPRINT_ERR_INVALID_ARG;
+  if (!a->Q || !a->Kb || !a->Vb || !a->h || !a->mask || !a->tokens || !a->m_hist || !a->O ||
+      !a->conf || !a->argmax || !a->status || !a->W)
+    return SPRINT_ERR_INVALID_ARG;
+  for (int t = 0; t < a->T; ++t)
+    if (!a->Q[t] || !a->Kb[t] || !a->Vb[t] || !a->h[t]) return SPRINT_ERR_INVALID_ARG;
+  const int S = a->S, LB = a->LB, M = S * LB;
+  if (cudaMemsetAsync(a->mask, 1, (size_t)M, stream) != cudaSuccess ||
+      cudaMemsetAsync(a->tokens, 0xff, (size_t)M * sizeof(int32_t), stream) != cudaSuccess)
+    return SPRINT_ERR_CUDA;
+  for (int t = 0; t < a->T; ++t) {
+    const Gate gate = t == 0 ? Gate{nullptr, 0} : Gate{a->m_hist + (size_t)(t - 1) * S, S};
+    const bool full = t == 0;
+    int rc = record(a->events, 6 * t + 0, stream);
+    if (rc == SPRINT_OK)
+      rc = block_attn_impl(a->Q[t], full ? a->Kf : a->Kp, full ? a->Vf : a->Vp,
+                           full ? a->prefix_off : a->kept_off, full ? a->max_rows : a->max_kept,
+                           full ? a->total_rows : a->total_kept, a->Kb[t], a->Vb[t], S, a->NL,
+                           LB, a->Hq, a->Hkv, a->d, a->dtype, a->O, a->ws_attn,
+                           a->ws_attn_bytes, a->status, gate, stream);
+    if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 1, stream);
+    if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 2, stream);
+    if (rc == SPRINT_OK)
+      rc = lmhead_confidence_impl(a->h[t], a->W, a->theta ? a->theta[t] : nullptr, M, a->D,
+                                  a->vocab, a->dtype, a->logits, a->conf, a->argmax, a->ws_lm,
+                                  a->ws_lm_bytes, a->status, gate, stream);
+    if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 3, stream);
+    if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 4, stream);
+    if (rc == SPRINT_OK)
+      rc = unmask_impl(a->conf, a->argmax, a->mask, a->tokens, a->m_hist + (size_t)t * S, S, LB,
+                       t, a->T, a->tau, a->mode,
+                       a->accepted ? a->accepted + (size_t)t * M : nullptr, a->status, gate,
+                       stream);
+    if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 5, stream);
+    if (rc != SPRINT_OK) return rc;
+  }
+  return SPRINT_OK;
+}

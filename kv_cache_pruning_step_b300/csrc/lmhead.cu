@@ -28,7 +28,8 @@ lmhead_simt_kernel(const T *__restrict__ h, const T *__restrict__ W,
                    const float *__restrict__ temp, int M, int D, int V,
                    T *__restrict__ logits, float *__restrict__ pmax,
                    float *__restrict__ psum, int32_t *__restrict__ parg,
-                   int32_t *status) {
+                   int32_t *status, Gate gate) {
+  if (gate_closed(gate)) return;
   constexpr int BM = 64, BN = 64, BK = 16;
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
@@ -139,7 +140,9 @@ constexpr int kCombRows = 32, kCombGroups = 8;
 __global__ void __launch_bounds__(kCombRows * kCombGroups)
 lmhead_combine_kernel(const float *__restrict__ pmax, const float *__restrict__ psum,
                       const int32_t *__restrict__ parg, const float *__restrict__ temp, int M,
-                      int strips, float *__restrict__ conf, int32_t *__restrict__ argmax) {
+                      int strips, float *__restrict__ conf, int32_t *__restrict__ argmax,
+                      Gate gate) {
+  if (gate_closed(gate)) return;
   __shared__ Part sh[kCombGroups][kCombRows];
   const int x = threadIdx.x, y = threadIdx.y;
   const int row = blockIdx.x * kCombRows + x;
@@ -172,7 +175,8 @@ __global__ void __launch_bounds__(128)
 lmhead_combine_rows_kernel(const float *__restrict__ pmax, const float *__restrict__ psum,
                            const int32_t *__restrict__ parg, const float *__restrict__ temp,
                            int M, int strips, float *__restrict__ conf,
-                           int32_t *__restrict__ argmax) {
+                           int32_t *__restrict__ argmax, Gate gate) {
+  if (gate_closed(gate)) return;
   __shared__ Part sh[4];
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float th = temp ? temp[row] : 1.0f;
@@ -218,11 +222,10 @@ extern "C" size_t sprint_lmhead_workspace_bytes(int M, int D, int V, int dtype) 
   return 3 * align_up((size_t)strips * M * 4, 256);
 }
 
-extern "C" int sprint_lmhead_confidence(const void *h, const void *W, const float *temp,
-                                        int M, int D, int V, int dtype, void *logits_out,
-                                        float *conf_out, int32_t *argmax_out, void *ws,
-                                        size_t ws_bytes, int32_t *status,
-                                        cudaStream_t stream) {
+int sprint::lmhead_confidence_impl(const void *h, const void *W, const float *temp, int M,
+                                   int D, int V, int dtype, void *logits_out, float *conf_out,
+                                   int32_t *argmax_out, void *ws, size_t ws_bytes,
+                                   int32_t *status, Gate gate, cudaStream_t stream) {
   if (M < 0 || D < 1 || V < 1) return SPRINT_ERR_INVALID_ARG;
   if (dtype != SPRINT_F32 && dtype != SPRINT_BF16) return SPRINT_ERR_INVALID_ARG;
   if (M == 0) return SPRINT_OK;
@@ -233,21 +236,31 @@ extern "C" int sprint_lmhead_confidence(const void *h, const void *W, const floa
     if (D % 8 != 0 || !aligned16(h) || !aligned16(W)) return SPRINT_ERR_UNSUPPORTED;
     const int rc = lmhead_tc_tiles(static_cast<const __nv_bfloat16 *>(h),
                                    static_cast<const __nv_bfloat16 *>(W), temp, M, D, V,
-                                   static_cast<__nv_bfloat16 *>(logits_out), p, status, stream);
+                                   static_cast<__nv_bfloat16 *>(logits_out), p, status, gate,
+                                   stream);
     if (rc != SPRINT_OK) return rc;
   } else {
     dim3 grid(p.strips, (M + 63) / 64);
     lmhead_simt_kernel<float><<<grid, 256, 0, stream>>>(
         static_cast<const float *>(h), static_cast<const float *>(W), temp, M, D, V,
-        static_cast<float *>(logits_out), p.pmax, p.psum, p.parg, status);
+        static_cast<float *>(logits_out), p.pmax, p.psum, p.parg, status, gate);
     if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   }
   if (M < 4096)
     lmhead_combine_rows_kernel<<<M, 128, 0, stream>>>(p.pmax, p.psum, p.parg, temp, M, p.strips,
-                                                      conf_out, argmax_out);
+                                                      conf_out, argmax_out, gate);
   else
     lmhead_combine_kernel<<<(M + kCombRows - 1) / kCombRows, dim3(kCombRows, kCombGroups), 0,
                             stream>>>(p.pmax, p.psum, p.parg, temp, M, p.strips, conf_out,
-                                      argmax_out);
+                                      argmax_out, gate);
   return launch_status();
+}
+
+extern "C" int sprint_lmhead_confidence(const void *h, const void *W, const float *temp,
+                                        int M, int D, int V, int dtype, void *logits_out,
+                                        float *conf_out, int32_t *argmax_out, void *ws,
+                                        size_t ws_bytes, int32_t *status,
+                                        cudaStream_t stream) {
+  return lmhead_confidence_impl(h, W, temp, M, D, V, dtype, logits_out, conf_out, argmax_out, ws,
+                                ws_bytes, status, Gate{nullptr, 0}, stream);
 }

@@ -4,7 +4,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include "../../include/sprint.h"
+#include "common.cuh"
 
 namespace sprint {
 
@@ -34,6 +34,6 @@ LmheadWs lmhead_ws_layout(void *ws, int M, int V, int cols);
 // the temperature-scaled logits when `logits` is not null).
 int lmhead_tc_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *temp, int M,
                     int D, int V, __nv_bfloat16 *logits, const LmheadWs &p, int32_t *status,
-                    cudaStream_t stream);
+                    Gate gate, cudaStream_t stream);
 
 }  // namespace sprint

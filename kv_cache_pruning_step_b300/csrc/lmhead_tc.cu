@@ -66,7 +66,8 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
                  const float *__restrict__ temp, int M, int D, int V,
                  __nv_bfloat16 *__restrict__ logits, float *__restrict__ pmax,
                  float *__restrict__ psum, int32_t *__restrict__ parg, int32_t *status,
-                 unsigned long long cap_ns, int stall_test) {
+                 unsigned long long cap_ns, int stall_test, Gate gate) {
+  if (gate_closed(gate)) return;
   // The final waits for in-flight copies and MMAs ignore the abort flag and
   // get at least one second.
   const unsigned long long drain_ns = cap_ns > 1000000000ull ? cap_ns : 1000000000ull;
@@ -323,7 +324,7 @@ int sm_count() {
 
 template <int BN>
 int launch_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *temp, int M, int D,
-                 int V, __nv_bfloat16 *logits, const LmheadWs &p, int32_t *status,
+                 int V, __nv_bfloat16 *logits, const LmheadWs &p, int32_t *status, Gate gate,
                  cudaStream_t stream) {
   constexpr size_t SMEM_BYTES = Tiles<BN>::SMEM_BYTES;
   CUtensorMap tm_h, tm_w;
@@ -341,17 +342,17 @@ int launch_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *te
   const int grid = tiles < sm_count() ? tiles : sm_count();
   lmhead_tc_kernel<BN><<<grid, THREADS, SMEM_BYTES, stream>>>(
       tm_h, tm_w, temp, M, D, V, logits, p.pmax, p.psum, p.parg, status, wait_cap_ns(),
-      stall_test_enabled());
+      stall_test_enabled(), gate);
   return launch_status();
 }
 
 int lmhead_tc_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *temp, int M,
                     int D, int V, __nv_bfloat16 *logits, const LmheadWs &p, int32_t *status,
-                    cudaStream_t stream) {
+                    Gate gate, cudaStream_t stream) {
   if (p.cols == kPartColsNarrow)
-    return launch_tiles<kPartColsNarrow>(h, W, temp, M, D, V, logits, p, status, stream);
+    return launch_tiles<kPartColsNarrow>(h, W, temp, M, D, V, logits, p, status, gate, stream);
   if (p.cols == kPartCols)
-    return launch_tiles<kPartCols>(h, W, temp, M, D, V, logits, p, status, stream);
+    return launch_tiles<kPartCols>(h, W, temp, M, D, V, logits, p, status, gate, stream);
   return SPRINT_ERR_UNSUPPORTED;
 }
 

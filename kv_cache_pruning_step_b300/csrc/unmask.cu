@@ -18,7 +18,14 @@ __global__ void unmask_kernel(const float *__restrict__ conf,
                               const int32_t *__restrict__ argmax,
                               uint8_t *__restrict__ mask, int32_t *__restrict__ tokens,
                               int32_t *__restrict__ m_out, int LB, int t, int T,
-                              float tau, int mode, uint8_t *__restrict__ accepted_out) {
+                              float tau, int mode, uint8_t *__restrict__ accepted_out,
+                              Gate gate) {
+  if (gate_closed(gate)) {  // the block finished earlier: nothing left to unmask
+    const size_t at = (size_t)blockIdx.x * LB + threadIdx.x;
+    if (accepted_out && (int)threadIdx.x < LB) accepted_out[at] = 0;
+    if (threadIdx.x == 0) m_out[blockIdx.x] = 0;
+    return;
+  }
   __shared__ float c_sh[1024];
   __shared__ uint8_t m_sh[1024];
   const int s = blockIdx.x, j = threadIdx.x;
@@ -60,10 +67,10 @@ __global__ void unmask_kernel(const float *__restrict__ conf,
 
 using namespace sprint;
 
-extern "C" int sprint_unmask(const float *conf, const int32_t *argmax, uint8_t *mask,
-                             int32_t *tokens, int32_t *m_out, int S, int LB, int t, int T,
-                             float tau, int mode, uint8_t *accepted_out, int32_t *status,
-                             cudaStream_t stream) {
+int sprint::unmask_impl(const float *conf, const int32_t *argmax, uint8_t *mask, int32_t *tokens,
+                        int32_t *m_out, int S, int LB, int t, int T, float tau, int mode,
+                        uint8_t *accepted_out, int32_t *status, Gate gate,
+                        cudaStream_t stream) {
   (void)status;
   if (S < 0 || LB < 1 || LB > 1024 || T < 1 || t < 0) return SPRINT_ERR_INVALID_ARG;
   if (mode != SPRINT_UNMASK_ADAPTIVE && mode != SPRINT_UNMASK_FIXED)
@@ -72,6 +79,14 @@ extern "C" int sprint_unmask(const float *conf, const int32_t *argmax, uint8_t *
   if (!conf || !argmax || !mask || !tokens || !m_out) return SPRINT_ERR_INVALID_ARG;
   const int threads = (LB + 31) / 32 * 32;
   unmask_kernel<<<S, threads, 0, stream>>>(conf, argmax, mask, tokens, m_out, LB, t, T, tau,
-                                           mode, accepted_out);
+                                           mode, accepted_out, gate);
   return launch_status();
+}
+
+extern "C" int sprint_unmask(const float *conf, const int32_t *argmax, uint8_t *mask,
+                             int32_t *tokens, int32_t *m_out, int S, int LB, int t, int T,
+                             float tau, int mode, uint8_t *accepted_out, int32_t *status,
+                             cudaStream_t stream) {
+  return unmask_impl(conf, argmax, mask, tokens, m_out, S, LB, t, T, tau, mode, accepted_out,
+                     status, Gate{nullptr, 0}, stream);
 }

@@ -10,8 +10,12 @@ unmasks a confidence-adaptive number of them.
 
 The driver only sequences library calls and sizes buffers.  All buffers are
 allocated once per decoder, so a decode call launches kernels and nothing
-else; the only device-to-host traffic is the per-step read of the masked
-counts that decides whether the block is finished.
+else.  decode() enqueues the prefix pass and then all T steps through the
+library's native step driver (sprint_decode_steps): the GPU itself skips the
+steps after the block is finished, and the host reads the per-step masked
+counts once, after the block.  decode_stepwise() issues the five calls one
+step at a time and reads the masked counts after every step (used when a
+caller wants to look at each step's outputs).
 """
 from __future__ import annotations
 
@@ -98,10 +102,15 @@ class BlockDecoder:
         self.m_out = torch.empty(S, **i32)
         self.accepted = torch.empty((S, LB), dtype=torch.uint8, device=self.dev)
         self.m_host = torch.empty(S, dtype=torch.int32, pin_memory=True)
+        self.m_hist = torch.empty((T, S), **i32)
+        self.m_hist_host = torch.empty((T, S), dtype=torch.int32, pin_memory=True)
         self.ev = torch.cuda.Event()
-        # When a dict, every stage records (start, end) CUDA events under its
-        # name on the current stream (used by the benchmark).
+        # When a dict, every stage records (start, end) CUDA events on the
+        # current stream; after the block the durations (ms) are appended to
+        # timing[stage] (used by the benchmark).
         self.timing = None
+        self._pending = []
+        self._step_events = None
 
     @contextlib.contextmanager
     def _stage(self, name):
@@ -113,7 +122,23 @@ class BlockDecoder:
         a.record()
         yield
         b.record()
-        self.timing.setdefault(name, []).append((a, b))
+        self._pending.append((name, a, b))
+
+    def _flush_timing(self):
+        """Durations of the stages recorded so far (their events are done)."""
+        if self.timing is not None:
+            for name, a, b in self._pending:
+                self.timing.setdefault(name, []).append(a.elapsed_time(b))
+        self._pending = []
+
+    def _events_for_steps(self):
+        """6 * T timing events for the native step driver, created once; each
+        is recorded once here so that its CUDA event exists."""
+        if self._step_events is None:
+            self._step_events = [torch.cuda.Event(enable_timing=True) for _ in range(6 * self.T)]
+            for e in self._step_events:
+                e.record()
+        return self._step_events
 
     # -- the individual stages (each is one or two library calls) --------
     def prefix_pass(self, K, V, H, theta, modality):
@@ -163,7 +188,46 @@ class BlockDecoder:
 
     def decode(self, prefix, steps, on_step=None) -> BlockResult:
         """Decode one block.  prefix: dict K, V, H, theta, modality (device,
-        sequences concatenated).  steps(t) -> dict Q, Kb, Vb, h, theta."""
+        sequences concatenated).  steps(t) -> dict Q, Kb, Vb, h, theta.
+        With on_step (called after each step with (t, self)) the block is
+        decoded step by step (decode_stepwise)."""
+        if on_step is not None:
+            return self.decode_stepwise(prefix, steps, on_step)
+        self.prefix_pass(prefix["K"], prefix["V"], prefix["H"], prefix["theta"],
+                         prefix["modality"])
+        xs = [steps(t) for t in range(self.T)]
+        events = self._events_for_steps() if self.timing is not None else None
+        sp.sprint_decode_steps(
+            Q=[x["Q"] for x in xs], Kb=[x["Kb"] for x in xs], Vb=[x["Vb"] for x in xs],
+            h=[x["h"] for x in xs], theta=[x.get("theta") for x in xs],
+            Kf=prefix["K"], Vf=prefix["V"], prefix_off=self.prefix_off,
+            max_rows=self.max_rows, total_rows=self.total_rows, Kp=self.Kp, Vp=self.Vp,
+            kept_off=self.kept_off, max_kept=self.max_kept, total_kept=self.total_kept,
+            W=self.W, T=self.T, tau=self.tau, mode=self.mode, O=self.O, conf=self.conf_blk,
+            argmax=self.argmax_blk, mask=self.mask, tokens=self.tokens, m_hist=self.m_hist,
+            ws_attn=self.ws_attn, ws_lm=self.ws_lm_blk, status=self.status,
+            logits=self.logits, events=events)
+        self.m_hist_host.copy_(self.m_hist, non_blocking=True)
+        self.ev.record()
+        self.ev.synchronize()
+        hist = self.m_hist_host.tolist()
+        accepted, prev, n_steps = [], [self.LB] * self.S, 0
+        for t in range(self.T):
+            if t > 0 and not any(hist[t - 1]):
+                break
+            n_steps += 1
+            accepted.append([p - q for p, q in zip(prev, hist[t])])
+            prev = hist[t]
+            if events is not None:
+                for k, name in enumerate(("attn_full" if t == 0 else "attn_pruned",
+                                          "lmhead_block", "unmask")):
+                    self._pending.append((name, events[6 * t + 2 * k], events[6 * t + 2 * k + 1]))
+        self._flush_timing()
+        return BlockResult(n_steps, self.tokens, accepted)
+
+    def decode_stepwise(self, prefix, steps, on_step=None) -> BlockResult:
+        """Decode one block one step at a time, reading the masked counts
+        after every step (on_step(t, self) is called after each step)."""
         self.mask.fill_(1)
         self.tokens.fill_(-1)
         self.prefix_pass(prefix["K"], prefix["V"], prefix["H"], prefix["theta"],
@@ -185,4 +249,5 @@ class BlockDecoder:
             prev = left
             if not any(left):
                 break
+        self._flush_timing()
         return BlockResult(n_steps, self.tokens, accepted)

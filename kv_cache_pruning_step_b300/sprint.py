@@ -45,7 +45,26 @@ SIGNATURES = {
     "sprint_block_attn": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
                                _P, _Z, _P, _P]),
     "sprint_unmask": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
+    "sprint_decode_steps": (_I, [_P, _P]),
 }
+
+
+class StepsArgs(ctypes.Structure):
+    """Mirror of sprint_steps_args (include/sprint.h)."""
+    _fields_ = [(n, ctypes.c_int) for n in ("S", "NL", "LB", "Hq", "Hkv", "d", "D", "vocab",
+                                            "dtype", "T")] + [
+        ("tau", ctypes.c_float), ("mode", ctypes.c_int),
+        ("Kf", _P), ("Vf", _P), ("prefix_off", _P), ("max_rows", ctypes.c_int),
+        ("total_rows", ctypes.c_int),
+        ("Kp", _P), ("Vp", _P), ("kept_off", _P), ("max_kept", ctypes.c_int),
+        ("total_kept", ctypes.c_int),
+        ("W", _P), ("Q", _P), ("Kb", _P), ("Vb", _P), ("h", _P), ("theta", _P),
+        ("O", _P), ("logits", _P), ("conf", _P), ("argmax", _P), ("mask", _P),
+        ("tokens", _P), ("m_hist", _P), ("accepted", _P),
+        ("ws_attn", _P), ("ws_attn_bytes", ctypes.c_size_t),
+        ("ws_lm", _P), ("ws_lm_bytes", ctypes.c_size_t),
+        ("status", _P), ("events", _P),
+    ]
 
 
 class SprintError(RuntimeError):
@@ -265,3 +284,54 @@ def sprint_unmask(conf, argmax, mask, tokens, t, T, tau, mode=UNMASK_ADAPTIVE, *
         _stream(stream))
     _check(rc, "sprint_unmask")
     return m_out, accepted
+
+
+def _ptr_array(tensors, dtype, name):
+    arr = (ctypes.c_void_p * len(tensors))()
+    for i, t in enumerate(tensors):
+        arr[i] = _ptr(t, dtype, f"{name}[{i}]") if t is not None else None
+    return arr
+
+
+def sprint_decode_steps(*, Q, Kb, Vb, h, theta, Kf, Vf, prefix_off, max_rows, total_rows,
+                        Kp, Vp, kept_off, max_kept, total_kept, W, T, tau, mode, O, conf,
+                        argmax, mask, tokens, m_hist, ws_attn, ws_lm, status, accepted=None,
+                        logits=None, events=None, stream=None):
+    """Every denoising step of one block in one call (see include/sprint.h).
+
+    Q, Kb, Vb: lists of T tensors [S][NL][LB][*][d]; h: list of T [S*LB][D];
+    theta: list of T [S*LB] fp32 or None.  m_hist: int32 [T][S] (out);
+    events: list of 6*T torch.cuda.Event or None."""
+    S, NL, LB, Hq, d = Q[0].shape
+    Hkv = Kb[0].shape[3]
+    dt = _dtype_code(Q[0])
+    a = StepsArgs()
+    a.S, a.NL, a.LB, a.Hq, a.Hkv, a.d = S, NL, LB, Hq, Hkv, d
+    a.D, a.vocab, a.dtype, a.T = W.shape[1], W.shape[0], dt, int(T)
+    a.tau, a.mode = float(tau), int(mode)
+    a.Kf, a.Vf = _ptr(Kf, Q[0].dtype, "Kf"), _ptr(Vf, Q[0].dtype, "Vf")
+    a.prefix_off = _ptr(prefix_off, torch.int32, "prefix_off")
+    a.max_rows, a.total_rows = int(max_rows), int(total_rows)
+    a.Kp, a.Vp = _ptr(Kp, Q[0].dtype, "Kp"), _ptr(Vp, Q[0].dtype, "Vp")
+    a.kept_off = _ptr(kept_off, torch.int32, "kept_off")
+    a.max_kept, a.total_kept = int(max_kept), int(total_kept)
+    a.W = _ptr(W, Q[0].dtype, "W")
+    keep = [_ptr_array(Q, Q[0].dtype, "Q"), _ptr_array(Kb, Q[0].dtype, "Kb"),
+            _ptr_array(Vb, Q[0].dtype, "Vb"), _ptr_array(h, Q[0].dtype, "h"),
+            _ptr_array(theta if theta is not None else [None] * T, torch.float32, "theta")]
+    a.Q, a.Kb, a.Vb, a.h, a.theta = [ctypes.cast(x, ctypes.c_void_p) for x in keep]
+    a.O, a.logits = _ptr(O, Q[0].dtype, "O"), _ptr(logits, Q[0].dtype, "logits")
+    a.conf, a.argmax = _ptr(conf, torch.float32, "conf"), _ptr(argmax, torch.int32, "argmax")
+    a.mask, a.tokens = _ptr(mask, torch.uint8, "mask"), _ptr(tokens, torch.int32, "tokens")
+    a.m_hist = _ptr(m_hist, torch.int32, "m_hist")
+    a.accepted = _ptr(accepted, torch.uint8, "accepted")
+    a.ws_attn, a.ws_attn_bytes = _ptr(ws_attn), ws_attn.numel()
+    a.ws_lm, a.ws_lm_bytes = _ptr(ws_lm), ws_lm.numel()
+    a.status = _ptr(status, torch.int32, "status")
+    ev = None
+    if events is not None:
+        ev = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        a.events = ctypes.cast(ev, ctypes.c_void_p)
+    rc = lib.sprint_decode_steps(ctypes.byref(a), _stream(stream))
+    _check(rc, "sprint_decode_steps")
+    del keep, ev

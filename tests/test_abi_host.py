@@ -93,3 +93,25 @@ def test_workspace_queries(sp):
     assert sp.sprint_score_prune_workspace_bytes(1, 32768) >= 8 * 32768
     assert sp.sprint_block_attn_workspace_bytes(1, 8, 32, 16, 4, 128, 32768, 1) > 0
     assert sp.sprint_block_attn_workspace_bytes(1, 8, 32, 16, 3, 128, 32768, 1) == 0
+
+
+def test_steps_args_struct_matches_header(sp, tmp_path):
+    """The ctypes mirror of sprint_steps_args has the C layout (field
+    offsets and size compiled from include/sprint.h with the host compiler)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no host C compiler")
+    names = [f[0] for f in sp.StepsArgs._fields_]
+    src = ["#include <stdio.h>", "#include <stddef.h>", '#include "sprint.h"', "int main(void){"]
+    src += [f'printf("%zu\\n", offsetof(sprint_steps_args, {n}));' for n in names]
+    src += ['printf("%zu\\n", sizeof(sprint_steps_args)); return 0;}']
+    c = tmp_path / "off.c"
+    c.write_text("\n".join(src))
+    exe = tmp_path / "off"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", "/usr/local/cuda/include",
+                    str(c), "-o", str(exe)], check=True)
+    out = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    assert out[:-1] == [getattr(sp.StepsArgs, n).offset for n in names]
+    assert out[-1] == ctypes.sizeof(sp.StepsArgs)

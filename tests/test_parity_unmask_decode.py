@@ -108,3 +108,60 @@ def test_tiny_block_end_to_end(sp):
             assert near.any(), f"step {t}: unmask decisions differ"
             return
     assert res.tokens[0].cpu().numpy().tolist() == ref["tokens"].tolist()
+
+
+def _decoder_and_steps(name, tau=None, mode=0):
+    from kv_cache_pruning_step_b300 import BlockDecoder
+    w = WORKLOADS[name]
+    W = lm_head_weight(w, device=DEV)
+    pre = prefix_inputs(w, device=DEV)
+    mod = pre["modality"].cpu().numpy()
+    counts = [(int((mod == 0).sum()), int((mod == 1).sum()))]
+    steps = []
+    for t in range(w.T):
+        x = step_inputs(w, 0, 0, t, device=DEV)
+        steps.append({"Q": x["Q"][None].contiguous(), "Kb": x["Kb"][None].contiguous(),
+                      "Vb": x["Vb"][None].contiguous(), "h": x["h"], "theta": x["theta"]})
+
+    def make():
+        return BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T,
+                            tau=w.tau if tau is None else tau, r_text=w.r_text, r_img=w.r_img,
+                            alpha=w.alpha, mode=mode, modality_counts=counts)
+    return w, pre, steps, make
+
+
+@pytest.mark.parametrize("name,mode", [("tiny-256", 0), ("tiny-256", 1), ("prefix-4k", 0)])
+def test_native_step_driver_matches_stepwise(sp, name, mode):
+    """sprint_decode_steps (all steps enqueued at once, gated on the device)
+    gives the same trajectory as issuing the five calls step by step."""
+    w, pre, steps, make = _decoder_and_steps(name, mode=mode)
+    a, b = make(), make()
+    a.timing, b.timing = {}, {}  # stage events recorded on both paths
+    ra = a.decode(pre, lambda t: steps[t])
+    rb = b.decode_stepwise(pre, lambda t: steps[t])
+    torch.cuda.synchronize()
+    for tm, n in ((a.timing, ra.steps), (b.timing, rb.steps)):
+        assert len(tm["lmhead_block"]) == n and len(tm["unmask"]) == n
+        assert len(tm["lmhead_prefix"]) == 1 and all(v > 0 for v in tm["lmhead_block"])
+    assert a.status.item() == 0 and b.status.item() == 0
+    assert ra.steps == rb.steps
+    assert ra.accepted_per_step == rb.accepted_per_step
+    assert torch.equal(ra.tokens, rb.tokens)
+    assert torch.equal(a.O, b.O)
+    assert torch.equal(a.conf_blk, b.conf_blk)
+
+
+def test_native_step_driver_skips_steps_after_the_block_is_done(sp):
+    """tau below every confidence: step 0 accepts all LB positions, and the
+    kernels of steps 1..T-1 return without touching any output."""
+    w, pre, steps, make = _decoder_and_steps("tiny-256", tau=-1.0)
+    a, b = make(), make()
+    ra = a.decode(pre, lambda t: steps[t])
+    rb = b.decode_stepwise(pre, lambda t: steps[t])
+    torch.cuda.synchronize()
+    assert ra.steps == rb.steps == 1
+    assert ra.accepted_per_step == [[w.LB]]
+    assert torch.equal(ra.tokens, rb.tokens)
+    assert a.m_hist.cpu().tolist() == [[0]] * w.T
+    # outputs still hold step 0's values: steps 1..T-1 did not run
+    assert torch.equal(a.O, b.O) and torch.equal(a.conf_blk, b.conf_blk)
