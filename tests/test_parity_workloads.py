@@ -1,0 +1,141 @@
+"""Whole-block decodes of the batched and the sequential workloads, checked
+stage by stage against the oracle.
+
+* batch-16x8k: 16 independent sequences of 8192 prefix positions with ragged
+  image fractions, decoded together at unmask thresholds 0.7, 0.9 and 0.95;
+* sequential-64-blocks: blocks 0 and 63 of a 64-block decode whose prefix
+  grows from 2048 to 4064 positions (1024 image, then text).
+
+Stage-wise: each stage is compared with the oracle given the GPU's own
+inputs to that stage (prefix confidences on sampled rows; kept set from the
+GPU's confidences; attention over the GPU's kept set; unmask decisions from
+the GPU's block confidences), so errors do not compound.  The native step
+driver and the call-per-step path must give the same tokens.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import sprint_oracle as orc
+from tests import gpu_cases as gc
+from workload import WORKLOADS, lm_head_weight, prefix_inputs, step_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def sp():
+    from kv_cache_pruning_step_b300 import sprint
+    return sprint
+
+
+_WEIGHTS = {}
+
+
+def weights_of(name):
+    """The workload's LM-head weight on the device and as an exact fp64 host
+    copy for the oracle (made once per workload)."""
+    if name not in _WEIGHTS:
+        _WEIGHTS.clear()
+        W = lm_head_weight(WORKLOADS[name], device=DEV)
+        _WEIGHTS[name] = (W, gc.host(W).astype(np.float64))
+    return _WEIGHTS[name]
+
+
+def _decode_and_check(sp, w, weights, prefixes, step_sets, check_seqs, tau):
+    W, W64 = weights
+    from kv_cache_pruning_step_b300 import BlockDecoder
+    S = len(prefixes)
+    cat = gc.concat_prefixes(prefixes)
+    counts = [(int((p["modality"] == 0).sum()), int((p["modality"] != 0).sum()))
+              for p in prefixes]
+    steps = []
+    for t in range(w.T):
+        xs = [step_sets[s][t] for s in range(S)]
+        steps.append({k: (torch.stack([x[k] for x in xs]) if k in ("Q", "Kb", "Vb")
+                          else torch.cat([x[k] for x in xs])).contiguous()
+                      for k in ("Q", "Kb", "Vb", "h", "theta")})
+
+    def make():
+        return BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=tau,
+                            r_text=w.r_text, r_img=w.r_img, alpha=w.alpha,
+                            modality_counts=counts)
+
+    native = make()
+    r_native = native.decode(cat, lambda t: steps[t])
+    seen = []
+
+    def on_step(t, d):
+        seen.append({"O": d.O.float().cpu(), "conf": d.conf_blk.cpu().numpy(),
+                     "argmax": d.argmax_blk.cpu().numpy(), "acc": d.accepted.cpu().numpy()})
+
+    dec = make()
+    res = dec.decode(cat, lambda t: steps[t], on_step=on_step)
+    torch.cuda.synchronize()
+    assert native.status.item() == 0 and dec.status.item() == 0
+    assert torch.equal(r_native.tokens, res.tokens) and r_native.steps == res.steps
+
+    conf_prefix = dec.conf_prefix.cpu().numpy()
+    kept = dec.kept_idx.cpu().numpy()
+    off, koff = dec.prefix_off_host, dec.kept_off_host
+    rng = np.random.default_rng(5)
+    for s in check_seqs:
+        p = prefixes[s]
+        n = off[s + 1] - off[s]
+        mod = p["modality"].cpu().numpy()
+        # (a) prefix confidences on sampled rows
+        rows = np.sort(rng.choice(n, size=min(24, n), replace=False))
+        gc.check_confidence(conf_prefix[off[s]:off[s + 1]][rows],
+                            dec.argmax_prefix.cpu().numpy()[off[s]:off[s + 1]][rows],
+                            p["H"], W64, p["theta"], rows, f"seq {s} prefix")
+        # (b) kept set from the GPU's confidences
+        score_o = orc.composite_score(orc.key_norm_importance(p["K"]),
+                                      conf_prefix[off[s]:off[s + 1]], w.alpha)
+        kept_s = kept[koff[s]:koff[s + 1]]
+        gc.check_kept(kept_s, score_o, mod, w.r_text, w.r_img, f"seq {s}")
+        # (c) attention of step 1 over the GPU's kept set, first and last layer
+        if len(seen) > 1:
+            x = step_sets[s][1]
+            want = orc.block_attention(x["Q"], orc.compact(p["K"], kept_s),
+                                       orc.compact(p["V"], kept_s), x["Kb"], x["Vb"],
+                                       layers=[0, w.NL - 1])
+            for layer in (0, w.NL - 1):
+                gc.assert_close(seen[1]["O"][s, layer].numpy(), want[layer], w.torch_dtype,
+                                f"seq {s} step 1 layer {layer}")
+        # (d) block confidences of step 0, (e) every unmask decision
+        rs = slice(s * w.LB, (s + 1) * w.LB)
+        x0 = step_sets[s][0]
+        gc.check_confidence(seen[0]["conf"][rs], seen[0]["argmax"][rs], x0["h"], W64,
+                            x0["theta"], np.arange(w.LB), f"seq {s} step 0")
+        mask = np.ones(w.LB, bool)
+        tokens = np.full(w.LB, -1)
+        for t, g in enumerate(seen):
+            mask, tokens, acc = orc.unmask_step(g["conf"][rs], g["argmax"][rs], mask, tokens,
+                                                t, w.T, tau)
+            assert g["acc"][s].astype(bool).tolist() == acc.tolist(), f"seq {s} step {t}"
+        assert res.tokens[s].cpu().numpy().tolist() == tokens.tolist()
+        assert not mask.any()  # every block ends within T steps
+    return res
+
+
+@pytest.mark.parametrize("tau", [0.7, 0.9, 0.95])
+def test_batch_16x8k_threshold_sweep(sp, tau):
+    w = WORKLOADS["batch-16x8k"]
+    prefixes = [prefix_inputs(w, seq=s, device=DEV) for s in range(w.S)]
+    step_sets = [[step_inputs(w, s, 0, t, device=DEV) for t in range(w.T)] for s in range(w.S)]
+    res = _decode_and_check(sp, w, weights_of(w.name), prefixes, step_sets, check_seqs=[0, 11],
+                            tau=tau)
+    assert res.steps <= w.T
+
+
+@pytest.mark.parametrize("block", [0, 63])
+def test_sequential_blocks(sp, block):
+    w = WORKLOADS["sequential-64-blocks"]
+    pre = prefix_inputs(w, seq=0, block=block, device=DEV)
+    assert pre["modality"].numel() == 2048 + 32 * block
+    # the cache grows by appending: block b's prefix starts with block 0's
+    first = prefix_inputs(w, seq=0, block=0, device=DEV)
+    assert torch.equal(pre["K"][:, :2048], first["K"])
+    step_sets = [[step_inputs(w, 0, block, t, device=DEV) for t in range(w.T)]]
+    _decode_and_check(sp, w, weights_of(w.name), [pre], step_sets, check_seqs=[0], tau=w.tau)
