@@ -8,10 +8,12 @@
 
 namespace sprint {
 
-// Vocabulary columns folded into one (max, sum-exp, argmax) partial per row:
-// 256 by default; 224 for bf16 calls with few rows (block steps), where the
-// column tiles are the whole grid's work and 702 tiles of 224 divide over
-// 148 SMs better than 614 tiles of 256.
+// Vocabulary columns folded into one (max, sum-exp, argmax) partial per row
+// (the tensor-core tile width in bf16): 256 by default; 224 for bf16 calls
+// with few rows (block steps), where the column tiles are the whole grid's
+// work, 702 tiles of 224 spread over 148 SMs more evenly than 614 of 256,
+// and a 44 KB stage leaves room for a 5-deep TMA ring.  (For many rows the
+// 256-wide MMA is the faster one.)
 constexpr int kPartCols = 256;
 constexpr int kPartColsNarrow = 224;
 constexpr int kNarrowMaxRows = 4096;

@@ -9,10 +9,11 @@
 //
 // Design (one persistent CTA per SM, 192 threads, 1 CTA/SM):
 //   warp 0      TMA producer: 128x64 tiles of h and BNx64 tiles of W (bf16,
-//               128-byte swizzle) into a 4-stage shared-memory ring; BN =
-//               256, or 224 when the call has few rows (the column tiles are
+//               128-byte swizzle) into a shared-memory ring of as many
+//               stages as fit in 227 KB; BN = 256 (4 stages), or 224 (5
+//               stages) when the call has few rows: the column tiles are
 //               then all the work, and 702 of them spread over 148 SMs more
-//               evenly than 614);
+//               evenly than 614;
 //   warp 1      allocates 512 TMEM columns; one lane issues
 //               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16) into
 //               one of two fp32 accumulators (TMEM columns 0 and 256);
@@ -35,7 +36,7 @@
 namespace sprint {
 namespace {
 
-constexpr int BM = 128, BK = 64, STAGES = 4, BAND = 32;
+constexpr int BM = 128, BK = 64, BAND = 32;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = 256;  // TMEM columns between the two accumulators
@@ -46,6 +47,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 template <int BN> struct Tiles {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  // As many stages as fit in 227 KB: 5 of 44 KB at BN = 224, 4 of 48 KB at 256.
+  static constexpr int STAGES = (227 * 1024 - 1024 - 256) / STAGE_BYTES;
   static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
   static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
   static_assert(BN % 32 == 0 && BN <= 256, "epilogue reads 32 columns at a time");
@@ -72,6 +75,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
   // get at least one second.
   const unsigned long long drain_ns = cap_ns > 1000000000ull ? cap_ns : 1000000000ull;
   constexpr int STAGE_BYTES = Tiles<BN>::STAGE_BYTES;
+  constexpr int STAGES = Tiles<BN>::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
