@@ -5,8 +5,8 @@
 // to the pruned prefix; attention inside the block is bidirectional.
 //
 // Work decomposition (stream-K).  For sequence s the keys of one (layer l,
-// KV head g) pair are ceil(k_s / 64) prefix tiles of 64 keys plus
-// ceil(LB / 64) tiles of the block's own keys.  All tiles of all pairs form
+// KV head g) pair are ceil(k_s / 128) prefix tiles of 128 keys plus
+// ceil(LB / 128) tiles of the block's own keys.  All tiles of all pairs form
 // one ordered list of T tiles; CTA c (of G = #SMs, one per SM) takes tiles
 // [c T / G, (c+1) T / G).  A CTA's range splits into segments at pair
 // boundaries; each segment writes two unnormalised partials (O rows, row
@@ -16,26 +16,29 @@
 // attn_tc_combine_kernel enumerates the segments of every pair the same way
 // and merges them in tile order.
 //
-// Per segment (320 threads):
+// Per segment (352 threads):
 //   warp 0      TMA: the pair's 128 query rows (LB block positions x G heads of
 //               the group, one 3-D box per 64 head-dim columns), then K and V
-//               tiles (64 keys x d) into a 4-stage ring (128-byte swizzle);
-//   warp 1      owns 512 TMEM columns: two S buffers (64 columns each) and two
-//               O accumulators (d each); one lane issues S = Q K^T (M=128,
-//               N=64) for tile q into S[q & 1] and O[q & 1] += P V (M=128,
-//               N=d, K=64, V read MN-major), QK of tile q+1 ahead of PV of q;
+//               tiles (128 keys x d) into a ring of as many 64 KB stages as
+//               fit (3 for a few sequences; 128-byte swizzle);
+//   warp 1      owns 512 TMEM columns: two S buffers (128 columns each) and
+//               two O accumulators (d each); one lane issues S = Q K^T
+//               (M=128, N=128) for tile q into S[q & 1] once the PV of tile
+//               q-2 (whose P lives there) is done;
+//   warp 10     one lane issues O[q & 1] += P V (M=128, N=d, K=128, P read
+//               from tensor memory as the A operand, V MN-major from shared
+//               memory); with one thread issuing both products the issue
+//               rate, not HBM, bounded the kernel;
 //   warps 2-9   softmax in two warpgroups that take alternate tiles:
 //               warpgroup h owns the tiles q with q & 1 == h, with its own S
-//               buffer, P buffer and O accumulator, and runs its own online
-//               softmax (row max m_h, row sum l_h), one query row per thread.
-//               S is read from TMEM once into registers; the reference max
-//               moves only when the tile max exceeds it by more than 2^8 (O_h
-//               is then rescaled in TMEM); P = exp2(S * log2e/sqrt(d) - m_h)
-//               goes as bf16 into the warpgroup's swizzled P buffer, the A
-//               operand of the PV MMA.  Writing P of tile q waits only for
-//               the PV of tile q-2, so the other warpgroup's tile hides the
-//               PV latency.  At the end of the segment each warpgroup writes
-//               its (O_h, m_h, l_h) partial.
+//               buffer and O accumulator, and runs its own online softmax
+//               (row max m_h, row sum l_h), one query row per thread.  A
+//               first pass over S in TMEM finds the tile max; the reference
+//               max moves only when the tile max exceeds it by more than 2^8
+//               (O_h is then rescaled in TMEM); a second pass writes P =
+//               exp2(S * log2e/sqrt(d) - m_h) as bf16 pairs over the first 64
+//               columns of S_h, where the PV product reads it.  At the end of
+//               the segment each warpgroup writes its (O_h, m_h, l_h) partial.
 #include <cuda.h>
 #include <math.h>
 
@@ -53,10 +56,10 @@ int sm_count();
 
 namespace {
 
-constexpr int TILE = 64;        // keys per tile
-constexpr int STAGES = 4;       // K/V ring depth
+constexpr int TILE = 128;       // keys per tile
+constexpr int MAX_STAGES = 4;   // K/V ring depth at most (as many as fit)
 constexpr int ROWS = 128;       // query rows per MMA tile (LB x G <= 128)
-constexpr int THREADS = 320;
+constexpr int THREADS = 352;
 constexpr int MAX_SEQ = 1024;   // sequences per call on this path
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
@@ -68,18 +71,20 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 
 template <int D> struct Layout {
   static constexpr int QBOX = ROWS * 128;          // 128 query rows x 64 cols
-  static constexpr int KBOX = TILE * 128;          // 64 keys x 64 cols
+  static constexpr int KBOX = TILE * 128;          // 128 keys x 64 cols
   static constexpr int Q_BYTES = (D / 64) * QBOX;
-  static constexpr int K_BYTES = (D / 64) * KBOX;  // 64 keys x d
+  static constexpr int K_BYTES = (D / 64) * KBOX;  // 128 keys x d
   static constexpr int STAGE = 2 * K_BYTES;        // K then V
-  static constexpr int P_BUF = ROWS * 128;         // 128 rows x 64 keys bf16
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = Q_BYTES;
-  static constexpr int OFF_P = OFF_KV + STAGES * STAGE;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BUF;
-  static constexpr int OFF_SEQ = OFF_BAR + 256;
-  static constexpr size_t SMEM = 1024 + OFF_SEQ + 4 * (MAX_SEQ + 1) * 4;
-  static constexpr uint32_t TMEM_O = 2 * TILE;     // S[0], S[1] at 0, 64; O_0, O_1 after
+  // Dynamic shared memory of a launch with `stages` ring stages and S
+  // sequences: [Q][stages x (K, V)][barriers 256 B][4 x (S+1) int tables].
+  static size_t smem_bytes(int stages, int S) {
+    return 1024 + (size_t)OFF_KV + (size_t)stages * STAGE + 256 + 16 * (size_t)(S + 1);
+  }
+  // TMEM columns: S[0], S[1] at 0 and 128 (P[h] overwrites the first 64
+  // columns of S[h] as bf16 pairs), O[0], O[1] after them.
+  static constexpr uint32_t TMEM_O = 2 * TILE;
 };
 
 struct Problem {
@@ -91,6 +96,7 @@ struct Problem {
   unsigned long long drain_ns;  // limit of the final waits for in-flight work
   int stall_test;               // failure-path test: the MMA role stalls first
   Gate gate;                    // step gate of the native block driver
+  int stages;                   // K/V ring stages of this launch (2..MAX_STAGES)
 };
 
 // Per-sequence tables: ts[s] = first global tile of sequence s; nt[s] =
@@ -157,12 +163,6 @@ __device__ __forceinline__ Seg locate(const Problem &pb, const int *ts, const in
   return sg;
 }
 
-// Swizzled (128-byte) address of 16-byte chunk `c` (0..7 over 64 keys) of
-// row r in a P buffer (128 rows x 128 bytes).
-__device__ __forceinline__ uint32_t p_chunk_addr(uint32_t buf, int r, int c) {
-  return buf + r * 128 + ((c ^ (r & 7)) << 4);
-}
-
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
@@ -178,16 +178,38 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return r;
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
       "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
       "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
-      "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
-      "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
-      "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
-      "f"(v[29]), "f"(v[30]), "f"(v[31])
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16: A (bf16 pairs packed in
+// 32-bit columns, one row per lane) read from tensor memory.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -202,48 +224,47 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+  const int stages = pb.stages;
+  const int off_bar = L::OFF_KV + stages * L::STAGE;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + off_bar);
   uint64_t *q_full = bar;                        // 1
-  uint64_t *k_full = bar + 1;                    // STAGES
-  uint64_t *v_full = k_full + STAGES;            // STAGES
-  uint64_t *kv_empty = v_full + STAGES;          // STAGES
-  uint64_t *s_full = kv_empty + STAGES;          // 2
-  uint64_t *s_free = s_full + 2;                 // 2
-  uint64_t *p_ready = s_free + 2;                // 2
+  uint64_t *kv_full = bar + 1;                   // MAX_STAGES
+  uint64_t *kv_empty = kv_full + MAX_STAGES;     // MAX_STAGES
+  uint64_t *s_full = kv_empty + MAX_STAGES;      // 2
+  uint64_t *p_ready = s_full + 2;                // 2
   uint64_t *pv_done = p_ready + 2;               // 2
-  uint64_t *o_full = pv_done + 2, *drain = o_full + 1;
-  uint64_t *never = drain + 1;  // no one arrives: the stall test waits on it
+  uint64_t *o_full = pv_done + 2, *drain = o_full + 1;  // drain[2]: one per issuer
+  uint64_t *never = drain + 2;  // no one arrives: the stall test waits on it
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(never + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  int *ts = reinterpret_cast<int *>(smem + L::OFF_SEQ);
-  int *nt = ts + (MAX_SEQ + 1), *ks = nt + (MAX_SEQ + 1), *k0 = ks + (MAX_SEQ + 1);
+  int *ts = reinterpret_cast<int *>(smem + off_bar + 256);
+  int *nt = ts + (pb.S + 1), *ks = nt + (pb.S + 1), *k0 = ks + (pb.S + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
   const int GQ = pb.Hq / pb.Hkv, R = pb.LB * GQ;
   const int BR = pb.LB < TILE ? pb.LB : TILE;  // rows of a block-key box
 
-  // Zero every operand buffer once: rows TMA never writes (query rows >= R,
-  // key rows past a short tile) then hold finite values.
-  for (int i = threadIdx.x * 16; i < L::OFF_BAR; i += THREADS * 16)
+  // Zero the query and K/V buffers once: rows TMA never writes (query rows
+  // >= R, key rows past a short tile) then hold finite values.
+  for (int i = threadIdx.x * 16; i < off_bar; i += THREADS * 16)
     *reinterpret_cast<uint4 *>(smem + i) = make_uint4(0, 0, 0, 0);
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   build_seq_tables(pb, ts, nt, ks, k0, pb.status);
   if (threadIdx.x == 0) {
     tc::mbar_init(tc::smem_u32(q_full), 1);
-    for (int i = 0; i < STAGES; ++i) {
-      tc::mbar_init(tc::smem_u32(k_full + i), 1);
-      tc::mbar_init(tc::smem_u32(v_full + i), 1);
+    for (int i = 0; i < MAX_STAGES; ++i) {
+      tc::mbar_init(tc::smem_u32(kv_full + i), 1);
       tc::mbar_init(tc::smem_u32(kv_empty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(tc::smem_u32(s_full + i), 1);
-      tc::mbar_init(tc::smem_u32(s_free + i), 4);   // the 4 warps of warpgroup i
-      tc::mbar_init(tc::smem_u32(p_ready + i), 4);
+      tc::mbar_init(tc::smem_u32(p_ready + i), 4);  // the 4 warps of warpgroup i
       tc::mbar_init(tc::smem_u32(pv_done + i), 1);
     }
     tc::mbar_init(tc::smem_u32(o_full), 1);
     tc::mbar_init(tc::smem_u32(drain), 1);
+    tc::mbar_init(tc::smem_u32(drain + 1), 1);
     tc::mbar_init(tc::smem_u32(never), 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -261,7 +282,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int x_end = (int)((long long)(blockIdx.x + 1) * T / G);
   const uint32_t sQ = tc::smem_u32(smem + L::OFF_Q);
   const uint32_t sKV = tc::smem_u32(smem + L::OFF_KV);
-  const uint32_t sP = tc::smem_u32(smem + L::OFF_P);
   const float qk_scale = kLog2e * rsqrtf((float)D);
 
   // Global tile counter (same in every role) and segment counter.
@@ -285,100 +305,103 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       q_par = seg_no & 1;
       for (int t = 0; t < sg.ntile; ++t) {
         const uint32_t q = tile_no + t;
-        const int stage = q % STAGES;
-        const uint32_t ph = (q / STAGES) & 1;
+        const int stage = q % stages;
+        const uint32_t ph = (q / stages) & 1;
         if (!tc::mbar_wait(tc::smem_u32(kv_empty + stage), ph ^ 1, pb.cap_ns, abort_flag)) break;
         const int i = sg.first_tile + t;
         const uint32_t kdst = sKV + stage * L::STAGE, vdst = kdst + L::K_BYTES;
-        const uint32_t kb = tc::smem_u32(k_full + stage), vb = tc::smem_u32(v_full + stage);
+        const uint32_t fb = tc::smem_u32(kv_full + stage);
         if (i < np) {
           const int z = pb.NL * sg.kv0 + sg.l * sg.k_s + i * TILE;
-          tc::mbar_arrive_expect_tx(kb, L::K_BYTES);
-          for (int b = 0; b < D / 64; ++b) tc::tma_load_3d(kdst + b * L::KBOX, &tm_kp, kb, b * 64, sg.g, z);
-          tc::mbar_arrive_expect_tx(vb, L::K_BYTES);
-          for (int b = 0; b < D / 64; ++b) tc::tma_load_3d(vdst + b * L::KBOX, &tm_vp, vb, b * 64, sg.g, z);
+          tc::mbar_arrive_expect_tx(fb, 2 * L::K_BYTES);
+          for (int b = 0; b < D / 64; ++b) {
+            tc::tma_load_3d(kdst + b * L::KBOX, &tm_kp, fb, b * 64, sg.g, z);
+            tc::tma_load_3d(vdst + b * L::KBOX, &tm_vp, fb, b * 64, sg.g, z);
+          }
         } else {
           const int z = (sg.s * pb.NL + sg.l) * pb.LB + (i - np) * TILE;
-          const uint32_t bytes = (uint32_t)((D / 64) * BR * 128);
-          tc::mbar_arrive_expect_tx(kb, bytes);
-          for (int b = 0; b < D / 64; ++b) tc::tma_load_3d(kdst + b * L::KBOX, &tm_kb, kb, b * 64, sg.g, z);
-          tc::mbar_arrive_expect_tx(vb, bytes);
-          for (int b = 0; b < D / 64; ++b) tc::tma_load_3d(vdst + b * L::KBOX, &tm_vb, vb, b * 64, sg.g, z);
+          tc::mbar_arrive_expect_tx(fb, (uint32_t)(2 * (D / 64) * BR * 128));
+          for (int b = 0; b < D / 64; ++b) {
+            tc::tma_load_3d(kdst + b * L::KBOX, &tm_kb, fb, b * 64, sg.g, z);
+            tc::tma_load_3d(vdst + b * L::KBOX, &tm_vb, fb, b * 64, sg.g, z);
+          }
         }
         issued |= 1u << stage;
         last_par = (last_par & ~(1u << stage)) | (ph << stage);
       }
     } else if (warp == 1 && lane == 0 && run) {
-      // ------------------------------------------------ MMA issuer
+      // ------------------------------------------------ QK issuer
       constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(ROWS, TILE, false, false);
-      constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(ROWS, D, false, true);
       // Failure-path test: wait on a barrier no one arrives on, so the
       // bounded wait expires and the CTA takes its abort path.
       if (pb.stall_test) tc::mbar_wait(tc::smem_u32(never), 0, pb.cap_ns, abort_flag);
       bool ok = !*abort_flag &&
                 tc::mbar_wait(tc::smem_u32(q_full), seg_no & 1, pb.cap_ns, abort_flag);
-      // Shared-memory descriptors: built once, then advanced by constant
-      // offsets (the start-address field counts 16-byte units and never
-      // carries: every address is below 256 KB).  The issuing warp shares
-      // its SM sub-partition with softmax warps, so every instruction here
-      // is on the critical path.
+      // Shared-memory descriptors, built once and advanced by constant
+      // offsets (16-byte units; no carry: every address is below 256 KB).
       const uint64_t qd = tc::desc_kmajor_sw128(sQ);
       const uint64_t kd0 = tc::desc_kmajor_sw128(sKV);
-      const uint64_t vd0 = tc::desc_mnmajor_sw128(sKV + L::K_BYTES, L::KBOX);
-      const uint64_t pd0 = tc::desc_kmajor_sw128(sP);
-      constexpr uint64_t kStageD = L::STAGE >> 4, kPbufD = L::P_BUF >> 4;
-      // O[q & 1] += P[q & 1] V for segment tile u (global tile q).
-      auto issue_pv = [&](int u) -> bool {
-        const uint32_t q = tile_no + u;
-        const int stage = q % STAGES, h = q & 1;
-        const uint32_t ph = (q / STAGES) & 1;
-        if (!tc::mbar_wait(tc::smem_u32(p_ready + h), (q >> 1) & 1, pb.cap_ns, abort_flag) ||
-            !tc::mbar_wait(tc::smem_u32(v_full + stage), ph, pb.cap_ns, abort_flag))
-          return false;
-        tc::fence_after_sync();
-        const uint64_t vd = vd0 + (uint64_t)stage * kStageD;
-        const uint64_t pd = pd0 + (uint64_t)h * kPbufD;
-        const uint32_t od = tmem + L::TMEM_O + h * D;
-        // A warpgroup's first tile of the segment (u < 2) starts its O.
-        tc::mma_bf16(od, pd, vd, idesc_pv, u >= 2 ? 1u : 0u);
-#pragma unroll
-        for (int k = 1; k < TILE / 16; ++k)  // 16 keys: 32 B of P, 16 rows of V
-          tc::mma_bf16(od, pd + 2 * k, vd + (16 * 128 >> 4) * k, idesc_pv, 1u);
-        tc::mma_commit(tc::smem_u32(pv_done + h));
-        tc::mma_commit(tc::smem_u32(kv_empty + stage));
-        return true;
-      };
+      constexpr uint64_t kStageD = L::STAGE >> 4;
       for (int t = 0; ok && t < sg.ntile; ++t) {
         const uint32_t q = tile_no + t;
-        const int stage = q % STAGES, sb = q & 1;
-        const uint32_t ph = (q / STAGES) & 1;
-        if (!tc::mbar_wait(tc::smem_u32(k_full + stage), ph, pb.cap_ns, abort_flag) ||
-            !tc::mbar_wait(tc::smem_u32(s_free + sb), ((q >> 1) & 1) ^ 1, pb.cap_ns, abort_flag)) {
+        const int stage = q % stages, h = q & 1;
+        const uint32_t ph = (q / stages) & 1;
+        // S[h] also holds P of tile q - 2: its PV must be done first.
+        if (!tc::mbar_wait(tc::smem_u32(kv_full + stage), ph, pb.cap_ns, abort_flag) ||
+            (t >= 2 && !tc::mbar_wait(tc::smem_u32(pv_done + h), ((q >> 1) & 1) ^ 1, pb.cap_ns,
+                                      abort_flag))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
         const uint64_t kd = kd0 + (uint64_t)stage * kStageD;
-        const uint32_t sd = tmem + sb * TILE;
+        const uint32_t sd = tmem + h * TILE;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           constexpr int kQBoxD = L::QBOX >> 4, kKBoxD = L::KBOX >> 4;
           tc::mma_bf16(sd, qd + (k >> 2) * kQBoxD + (k & 3) * 2, kd + (k >> 2) * kKBoxD + (k & 3) * 2,
                        idesc_qk, k > 0 ? 1u : 0u);
         }
-        tc::mma_commit(tc::smem_u32(s_full + sb));
-        if (t > 0 && !issue_pv(t - 1)) { ok = false; break; }
+        tc::mma_commit(tc::smem_u32(s_full + h));
       }
-      if (ok) ok = issue_pv(sg.ntile - 1);
+    } else if (warp == 10 && lane == 0 && run) {
+      // ------------------------------------------------ PV issuer
+      // O[h] += P[h] V for every tile (h = q & 1); P is the A operand, read
+      // from tensor memory where the softmax left it.  A second issuing
+      // thread: one thread issuing both products could not keep up with HBM.
+      constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(ROWS, D, false, true);
+      const uint64_t vd0 = tc::desc_mnmajor_sw128(sKV + L::K_BYTES, L::KBOX);
+      constexpr uint64_t kStageD = L::STAGE >> 4;
+      bool ok = true;
+      for (int u = 0; u < sg.ntile; ++u) {
+        const uint32_t q = tile_no + u;
+        const int stage = q % stages, h = q & 1;
+        const uint32_t ph = (q / stages) & 1;
+        if (!tc::mbar_wait(tc::smem_u32(p_ready + h), (q >> 1) & 1, pb.cap_ns, abort_flag) ||
+            !tc::mbar_wait(tc::smem_u32(kv_full + stage), ph, pb.cap_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint64_t vd = vd0 + (uint64_t)stage * kStageD;
+        const uint32_t pa = tmem + h * TILE;          // P[h]: 64 columns of bf16 pairs
+        const uint32_t od = tmem + L::TMEM_O + h * D;
+        // A warpgroup's first tile of the segment (u < 2) starts its O.
+        mma_bf16_ts(od, pa, vd, idesc_pv, u >= 2 ? 1u : 0u);
+#pragma unroll
+        for (int k = 1; k < TILE / 16; ++k)  // 16 keys: 8 columns of P, 16 rows of V
+          mma_bf16_ts(od, pa + 8 * k, vd + (16 * 128 >> 4) * k, idesc_pv, 1u);
+        tc::mma_commit(tc::smem_u32(pv_done + h));
+        tc::mma_commit(tc::smem_u32(kv_empty + stage));
+      }
       if (ok) tc::mma_commit(tc::smem_u32(o_full));
-    } else if (warp >= 2 && run) {
+    } else if (warp >= 2 && warp < 10 && run) {
       // ------------------------------------------------ softmax, warpgroup h
       const int h = (warp - 2) >> 2;
       const int q4 = warp & 3, r = q4 * 32 + lane;
       const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
       const uint32_t o_addr = tmem + lane_off + L::TMEM_O + h * D;
       const uint32_t s_addr = tmem + lane_off + h * TILE;
-      const uint32_t pbuf = sP + h * L::P_BUF;
       float m_used = -INFINITY, l_sum = 0.f;
       bool ok = true, mine = false;
       for (int t = 0; t < sg.ntile; ++t) {
@@ -388,49 +411,37 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int i = sg.first_tile + t;
         const int nvalid = i < np ? min(TILE, sg.k_s - i * TILE)
                                   : min(TILE, pb.LB - (i - np) * TILE);
+        // S of tile q is complete, and (by the issue order) so is the PV of
+        // tile q - 2: O[h] is stable and S[h] may take P.
         if (!__all_sync(0xffffffffu, tc::mbar_wait(tc::smem_u32(s_full + h), (q >> 1) & 1,
                                                    pb.cap_ns, abort_flag))) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        float v[64];
-        {
-          float (&v0)[32] = *reinterpret_cast<float (*)[32]>(&v[0]);
-          float (&v1)[32] = *reinterpret_cast<float (*)[32]>(&v[32]);
-          tc::tmem_ld32(s_addr, v0);
-          tc::tmem_ld32(s_addr + 32, v1);
+        // Pass 1: row max of the raw scores, 32 columns of S at a time.
+        float mraw = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < TILE / 32; ++c) {
+          float v[32];
+          tc::tmem_ld32(s_addr + c * 32, v);
           tc::tmem_wait_ld();
+          if (nvalid < TILE) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (c * 32 + j >= nvalid) v[j] = -INFINITY;
+          }
+          float a0 = v[0], a1 = v[1], a2 = v[2], a3 = v[3];
+#pragma unroll
+          for (int j = 4; j < 32; j += 8) {
+            a0 = max3(a0, v[j], v[j + 1]);
+            a1 = max3(a1, v[j + 2], v[j + 3]);
+            a2 = max3(a2, v[j + 4], v[j + 5]);
+            a3 = max3(a3, v[j + 6], v[j + 7]);
+          }
+          mraw = max3(mraw, max3(a0, a1, a2), a3);
         }
-        // S of this tile is in registers: its TMEM columns may be reused.
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(tc::smem_u32(s_free + h));
-        const bool full = nvalid == TILE;
-        if (!full) {
-#pragma unroll
-          for (int j = 0; j < 64; ++j)
-            if (j >= nvalid) v[j] = -INFINITY;  // masked keys: exp2 gives 0
-        }
-        // Row max of the 64 raw scores: a tree of 3-input maxima.
-        float m1[22], m2[8];
-#pragma unroll
-        for (int j = 0; j < 21; ++j) m1[j] = max3(v[3 * j], v[3 * j + 1], v[3 * j + 2]);
-        m1[21] = v[63];
-#pragma unroll
-        for (int j = 0; j < 7; ++j) m2[j] = max3(m1[3 * j], m1[3 * j + 1], m1[3 * j + 2]);
-        m2[7] = m1[21];
-        const float mraw = max3(max3(m2[0], m2[1], m2[2]), max3(m2[3], m2[4], m2[5]),
-                                fmaxf(m2[6], m2[7]));
         const float mx = mraw * qk_scale;
-        // This warpgroup's P buffer and O are free once the PV of its
-        // previous tile (q - 2) is done; within a segment only.
-        if (t >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(tc::smem_u32(pv_done + h),
-                                                             ((q >> 1) & 1) ^ 1, pb.cap_ns,
-                                                             abort_flag))) {
-          ok = false;
-          break;
-        }
         // Lazy rescale: a row moves its reference max only when the tile max
         // exceeds it by more than 2^8; O rows are then rescaled in TMEM.
         const bool need = mx > m_used + kRescaleLog2;
@@ -440,41 +451,43 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           m_used = mx;
         }
         if (t >= 2 && __any_sync(0xffffffffu, need)) {
-          tc::fence_after_sync();
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             float o[32];
             tc::tmem_ld32(o_addr + c * 32, o);
             tc::tmem_wait_ld();
+            uint32_t u[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] *= alpha;
-            tmem_st32(o_addr + c * 32, o);
+            for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(o[j] * alpha);
+            tmem_st32(o_addr + c * 32, u);
           }
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
-        // P = exp2(S * scale - m) in bf16, written to the swizzled P buffer
-        // (masked keys hold -inf and give 0).
-        float lsum = 0.f;
+        // Pass 2: P = exp2(S * scale - m) as bf16 pairs, 32 keys at a time,
+        // written over the first 64 columns of S[h] (P chunk c lands in
+        // columns 16c..16c+15, all read already; masked keys give 0).
         const float nm = -m_used;
+        float lsum = 0.f;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t pk[4];
+        for (int c = 0; c < TILE / 32; ++c) {
+          float v[32];
+          tc::tmem_ld32(s_addr + c * 32, v);
+          tc::tmem_wait_ld();
+          uint32_t pk[16];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int j = c * 8 + 2 * u;
-            const float p0 = fast_exp2(fmaf(v[j], qk_scale, nm));
-            const float p1 = fast_exp2(fmaf(v[j + 1], qk_scale, nm));
+          for (int u = 0; u < 16; ++u) {
+            const int j = 2 * u;
+            const float p0 = c * 32 + j < nvalid ? fast_exp2(fmaf(v[j], qk_scale, nm)) : 0.f;
+            const float p1 = c * 32 + j + 1 < nvalid ? fast_exp2(fmaf(v[j + 1], qk_scale, nm))
+                                                    : 0.f;
             lsum += p0 + p1;
             __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
             pk[u] = *reinterpret_cast<uint32_t *>(&h2);
           }
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(p_chunk_addr(pbuf, r, c)),
-                       "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
-                       : "memory");
+          tmem_st16(s_addr + c * 16, pk);
         }
         l_sum += lsum;
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc::fence_before_sync();
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(tc::smem_u32(p_ready + h));
       }
@@ -513,16 +526,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (warp == 0 && lane == 0) {
     volatile int no_abort = 0;
     if (q_issued) tc::mbar_wait(tc::smem_u32(q_full), q_par, pb.drain_ns, &no_abort);
-    for (int s = 0; s < STAGES; ++s)
-      if (issued >> s & 1u) {
-        tc::mbar_wait(tc::smem_u32(k_full + s), last_par >> s & 1u, pb.drain_ns, &no_abort);
-        tc::mbar_wait(tc::smem_u32(v_full + s), last_par >> s & 1u, pb.drain_ns, &no_abort);
-      }
+    for (int s = 0; s < stages; ++s)
+      if (issued >> s & 1u)
+        tc::mbar_wait(tc::smem_u32(kv_full + s), last_par >> s & 1u, pb.drain_ns, &no_abort);
   }
-  if (warp == 1 && lane == 0) {
-    tc::mma_commit(tc::smem_u32(drain));
+  if ((warp == 1 || warp == 10) && lane == 0) {  // each issuer drains its own MMAs
+    const uint32_t db = tc::smem_u32(drain + (warp == 10));
+    tc::mma_commit(db);
     volatile int no_abort = 0;
-    tc::mbar_wait(tc::smem_u32(drain), 0, pb.drain_ns, &no_abort);
+    tc::mbar_wait(db, 0, pb.drain_ns, &no_abort);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -532,7 +544,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 }
 
 // One warp per (pair, query row): merge both warpgroup partials of every
-// segment of the pair in tile order with a running max (single pass).
+// segment of the pair in tile order (max of the row maxima, then the
+// weighted sums).
 template <int D>
 __global__ void __launch_bounds__(256)
 attn_tc_combine_kernel(Problem pb, int G, __nv_bfloat16 *__restrict__ O) {
@@ -551,35 +564,44 @@ attn_tc_combine_kernel(Problem pb, int G, __nv_bfloat16 *__restrict__ O) {
   const int l = pis / pb.Hkv, g = pis % pb.Hkv;
   const long long T = ts[pb.S];
   const int p0 = ts[s] + pis * nt[s], p1 = p0 + nt[s];
-  float mx = -INFINITY, den = 0.f, acc[D / 32];
+  // The CTAs whose tile ranges meet [p0, p1) are c_first..c_last, and CTA c
+  // wrote this pair's partials into slot pair + c.  When T < G some CTAs
+  // have empty ranges and hold no segment: they are skipped.
+  const int c_first = (int)starts_le(p0, G, T) - 1;
+  const int c_last = (int)starts_le(p1 - 1, G, T) - 1;
+  const bool dense = T >= G;
+  auto holds = [&](int c) {
+    return dense || (long long)c * T / G < (long long)(c + 1) * T / G;
+  };
+  // Pass 1: the largest row max over all partials (independent loads).
+  float mx = -INFINITY;
+#pragma unroll 4
+  for (int c = c_first; c <= c_last; ++c) {
+    if (!holds(c)) continue;
+    const size_t part = (size_t)(2 * (pair + c)) * ROWS + r;
+    mx = fmaxf(mx, fmaxf(pb.ws_ml[part * 2], pb.ws_ml[(part + ROWS) * 2]));
+  }
+  // Pass 2: weighted sum of the partials in tile order.
+  float den = 0.f, acc[D / 32];
 #pragma unroll
   for (int q = 0; q < D / 32; ++q) acc[q] = 0.f;
-  for (long long x = p0; x < p1;) {
-    const long long c = starts_le(x, G, T);
-    const long long nxt = c < G ? c * T / G : T;
-    const int slot = pair + (int)c - 1;
+#pragma unroll 2
+  for (int c = c_first; c <= c_last; ++c) {
+    if (!holds(c)) continue;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const size_t part = (size_t)(2 * slot + h) * ROWS + r;
+      const size_t part = (size_t)(2 * (pair + c) + h) * ROWS + r;
       const float2 ml = *reinterpret_cast<const float2 *>(pb.ws_ml + part * 2);
-      if (ml.x == -INFINITY) continue;  // this warpgroup saw no key of the segment
       const float *oc = pb.ws_o + part * D;
-      float oq[D / 32];
+      // A warpgroup that saw no key of the segment left m = -inf: weight 0.
+      const float wgt = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mx);
+      den = fmaf(wgt, ml.x == -INFINITY ? 0.f : ml.y, den);
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) oq[q] = oc[lane + 32 * q];
-      if (ml.x > mx) {
-        const float sc = exp2f(mx - ml.x);  // 0 while mx is -inf
-        den *= sc;
-#pragma unroll
-        for (int q = 0; q < D / 32; ++q) acc[q] *= sc;
-        mx = ml.x;
+      for (int q = 0; q < D / 32; ++q) {
+        const float o = oc[lane + 32 * q];
+        acc[q] = fmaf(wgt, ml.x == -INFINITY ? 0.f : o, acc[q]);
       }
-      const float wgt = exp2f(ml.x - mx);
-      den = fmaf(wgt, ml.y, den);
-#pragma unroll
-      for (int q = 0; q < D / 32; ++q) acc[q] = fmaf(wgt, oq[q], acc[q]);
     }
-    x = nxt < p1 ? nxt : p1;
   }
   const int j = r / GQ, hh = r % GQ;
   __nv_bfloat16 *dst =
@@ -637,13 +659,23 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
     tkp = tkb;
     tvp = tvb;
   }
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)Lt::SMEM) != cudaSuccess)
+  // As many ring stages as fit next to Q, the barriers and the tables.
+  static int optin = 0;
+  if (!optin) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - 256) != cudaSuccess) {
+      optin = 0;
       return SPRINT_ERR_CUDA;
-    attr = true;
+    }
   }
+  int stages = MAX_STAGES;
+  while (stages > 2 && Lt::smem_bytes(stages, S) > (size_t)(optin - 256)) --stages;
+  const size_t smem = Lt::smem_bytes(stages, S);
+  if (smem > (size_t)(optin - 256)) return SPRINT_ERR_UNSUPPORTED;
   const int G = sm_count();
   const size_t pairs = (size_t)S * NL * Hkv;
   Problem pb;
@@ -658,7 +690,8 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
   pb.drain_ns = pb.cap_ns > 1000000000ull ? pb.cap_ns : 1000000000ull;
   pb.stall_test = stall_test_enabled();
   pb.gate = gate;
-  attn_tc_kernel<D><<<G, THREADS, Lt::SMEM, stream>>>(tq, tkp, tvp, tkb, tvb, pb);
+  pb.stages = stages;
+  attn_tc_kernel<D><<<G, THREADS, smem, stream>>>(tq, tkp, tvp, tkb, tvb, pb);
   if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   const long long warps = (long long)pairs * LB * GQ;
   attn_tc_combine_kernel<D><<<(int)((warps * 32 + 255) / 256), 256, 0, stream>>>(
