@@ -401,12 +401,18 @@ def run_ours(args):
         barrier(world)
         torch.cuda.synchronize()
         start.record()
-        for _ in range(args.steps):
-            res = dec.decode(prefix, step_fn)
-            n_steps += res.steps
-            for a in res.accepted_per_step:
-                for v in a:
-                    hist[v] = hist.get(v, 0) + 1
+        # Block i+1 is enqueued before block i's step counts are read, so the
+        # GPU never waits for the host between blocks.
+        pend = None
+        for i in range(args.steps + 1):
+            cur = dec.decode(prefix, step_fn, wait=False) if i < args.steps else None
+            if pend is not None:
+                res = dec.finish(pend)
+                n_steps += res.steps
+                for a in res.accepted_per_step:
+                    for v in a:
+                        hist[v] = hist.get(v, 0) + 1
+            pend = cur
         end.record()
         torch.cuda.synchronize()
         barrier(world)
@@ -427,6 +433,7 @@ def run_ours(args):
     # memory and the decoded tokens read back.  Copies run on their own
     # stream into two alternating device buffer sets, so block i+1's inputs
     # travel while block i computes; the first copy is inside the timed region.
+    # As above, block i's step counts are read after block i+1 is enqueued.
     e2e = None
     if not args.no_e2e:
         pin = lambda d: {k: v.pin_memory() for k, v in d.items()}  # noqa: E731
@@ -462,16 +469,20 @@ def run_ours(args):
         s2.record(compute)
         copy_stream.wait_event(s2)
         enqueue_copy(0)
+        pend = None
         for i in range(args.steps):
             b = i % 2
             if i + 1 < args.steps:
                 enqueue_copy(1 - b)
             compute.wait_event(ready[b])
             pre_b, steps_b = bufs[b]
-            res = dec.decode(pre_b, lambda t: steps_b[t])
-            tok_host.copy_(res.tokens, non_blocking=True)
+            cur = dec.decode(pre_b, lambda t, s=steps_b: s[t], wait=False)
+            tok_host.copy_(cur.tokens, non_blocking=True)
             free[b].record(compute)
-            e_steps += res.steps
+            if pend is not None:
+                e_steps += dec.finish(pend).steps
+            pend = cur
+        e_steps += dec.finish(pend).steps
         e2.record(compute)
         torch.cuda.synchronize()
         barrier(world)

@@ -34,6 +34,18 @@ class BlockResult:
     accepted_per_step: list    # per step: [S] accepted counts (host ints)
 
 
+@dataclass
+class PendingBlock:
+    """A block enqueued by BlockDecoder.decode(wait=False)."""
+    slot: int
+    done: torch.cuda.Event     # recorded after the block's last work
+    m_hist_host: torch.Tensor  # pinned [T][S] masked counts, valid after `done`
+    step_events: list          # 6 * T timing events, or None
+    stage_events: list         # (stage, start, end) of the prefix pass
+    tokens: torch.Tensor       # live device token buffer of the decoder
+    result: BlockResult = None
+
+
 class BlockDecoder:
     """Buffers and call sequence for decoding blocks of S sequences.
 
@@ -103,14 +115,19 @@ class BlockDecoder:
         self.accepted = torch.empty((S, LB), dtype=torch.uint8, device=self.dev)
         self.m_host = torch.empty(S, dtype=torch.int32, pin_memory=True)
         self.m_hist = torch.empty((T, S), **i32)
-        self.m_hist_host = torch.empty((T, S), dtype=torch.int32, pin_memory=True)
         self.ev = torch.cuda.Event()
         # When a dict, every stage records (start, end) CUDA events on the
         # current stream; after the block the durations (ms) are appended to
         # timing[stage] (used by the benchmark).
         self.timing = None
         self._pending = []
-        self._step_events = None
+        # Two slots for blocks decoded without waiting (decode(wait=False)).
+        self._step_events = [None, None]
+        self._m_hist_host = [torch.empty((T, S), dtype=torch.int32, pin_memory=True)
+                             for _ in range(2)]
+        self._done = [torch.cuda.Event(), torch.cuda.Event()]
+        self._slots = [None, None]
+        self._next_slot = 0
 
     @contextlib.contextmanager
     def _stage(self, name):
@@ -131,14 +148,16 @@ class BlockDecoder:
                 self.timing.setdefault(name, []).append(a.elapsed_time(b))
         self._pending = []
 
-    def _events_for_steps(self):
-        """6 * T timing events for the native step driver, created once; each
-        is recorded once here so that its CUDA event exists."""
-        if self._step_events is None:
-            self._step_events = [torch.cuda.Event(enable_timing=True) for _ in range(6 * self.T)]
-            for e in self._step_events:
+    def _events_for_steps(self, slot):
+        """6 * T timing events for the native step driver (one set per
+        pending-block slot), created once; each is recorded once here so that
+        its CUDA event exists."""
+        if self._step_events[slot] is None:
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(6 * self.T)]
+            for e in evs:
                 e.record()
-        return self._step_events
+            self._step_events[slot] = evs
+        return self._step_events[slot]
 
     # -- the individual stages (each is one or two library calls) --------
     def prefix_pass(self, K, V, H, theta, modality):
@@ -186,17 +205,26 @@ class BlockDecoder:
         self.ev.synchronize()
         return self.m_host.tolist()
 
-    def decode(self, prefix, steps, on_step=None) -> BlockResult:
+    def decode(self, prefix, steps, on_step=None, wait=True):
         """Decode one block.  prefix: dict K, V, H, theta, modality (device,
         sequences concatenated).  steps(t) -> dict Q, Kb, Vb, h, theta.
         With on_step (called after each step with (t, self)) the block is
-        decoded step by step (decode_stepwise)."""
+        decoded step by step (decode_stepwise).
+
+        wait=False returns a PendingBlock at once (nothing waits for the
+        GPU); finish(pending) later returns its BlockResult.  Two blocks may
+        be pending; `pending.tokens` is the live token buffer, which the
+        next block overwrites, so copy it (on the stream) before that."""
         if on_step is not None:
             return self.decode_stepwise(prefix, steps, on_step)
+        slot = self._next_slot
+        self._next_slot ^= 1
+        if self._slots[slot] is not None:  # at most two blocks in flight
+            self.finish(self._slots[slot])
         self.prefix_pass(prefix["K"], prefix["V"], prefix["H"], prefix["theta"],
                          prefix["modality"])
         xs = [steps(t) for t in range(self.T)]
-        events = self._events_for_steps() if self.timing is not None else None
+        events = self._events_for_steps(slot) if self.timing is not None else None
         sp.sprint_decode_steps(
             Q=[x["Q"] for x in xs], Kb=[x["Kb"] for x in xs], Vb=[x["Vb"] for x in xs],
             h=[x["h"] for x in xs], theta=[x.get("theta") for x in xs],
@@ -207,23 +235,41 @@ class BlockDecoder:
             argmax=self.argmax_blk, mask=self.mask, tokens=self.tokens, m_hist=self.m_hist,
             ws_attn=self.ws_attn, ws_lm=self.ws_lm_blk, status=self.status,
             logits=self.logits, events=events)
-        self.m_hist_host.copy_(self.m_hist, non_blocking=True)
-        self.ev.record()
-        self.ev.synchronize()
-        hist = self.m_hist_host.tolist()
+        m_host = self._m_hist_host[slot]
+        m_host.copy_(self.m_hist, non_blocking=True)
+        done = self._done[slot]
+        done.record()
+        pending = PendingBlock(slot, done, m_host, events, self._pending, self.tokens)
+        self._pending = []
+        self._slots[slot] = pending
+        return self.finish(pending) if wait else pending
+
+    def finish(self, pending) -> BlockResult:
+        """Wait for a pending block and return its result (idempotent)."""
+        if pending.result is not None:
+            return pending.result
+        pending.done.synchronize()
+        hist = pending.m_hist_host.tolist()
         accepted, prev, n_steps = [], [self.LB] * self.S, 0
+        timing = pending.stage_events
         for t in range(self.T):
             if t > 0 and not any(hist[t - 1]):
                 break
             n_steps += 1
             accepted.append([p - q for p, q in zip(prev, hist[t])])
             prev = hist[t]
-            if events is not None:
+            if pending.step_events is not None:
+                ev = pending.step_events
                 for k, name in enumerate(("attn_full" if t == 0 else "attn_pruned",
                                           "lmhead_block", "unmask")):
-                    self._pending.append((name, events[6 * t + 2 * k], events[6 * t + 2 * k + 1]))
-        self._flush_timing()
-        return BlockResult(n_steps, self.tokens, accepted)
+                    timing.append((name, ev[6 * t + 2 * k], ev[6 * t + 2 * k + 1]))
+        if self.timing is not None:
+            for name, a, b in timing:
+                self.timing.setdefault(name, []).append(a.elapsed_time(b))
+        pending.result = BlockResult(n_steps, pending.tokens, accepted)
+        if self._slots[pending.slot] is pending:
+            self._slots[pending.slot] = None
+        return pending.result
 
     def decode_stepwise(self, prefix, steps, on_step=None) -> BlockResult:
         """Decode one block one step at a time, reading the masked counts

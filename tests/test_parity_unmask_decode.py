@@ -165,3 +165,21 @@ def test_native_step_driver_skips_steps_after_the_block_is_done(sp):
     assert a.m_hist.cpu().tolist() == [[0]] * w.T
     # outputs still hold step 0's values: steps 1..T-1 did not run
     assert torch.equal(a.O, b.O) and torch.equal(a.conf_blk, b.conf_blk)
+
+
+def test_pipelined_blocks_match_waiting_decode(sp):
+    """decode(wait=False) lets the next block be enqueued before a block's
+    step counts are read; results equal the waiting decode's."""
+    w, pre, steps, make = _decoder_and_steps("tiny-256")
+    a, b = make(), make()
+    ref = a.decode(pre, lambda t: steps[t])
+    ref_tokens = ref.tokens.clone()
+    p1 = b.decode(pre, lambda t: steps[t], wait=False)
+    t1 = p1.tokens.clone()  # stream-ordered copy before the next block
+    p2 = b.decode(pre, lambda t: steps[t], wait=False)
+    r1, r2 = b.finish(p1), b.finish(p2)
+    torch.cuda.synchronize()
+    assert r1.steps == r2.steps == ref.steps
+    assert r1.accepted_per_step == r2.accepted_per_step == ref.accepted_per_step
+    assert torch.equal(t1, ref_tokens) and torch.equal(b.tokens, ref_tokens)
+    assert b.finish(p1) is r1  # finishing twice returns the same result
