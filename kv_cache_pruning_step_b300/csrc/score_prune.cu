@@ -14,15 +14,18 @@
 //                   concatenated KV heads.
 //   select_kernel   latency-bound: one 1024-thread CTA per sequence.  Mean of
 //                   u (fp32 per thread, fp64 across threads), composite score
-//                   s_i in fp32, then a 4-pass
-//                   8-bit radix select on the orderable 32-bit key of s_i for
-//                   both modalities at once, ties at the threshold resolved
-//                   by ascending position with a block scan, and a stable
-//                   block-scan compaction writing kept indices in ascending
-//                   position order.  The sequence's keys and modality tags
-//                   are staged in shared memory (5 bytes per position) when
-//                   they fit, so global memory is read once and the six
-//                   passes run at shared-memory latency; longer sequences
+//                   s_i in fp32 and its orderable 32-bit key; then a radix
+//                   select on the key minus its modality's smallest key,
+//                   12 bits at a time from the top (4096-bin histograms,
+//                   both modalities at once), giving each modality's
+//                   threshold key and how many keys equal to it are kept;
+//                   then a stable compaction: each warp counts its range's
+//                   definite keeps and threshold ties with ballots, the warp
+//                   totals are scanned, and each warp writes its kept
+//                   positions (ties by ascending position) to consecutive
+//                   output slots.  The sequence's keys and modality tags are
+//                   staged in shared memory (5 bytes per position) when they
+//                   fit, so global memory is read once; longer sequences
 //                   keep them in the workspace.
 #include <math.h>
 
@@ -118,10 +121,10 @@ keynorm_kernel(const T *__restrict__ K, const int32_t *__restrict__ prefix_off,
 }
 
 constexpr int kSelThreads = 1024;
-constexpr int kSelPer = 8;  // consecutive positions per thread per chunk
+constexpr int kDigit = 12, kBins = 1 << kDigit;  // radix digit of the selection
 // Longest sequence whose keys and tags are staged in shared memory:
-// 40,960 x 5 bytes = 200 KB of the 227 KB a CTA may hold.
-constexpr int kStageMax = 40960;
+// 36,864 x 5 bytes = 180 KB, next to 34 KB of histograms and scan space.
+constexpr int kStageMax = 36864;
 
 __device__ __forceinline__ int keep_count_dev(int n, double r) {
   return (int)floor(r * (double)n + 1e-9);
@@ -135,11 +138,15 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
               float alpha, double r_text, double r_img,
               uint32_t *__restrict__ keys_ws, int32_t *__restrict__ kept_idx,
               float *__restrict__ score_out, int32_t *status, int stage_cap) {
-  extern __shared__ uint32_t stage_sh[];  // [stage_cap] keys, then [stage_cap] tags
-  __shared__ uint32_t hist[2][256];
+  extern __shared__ uint4 stage_raw[];  // [stage_cap rounded up to 4] keys, then tags
+  uint32_t *stage_sh = reinterpret_cast<uint32_t *>(stage_raw);
+  __shared__ uint32_t hist[2][kBins];
+  __shared__ uint32_t kmin_sh[2], kmax_sh[2], prefix_sh[2];
+  __shared__ int shift_sh[2];
   __shared__ int scan_sh[33];
   __shared__ double dsum_sh[32];
   __shared__ int cnt_sh[32];
+  __shared__ float mean_sh;
   __shared__ uint32_t thresh_sh[2];
   __shared__ int need_sh[2];
   __shared__ int mode_sh[2];  // 0 keep none, 1 keep all, 2 threshold
@@ -156,24 +163,38 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
   // they fit, else read from the workspace / the caller's array.
   const bool staged = n <= stage_cap;
   uint32_t *keys = staged ? stage_sh : keys_ws + p0;
-  uint8_t *mod_sh = reinterpret_cast<uint8_t *>(stage_sh + stage_cap);
+  // The tags start 16-byte aligned (the key area is rounded up to 4 keys):
+  // the compaction reads 8 tags at a time with one 8-byte load.
+  uint8_t *mod_sh = reinterpret_cast<uint8_t *>(stage_sh + ((stage_cap + 3) & ~3));
   const uint8_t *mods = staged ? mod_sh : modality + p0;
 
   // Pass 1: sum of u and the image count; u is kept (as raw bits) where the
   // keys will go.  Each thread sums its positions in fp32; the 1024 thread
   // sums are added in fp64 (FP64 throughput is low on this GPU, so fp64 is
-  // kept off the per-position path).
+  // kept off the per-position path).  Loads come in batches of kB per
+  // thread, all issued before any store (stores through `keys` might alias
+  // the byte-typed tag loads, so the compiler would not reorder them).
+  constexpr int kB = 8;
   float su_f = 0.f;
   int nimg = 0;
-#pragma unroll 8
-  for (int i = tid; i < n; i += kSelThreads) {
-    const float ui = u[p0 + i];
-    const uint8_t mi = modality[p0 + i] != 0;
-    su_f += ui;
-    nimg += mi;
-    if (staged) {
-      keys[i] = __float_as_uint(ui);
-      mod_sh[i] = mi;
+  for (int i0 = tid; i0 < n; i0 += kB * kSelThreads) {
+    float ub[kB];
+    uint8_t mb[kB];
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int i = i0 + j * kSelThreads;
+      ub[j] = i < n ? __ldg(u + p0 + i) : 0.f;
+      mb[j] = i < n ? (__ldg(modality + p0 + i) != 0) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int i = i0 + j * kSelThreads;
+      su_f += ub[j];
+      nimg += mb[j];
+      if (staged && i < n) {
+        keys[i] = __float_as_uint(ub[j]);
+        mod_sh[i] = mb[j];
+      }
     }
   }
   double su = warp_sum((double)su_f);
@@ -185,149 +206,212 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
     int c = cnt_sh[lane];
     v = warp_sum(v);
     c = warp_sum(c);
-    if (lane == 0) { dsum_sh[0] = v; cnt_sh[0] = c; }
+    if (lane == 0) {
+      // One thread does the fp64 division and the keep counts.
+      const int ni = c, nt = n - c;
+      mean_sh = n > 0 ? (float)(v / (double)n) : 0.f;
+      cnt_sh[0] = ni;
+      cnt_sh[1] = keep_count_dev(nt, r_text);
+      cnt_sh[2] = keep_count_dev(ni, r_img);
+    }
   }
   __syncthreads();
-  const double mean = n > 0 ? dsum_sh[0] / (double)n : 0.0;
+  const float mean_f = mean_sh;
   const int n_img = cnt_sh[0], n_txt = n - n_img;
-  const int k_txt = keep_count_dev(n_txt, r_text), k_img = keep_count_dev(n_img, r_img);
+  const int k_txt = cnt_sh[1], k_img = cnt_sh[2];
   if (k1 - k0 != k_txt + k_img) {
     if (tid == 0) report(status, SPRINT_STATUS_KEPT_MISMATCH);
     return;
   }
 
   // Pass 2: composite score s_i = alpha I_i + (1 - alpha) c_i in fp32
-  // (I_i = u_i / mean, an fp32 division by the fp32-rounded mean).
-  const float one_m_alpha = 1.0f - alpha;
-  const float mean_f = (float)mean;
-#pragma unroll 8
-  for (int i = tid; i < n; i += kSelThreads) {
-    const float ui = staged ? __uint_as_float(keys[i]) : u[p0 + i];
-    const float imp = mean_f > 0.0f ? ui / mean_f : 0.0f;
-    const float sc = fmaf(alpha, imp, one_m_alpha * conf[p0 + i]);
-    keys[i] = float_key(sc);
-    if (score_out) score_out[p0 + i] = sc;
+  // (I_i = u_i / mean, an fp32 division by the fp32-rounded mean), its
+  // orderable key, and the smallest and largest key of each modality.
+  if (tid < 2) {
+    kmin_sh[tid] = 0xffffffffu;
+    kmax_sh[tid] = 0u;
   }
+  __syncthreads();
+  const float one_m_alpha = 1.0f - alpha;
+  uint32_t lo0 = 0xffffffffu, lo1 = 0xffffffffu, hi0 = 0u, hi1 = 0u;
+  for (int i0 = tid; i0 < n; i0 += kB * kSelThreads) {
+    float ub[kB], cb[kB];
+    bool ib[kB];
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int i = i0 + j * kSelThreads;
+      ub[j] = i < n ? (staged ? __uint_as_float(keys[i]) : __ldg(u + p0 + i)) : 0.f;
+      cb[j] = i < n ? __ldg(conf + p0 + i) : 0.f;
+      ib[j] = i < n && mods[i] != 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int i = i0 + j * kSelThreads;
+      if (i >= n) continue;
+      const float imp = mean_f > 0.0f ? ub[j] / mean_f : 0.0f;
+      const float sc = fmaf(alpha, imp, one_m_alpha * cb[j]);
+      const uint32_t key = float_key(sc);
+      keys[i] = key;
+      if (ib[j]) {
+        lo1 = min(lo1, key);
+        hi1 = max(hi1, key);
+      } else {
+        lo0 = min(lo0, key);
+        hi0 = max(hi0, key);
+      }
+      if (score_out) score_out[p0 + i] = sc;
+    }
+  }
+  lo0 = __reduce_min_sync(0xffffffffu, lo0);
+  lo1 = __reduce_min_sync(0xffffffffu, lo1);
+  hi0 = __reduce_max_sync(0xffffffffu, hi0);
+  hi1 = __reduce_max_sync(0xffffffffu, hi1);
+  if (lane == 0) {
+    atomicMin(&kmin_sh[0], lo0);
+    atomicMin(&kmin_sh[1], lo1);
+    atomicMax(&kmax_sh[0], hi0);
+    atomicMax(&kmax_sh[1], hi1);
+  }
+  __syncthreads();
   if (tid < 2) {
     const int k = tid == 0 ? k_txt : k_img, nm = tid == 0 ? n_txt : n_img;
     mode_sh[tid] = k <= 0 ? 0 : (k >= nm ? 1 : 2);
     need_sh[tid] = k;
-    thresh_sh[tid] = 0u;
+    // Keys of the modality relative to its smallest key span `shift` bits;
+    // the selection resolves them kDigit bits at a time from the top.
+    const uint32_t range = kmax_sh[tid] - kmin_sh[tid];
+    shift_sh[tid] = mode_sh[tid] == 2 && range ? 32 - __clz(range) : 0;
+    prefix_sh[tid] = 0u;
   }
   __syncthreads();
 
-  // Radix select, most significant byte first, both modalities together:
-  // find the k-th largest key T and how many keys equal to T are kept.
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int b = tid; b < 512; b += kSelThreads) (&hist[0][0])[b] = 0u;
+  // Radix select on d = key - (smallest key of the modality), kDigit bits at
+  // a time from the top, both modalities together: find the k-th largest
+  // key T and how many keys equal to T are kept (ties then go by position).
+  // Range reduction and 4096 bins keep atomic collisions rare.
+  while (__syncthreads_or(tid < 2 && shift_sh[tid] > 0)) {
+    for (int b = tid; b < 2 * kBins; b += kSelThreads) (&hist[0][0])[b] = 0u;
     __syncthreads();
-    const uint32_t hi_mask = shift == 24 ? 0u : (0xffffffffu << (shift + 8));
-    const uint32_t pre0 = thresh_sh[0], pre1 = thresh_sh[1];
-    const bool act0 = mode_sh[0] == 2, act1 = mode_sh[1] == 2;
-    for (int base = 0; base < n; base += kSelThreads) {
-      const int i = base + tid;
-      int bin = -1;
-      if (i < n) {
-        const uint32_t key = keys[i];
-        const int mu = mods[i] != 0;
-        const uint32_t pre = mu ? pre1 : pre0;
-        const bool act = mu ? act1 : act0;
-        if (act && ((key ^ pre) & hi_mask) == 0u) bin = mu * 256 + ((key >> shift) & 255u);
-      }
-      // Warp-aggregated histogram update: one atomic per distinct bin.
-      const unsigned peers = __match_any_sync(0xffffffffu, bin);
-      if (bin >= 0 && lane == __ffs(peers) - 1)
-        atomicAdd(&hist[0][0] + bin, (uint32_t)__popc(peers));
+    const int sh0 = shift_sh[0], sh1 = shift_sh[1];
+    const int w0 = sh0 < kDigit ? sh0 : kDigit, w1 = sh1 < kDigit ? sh1 : kDigit;
+    const uint32_t pre0 = prefix_sh[0], pre1 = prefix_sh[1];
+    const uint32_t base0 = kmin_sh[0], base1 = kmin_sh[1];
+    // Read before the scans below: one thread rewrites need_sh after them.
+    const uint32_t needv0 = (uint32_t)need_sh[0], needv1 = (uint32_t)need_sh[1];
+#pragma unroll 4
+    for (int i = tid; i < n; i += kSelThreads) {
+      const bool img = mods[i] != 0;
+      const int sh = img ? sh1 : sh0, w = img ? w1 : w0;
+      if (sh == 0) continue;
+      const uint64_t d = (uint64_t)(keys[i] - (img ? base1 : base0));
+      if ((uint32_t)(d >> sh) == (img ? pre1 : pre0))
+        atomicAdd(&hist[img][(uint32_t)(d >> (sh - w)) & ((1u << w) - 1u)], 1u);
     }
     __syncthreads();
-    if (warp < 2 && mode_sh[warp] == 2) {
-      // Lane L owns bins 255-8L .. 248-8L (descending); find the bin where
-      // the running count from the top reaches `need`.
-      const int mu = warp;
-      uint32_t c[8];
-      uint32_t mine = 0;
+    // Counts above each thread's 4 bins (bins in descending order), one
+    // block scan per modality.
+    uint32_t c0[4], c1[4];
+    int mine0 = 0, mine1 = 0;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) { c[q] = hist[mu][255 - 8 * lane - q]; mine += c[q]; }
-      uint32_t incl = mine;
+    for (int q = 0; q < 4; ++q) {
+      const int bin = kBins - 1 - 4 * tid - q;
+      c0[q] = hist[0][bin];
+      c1[q] = hist[1][bin];
+      mine0 += (int)c0[q];
+      mine1 += (int)c1[q];
+    }
+    int total;
+    const int above0 = block_excl_scan(mine0, scan_sh, &total);
+    const int above1 = block_excl_scan(mine1, scan_sh, &total);
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const uint32_t excl = incl - mine;
-      const uint32_t need = (uint32_t)need_sh[mu];
-      const bool hit = excl < need && incl >= need;
-      const unsigned who = __ballot_sync(0xffffffffu, hit);
-      if (hit) {
-        uint32_t run = excl;
-        int q = 0;
-        for (; q < 8; ++q) {
-          if (run + c[q] >= need) break;
-          run += c[q];
+    for (int mu = 0; mu < 2; ++mu) {
+      const int sh = mu ? sh1 : sh0, w = mu ? w1 : w0;
+      if (sh == 0) continue;
+      const uint32_t need = mu ? needv1 : needv0;
+      uint32_t run = (uint32_t)(mu ? above1 : above0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t cq = mu ? c1[q] : c0[q];
+        if (run < need && run + cq >= need) {  // the k-th largest lies in this bin
+          const uint32_t digit = (uint32_t)(kBins - 1 - 4 * tid - q);
+          prefix_sh[mu] = ((mu ? pre1 : pre0) << w) | digit;
+          need_sh[mu] = (int)(need - run);
+          shift_sh[mu] = sh - w;
         }
-        const uint32_t digit = 255u - 8u * lane - q;
-        thresh_sh[mu] |= digit << shift;
-        need_sh[mu] = (int)(need - run);
+        run += cq;
       }
-      (void)who;
     }
     __syncthreads();
   }
+  if (tid < 2) thresh_sh[tid] = kmin_sh[tid] + prefix_sh[tid];
+  __syncthreads();
 
   // Pass 3: stable compaction in ascending position order.  A position is
-  // kept if its key exceeds its modality's threshold, or equals it and it
-  // is among the first need_sh ties by position.
+  // kept if its key exceeds its modality's threshold (or the modality keeps
+  // everything), or equals the threshold and is among the first need_sh
+  // such ties by position.  Warp w owns positions [w R, (w+1) R): it counts
+  // its definite keeps and ties with ballots, the 32 warp totals are
+  // scanned, then every warp walks its range again and writes its kept
+  // positions at consecutive output slots (coalesced stores).
   const uint32_t T0 = thresh_sh[0], T1 = thresh_sh[1];
   const int m0 = mode_sh[0], m1 = mode_sh[1];
   const int need0 = need_sh[0], need1 = need_sh[1];
-  int tie_base0 = 0, tie_base1 = 0, out_base = 0;
-  for (int c0 = 0; c0 < n; c0 += kSelThreads * kSelPer) {
-    const int first = c0 + tid * kSelPer;
-    uint32_t kk[kSelPer];
-    uint8_t mm[kSelPer];
-    int ties = 0;  // text ties in the low 16 bits, image ties in the high 16
-#pragma unroll
-    for (int q = 0; q < kSelPer; ++q) {
-      const int i = first + q;
-      kk[q] = 0u;
-      mm[q] = 0;
-      if (i < n) {
-        kk[q] = keys[i];
-        mm[q] = mods[i] != 0;
-        if (mm[q] == 0 && m0 == 2 && kk[q] == T0) ties += 1;
-        if (mm[q] != 0 && m1 == 2 && kk[q] == T1) ties += 1 << 16;
-      }
+  const int k_all = k1 - k0;
+  const int per_warp = ((n + 32 * 32 - 1) / (32 * 32)) * 32;  // multiple of 32
+  const int w_lo = warp * per_warp, w_hi = min(n, w_lo + per_warp);
+  auto classify = [&](int i, bool &def, bool &tie0, bool &tie1) {
+    def = tie0 = tie1 = false;
+    if (i >= w_hi) return;
+    const uint32_t key = keys[i];
+    if (mods[i] != 0) {
+      def = m1 == 1 || (m1 == 2 && key > T1);
+      tie1 = m1 == 2 && key == T1;
+    } else {
+      def = m0 == 1 || (m0 == 2 && key > T0);
+      tie0 = m0 == 2 && key == T0;
     }
-    int ties_total;
-    const int ties_excl = block_excl_scan(ties, scan_sh, &ties_total);
-    int run0 = tie_base0 + (ties_excl & 0xffff), run1 = tie_base1 + (ties_excl >> 16);
-    uint32_t keep_bits = 0u;
-#pragma unroll
-    for (int q = 0; q < kSelPer; ++q) {
-      const int i = first + q;
-      if (i >= n) continue;
-      bool keep;
-      if (mm[q] == 0) {
-        keep = m0 == 1 || (m0 == 2 && (kk[q] > T0 || (kk[q] == T0 && run0 < need0)));
-        if (m0 == 2 && kk[q] == T0) ++run0;
-      } else {
-        keep = m1 == 1 || (m1 == 2 && (kk[q] > T1 || (kk[q] == T1 && run1 < need1)));
-        if (m1 == 2 && kk[q] == T1) ++run1;
-      }
-      keep_bits |= (uint32_t)keep << q;
+  };
+  int c_def = 0, c_t0 = 0, c_t1 = 0;
+  for (int i0 = w_lo; i0 < w_hi; i0 += 32) {
+    bool d, t0, t1;
+    classify(i0 + lane, d, t0, t1);
+    c_def += __popc(__ballot_sync(0xffffffffu, d));
+    c_t0 += __popc(__ballot_sync(0xffffffffu, t0));
+    c_t1 += __popc(__ballot_sync(0xffffffffu, t1));
+  }
+  // Exclusive scan of the warp totals (thread w of warp 0 handles warp w).
+  __shared__ int wdef[32], wt0[32], wt1[32];
+  if (lane == 0) { wdef[warp] = c_def; wt0[warp] = c_t0; wt1[warp] = c_t1; }
+  __syncthreads();
+  if (warp == 0) {
+    const int a = wdef[lane], b = wt0[lane], c = wt1[lane];
+    const int ia = warp_incl_scan(a), ib = warp_incl_scan(b), ic = warp_incl_scan(c);
+    wdef[lane] = ia - a;
+    wt0[lane] = ib - b;
+    wt1[lane] = ic - c;
+  }
+  __syncthreads();
+  int r_def = wdef[warp], r_t0 = wt0[warp], r_t1 = wt1[warp];
+  const unsigned lt = (1u << lane) - 1u;
+  for (int i0 = w_lo; i0 < w_hi; i0 += 32) {
+    bool d, t0, t1;
+    classify(i0 + lane, d, t0, t1);
+    const unsigned bd = __ballot_sync(0xffffffffu, d);
+    const unsigned b0 = __ballot_sync(0xffffffffu, t0);
+    const unsigned b1 = __ballot_sync(0xffffffffu, t1);
+    const bool keep = d || (t0 && r_t0 + __popc(b0 & lt) < need0) ||
+                      (t1 && r_t1 + __popc(b1 & lt) < need1);
+    const unsigned bk = __ballot_sync(0xffffffffu, keep);
+    // kept before this group = definite keeps + the first `need` ties
+    const int base = r_def + min(r_t0, need0) + min(r_t1, need1);
+    if (keep) {
+      const int out = base + __popc(bk & lt);
+      if (out < k_all) kept_idx[k0 + out] = i0 + lane;
+      else report(status, SPRINT_STATUS_KEPT_MISMATCH);
     }
-    int kept_total;
-    int out = out_base + block_excl_scan(__popc(keep_bits), scan_sh, &kept_total);
-#pragma unroll
-    for (int q = 0; q < kSelPer; ++q)
-      if (keep_bits >> q & 1u) {
-        if (out < k1 - k0) kept_idx[k0 + out] = first + q;
-        else report(status, SPRINT_STATUS_KEPT_MISMATCH);
-        ++out;
-      }
-    tie_base0 += ties_total & 0xffff;
-    tie_base1 += ties_total >> 16;
-    out_base += kept_total;
+    r_def += __popc(bd);
+    r_t0 += __popc(b0);
+    r_t1 += __popc(b1);
   }
 }
 
@@ -383,7 +467,7 @@ extern "C" int sprint_score_prune(const void *K, int S, const int32_t *prefix_of
   // Stage up to kStageMax positions per sequence in shared memory (5 bytes
   // each); the capacity follows the longest sequence the call can hold.
   const int stage_cap = total_rows < kStageMax ? total_rows : kStageMax;
-  const size_t stage_bytes = (size_t)stage_cap * 5 + 16;
+  const size_t stage_bytes = (size_t)((stage_cap + 3) & ~3) * 4 + (size_t)stage_cap + 16;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
