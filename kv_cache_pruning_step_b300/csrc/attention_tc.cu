@@ -231,8 +231,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   uint64_t *kv_full = bar + 1;                   // MAX_STAGES
   uint64_t *kv_empty = kv_full + MAX_STAGES;     // MAX_STAGES
   uint64_t *s_full = kv_empty + MAX_STAGES;      // 2
-  uint64_t *p_ready = s_full + 2;                // 2
-  uint64_t *pv_done = p_ready + 2;               // 2
+  uint64_t *p_ready = s_full + 2;                // 4: [warpgroup][key half]
+  uint64_t *pv_done = p_ready + 4;               // 2
   uint64_t *o_full = pv_done + 2, *drain = o_full + 1;  // drain[2]: one per issuer
   uint64_t *never = drain + 2;  // no one arrives: the stall test waits on it
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(never + 1);
@@ -259,7 +259,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(tc::smem_u32(s_full + i), 1);
-      tc::mbar_init(tc::smem_u32(p_ready + i), 4);  // the 4 warps of warpgroup i
+      tc::mbar_init(tc::smem_u32(p_ready + 2 * i), 4);  // the 4 warps of warpgroup i,
+      tc::mbar_init(tc::smem_u32(p_ready + 2 * i + 1), 4);  // one per key half
       tc::mbar_init(tc::smem_u32(pv_done + i), 1);
     }
     tc::mbar_init(tc::smem_u32(o_full), 1);
@@ -377,20 +378,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const uint32_t q = tile_no + u;
         const int stage = q % stages, h = q & 1;
         const uint32_t ph = (q / stages) & 1;
-        if (!tc::mbar_wait(tc::smem_u32(p_ready + h), (q >> 1) & 1, pb.cap_ns, abort_flag) ||
-            !tc::mbar_wait(tc::smem_u32(kv_full + stage), ph, pb.cap_ns, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc::fence_after_sync();
         const uint64_t vd = vd0 + (uint64_t)stage * kStageD;
         const uint32_t pa = tmem + h * TILE;          // P[h]: 64 columns of bf16 pairs
         const uint32_t od = tmem + L::TMEM_O + h * D;
-        // A warpgroup's first tile of the segment (u < 2) starts its O.
-        mma_bf16_ts(od, pa, vd, idesc_pv, u >= 2 ? 1u : 0u);
+        // P arrives in two halves of 64 keys: the first half's products run
+        // while the softmax still computes the second.
 #pragma unroll
-        for (int k = 1; k < TILE / 16; ++k)  // 16 keys: 8 columns of P, 16 rows of V
-          mma_bf16_ts(od, pa + 8 * k, vd + (16 * 128 >> 4) * k, idesc_pv, 1u);
+        for (int half = 0; half < 2; ++half) {
+          if (!tc::mbar_wait(tc::smem_u32(p_ready + 2 * h + half), (q >> 1) & 1, pb.cap_ns,
+                             abort_flag) ||
+              (half == 0 &&
+               !tc::mbar_wait(tc::smem_u32(kv_full + stage), ph, pb.cap_ns, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < TILE / 32; ++kk) {  // 16 keys: 8 columns of P, 16 rows of V
+            const int k = half * (TILE / 32) + kk;
+            // A warpgroup's first tile of the segment (u < 2) starts its O.
+            mma_bf16_ts(od, pa + 8 * k, vd + (16 * 128 >> 4) * k, idesc_pv,
+                        (u >= 2 || k > 0) ? 1u : 0u);
+          }
+        }
+        if (!ok) break;
         tc::mma_commit(tc::smem_u32(pv_done + h));
         tc::mma_commit(tc::smem_u32(kv_empty + stage));
       }
@@ -484,12 +495,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             pk[u] = *reinterpret_cast<uint32_t *>(&h2);
           }
           tmem_st16(s_addr + c * 16, pk);
+          if (c == TILE / 64 - 1 || c == TILE / 32 - 1) {  // a 64-key half of P is written
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(p_ready + 2 * h + (c * 32 >= TILE / 2)));
+          }
         }
         l_sum += lsum;
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(tc::smem_u32(p_ready + h));
       }
       if (ok && __all_sync(0xffffffffu, tc::mbar_wait(tc::smem_u32(o_full), seg_no & 1,
                                                       pb.cap_ns, abort_flag))) {
