@@ -120,3 +120,21 @@ def test_full_retention_pruned_cache_equals_full_prefix_bitwise(sp):
     torch.cuda.synchronize()
     assert status.item() == 0
     assert torch.equal(O_full, O_pruned)
+
+
+def test_many_short_sequences_two_stage_ring(sp):
+    """300 sequences of 0..200 prefix rows: the per-sequence tables take
+    enough shared memory that the bf16 kernel runs a 2-stage K/V ring, and
+    most segments are short (many pairs per CTA)."""
+    rng = torch.Generator().manual_seed(11)
+    lens = torch.randint(0, 201, (300,), generator=rng).tolist()
+    prefixes, steps = [], []
+    for s, n in enumerate(lens):
+        w = small_workload(dtype="bf16", NL=1, Hq=8, Hkv=2, d=128, LB=16, n=n, n_img=n // 4,
+                           seed=700 + s)
+        prefixes.append(prefix_inputs(w, seq=s, device=DEV))
+        steps.append(step_inputs(w, s, 0, 1, device=DEV))
+    O = run_attn(sp, w, prefixes, steps)
+    picks = [0, 1, 57, 150, 299] + [s for s, n in enumerate(lens) if n == 0][:2]
+    check(w, [prefixes[s] for s in picks], [steps[s] for s in picks], O[picks],
+          what="many sequences")
