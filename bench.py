@@ -568,6 +568,104 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- sequential blocks
+def run_sequential(args):
+    """Workloads of several blocks decoded in order on one sequence whose
+    prefix grows by the generated block each time (the 64-block workload).
+    One bench step decodes every block; with the prefix-confidence cache on,
+    a block's step-0 LM head runs only on the rows added since the previous
+    block (bit-identical results below 4096 prefix rows).  The same pass
+    without the cache is timed alongside."""
+    import torch
+
+    from kv_cache_pruning_step_b300 import BlockDecoder
+    from kv_cache_pruning_step_b300 import sprint as sp
+    from workload import WORKLOADS, lm_head_weight, prefix_inputs, step_inputs
+
+    rank, world, local = rank_info()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    w = WORKLOADS[args.workload]
+    W = lm_head_weight(w, device="cpu").to(dev)
+    pres, steps, counts = [], [], []
+    for b in range(w.blocks):
+        p = prefix_inputs(w, seq=rank, block=b, device="cpu")
+        pres.append({k: v.to(dev) for k, v in p.items()})
+        m = p["modality"]
+        counts.append([(int((m == 0).sum()), int((m != 0).sum()))])
+        xs = [step_inputs(w, rank, b, t, device="cpu") for t in range(w.T)]
+        steps.append([{"Q": x["Q"][None].contiguous().to(dev),
+                       "Kb": x["Kb"][None].contiguous().to(dev),
+                       "Vb": x["Vb"][None].contiguous().to(dev),
+                       "h": x["h"].to(dev), "theta": x["theta"].to(dev)} for x in xs])
+    dec = BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
+                       r_text=w.r_text, r_img=w.r_img, alpha=w.alpha,
+                       modality_counts=counts[-1])  # the largest: no buffer growth
+
+    def one_pass(cache):
+        n_steps, prev = 0, 0
+        for b in range(w.blocks):
+            dec.set_prefix(counts[b])
+            res = dec.decode(pres[b], lambda t, s=steps[b]: s[t],
+                             conf_from=prev if cache and b > 0 else 0)
+            n_steps += res.steps
+            prev = dec.total_rows
+        return n_steps
+
+    for _ in range(args.warmup):
+        one_pass(True)
+    torch.cuda.synchronize()
+    timings = {}
+    for cache in (True, False):
+        dec.timing = {} if cache else None
+        launches0 = sp.sprint_kernel_launches()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_steps = 0
+        reps = args.steps if cache else max(1, args.steps // 4)
+        with ClockSampler(str(local)) as clk:
+            barrier(world)
+            torch.cuda.synchronize()
+            a.record()
+            for _ in range(reps):
+                n_steps += one_pass(cache)
+            b.record()
+            torch.cuda.synchronize()
+        timings[cache] = (a.elapsed_time(b) / 1e3, n_steps, reps,
+                          sp.sprint_kernel_launches() - launches0, clk.summary(),
+                          dict(dec.timing or {}))
+    assert dec.status.item() == 0, f"device status {dec.status.item()}"
+    t, n_steps, reps, launches, clocks, stage = timings[True]
+    t_job = max_over_ranks(t, world, dev)
+    total = sum_over_ranks(n_steps, world, dev)
+    stage_ms = {k: statistics.mean(v) for k, v in stage.items()}
+    peaks, peak_kind = load_peaks()
+    ach = w.V * w.D * 2 / (stage_ms["lmhead_block"] / 1e3) / 1e9
+    t0, s0, r0, _, _, _ = timings[False]
+    out = {
+        "metric": METRIC, "value": total / t_job, "unit": "steps/s",
+        "tokens_per_s": reps * world * w.blocks * w.LB / t_job, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_job / reps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded; shapes and modality layout of the workload)",
+        "config": {"workload": w.name, "description": w.description, "blocks": w.blocks,
+                   "bench_step": f"all {w.blocks} blocks in order, prefix growing by LB",
+                   "prefix_confidence_cache": True,
+                   "parallelism": f"replicas x{world}, one sequence per GPU"},
+        "decode_steps_per_pass": n_steps / reps, "stages_ms": stage_ms,
+        "roofline": {"kernel": "lmhead_block", "bound": "hbm", "achieved": ach,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+                     "traffic": None, "peak_source": f"{peak_kind} (copy bandwidth)"},
+        "without_cache": {"ms_per_pass": 1e3 * t0 / r0, "steps_per_pass": s0 / r0,
+                          "speedup_of_cache": (t0 / r0) / (t / reps)},
+        "gpu_launches": launches, "clocks": clocks, "e2e": None,
+    }
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        dist.destroy_process_group()
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args):
     """The CPU oracle as the reference arm: each bench step is one bounded
@@ -607,7 +705,11 @@ def main(argv=None):
     if args.impl == "reference":
         run_reference(args)
     else:
-        run_ours(args)
+        from workload import WORKLOADS
+        if WORKLOADS[args.workload].blocks > 1:
+            run_sequential(args)
+        else:
+            run_ours(args)
 
 
 if __name__ == "__main__":

@@ -49,8 +49,10 @@ class PendingBlock:
 class BlockDecoder:
     """Buffers and call sequence for decoding blocks of S sequences.
 
-    prefix_lens[s] and modality_counts[s] = (n_text, n_image) describe the
-    prefixes the decoder will see; they fix every buffer size.
+    modality_counts[s] = (n_text, n_image) describes sequence s's prefix;
+    set_prefix() re-targets the decoder to new counts (for a prefix that
+    grows block by block) and decode(conf_from=...) reuses the confidences of
+    prefix rows that did not change.
     """
 
     def __init__(self, W, *, NL, Hq, Hkv, d, LB, T, tau, r_text, r_img, alpha=0.5,
@@ -63,44 +65,14 @@ class BlockDecoder:
         self.r_text, self.r_img, self.alpha = r_text, r_img, alpha
         self.V, self.D = W.shape
         self.S = S = len(modality_counts)
-        lens = [nt + ni for nt, ni in modality_counts]
-        kept = [sp.sprint_keep_count(nt, r_text) + sp.sprint_keep_count(ni, r_img)
-                for nt, ni in modality_counts]
-        self.prefix_off_host = [0]
-        self.kept_off_host = [0]
-        for n, k in zip(lens, kept):
-            self.prefix_off_host.append(self.prefix_off_host[-1] + n)
-            self.kept_off_host.append(self.kept_off_host[-1] + k)
-        self.total_rows = self.prefix_off_host[-1]
-        self.total_kept = self.kept_off_host[-1]
-        self.max_rows = max(lens) if lens else 0
-        self.max_kept = max(kept) if kept else 0
-        i32 = dict(dtype=torch.int32, device=self.dev)
-        self.prefix_off = torch.tensor(self.prefix_off_host, **i32)
-        self.kept_off = torch.tensor(self.kept_off_host, **i32)
-        f32 = dict(dtype=torch.float32, device=self.dev)
-        dt = sp.BF16 if self.dtype == torch.bfloat16 else sp.F32
         self.status = sp.new_status(self.dev)
-        # step-0 prefix pass
-        self.conf_prefix = torch.empty(self.total_rows, **f32)
-        self.argmax_prefix = torch.empty(self.total_rows, **i32)
-        self.ws_lm_prefix = torch.empty(
-            max(16, sp.sprint_lmhead_workspace_bytes(self.total_rows, self.D, self.V, dt)),
-            dtype=torch.uint8, device=self.dev)
-        self.kept_idx = torch.empty(self.total_kept, **i32)
-        self.score = torch.empty(self.total_rows, **f32)
-        self.ws_score = torch.empty(
-            max(16, sp.sprint_score_prune_workspace_bytes(S, self.total_rows)),
-            dtype=torch.uint8, device=self.dev)
-        row = NL * Hkv * d
-        self.Kp = torch.empty(self.total_kept * row, dtype=self.dtype, device=self.dev)
-        self.Vp = torch.empty(self.total_kept * row, dtype=self.dtype, device=self.dev)
+        self._cap = {}  # capacity tensors of the prefix-sized buffers
+        self.set_prefix(modality_counts)
+        dt = self._dt
+        i32 = dict(dtype=torch.int32, device=self.dev)
+        f32 = dict(dtype=torch.float32, device=self.dev)
         # per-step buffers
         self.O = torch.empty((S, NL, LB, Hq, d), dtype=self.dtype, device=self.dev)
-        self.ws_attn = torch.empty(
-            max(16, sp.sprint_block_attn_workspace_bytes(S, NL, LB, Hq, Hkv, d,
-                                                         self.max_rows, dt)),
-            dtype=torch.uint8, device=self.dev)
         self.conf_blk = torch.empty(S * LB, **f32)
         self.argmax_blk = torch.empty(S * LB, **i32)
         self.logits = (torch.empty((S * LB, self.V), dtype=self.dtype, device=self.dev)
@@ -128,6 +100,63 @@ class BlockDecoder:
         self._done = [torch.cuda.Event(), torch.cuda.Event()]
         self._slots = [None, None]
         self._next_slot = 0
+
+    def _buf(self, name, numel, dtype):
+        """A contiguous view of `numel` elements of a buffer that only grows
+        (a grown buffer keeps the old contents in its first elements, so the
+        prefix confidences survive a longer prefix)."""
+        t = self._cap.get(name)
+        if t is None or t.numel() < numel:
+            grown = torch.empty(max(int(numel), 1), dtype=dtype, device=self.dev)
+            if t is not None:
+                grown[:t.numel()].copy_(t)
+            t = grown
+            self._cap[name] = t
+        return t[:numel]
+
+    def set_prefix(self, modality_counts):
+        """(Re)target the decoder to prefixes with these (n_text, n_image)
+        counts per sequence (the number of sequences is fixed).  Buffers
+        sized by the prefix grow when needed and are otherwise reused, so a
+        prefix that grows block by block costs no reallocation once the
+        largest has been seen."""
+        if len(modality_counts) != self.S:
+            raise ValueError("set_prefix keeps the number of sequences")
+        S, NL, Hkv, d = self.S, self.NL, self.Hkv, self.d
+        self.modality_counts = [tuple(c) for c in modality_counts]
+        lens = [nt + ni for nt, ni in modality_counts]
+        kept = [sp.sprint_keep_count(nt, self.r_text) + sp.sprint_keep_count(ni, self.r_img)
+                for nt, ni in modality_counts]
+        self.prefix_off_host = [0]
+        self.kept_off_host = [0]
+        for n, k in zip(lens, kept):
+            self.prefix_off_host.append(self.prefix_off_host[-1] + n)
+            self.kept_off_host.append(self.kept_off_host[-1] + k)
+        self.total_rows = self.prefix_off_host[-1]
+        self.total_kept = self.kept_off_host[-1]
+        self.max_rows = max(lens) if lens else 0
+        self.max_kept = max(kept) if kept else 0
+        i32 = dict(dtype=torch.int32, device=self.dev)
+        self.prefix_off = torch.tensor(self.prefix_off_host, **i32)
+        self.kept_off = torch.tensor(self.kept_off_host, **i32)
+        dt = self._dt = sp.BF16 if self.dtype == torch.bfloat16 else sp.F32
+        u8 = torch.uint8
+        # step-0 prefix pass
+        self.conf_prefix = self._buf("conf_prefix", self.total_rows, torch.float32)
+        self.argmax_prefix = self._buf("argmax_prefix", self.total_rows, torch.int32)
+        self.ws_lm_prefix = self._buf(
+            "ws_lm_prefix",
+            max(16, sp.sprint_lmhead_workspace_bytes(self.total_rows, self.D, self.V, dt)), u8)
+        self.kept_idx = self._buf("kept_idx", self.total_kept, torch.int32)
+        self.score = self._buf("score", self.total_rows, torch.float32)
+        self.ws_score = self._buf(
+            "ws_score", max(16, sp.sprint_score_prune_workspace_bytes(S, self.total_rows)), u8)
+        row = NL * Hkv * d
+        self.Kp = self._buf("Kp", self.total_kept * row, self.dtype)
+        self.Vp = self._buf("Vp", self.total_kept * row, self.dtype)
+        self.ws_attn = self._buf(
+            "ws_attn", max(16, sp.sprint_block_attn_workspace_bytes(
+                S, NL, self.LB, self.Hq, Hkv, d, self.max_rows, dt)), u8)
 
     @contextlib.contextmanager
     def _stage(self, name):
@@ -160,13 +189,27 @@ class BlockDecoder:
         return self._step_events[slot]
 
     # -- the individual stages (each is one or two library calls) --------
-    def prefix_pass(self, K, V, H, theta, modality):
+    def prefix_pass(self, K, V, H, theta, modality, conf_from=0):
         """Step-0 scoring and pruning: confidences of every prefix row, the
-        kept set, and the pruned cache (self.Kp / self.Vp)."""
+        kept set, and the pruned cache (self.Kp / self.Vp).
+
+        conf_from > 0 (one sequence only): rows [0, conf_from) of H are the
+        rows of the previous call's prefix, unchanged, whose confidences are
+        still in self.conf_prefix; only rows [conf_from, n) go through the LM
+        head.  A row's confidence depends on that row alone.  While the whole
+        prefix stays below 4096 rows both ways of computing it use the same
+        vocabulary strips and fold order, so the result is bit-identical;
+        above that the full-prefix call folds wider strips and the two agree
+        to rounding."""
+        r0 = int(conf_from)
+        if r0:
+            if self.S != 1 or not 0 < r0 <= self.total_rows:
+                raise ValueError("conf_from needs one sequence and 0 < conf_from <= rows")
         with self._stage("lmhead_prefix"):
-            sp.sprint_lmhead_confidence(H, self.W, theta, conf=self.conf_prefix,
-                                        argmax=self.argmax_prefix, ws=self.ws_lm_prefix,
-                                        status=self.status)
+            if r0 < self.total_rows:
+                sp.sprint_lmhead_confidence(
+                    H[r0:], self.W, theta[r0:], conf=self.conf_prefix[r0:],
+                    argmax=self.argmax_prefix[r0:], ws=self.ws_lm_prefix, status=self.status)
         with self._stage("score_prune"):
             sp.sprint_score_prune(K, self.prefix_off, self.total_rows, self.NL, self.Hkv,
                                   self.d, self.conf_prefix, modality, self.alpha, self.r_text,
@@ -205,7 +248,7 @@ class BlockDecoder:
         self.ev.synchronize()
         return self.m_host.tolist()
 
-    def decode(self, prefix, steps, on_step=None, wait=True):
+    def decode(self, prefix, steps, on_step=None, wait=True, conf_from=0):
         """Decode one block.  prefix: dict K, V, H, theta, modality (device,
         sequences concatenated).  steps(t) -> dict Q, Kb, Vb, h, theta.
         With on_step (called after each step with (t, self)) the block is
@@ -216,13 +259,13 @@ class BlockDecoder:
         be pending; `pending.tokens` is the live token buffer, which the
         next block overwrites, so copy it (on the stream) before that."""
         if on_step is not None:
-            return self.decode_stepwise(prefix, steps, on_step)
+            return self.decode_stepwise(prefix, steps, on_step, conf_from=conf_from)
         slot = self._next_slot
         self._next_slot ^= 1
         if self._slots[slot] is not None:  # at most two blocks in flight
             self.finish(self._slots[slot])
         self.prefix_pass(prefix["K"], prefix["V"], prefix["H"], prefix["theta"],
-                         prefix["modality"])
+                         prefix["modality"], conf_from=conf_from)
         xs = [steps(t) for t in range(self.T)]
         events = self._events_for_steps(slot) if self.timing is not None else None
         sp.sprint_decode_steps(
@@ -271,13 +314,13 @@ class BlockDecoder:
             self._slots[pending.slot] = None
         return pending.result
 
-    def decode_stepwise(self, prefix, steps, on_step=None) -> BlockResult:
+    def decode_stepwise(self, prefix, steps, on_step=None, conf_from=0) -> BlockResult:
         """Decode one block one step at a time, reading the masked counts
         after every step (on_step(t, self) is called after each step)."""
         self.mask.fill_(1)
         self.tokens.fill_(-1)
         self.prefix_pass(prefix["K"], prefix["V"], prefix["H"], prefix["theta"],
-                         prefix["modality"])
+                         prefix["modality"], conf_from=conf_from)
         accepted = []
         prev = [self.LB] * self.S
         n_steps = 0

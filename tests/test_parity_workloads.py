@@ -139,3 +139,44 @@ def test_sequential_blocks(sp, block):
     assert torch.equal(pre["K"][:, :2048], first["K"])
     step_sets = [[step_inputs(w, 0, block, t, device=DEV) for t in range(w.T)]]
     _decode_and_check(sp, w, weights_of(w.name), [pre], step_sets, check_seqs=[0], tau=w.tau)
+
+
+def test_sequential_prefix_confidence_cache_is_bit_exact(sp):
+    """Block b+1's prefix is block b's plus the rows generated in between:
+    reusing block b's prefix confidences and sending only the new rows
+    through the LM head gives bit-identical confidences, kept set and
+    decoded tokens."""
+    from kv_cache_pruning_step_b300 import BlockDecoder
+    w = WORKLOADS["sequential-64-blocks"]
+    W, _ = weights_of(w.name)
+
+    def counts(p):
+        m = p["modality"]
+        return [(int((m == 0).sum()), int((m != 0).sum()))]
+
+    def steps_of(block):
+        xs = [step_inputs(w, 0, block, t, device=DEV) for t in range(w.T)]
+        return lambda t: {"Q": xs[t]["Q"][None].contiguous(), "Kb": xs[t]["Kb"][None].contiguous(),
+                          "Vb": xs[t]["Vb"][None].contiguous(), "h": xs[t]["h"],
+                          "theta": xs[t]["theta"]}
+
+    b = 20
+    pre_a = prefix_inputs(w, seq=0, block=b, device=DEV)
+    pre_b = prefix_inputs(w, seq=0, block=b + 1, device=DEV)
+    n_a = pre_a["modality"].numel()
+
+    def make(c):
+        return BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
+                            r_text=w.r_text, r_img=w.r_img, alpha=w.alpha, modality_counts=c)
+    dec = make(counts(pre_a))
+    dec.decode(pre_a, steps_of(b))
+    dec.set_prefix(counts(pre_b))  # grows: old confidences are kept
+    cached = dec.decode(pre_b, steps_of(b + 1), conf_from=n_a)
+    fresh_dec = make(counts(pre_b))
+    fresh = fresh_dec.decode(pre_b, steps_of(b + 1))
+    torch.cuda.synchronize()
+    assert dec.status.item() == 0 and fresh_dec.status.item() == 0
+    assert torch.equal(dec.conf_prefix, fresh_dec.conf_prefix)
+    assert torch.equal(dec.argmax_prefix, fresh_dec.argmax_prefix)
+    assert torch.equal(dec.kept_idx, fresh_dec.kept_idx)
+    assert cached.steps == fresh.steps and torch.equal(cached.tokens, fresh.tokens)
