@@ -45,6 +45,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the full-retention (r = 1) comparison runs")
+    ap.add_argument("--prefix-layout", default="compacted", choices=["compacted", "indexed"],
+                    help="later steps read a compacted copy of the kept rows, or the kept "
+                         "rows of the full cache through their indices")
     return ap.parse_args(argv)
 
 
@@ -304,8 +307,30 @@ def compare_full_retention(args, w, prefix, steps, counts, W, ms_block, later_ms
     from kv_cache_pruning_step_b300 import sprint as sp
     step_fn = lambda t: steps[t]  # noqa: E731
     reps = max(3, args.steps // 4)
+    indexed = args.prefix_layout == "indexed"
     out = {"sprint": {"r_text": w.r_text, "r_img": w.r_img, "mode": "adaptive",
+                      "prefix_layout": args.prefix_layout,
                       "ms_per_block": ms_block, "ms_per_later_step": later_ms}}
+    # The same SPRINT decode with the other layout of the pruned prefix.
+    other = "compacted" if indexed else "indexed"
+    dl = BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
+                      r_text=w.r_text, r_img=w.r_img, alpha=w.alpha, modality_counts=counts,
+                      indexed=not indexed)
+    dl.decode(prefix, step_fn)
+    torch.cuda.synchronize()
+    dl.timing = {}
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        dl.decode(prefix, step_fn)
+    b.record()
+    torch.cuda.synchronize()
+    assert dl.status.item() == 0, f"device status {dl.status.item()}"
+    out[f"sprint_{other}"] = {
+        "prefix_layout": other, "ms_per_block": a.elapsed_time(b) / reps,
+        "ms_per_later_step": _later_step_ms(dl),
+        "stages_ms": {k: statistics.mean(v) for k, v in dl.timing.items()}}
+    del dl
     r1_equal = None
     for mode_name, mode in (("adaptive", sp.UNMASK_ADAPTIVE), ("fixed", sp.UNMASK_FIXED)):
         d1 = BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
@@ -382,7 +407,8 @@ def run_ours(args):
     prefix = to_device(prefix_h, dev)
     steps = [to_device(x, dev) for x in steps_h]
     dec = BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
-                       r_text=w.r_text, r_img=w.r_img, alpha=w.alpha, modality_counts=counts)
+                       r_text=w.r_text, r_img=w.r_img, alpha=w.alpha, modality_counts=counts,
+                       indexed=args.prefix_layout == "indexed")
     step_fn = lambda t: steps[t]  # noqa: E731
 
     for _ in range(args.warmup):
@@ -552,6 +578,7 @@ def run_ours(args):
                    "LB": w.LB, "T": w.T, "tau": w.tau, "r_text": w.r_text, "r_img": w.r_img,
                    "alpha": w.alpha, "NL": w.NL, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "D": w.D,
                    "V": w.V, "bench_step": "one block decoded to completion",
+                   "prefix_layout": args.prefix_layout,
                    "l2": "inputs larger than L2 (K+V+W+H well above 126 MB)",
                    "parallelism": f"replicas x{world}, one sequence set per GPU"},
         "decode_steps_per_block": n_steps / args.steps,
@@ -601,7 +628,8 @@ def run_sequential(args):
                        "h": x["h"].to(dev), "theta": x["theta"].to(dev)} for x in xs])
     dec = BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
                        r_text=w.r_text, r_img=w.r_img, alpha=w.alpha,
-                       modality_counts=counts[-1])  # the largest: no buffer growth
+                       modality_counts=counts[-1],  # the largest: no buffer growth
+                       indexed=args.prefix_layout == "indexed")
 
     def one_pass(cache):
         n_steps, prev = 0, 0
@@ -650,7 +678,7 @@ def run_sequential(args):
         "dtype": "bf16", "data": "synthetic (seeded; shapes and modality layout of the workload)",
         "config": {"workload": w.name, "description": w.description, "blocks": w.blocks,
                    "bench_step": f"all {w.blocks} blocks in order, prefix growing by LB",
-                   "prefix_confidence_cache": True,
+                   "prefix_confidence_cache": True, "prefix_layout": args.prefix_layout,
                    "parallelism": f"replicas x{world}, one sequence per GPU"},
         "decode_steps_per_pass": n_steps / reps, "stages_ms": stage_ms,
         "roofline": {"kernel": "lmhead_block", "bound": "hbm", "achieved": ach,

@@ -16,6 +16,8 @@
  *   sprint_compact_kv         gather of the kept rows of K and V
  *   sprint_block_attn         bidirectional block attention over
  *                             [pruned prefix ; block]
+ *   sprint_block_attn_indexed the same, reading the kept rows of the full
+ *                             cache through the kept indices (no compaction)
  *   sprint_unmask             confidence-adaptive (or fixed) unmasking
  *
  * Conventions shared by every entry point
@@ -242,6 +244,43 @@ int sprint_block_attn(const void *Q, const void *Kp, const void *Vp,
                       int32_t *status, cudaStream_t stream);
 
 /*
+ * sprint_block_attn_indexed -- sprint_block_attn over the pruned prefix
+ * without the compacted copy: the kept rows are read from the full cache
+ * through the kept indices.  LLaDA2.0-Uni paper, Sparse Prefix Retention
+ * paragraph: later steps attend only to the retained prefix positions; this
+ * call computes exactly what sprint_compact_kv followed by sprint_block_attn
+ * computes (bit for bit on the same device), without writing Kp / Vp.
+ *
+ *   key i of sequence s (i < k_s = kept_off[s+1] - kept_off[s]) is prefix
+ *   row kept_idx[kept_off[s] + i] of that sequence, i.e. K[l] row
+ *   NL * prefix_off[s] + l * n_s + kept_idx[...] with n_s =
+ *   prefix_off[s+1] - prefix_off[s].
+ *
+ *   Q, Kb, Vb, O  as for sprint_block_attn
+ *   K, V          the full prefix cache, per sequence [NL][n_s][Hkv][d]
+ *   prefix_off    int32 [S+1] (device); total_rows = prefix_off[S] (host)
+ *   kept_idx      int32 [total_kept] (device), local to each sequence, as
+ *                 sprint_score_prune writes them (any order is accepted;
+ *                 the keys are summed in the order given); may be NULL
+ *                 when total_kept = 0
+ *   kept_off      int32 [S+1] (device); max_kept, total_kept (host)
+ *   ws            workspace of sprint_block_attn_workspace_bytes(S, NL, LB,
+ *                 Hq, Hkv, d, max_kept, dtype)
+ *
+ * Constraints as for sprint_block_attn; total_kept <= total_rows.
+ * Device status: SPRINT_STATUS_BAD_OFFSETS, SPRINT_STATUS_BAD_INDEX (an
+ * index outside [0, n_s): that key is read as zeros), SPRINT_STATUS_TIMEOUT.
+ */
+int sprint_block_attn_indexed(const void *Q, const void *K, const void *V,
+                              const int32_t *prefix_off, int total_rows,
+                              const int32_t *kept_idx, const int32_t *kept_off,
+                              int max_kept, int total_kept, const void *Kb,
+                              const void *Vb, int S, int NL, int LB, int Hq,
+                              int Hkv, int d, int dtype, void *O, void *ws,
+                              size_t ws_bytes, int32_t *status,
+                              cudaStream_t stream);
+
+/*
  * sprint_unmask -- one unmask decision per sequence.  LLaDA2.0-Uni paper,
  * Non-uniform Token Unmasking paragraph:
  *   ADAPTIVE  accept every masked position whose confidence exceeds tau
@@ -282,7 +321,9 @@ int sprint_unmask(const float *conf, const int32_t *argmax, uint8_t *mask,
  * once when all are zero (the block finished earlier).  Before step 0 the
  * call sets mask to 1 and tokens to -1 (cudaMemsetAsync).  The prefix pass
  * (prefix confidences, sprint_score_prune, sprint_compact_kv) is not part
- * of this call.
+ * of this call.  With kept_idx set, steps t >= 1 attend as
+ * sprint_block_attn_indexed does (kept rows of Kf / Vf read through
+ * kept_idx; Kp / Vp are ignored and may be NULL).
  *
  * Steps executed = 1 + the number of t in [1, T) with some m_hist[t-1][s]
  * > 0; the caller reads m_hist after synchronising.
@@ -310,6 +351,8 @@ int sprint_unmask(const float *conf, const int32_t *argmax, uint8_t *mask,
  *   events                                   NULL or a HOST array of 6*T
  *                                            cudaEvent_t: per step, start and
  *                                            end of attention, LM head, unmask
+ *   kept_idx                                 NULL, or int32 [total_kept]: the
+ *                                            indexed pruned prefix (t >= 1)
  * Returns the first non-zero code of the enqueued calls (nothing after it
  * is enqueued), SPRINT_ERR_INVALID_ARG for a missing field.
  */
@@ -339,6 +382,7 @@ typedef struct sprint_steps_args {
   size_t ws_lm_bytes;
   int32_t *status;
   void *const *events;
+  const int32_t *kept_idx;
 } sprint_steps_args;
 
 int sprint_decode_steps(const sprint_steps_args *args, cudaStream_t stream);

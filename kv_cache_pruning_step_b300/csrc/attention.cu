@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(256)
 attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ Kp, const T *__restrict__ Vp,
                  const int32_t *__restrict__ kv_off, int total_kv_rows,
                  const T *__restrict__ Kb, const T *__restrict__ Vb, int NL, int LB, int Hq,
-                 int Hkv, AttnWs ws, int32_t *status, Gate gate) {
+                 int Hkv, AttnWs ws, int32_t *status, KvIndex kvi, Gate gate) {
   constexpr int TK = 32;
   if (gate_closed(gate)) return;
   extern __shared__ float smem[];
@@ -47,6 +47,19 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ Kp, const T *__r
     for (int r = tid; r < R; r += 256) { out_ml[2 * r] = -INFINITY; out_ml[2 * r + 1] = 0.f; }
     for (int e = tid; e < R * D; e += 256) out_o[e] = 0.f;
     return;
+  }
+  // Rows of the prefix keys: contiguous from NL * o0 + l * kn, or (indexed)
+  // row idx[o0 + key] of layer l of the sequence's full prefix.
+  int pf0 = 0, n_full = 0;
+  if (kvi.idx) {
+    pf0 = kvi.prefix_off[s];
+    const int pf1 = kvi.prefix_off[s + 1];
+    if (pf0 < 0 || pf1 < pf0 || pf1 > kvi.total_prefix_rows) {
+      if (tid == 0 && chunk == 0) report(status, SPRINT_STATUS_BAD_OFFSETS);
+      pf0 = 0;
+    } else {
+      n_full = pf1 - pf0;
+    }
   }
   const int kn = o1 - o0, N = kn + LB;
   const int lo = chunk * ws.chunk_keys;
@@ -79,9 +92,17 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ Kp, const T *__r
       if (key < hi) {
         size_t at;
         if (key < kn) {
-          at = (((size_t)NL * o0 + (size_t)l * kn + key) * Hkv + g) * D + x;
-          kv = to_f32(Kp[at]);
-          vv = to_f32(Vp[at]);
+          size_t row = (size_t)NL * o0 + (size_t)l * kn + key;
+          bool ok = true;
+          if (kvi.idx) {
+            const int src = kvi.idx[o0 + key];
+            ok = src >= 0 && src < n_full;
+            if (!ok && x == 0) report(status, SPRINT_STATUS_BAD_INDEX);
+            row = (size_t)NL * pf0 + (size_t)l * n_full + (ok ? src : 0);
+          }
+          at = (row * Hkv + g) * D + x;
+          kv = ok ? to_f32(Kp[at]) : 0.f;
+          vv = ok ? to_f32(Vp[at]) : 0.f;
         } else {
           at = ((((size_t)s * NL + l) * LB + (key - kn)) * Hkv + g) * D + x;
           kv = to_f32(Kb[at]);
@@ -210,7 +231,7 @@ int sprint::block_attn_impl(const void *Q, const void *Kp, const void *Vp,
                             const int32_t *kv_off, int max_kv_rows, int total_kv_rows,
                             const void *Kb, const void *Vb, int S, int NL, int LB, int Hq,
                             int Hkv, int d, int dtype, void *O, void *ws, size_t ws_bytes,
-                            int32_t *status, Gate gate, cudaStream_t stream) {
+                            int32_t *status, KvIndex kvi, Gate gate, cudaStream_t stream) {
   if (S < 0 || NL < 1 || LB < 1 || Hq < 1 || Hkv < 1 || max_kv_rows < 0 || total_kv_rows < 0)
     return SPRINT_ERR_INVALID_ARG;
   if (dtype != SPRINT_F32 && dtype != SPRINT_BF16) return SPRINT_ERR_INVALID_ARG;
@@ -220,6 +241,8 @@ int sprint::block_attn_impl(const void *Q, const void *Kp, const void *Vp,
   if (S == 0) return SPRINT_OK;
   if (!Q || !kv_off || !Kb || !Vb || !O || !ws || !status) return SPRINT_ERR_INVALID_ARG;
   if (total_kv_rows > 0 && (!Kp || !Vp)) return SPRINT_ERR_INVALID_ARG;
+  if (kvi.idx && (!kvi.prefix_off || kvi.total_prefix_rows < total_kv_rows))
+    return SPRINT_ERR_INVALID_ARG;
   if (ws_bytes < sprint_block_attn_workspace_bytes(S, NL, LB, Hq, Hkv, d, max_kv_rows, dtype))
     return SPRINT_ERR_WORKSPACE;
   if (dtype == SPRINT_BF16) {
@@ -231,7 +254,7 @@ int sprint::block_attn_impl(const void *Q, const void *Kp, const void *Vp,
                            static_cast<const __nv_bfloat16 *>(Vp), kv_off, total_kv_rows,
                            static_cast<const __nv_bfloat16 *>(Kb),
                            static_cast<const __nv_bfloat16 *>(Vb), S, NL, LB, Hq, Hkv, d, O, ws,
-                           status, gate, stream);
+                           status, kvi, gate, stream);
   }
   const int ck = attn_chunk_policy(S, NL, Hkv, LB, max_kv_rows);
   const AttnWs w = attn_ws_layout(ws, S, NL, LB, Hq, Hkv, d, max_kv_rows, ck);
@@ -245,14 +268,14 @@ int sprint::block_attn_impl(const void *Q, const void *Kp, const void *Vp,
       attn_simt_kernel<float, 64><<<grid, 256, sm, stream>>>(
           static_cast<const float *>(Q), static_cast<const float *>(Kp),
           static_cast<const float *>(Vp), kv_off, total_kv_rows, static_cast<const float *>(Kb),
-          static_cast<const float *>(Vb), NL, LB, Hq, Hkv, w, status, gate);
+          static_cast<const float *>(Vb), NL, LB, Hq, Hkv, w, status, kvi, gate);
     } else {
       cudaFuncSetAttribute(attn_simt_kernel<float, 128>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
       attn_simt_kernel<float, 128><<<grid, 256, sm, stream>>>(
           static_cast<const float *>(Q), static_cast<const float *>(Kp),
           static_cast<const float *>(Vp), kv_off, total_kv_rows, static_cast<const float *>(Kb),
-          static_cast<const float *>(Vb), NL, LB, Hq, Hkv, w, status, gate);
+          static_cast<const float *>(Vb), NL, LB, Hq, Hkv, w, status, kvi, gate);
     }
     if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   }
@@ -269,5 +292,22 @@ extern "C" int sprint_block_attn(const void *Q, const void *Kp, const void *Vp,
                                  int Hkv, int d, int dtype, void *O, void *ws, size_t ws_bytes,
                                  int32_t *status, cudaStream_t stream) {
   return block_attn_impl(Q, Kp, Vp, kv_off, max_kv_rows, total_kv_rows, Kb, Vb, S, NL, LB, Hq,
-                         Hkv, d, dtype, O, ws, ws_bytes, status, Gate{nullptr, 0}, stream);
+                         Hkv, d, dtype, O, ws, ws_bytes, status, KvIndex{nullptr, nullptr, 0},
+                         Gate{nullptr, 0}, stream);
+}
+
+extern "C" int sprint_block_attn_indexed(const void *Q, const void *K, const void *V,
+                                         const int32_t *prefix_off, int total_rows,
+                                         const int32_t *kept_idx, const int32_t *kept_off,
+                                         int max_kept, int total_kept, const void *Kb,
+                                         const void *Vb, int S, int NL, int LB, int Hq, int Hkv,
+                                         int d, int dtype, void *O, void *ws, size_t ws_bytes,
+                                         int32_t *status, cudaStream_t stream) {
+  if ((!kept_idx && total_kept > 0) || !prefix_off || total_rows < 0)
+    return SPRINT_ERR_INVALID_ARG;
+  // Nothing kept: only the block's own keys, as in the contiguous layout.
+  const KvIndex kvi = total_kept > 0 ? KvIndex{kept_idx, prefix_off, total_rows}
+                                     : KvIndex{nullptr, nullptr, 0};
+  return block_attn_impl(Q, K, V, kept_off, max_kept, total_kept, Kb, Vb, S, NL, LB, Hq, Hkv, d,
+                         dtype, O, ws, ws_bytes, status, kvi, Gate{nullptr, 0}, stream);
 }

@@ -39,6 +39,17 @@
 //               exp2(S * log2e/sqrt(d) - m_h) as bf16 pairs over the first 64
 //               columns of S_h, where the PV product reads it.  At the end of
 //               the segment each warpgroup writes its (O_h, m_h, l_h) partial.
+//
+// Indexed prefix (no compacted copy): the kept rows are gathered from the
+// full cache through the kept indices.  Then warps 0 and 11 each load half
+// of a prefix tile with 16-byte cp.async copies (a 256-byte head row per 16
+// lanes) into the same 128-byte-swizzled layout the TMA writes; each lane
+// waits for its own copies and fences them for the tensor cores (generic to
+// async proxy), and lane 0 of each warp arrives on the stage's full barrier.
+// With three or more stages a warp does not wait for tile q's copies right
+// after issuing them: it arrives for tile q once it has issued the first
+// quarter of tile q+1 (the stage of q+1 frees when the PV of tile q-2 ends,
+// which is also when the QK of tile q may start).
 #include <cuda.h>
 #include <math.h>
 
@@ -60,6 +71,10 @@ constexpr int TILE = 128;       // keys per tile
 constexpr int MAX_STAGES = 4;   // K/V ring depth at most (as many as fit)
 constexpr int ROWS = 128;       // query rows per MMA tile (LB x G <= 128)
 constexpr int THREADS = 352;
+// The indexed-prefix kernel adds a second gathering warp; 384 threads still
+// leave 168 registers per thread.
+constexpr int GATHER_WARP = 11;
+constexpr int THREADS_INDEXED = 384;
 constexpr int MAX_SEQ = 1024;   // sequences per call on this path
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
@@ -97,6 +112,8 @@ struct Problem {
   int stall_test;               // failure-path test: the MMA role stalls first
   Gate gate;                    // step gate of the native block driver
   int stages;                   // K/V ring stages of this launch (2..MAX_STAGES)
+  KvIndex kvi;                  // indexed prefix (kvi.idx != nullptr): gathered
+  const __nv_bfloat16 *Kf, *Vf; // from these full caches
 };
 
 // Per-sequence tables: ts[s] = first global tile of sequence s; nt[s] =
@@ -163,6 +180,19 @@ __device__ __forceinline__ Seg locate(const Problem &pb, const int *ts, const in
   return sg;
 }
 
+// 16-byte global -> shared copy (L2 only); src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
@@ -213,8 +243,8 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
-template <int D>
-__global__ void __launch_bounds__(THREADS, 1)
+template <int D, bool kIndexed>
+__global__ void __launch_bounds__(kIndexed ? THREADS_INDEXED : THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
                const __grid_constant__ CUtensorMap tm_vp,
                const __grid_constant__ CUtensorMap tm_kb,
@@ -247,14 +277,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   // Zero the query and K/V buffers once: rows TMA never writes (query rows
   // >= R, key rows past a short tile) then hold finite values.
-  for (int i = threadIdx.x * 16; i < off_bar; i += THREADS * 16)
+  for (int i = threadIdx.x * 16; i < off_bar; i += (int)blockDim.x * 16)
     *reinterpret_cast<uint4 *>(smem + i) = make_uint4(0, 0, 0, 0);
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   build_seq_tables(pb, ts, nt, ks, k0, pb.status);
   if (threadIdx.x == 0) {
     tc::mbar_init(tc::smem_u32(q_full), 1);
     for (int i = 0; i < MAX_STAGES; ++i) {
-      tc::mbar_init(tc::smem_u32(kv_full + i), 1);
+      tc::mbar_init(tc::smem_u32(kv_full + i), kIndexed ? 2 : 1);  // one per producer warp
       tc::mbar_init(tc::smem_u32(kv_empty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -295,7 +325,124 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     x += sg.ntile;
     const int np = (sg.k_s + TILE - 1) / TILE;  // prefix tiles of the pair
     const bool run = !*abort_flag;
-    if (warp == 0 && lane == 0 && run) {
+    if (kIndexed && (warp == 0 || warp == GATHER_WARP) && run) {
+      // ------------------------------------------------ producers, indexed prefix
+      // Warps 0 and GATHER_WARP each gather half of a prefix tile's rows
+      // (gw = 0: rows 0-63, gw = 1: rows 64-127) and each arrive once on
+      // the stage's full barrier (count 2); lane 0 of warp 0 also loads Q
+      // and the block's own key tiles by TMA.
+      const int gw = warp == 0 ? 0 : 1;
+      if (gw == 0 && lane == 0) {
+        const uint32_t qb = tc::smem_u32(q_full);
+        tc::mbar_arrive_expect_tx(qb, (uint32_t)((D / 64) * R * 128));
+        const int qrow = (sg.s * pb.NL + sg.l) * pb.LB;
+        for (int b = 0; b < D / 64; ++b)
+          tc::tma_load_3d(sQ + b * L::QBOX, &tm_q, qb, b * 64, sg.g * GQ, qrow);
+      }
+      q_issued = 1;
+      q_par = seg_no & 1;
+      // The sequence's full prefix: rows [pf0, pf1) of every layer.
+      int pf0 = __ldg(pb.kvi.prefix_off + sg.s), pf1 = __ldg(pb.kvi.prefix_off + sg.s + 1);
+      if (pf0 < 0 || pf1 < pf0 || pf1 > pb.kvi.total_prefix_rows) {
+        if (lane == 0 && gw == 0) report(pb.status, SPRINT_STATUS_BAD_OFFSETS);
+        pf0 = pf1 = 0;
+      }
+      const int n_full = pf1 - pf0;
+      constexpr int CH = D / 8, RPI = 32 / CH;  // 16-byte chunks per row, rows per pass
+      const int sub = lane / CH, c16 = lane % CH;
+      const int chunk = c16 & 7;
+      // This lane's chunk of row 0 of (layer l, KV head g) of the sequence
+      // (row 0 is a valid address whenever the sequence has prefix rows).
+      const size_t lane_off =
+          n_full ? ((size_t)pb.NL * pf0 + (size_t)sg.l * n_full) * ((size_t)pb.Hkv * D) +
+                       (size_t)sg.g * D + (size_t)c16 * 8
+                 : 0;
+      const __nv_bfloat16 *kl = pb.Kf + lane_off, *vl = pb.Vf + lane_off;
+      const uint32_t row_bytes = (uint32_t)pb.Hkv * D * 2;
+      // Shared-memory offset of this lane's chunk in row 64 gw + j RPI + sub:
+      // box (c16 / 8), row, and the 128-byte swizzle (chunk ^ (row % 8)),
+      // where row % 8 = (j RPI % 8 + sub) % 8 takes 8 / RPI values.
+      uint32_t xo[8 / RPI];
+#pragma unroll
+      for (int m = 0; m < 8 / RPI; ++m)
+        xo[m] = (c16 >> 3) * L::KBOX + (64 * gw + sub) * 128 +
+                ((chunk ^ ((m * RPI + sub) & 7)) << 4);
+      const int lag = stages >= 3 ? 1 : 0;  // gathered tiles whose arrival is deferred
+      int pend_stage = -1;                  // the deferred tile's stage
+      auto arrive_pending = [&](bool all) {
+        if (pend_stage < 0) return;
+        if (all) cp_async_wait<0>(); else cp_async_wait<1>();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(kv_full + pend_stage));
+        pend_stage = -1;
+      };
+      for (int t = 0; t < sg.ntile; ++t) {
+        const uint32_t q = tile_no + t;
+        const int stage = q % stages;
+        const uint32_t ph = (q / stages) & 1;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(tc::smem_u32(kv_empty + stage), ph ^ 1,
+                                                   pb.cap_ns, abort_flag)))
+          break;
+        const int i = sg.first_tile + t;
+        const uint32_t kdst = sKV + stage * L::STAGE, vdst = kdst + L::K_BYTES;
+        if (i < np) {
+          // Kept indices of this warp's 64 rows: row 64 gw + lane in ixa,
+          // row 64 gw + 32 + lane in ixb; -1 past the tile's keys or for an
+          // index outside the sequence's prefix (reported).
+          const int nvalid = min(TILE, sg.k_s - i * TILE) - 64 * gw;
+          const int32_t *ip = pb.kvi.idx + sg.kv0 + i * TILE + 64 * gw;
+          int ixa = lane < nvalid ? __ldg(ip + lane) : -1;
+          int ixb = lane + 32 < nvalid ? __ldg(ip + lane + 32) : -1;
+          const bool bad = (lane < nvalid && (ixa < 0 || ixa >= n_full)) ||
+                           (lane + 32 < nvalid && (ixb < 0 || ixb >= n_full));
+          if (ixa >= n_full) ixa = -1;
+          if (ixb >= n_full) ixb = -1;
+          if (__any_sync(0xffffffffu, bad) && lane == 0)
+            report(pb.status, SPRINT_STATUS_BAD_INDEX);
+          // Rows [32 p, 32 p + 32) of this warp's half, as one copy group.
+          auto issue_rows = [&](int p) {
+#pragma unroll
+            for (int jj = 0; jj < 32 / RPI; ++jj) {
+              const int j = p * (32 / RPI) + jj;
+              const int src = __shfl_sync(0xffffffffu, p ? ixb : ixa, (jj * RPI + sub) & 31);
+              const uint32_t n = src >= 0 ? 16u : 0u;
+              const size_t go = (size_t)(uint32_t)max(src, 0) * row_bytes;
+              const uint32_t so = xo[((j * RPI) & 7) / RPI] + j * RPI * 128;
+              cp_async16(kdst + so, reinterpret_cast<const char *>(kl) + go, n);
+              cp_async16(vdst + so, reinterpret_cast<const char *>(vl) + go, n);
+            }
+            cp_async_commit();
+          };
+          // The deferred arrival of the previous gathered tile comes after
+          // the first group of this one (only that group may still be in
+          // flight), so the QK of that tile waits for a quarter tile's
+          // issue, not a whole one.
+          issue_rows(0);
+          if (lag) arrive_pending(false);
+          issue_rows(1);
+          pend_stage = stage;
+          if (!lag) arrive_pending(true);
+          issued &= ~(1u << stage);  // nothing of the TMA in flight on this stage
+        } else {
+          arrive_pending(true);
+          const uint32_t fb = tc::smem_u32(kv_full + stage);
+          if (gw == 0 && lane == 0) {
+            const int z = (sg.s * pb.NL + sg.l) * pb.LB + (i - np) * TILE;
+            tc::mbar_arrive_expect_tx(fb, (uint32_t)(2 * (D / 64) * BR * 128));
+            for (int b = 0; b < D / 64; ++b) {
+              tc::tma_load_3d(kdst + b * L::KBOX, &tm_kb, fb, b * 64, sg.g, z);
+              tc::tma_load_3d(vdst + b * L::KBOX, &tm_vb, fb, b * 64, sg.g, z);
+            }
+          } else if (gw == 1 && lane == 0) {
+            tc::mbar_arrive(fb);  // the second of the barrier's two arrivals
+          }
+          issued |= 1u << stage;
+          last_par = (last_par & ~(1u << stage)) | (ph << stage);
+        }
+      }
+      arrive_pending(true);
+    } else if (warp == 0 && lane == 0 && run) {
       // ------------------------------------------------ producer
       const uint32_t qb = tc::smem_u32(q_full);
       tc::mbar_arrive_expect_tx(qb, (uint32_t)((D / 64) * R * 128));
@@ -536,6 +683,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   // Drain: no copy or MMA of this CTA may be in flight when it exits.  These
   // waits ignore the abort flag and use the longer drain limit.
+  if (kIndexed && (warp == 0 || warp == GATHER_WARP))
+    asm volatile("cp.async.wait_all;" ::: "memory");
   if (warp == 0 && lane == 0) {
     volatile int no_abort = 0;
     if (q_issued) tc::mbar_wait(tc::smem_u32(q_full), q_par, pb.drain_ns, &no_abort);
@@ -655,7 +804,7 @@ template <int D>
 int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 *Vp,
            const int32_t *kv_off, int total_kv_rows, const __nv_bfloat16 *Kb,
            const __nv_bfloat16 *Vb, int S, int NL, int LB, int Hq, int Hkv, void *O, void *ws,
-           int32_t *status, Gate gate, cudaStream_t stream) {
+           int32_t *status, KvIndex kvi, Gate gate, cudaStream_t stream) {
   using Lt = Layout<D>;
   const int GQ = Hq / Hkv;
   CUtensorMap tq, tkp, tvp, tkb, tvb;
@@ -664,11 +813,11 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
   if (!make_tmap_3d(&tq, Q, D, Hq, brows, GQ, LB) || !make_tmap_3d(&tkb, Kb, D, Hkv, brows, 1, BR) ||
       !make_tmap_3d(&tvb, Vb, D, Hkv, brows, 1, BR))
     return SPRINT_ERR_CUDA;
-  if (total_kv_rows > 0) {
+  if (total_kv_rows > 0 && !kvi.idx) {
     if (!make_tmap_3d(&tkp, Kp, D, Hkv, (uint64_t)NL * total_kv_rows, 1, TILE) ||
         !make_tmap_3d(&tvp, Vp, D, Hkv, (uint64_t)NL * total_kv_rows, 1, TILE))
       return SPRINT_ERR_CUDA;
-  } else {  // no prefix rows at all: never dereferenced
+  } else {  // no contiguous prefix rows: never dereferenced
     tkp = tkb;
     tvp = tvb;
   }
@@ -679,7 +828,11 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
             cudaSuccess ||
-        cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(attn_tc_kernel<D, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - 256) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_tc_kernel<D, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              optin - 256) != cudaSuccess) {
       optin = 0;
       return SPRINT_ERR_CUDA;
@@ -704,7 +857,13 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
   pb.stall_test = stall_test_enabled();
   pb.gate = gate;
   pb.stages = stages;
-  attn_tc_kernel<D><<<G, THREADS, smem, stream>>>(tq, tkp, tvp, tkb, tvb, pb);
+  pb.kvi = kvi;
+  pb.Kf = kvi.idx ? Kp : nullptr;
+  pb.Vf = kvi.idx ? Vp : nullptr;
+  if (kvi.idx)
+    attn_tc_kernel<D, true><<<G, THREADS_INDEXED, smem, stream>>>(tq, tkp, tvp, tkb, tvb, pb);
+  else
+    attn_tc_kernel<D, false><<<G, THREADS, smem, stream>>>(tq, tkp, tvp, tkb, tvb, pb);
   if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   const long long warps = (long long)pairs * LB * GQ;
   attn_tc_combine_kernel<D><<<(int)((warps * 32 + 255) / 256), 256, 0, stream>>>(
@@ -722,12 +881,13 @@ size_t attn_tc_workspace_bytes(int S, int NL, int Hkv, int d) {
 int attn_tc_forward(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 *Vp,
                     const int32_t *kv_off, int total_kv_rows, const __nv_bfloat16 *Kb,
                     const __nv_bfloat16 *Vb, int S, int NL, int LB, int Hq, int Hkv, int d,
-                    void *O, void *ws, int32_t *status, Gate gate, cudaStream_t stream) {
+                    void *O, void *ws, int32_t *status, KvIndex kvi, Gate gate,
+                    cudaStream_t stream) {
   if (S > MAX_SEQ) return SPRINT_ERR_UNSUPPORTED;
   return d == 64 ? launch<64>(Q, Kp, Vp, kv_off, total_kv_rows, Kb, Vb, S, NL, LB, Hq, Hkv, O,
-                              ws, status, gate, stream)
+                              ws, status, kvi, gate, stream)
                  : launch<128>(Q, Kp, Vp, kv_off, total_kv_rows, Kb, Vb, S, NL, LB, Hq, Hkv, O,
-                               ws, status, gate, stream);
+                               ws, status, kvi, gate, stream);
 }
 
 }  // namespace sprint

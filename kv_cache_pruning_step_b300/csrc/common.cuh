@@ -153,6 +153,17 @@ __device__ __forceinline__ bool gate_closed(const Gate &g) {
   return closed_sh != 0;
 }
 
+// Prefix keys read through an index instead of a compacted copy: key i of
+// sequence s is row idx[kv_off[s] + i] of that sequence's full prefix, which
+// starts at row prefix_off[s] of the full K / V and has prefix_off[s+1] -
+// prefix_off[s] rows.  idx == nullptr: the prefix keys are stored
+// contiguously (a compacted or full cache located by kv_off).
+struct KvIndex {
+  const int32_t *idx;
+  const int32_t *prefix_off;
+  int total_prefix_rows;
+};
+
 // Entry points with a step gate, shared by the C ABI (gate open) and the
 // native block driver.
 int lmhead_confidence_impl(const void *h, const void *W, const float *temp, int M, int D, int V,
@@ -162,7 +173,8 @@ int lmhead_confidence_impl(const void *h, const void *W, const float *temp, int 
 int block_attn_impl(const void *Q, const void *Kp, const void *Vp, const int32_t *kv_off,
                     int max_kv_rows, int total_kv_rows, const void *Kb, const void *Vb, int S,
                     int NL, int LB, int Hq, int Hkv, int d, int dtype, void *O, void *ws,
-                    size_t ws_bytes, int32_t *status, Gate gate, cudaStream_t stream);
+                    size_t ws_bytes, int32_t *status, KvIndex kvi, Gate gate,
+                    cudaStream_t stream);
 int unmask_impl(const float *conf, const int32_t *argmax, uint8_t *mask, int32_t *tokens,
                 int32_t *m_out, int S, int LB, int t, int T, float tau, int mode,
                 uint8_t *accepted_out, int32_t *status, Gate gate, cudaStream_t stream);

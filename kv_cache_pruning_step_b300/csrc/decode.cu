@@ -37,14 +37,17 @@ extern "C" int sprint_decode_steps(const sprint_steps_args *a, cudaStream_t stre
     return SPRINT_ERR_CUDA;
   for (int t = 0; t < a->T; ++t) {
     const Gate gate = t == 0 ? Gate{nullptr, 0} : Gate{a->m_hist + (size_t)(t - 1) * S, S};
-    const bool full = t == 0;
+    const bool full = t == 0, indexed = !full && a->kept_idx;
+    const KvIndex kvi = indexed ? KvIndex{a->kept_idx, a->prefix_off, a->total_rows}
+                                : KvIndex{nullptr, nullptr, 0};
     int rc = record(a->events, 6 * t + 0, stream);
     if (rc == SPRINT_OK)
-      rc = block_attn_impl(a->Q[t], full ? a->Kf : a->Kp, full ? a->Vf : a->Vp,
-                           full ? a->prefix_off : a->kept_off, full ? a->max_rows : a->max_kept,
+      rc = block_attn_impl(a->Q[t], full || indexed ? a->Kf : a->Kp,
+                           full || indexed ? a->Vf : a->Vp, full ? a->prefix_off : a->kept_off,
+                           full ? a->max_rows : a->max_kept,
                            full ? a->total_rows : a->total_kept, a->Kb[t], a->Vb[t], S, a->NL,
                            LB, a->Hq, a->Hkv, a->d, a->dtype, a->O, a->ws_attn,
-                           a->ws_attn_bytes, a->status, gate, stream);
+                           a->ws_attn_bytes, a->status, kvi, gate, stream);
     if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 1, stream);
     if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 2, stream);
     if (rc == SPRINT_OK)

@@ -53,16 +53,21 @@ class BlockDecoder:
     set_prefix() re-targets the decoder to new counts (for a prefix that
     grows block by block) and decode(conf_from=...) reuses the confidences of
     prefix rows that did not change.
+
+    indexed=True: no pruned copy of the cache is made; the steps after the
+    first read the kept rows of the full cache through the kept indices
+    (sprint_block_attn_indexed), with the same result.
     """
 
     def __init__(self, W, *, NL, Hq, Hkv, d, LB, T, tau, r_text, r_img, alpha=0.5,
-                 mode=sp.UNMASK_ADAPTIVE, modality_counts, want_logits=False):
+                 mode=sp.UNMASK_ADAPTIVE, modality_counts, want_logits=False, indexed=False):
         self.W = W
         self.dev = W.device
         self.dtype = W.dtype
         self.NL, self.Hq, self.Hkv, self.d = NL, Hq, Hkv, d
         self.LB, self.T, self.tau, self.mode = LB, T, tau, mode
         self.r_text, self.r_img, self.alpha = r_text, r_img, alpha
+        self.indexed = bool(indexed)
         self.V, self.D = W.shape
         self.S = S = len(modality_counts)
         self.status = sp.new_status(self.dev)
@@ -152,8 +157,11 @@ class BlockDecoder:
         self.ws_score = self._buf(
             "ws_score", max(16, sp.sprint_score_prune_workspace_bytes(S, self.total_rows)), u8)
         row = NL * Hkv * d
-        self.Kp = self._buf("Kp", self.total_kept * row, self.dtype)
-        self.Vp = self._buf("Vp", self.total_kept * row, self.dtype)
+        if self.indexed:
+            self.Kp = self.Vp = None
+        else:
+            self.Kp = self._buf("Kp", self.total_kept * row, self.dtype)
+            self.Vp = self._buf("Vp", self.total_kept * row, self.dtype)
         self.ws_attn = self._buf(
             "ws_attn", max(16, sp.sprint_block_attn_workspace_bytes(
                 S, NL, self.LB, self.Hq, Hkv, d, self.max_rows, dt)), u8)
@@ -191,7 +199,8 @@ class BlockDecoder:
     # -- the individual stages (each is one or two library calls) --------
     def prefix_pass(self, K, V, H, theta, modality, conf_from=0):
         """Step-0 scoring and pruning: confidences of every prefix row, the
-        kept set, and the pruned cache (self.Kp / self.Vp).
+        kept set, and the pruned cache (self.Kp / self.Vp; not made when the
+        decoder reads the kept rows through their indices).
 
         conf_from > 0 (one sequence only): rows [0, conf_from) of H are the
         rows of the previous call's prefix, unchanged, whose confidences are
@@ -216,18 +225,28 @@ class BlockDecoder:
                                   self.r_img, self.kept_off, self.total_kept,
                                   kept_idx=self.kept_idx, score=self.score, ws=self.ws_score,
                                   status=self.status)
+        if self.indexed:
+            return
         with self._stage("compact"):
             sp.sprint_compact_kv(K, V, self.prefix_off, self.total_rows, self.NL, self.Hkv,
                                  self.d, self.kept_idx, self.kept_off, self.total_kept,
                                  Kp=self.Kp, Vp=self.Vp, status=self.status)
 
-    def step(self, t, x, K=None, V=None):
-        """One denoising step; K/V given = attend to the full prefix."""
-        if K is not None:
+    def step(self, t, x, K, V):
+        """One denoising step.  K, V: the full prefix cache; step 0 attends
+        to all of it, later steps to the kept rows (the pruned copy, or K / V
+        read through the kept indices)."""
+        if t == 0:
             with self._stage("attn_full"):
                 sp.sprint_block_attn(x["Q"], K, V, self.prefix_off, self.max_rows,
                                      self.total_rows, x["Kb"], x["Vb"], O=self.O,
                                      ws=self.ws_attn, status=self.status)
+        elif self.indexed:
+            with self._stage("attn_pruned"):
+                sp.sprint_block_attn_indexed(x["Q"], K, V, self.prefix_off, self.total_rows,
+                                             self.kept_idx, self.kept_off, self.max_kept,
+                                             self.total_kept, x["Kb"], x["Vb"], O=self.O,
+                                             ws=self.ws_attn, status=self.status)
         else:
             with self._stage("attn_pruned"):
                 sp.sprint_block_attn(x["Q"], self.Kp, self.Vp, self.kept_off, self.max_kept,
@@ -277,7 +296,8 @@ class BlockDecoder:
             W=self.W, T=self.T, tau=self.tau, mode=self.mode, O=self.O, conf=self.conf_blk,
             argmax=self.argmax_blk, mask=self.mask, tokens=self.tokens, m_hist=self.m_hist,
             ws_attn=self.ws_attn, ws_lm=self.ws_lm_blk, status=self.status,
-            logits=self.logits, events=events)
+            logits=self.logits, events=events,
+            kept_idx=self.kept_idx if self.indexed else None)
         m_host = self._m_hist_host[slot]
         m_host.copy_(self.m_hist, non_blocking=True)
         done = self._done[slot]
@@ -325,11 +345,7 @@ class BlockDecoder:
         prev = [self.LB] * self.S
         n_steps = 0
         for t in range(self.T):
-            x = steps(t)
-            if t == 0:
-                self.step(0, x, prefix["K"], prefix["V"])
-            else:
-                self.step(t, x)
+            self.step(t, steps(t), prefix["K"], prefix["V"])
             n_steps += 1
             if on_step is not None:
                 on_step(t, self)

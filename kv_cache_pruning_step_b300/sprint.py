@@ -44,6 +44,8 @@ SIGNATURES = {
     "sprint_block_attn_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "sprint_block_attn": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
                                _P, _Z, _P, _P]),
+    "sprint_block_attn_indexed": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _P, _P, _I, _I, _I,
+                                       _I, _I, _I, _I, _P, _P, _Z, _P, _P]),
     "sprint_unmask": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
     "sprint_decode_steps": (_I, [_P, _P]),
 }
@@ -63,7 +65,7 @@ class StepsArgs(ctypes.Structure):
         ("tokens", _P), ("m_hist", _P), ("accepted", _P),
         ("ws_attn", _P), ("ws_attn_bytes", ctypes.c_size_t),
         ("ws_lm", _P), ("ws_lm_bytes", ctypes.c_size_t),
-        ("status", _P), ("events", _P),
+        ("status", _P), ("events", _P), ("kept_idx", _P),
     ]
 
 
@@ -268,6 +270,30 @@ def sprint_block_attn(Q, Kp, Vp, kv_off, max_kv_rows, total_kv_rows, Kb, Vb, *, 
     return O
 
 
+def sprint_block_attn_indexed(Q, K, V, prefix_off, total_rows, kept_idx, kept_off, max_kept,
+                              total_kept, Kb, Vb, *, O=None, ws=None, status=None, stream=None):
+    """Block attention over the kept rows of the full cache K / V, read
+    through kept_idx (no compacted copy); same output as sprint_compact_kv
+    followed by sprint_block_attn."""
+    S, NL, LB, Hq, d = Q.shape
+    Hkv = Kb.shape[3]
+    dev = Q.device
+    dt = _dtype_code(Q)
+    O = torch.empty_like(Q) if O is None else O
+    status = new_status(dev) if status is None else status
+    ws = _ws(ws, sprint_block_attn_workspace_bytes(S, NL, LB, Hq, Hkv, d, int(max_kept), dt),
+             dev)
+    rc = lib.sprint_block_attn_indexed(
+        _ptr(Q, Q.dtype, "Q"), _ptr(K, Q.dtype, "K"), _ptr(V, Q.dtype, "V"),
+        _ptr(prefix_off, torch.int32, "prefix_off"), int(total_rows),
+        _ptr(kept_idx, torch.int32, "kept_idx"), _ptr(kept_off, torch.int32, "kept_off"),
+        int(max_kept), int(total_kept), _ptr(Kb, Q.dtype, "Kb"), _ptr(Vb, Q.dtype, "Vb"),
+        S, NL, LB, Hq, Hkv, d, dt, _ptr(O, Q.dtype, "O"), _ptr(ws), ws.numel(),
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "sprint_block_attn_indexed")
+    return O
+
+
 def sprint_unmask(conf, argmax, mask, tokens, t, T, tau, mode=UNMASK_ADAPTIVE, *, m_out=None,
                   accepted=None, status=None, stream=None):
     """One unmask step in place on mask/tokens ([S][LB]); returns (m_out, accepted)."""
@@ -296,12 +322,13 @@ def _ptr_array(tensors, dtype, name):
 def sprint_decode_steps(*, Q, Kb, Vb, h, theta, Kf, Vf, prefix_off, max_rows, total_rows,
                         Kp, Vp, kept_off, max_kept, total_kept, W, T, tau, mode, O, conf,
                         argmax, mask, tokens, m_hist, ws_attn, ws_lm, status, accepted=None,
-                        logits=None, events=None, stream=None):
+                        logits=None, events=None, kept_idx=None, stream=None):
     """Every denoising step of one block in one call (see include/sprint.h).
 
     Q, Kb, Vb: lists of T tensors [S][NL][LB][*][d]; h: list of T [S*LB][D];
     theta: list of T [S*LB] fp32 or None.  m_hist: int32 [T][S] (out);
-    events: list of 6*T torch.cuda.Event or None."""
+    events: list of 6*T torch.cuda.Event or None; kept_idx: steps t >= 1
+    read the kept rows of Kf / Vf through it (Kp / Vp unused)."""
     S, NL, LB, Hq, d = Q[0].shape
     Hkv = Kb[0].shape[3]
     dt = _dtype_code(Q[0])
@@ -328,6 +355,7 @@ def sprint_decode_steps(*, Q, Kb, Vb, h, theta, Kf, Vf, prefix_off, max_rows, to
     a.ws_attn, a.ws_attn_bytes = _ptr(ws_attn), ws_attn.numel()
     a.ws_lm, a.ws_lm_bytes = _ptr(ws_lm), ws_lm.numel()
     a.status = _ptr(status, torch.int32, "status")
+    a.kept_idx = _ptr(kept_idx, torch.int32, "kept_idx")
     ev = None
     if events is not None:
         ev = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])

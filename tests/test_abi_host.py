@@ -77,6 +77,15 @@ def test_invalid_arguments_rejected_without_launch(sp):
     # LB * group > 128 rows is not supported
     assert lib.sprint_block_attn(None, None, None, None, 4, 4, None, None, 1, 1, 64, 8, 2, 64,
                                  0, None, None, 0, None, None) == -2
+    # indexed attention: no kept indices / more kept rows than prefix rows
+    assert lib.sprint_block_attn_indexed(None, None, None, None, 8, None, None, 4, 4, None, None,
+                                         1, 1, 32, 4, 2, 64, 1, None, None, 0, None, None) == -1
+    assert lib.sprint_block_attn_indexed(P(16), P(16), P(16), P(16), 2, P(16), P(16), 4, 4,
+                                         P(16), P(16), 1, 1, 32, 4, 2, 64, 1, P(16), P(16),
+                                         1 << 30, P(16), None) == -1
+    assert lib.sprint_block_attn_indexed(None, None, None, P(16), 8, P(16), None, 4, 4, None,
+                                         None, 1, 1, 32, 4, 2, 96, 1, None, None, 0, None,
+                                         None) == -2
     assert lib.sprint_unmask(None, None, None, None, None, 1, 0, 0, 4, 0.9, 0, None, None,
                              None) == -1
     assert lib.sprint_unmask(None, None, None, None, None, 1, 32, 0, 4, 0.9, 5, None, None,

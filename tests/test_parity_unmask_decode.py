@@ -64,8 +64,11 @@ def test_random_trajectories_match_oracle(sp, mode, LB, T):
         assert int(mask.sum()) == 0  # terminates within T
 
 
-def test_tiny_block_end_to_end(sp):
-    """Whole block on the fp32 tiny workload, every step compared."""
+@pytest.mark.parametrize("indexed", [False, True])
+def test_tiny_block_end_to_end(sp, indexed):
+    """Whole block on the fp32 tiny workload, every step compared (later
+    steps over the compacted cache, or over the full cache through the kept
+    indices)."""
     from kv_cache_pruning_step_b300 import BlockDecoder
     w = WORKLOADS["tiny-256"]
     W = lm_head_weight(w, device=DEV)
@@ -75,7 +78,7 @@ def test_tiny_block_end_to_end(sp):
     counts = [(int((mod == 0).sum()), int((mod == 1).sum()))]
     dec = BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
                        r_text=w.r_text, r_img=w.r_img, alpha=w.alpha, modality_counts=counts,
-                       want_logits=True)
+                       want_logits=True, indexed=indexed)
     seen = []
 
     def on_step(t, d):
@@ -123,10 +126,10 @@ def _decoder_and_steps(name, tau=None, mode=0):
         steps.append({"Q": x["Q"][None].contiguous(), "Kb": x["Kb"][None].contiguous(),
                       "Vb": x["Vb"][None].contiguous(), "h": x["h"], "theta": x["theta"]})
 
-    def make():
+    def make(indexed=False):
         return BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T,
                             tau=w.tau if tau is None else tau, r_text=w.r_text, r_img=w.r_img,
-                            alpha=w.alpha, mode=mode, modality_counts=counts)
+                            alpha=w.alpha, mode=mode, modality_counts=counts, indexed=indexed)
     return w, pre, steps, make
 
 
@@ -183,3 +186,24 @@ def test_pipelined_blocks_match_waiting_decode(sp):
     assert r1.accepted_per_step == r2.accepted_per_step == ref.accepted_per_step
     assert torch.equal(t1, ref_tokens) and torch.equal(b.tokens, ref_tokens)
     assert b.finish(p1) is r1  # finishing twice returns the same result
+
+
+@pytest.mark.parametrize("name", ["tiny-256", "prefix-4k"])
+def test_indexed_layout_matches_compacted(sp, name):
+    """Later steps reading the kept rows through their indices give the same
+    block, bit for bit, as the compacted cache: native driver and stepwise."""
+    w, pre, steps, make = _decoder_and_steps(name)
+    a, b, c = make(), make(indexed=True), make(indexed=True)
+    ra = a.decode(pre, lambda t: steps[t])
+    rb = b.decode(pre, lambda t: steps[t])
+    outs = []
+    rc = c.decode_stepwise(pre, lambda t: steps[t],
+                           on_step=lambda t, d: outs.append(d.O.clone()))
+    torch.cuda.synchronize()
+    assert a.status.item() == b.status.item() == c.status.item() == 0
+    assert b.Kp is None and b.Vp is None  # no compacted copy was made
+    assert ra.steps == rb.steps == rc.steps
+    assert ra.accepted_per_step == rb.accepted_per_step == rc.accepted_per_step
+    assert torch.equal(ra.tokens, rb.tokens) and torch.equal(ra.tokens, rc.tokens)
+    assert torch.equal(a.O, b.O) and torch.equal(a.O, outs[-1])
+    assert torch.equal(a.conf_blk, b.conf_blk)

@@ -43,7 +43,7 @@ def weights_of(name):
     return _WEIGHTS[name]
 
 
-def _decode_and_check(sp, w, weights, prefixes, step_sets, check_seqs, tau):
+def _decode_and_check(sp, w, weights, prefixes, step_sets, check_seqs, tau, indexed=False):
     W, W64 = weights
     from kv_cache_pruning_step_b300 import BlockDecoder
     S = len(prefixes)
@@ -60,7 +60,7 @@ def _decode_and_check(sp, w, weights, prefixes, step_sets, check_seqs, tau):
     def make():
         return BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=tau,
                             r_text=w.r_text, r_img=w.r_img, alpha=w.alpha,
-                            modality_counts=counts)
+                            modality_counts=counts, indexed=indexed)
 
     native = make()
     r_native = native.decode(cat, lambda t: steps[t])
@@ -119,13 +119,16 @@ def _decode_and_check(sp, w, weights, prefixes, step_sets, check_seqs, tau):
     return res
 
 
-@pytest.mark.parametrize("tau", [0.7, 0.9, 0.95])
-def test_batch_16x8k_threshold_sweep(sp, tau):
+@pytest.mark.parametrize("tau,indexed", [(0.7, False), (0.9, False), (0.93, False),
+                                         (0.95, False), (0.9, True)])
+def test_batch_16x8k_threshold_sweep(sp, tau, indexed):
+    """tau sweep of the batched workload (0.93 is the paper's own setting);
+    at 0.9 also with the later steps reading the kept rows through indices."""
     w = WORKLOADS["batch-16x8k"]
     prefixes = [prefix_inputs(w, seq=s, device=DEV) for s in range(w.S)]
     step_sets = [[step_inputs(w, s, 0, t, device=DEV) for t in range(w.T)] for s in range(w.S)]
     res = _decode_and_check(sp, w, weights_of(w.name), prefixes, step_sets, check_seqs=[0, 11],
-                            tau=tau)
+                            tau=tau, indexed=indexed)
     assert res.steps <= w.T
 
 
