@@ -13,7 +13,7 @@ definition: no blocking, fusion or reordering.  Rows of independent outputs
 may be processed a slice at a time to bound memory.
 
 Readings taken where the paper is silent or its equation was lost in
-extraction (each listed again in the design doc):
+extraction:
   R1  composite score s_i = alpha * I_i + (1 - alpha) * c_i, alpha = 0.5
       (the paper's equation for s_i is missing; parity unpinned against it);
   R2  ||k_i|| is the L2 norm of position i's keys concatenated over KV heads,
@@ -31,7 +31,14 @@ extraction (each listed again in the design doc):
       logits z = (h . W_v) / theta; argmax ties go to the lowest index;
   R8  the block's first step attends to the full prefix, later steps to the
       pruned prefix; attention is bidirectional over [prefix ; block] with
-      softmax scale 1/sqrt(d) and GQA head group floor(h Hkv / Hq).
+      softmax scale 1/sqrt(d) and GQA head group floor(h Hkv / Hq);
+  R13 keep pools (selection variants beyond the paper's two modality pools):
+      positions are grouped into pools, each with its own keep count, and
+      each pool keeps its top positions as in R4.  'modality' is the paper's
+      keep (text pool, image pool); 'per_image' gives every image (maximal
+      run of image positions) its own pool at r_img; 'global' is one pool
+      over the whole prefix at one ratio r (the paper's "global keep ratio
+      r = 0.5" sentence read as a budget for the whole prefix).
 """
 from __future__ import annotations
 
@@ -157,6 +164,54 @@ def select_kept(score, modality, r_text, r_img):
         ranked = sorted(pos, key=lambda i: (-s[i], i))
         kept += ranked[:k]
     return np.array(sorted(kept), dtype=np.int64)
+
+
+def select_kept_pools(score, pool, keep):
+    """Kept prefix positions, ascending, when every position belongs to a
+    keep pool (reading R13): pool p retains its keep[p] highest-scoring
+    members, ties by ascending index (R4).
+
+    Paper, Sparse Prefix Retention paragraph: within each group the top
+    positions by s_i are retained and the rest evicted.
+    """
+    s = _f64(score)
+    pid = _np(pool).astype(np.int64)
+    kept = []
+    for p, k in enumerate(keep):
+        members = [int(i) for i in np.nonzero(pid == p)[0]]
+        if not 0 <= int(k) <= len(members):
+            raise ValueError(f"pool {p}: keep {k} of {len(members)}")
+        ranked = sorted(members, key=lambda i: (-s[i], i))
+        kept += ranked[:int(k)]
+    return np.array(sorted(kept), dtype=np.int64)
+
+
+def image_pool_ids(modality):
+    """Pool id of every position for the 'per_image' policy (reading R13):
+    0 for text, 1 + j for the j-th maximal run of image positions."""
+    mod = _np(modality).astype(np.int64) != 0
+    ids = np.zeros(len(mod), dtype=np.int64)
+    run = 0
+    for i in range(len(mod)):
+        if mod[i]:
+            if i == 0 or not mod[i - 1]:
+                run += 1
+            ids[i] = run
+    return ids
+
+
+def pool_keep_counts(pool_sizes, policy, r_text=1.0, r_img=0.8, r=0.5):
+    """Keep count of every pool (reading R13), pool_sizes[p] = members of
+    pool p: 'modality' and 'per_image' keep floor(r_text n) of pool 0 (text)
+    and floor(r_img n) of every other pool; 'global' has the single pool 0
+    and keeps floor(r n) of it."""
+    if policy == "global":
+        if len(pool_sizes) != 1:
+            raise ValueError("the global policy has one pool")
+        return [keep_count(pool_sizes[0], r)]
+    if policy not in ("modality", "per_image"):
+        raise ValueError(policy)
+    return [keep_count(n, r_text if p == 0 else r_img) for p, n in enumerate(pool_sizes)]
 
 
 def compact(K, kept):

@@ -266,6 +266,78 @@ def test_select_alpha_extremes_and_counts():
     assert k_a == k_b
 
 
+def brute_kept_pools(s, pool, keep):
+    """Rank definition per pool: i survives iff fewer than keep[p] members
+    of its pool p beat it (higher s, or equal s at a lower index)."""
+    return [i for i in range(len(s))
+            if sum(1 for j in range(len(s)) if pool[j] == pool[i] and
+                   (s[j] > s[i] or (s[j] == s[i] and j < i))) < keep[pool[i]]]
+
+
+def check_pools_golden(fn):
+    g = load("select_pools_hand.json")
+    for case in g["cases"]:
+        kept = fn(np.array(g["score"]), np.array(g["pool"]), case["keep"])
+        assert list(kept) == case["expected_kept"], case
+
+
+def check_pools_brute(fn):
+    rng = np.random.default_rng(16)
+    for trial in range(300):
+        n = int(rng.integers(0, 16))
+        P = int(rng.integers(1, 5))
+        pool = rng.integers(0, P, size=n)
+        s = rng.integers(0, 4, size=n) / 3.0  # coarse: frequent ties
+        keep = [int(rng.integers(0, (pool == p).sum() + 1)) for p in range(P)]
+        assert list(fn(s, pool, keep)) == brute_kept_pools(s, pool, keep), (s, pool, keep)
+
+
+def test_select_pools_golden_and_brute_force():
+    check_pools_golden(orc.select_kept_pools)
+    check_pools_brute(orc.select_kept_pools)
+
+
+def test_select_pools_special_cases():
+    rng = np.random.default_rng(17)
+    n = 50
+    s = rng.uniform(size=n)
+    pool = rng.integers(0, 3, size=n)
+    sizes = [int((pool == p).sum()) for p in range(3)]
+    assert list(orc.select_kept_pools(s, pool, sizes)) == list(range(n))   # keep all
+    assert len(orc.select_kept_pools(s, pool, [0, 0, 0])) == 0             # keep none
+    # one pool at half: exactly the floor(n/2) largest scores
+    kept = orc.select_kept_pools(s, np.zeros(n, int), [n // 2])
+    assert sorted(kept) == sorted(np.argsort(-s, kind="stable")[:n // 2])
+    # pools are independent: rescoring one pool leaves the others' keeps
+    s2 = s.copy()
+    s2[pool == 1] = rng.uniform(size=sizes[1])
+    keep = [3, 4, 5]
+    a = set(orc.select_kept_pools(s, pool, keep)) - set(np.nonzero(pool == 1)[0])
+    b = set(orc.select_kept_pools(s2, pool, keep)) - set(np.nonzero(pool == 1)[0])
+    assert a == b
+    with pytest.raises(ValueError):
+        orc.select_kept_pools(s, pool, [sizes[0] + 1, 0, 0])
+    # the two modality pools with floor(r n) counts are the paper's keep
+    mod = rng.integers(0, 2, size=n)
+    counts = orc.pool_keep_counts([int((mod == 0).sum()), int((mod == 1).sum())], "modality",
+                                  r_text=0.5, r_img=0.8)
+    assert list(orc.select_kept_pools(s, mod, counts)) == list(
+        orc.select_kept(s, mod, 0.5, 0.8))
+
+
+def test_pool_ids_and_counts_golden():
+    g = load("select_pools_hand.json")
+    runs = g["image_runs"]
+    assert list(orc.image_pool_ids(np.array(runs["modality"]))) == runs["expected_pool"]
+    assert list(orc.image_pool_ids(np.zeros(5, int))) == [0] * 5
+    assert list(orc.image_pool_ids(np.ones(3, int))) == [1, 1, 1]
+    c = g["counts"]
+    assert orc.pool_keep_counts(c["sizes"], "per_image", c["r_text"], c["r_img"]) == \
+        c["expected_per_image"]
+    for n, r, k in c["global"]:
+        assert orc.pool_keep_counts([n], "global", r=r) == [k]
+
+
 def test_compact_identity_and_gather():
     rng = np.random.default_rng(8)
     K = rng.normal(size=(2, 10, 3, 4))
@@ -521,6 +593,27 @@ def test_planted_mistakes_are_caught():
         with pytest.raises(AssertionError):
             check_select_golden(orc.composite_score, bad)
             check_select_brute(bad)
+    # keep pools: pool ids ignored / ties to the higher index / one too many
+    def pools_ignored(s, pool, keep):
+        return np.array(sorted(sorted(range(len(s)), key=lambda i: (-s[i], i))[:sum(keep)]))
+
+    def pools_ties_high(s, pool, keep):
+        s, pool = np.asarray(s, float), np.asarray(pool)
+        kept = []
+        for p, k in enumerate(keep):
+            kept += sorted(np.nonzero(pool == p)[0], key=lambda i: (-s[i], -i))[:k]
+        return np.array(sorted(kept))
+
+    def pools_one_more(s, pool, keep):
+        s, pool = np.asarray(s, float), np.asarray(pool)
+        kept = []
+        for p, k in enumerate(keep):
+            kept += sorted(np.nonzero(pool == p)[0], key=lambda i: (-s[i], i))[:k + 1]
+        return np.array(sorted(kept))
+    for bad in (pools_ignored, pools_ties_high, pools_one_more):
+        _fails(check_pools_golden, bad)
+        _fails(check_pools_brute, bad)
+
     # the blend with its weights swapped agrees at alpha = 0.5; the alpha = 1
     # pin (pure key-norm order) catches it
     _fails(check_select_alpha_extremes, lambda I, c, a: a * c + (1 - a) * I)
