@@ -45,6 +45,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the full-retention (r = 1) comparison runs")
+    ap.add_argument("--selection", default="modality", choices=["modality", "per_image", "global"],
+                    help="keep pools: the two modalities (the paper's), text plus one pool per "
+                         "image, or one pool over the whole prefix at --r-global")
+    ap.add_argument("--r-global", type=float, default=0.5)
     ap.add_argument("--prefix-layout", default="compacted", choices=["compacted", "indexed"],
                     help="later steps read a compacted copy of the kept rows, or the kept "
                          "rows of the full cache through their indices")
@@ -205,6 +209,7 @@ def build_inputs(w, seqs, device):
         "H": torch.cat([p["H"] for p in pres]),
         "theta": torch.cat([p["theta"] for p in pres]),
         "modality": torch.cat([p["modality"] for p in pres]),
+        "image": torch.cat([p["image"] for p in pres]),
     }
     counts = [(int((p["modality"] == 0).sum()), int((p["modality"] != 0).sum())) for p in pres]
     steps = []
@@ -221,6 +226,17 @@ def build_inputs(w, seqs, device):
     return prefix, steps, W, counts, pres
 
 
+def selection_args(args, prefix, pres=None):
+    """BlockDecoder keywords for the --selection keep pools."""
+    out = {"selection": args.selection, "r_global": args.r_global}
+    if args.selection == "per_image":
+        import torch
+        if pres is None:
+            raise ValueError("per-image pool sizes need the per-sequence prefixes")
+        out["pool_sizes"] = [torch.bincount(p["image"].long().cpu()).tolist() for p in pres]
+    return out
+
+
 def to_device(d, device, non_blocking=False):
     return {k: v.to(device, non_blocking=non_blocking) for k, v in d.items()}
 
@@ -230,7 +246,8 @@ def nbytes(d):
 
 
 # ---------------------------------------------------------------- oracle timing
-def cpu_baseline(w, pres, steps_host, W, steps_per_block, sample_rows=128):
+def cpu_baseline(w, pres, steps_host, W, steps_per_block, sample_rows=128,
+                 selection="modality", r_global=0.5):
     """The oracle, as it stands, on a bounded sample of one block.
 
     Measured: key-norm importance, selection and compaction of the whole
@@ -258,7 +275,13 @@ def cpu_baseline(w, pres, steps_host, W, steps_per_block, sample_rows=128):
     conf_all[rows] = c_s
     t0 = time.perf_counter()
     score = orc.composite_score(imp, conf_all, w.alpha)
-    kept = orc.select_kept(score, p["modality"].numpy(), w.r_text, w.r_img)
+    if selection == "modality":
+        kept = orc.select_kept(score, p["modality"].numpy(), w.r_text, w.r_img)
+    else:
+        pool = p["image"].numpy() if selection == "per_image" else np.zeros(n, np.int64)
+        sizes = np.bincount(pool).tolist()
+        keep = orc.pool_keep_counts(sizes, selection, w.r_text, w.r_img, r_global)
+        kept = orc.select_kept_pools(score, pool, keep)
     Kp = orc.compact(p["K"], kept)
     Vp = orc.compact(p["V"], kept)
     t_sel = time.perf_counter() - t0
@@ -296,7 +319,7 @@ def cpu_baseline(w, pres, steps_host, W, steps_per_block, sample_rows=128):
 
 
 # ---------------------------------------------------------------- r = 1 comparison
-def compare_full_retention(args, w, prefix, steps, counts, W, ms_block, later_ms):
+def compare_full_retention(args, w, prefix, steps, counts, W, ms_block, later_ms, pres=None):
     """SPRINT at the workload's keep ratios against full prefix retention
     (r_text = r_img = 1), adaptive and fixed schedule, on the same inputs;
     plus the exactness of r = 1: attention over the "pruned" cache equals
@@ -315,7 +338,7 @@ def compare_full_retention(args, w, prefix, steps, counts, W, ms_block, later_ms
     other = "compacted" if indexed else "indexed"
     dl = BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
                       r_text=w.r_text, r_img=w.r_img, alpha=w.alpha, modality_counts=counts,
-                      indexed=not indexed)
+                      indexed=not indexed, **selection_args(args, prefix, pres))
     dl.decode(prefix, step_fn)
     torch.cuda.synchronize()
     dl.timing = {}
@@ -408,7 +431,8 @@ def run_ours(args):
     steps = [to_device(x, dev) for x in steps_h]
     dec = BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
                        r_text=w.r_text, r_img=w.r_img, alpha=w.alpha, modality_counts=counts,
-                       indexed=args.prefix_layout == "indexed")
+                       indexed=args.prefix_layout == "indexed",
+                       **selection_args(args, prefix_h, pres))
     step_fn = lambda t: steps[t]  # noqa: E731
 
     for _ in range(args.warmup):
@@ -565,7 +589,7 @@ def run_ours(args):
     if not args.no_compare:
         later = sum(stage_ms.get(k, 0.0) for k in ("attn_pruned", "lmhead_block", "unmask"))
         compare = compare_full_retention(args, w, prefix, steps, counts, W,
-                                         1e3 * elapsed / args.steps, later)
+                                         1e3 * elapsed / args.steps, later, pres=pres)
 
     out = {
         "metric": METRIC, "value": value, "unit": "steps/s", "tokens_per_s": tokens_per_s,
@@ -578,7 +602,8 @@ def run_ours(args):
                    "LB": w.LB, "T": w.T, "tau": w.tau, "r_text": w.r_text, "r_img": w.r_img,
                    "alpha": w.alpha, "NL": w.NL, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "D": w.D,
                    "V": w.V, "bench_step": "one block decoded to completion",
-                   "prefix_layout": args.prefix_layout,
+                   "prefix_layout": args.prefix_layout, "selection": args.selection,
+                   **({"r_global": args.r_global} if args.selection == "global" else {}),
                    "l2": "inputs larger than L2 (K+V+W+H well above 126 MB)",
                    "parallelism": f"replicas x{world}, one sequence set per GPU"},
         "decode_steps_per_block": n_steps / args.steps,
@@ -588,7 +613,8 @@ def run_ours(args):
         "e2e": e2e, "full_retention_comparison": compare,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, pres, steps_h, W_h, n_steps / args.steps)
+        out["cpu_baseline"] = cpu_baseline(w, pres, steps_h, W_h, n_steps / args.steps,
+                                           selection=args.selection, r_global=args.r_global)
     if rank == 0:
         print(json.dumps(out))
     if world > 1:

@@ -13,6 +13,8 @@
  *                             rows on every step); optional logits
  *   sprint_score_prune        key-norm importance, composite score, and the
  *                             per-modality top-floor(r n) kept set
+ *   sprint_score_prune_pools  the same scores, kept set with one keep count
+ *                             per pool (per-image or whole-prefix pools)
  *   sprint_compact_kv         gather of the kept rows of K and V
  *   sprint_block_attn         bidirectional block attention over
  *                             [pruned prefix ; block]
@@ -189,6 +191,48 @@ int sprint_score_prune(const void *K, int S, const int32_t *prefix_off,
                        double r_text, double r_img, int32_t *kept_idx,
                        const int32_t *kept_off, float *score_out, void *ws,
                        size_t ws_bytes, int32_t *status, cudaStream_t stream);
+
+/*
+ * sprint_score_prune_pools -- kept set with a keep count per pool.
+ *
+ * LLaDA2.0-Uni paper, Sparse Prefix Retention paragraph: scores as for
+ * sprint_score_prune; within each group the top positions by s_i are
+ * retained.  The paper's groups are the two modalities; here position i of
+ * sequence s belongs to pool pool[i] and that pool keeps its keep[s][pool]
+ * highest-scoring members (s descending, index ascending).  With pool =
+ * modality and keep = sprint_keep_count(n_mu, r_mu) the result equals
+ * sprint_score_prune's bit for bit.  Other groupings: text plus one pool
+ * per image (each image at r_img), or a single pool for the whole prefix
+ * (one budget floor(r n) for both modalities).
+ *
+ *   K, prefix_off, total_rows, NL, Hkv, d, dtype, conf, alpha, score_out
+ *                as for sprint_score_prune
+ *   pool         uint8 [total_rows] pool id of every prefix position,
+ *                below n_pools
+ *   n_pools      pools per sequence, 1..256
+ *   keep         int32 [S][n_pools] device: keep count of every pool
+ *                (0 <= keep <= pool size)
+ *   kept_off     int32 [S+1] device CSR offsets of the kept sets; sequence
+ *                s must have kept_off[s+1]-kept_off[s] = sum_p keep[s][p]
+ *   total_kept   kept_off[S] (host copy; bounds the offsets)
+ *   kept_idx     int32 [total_kept] OUT: kept positions of each sequence,
+ *                ascending, local to the sequence's prefix
+ *   ws           workspace of sprint_score_prune_pools_workspace_bytes(S,
+ *                total_rows, n_pools)
+ *
+ * Device status: SPRINT_STATUS_BAD_OFFSETS, SPRINT_STATUS_KEPT_MISMATCH (a
+ * keep count outside its pool or not summing to the kept offsets),
+ * SPRINT_STATUS_BAD_INDEX (a pool id >= n_pools); a sequence with any of
+ * these keeps nothing (its kept_idx range is left unwritten).
+ */
+size_t sprint_score_prune_pools_workspace_bytes(int S, int total_rows, int n_pools);
+int sprint_score_prune_pools(const void *K, int S, const int32_t *prefix_off,
+                             int total_rows, int NL, int Hkv, int d, int dtype,
+                             const float *conf, const uint8_t *pool, int n_pools,
+                             const int32_t *keep, float alpha, int32_t *kept_idx,
+                             const int32_t *kept_off, int total_kept,
+                             float *score_out, void *ws, size_t ws_bytes,
+                             int32_t *status, cudaStream_t stream);
 
 /*
  * sprint_compact_kv -- pruned prefix cache: Kp[l][j] = K[l][kept_idx[j]],

@@ -179,6 +179,11 @@ int unmask_impl(const float *conf, const int32_t *argmax, uint8_t *mask, int32_t
                 int32_t *m_out, int S, int LB, int t, int T, float tau, int mode,
                 uint8_t *accepted_out, int32_t *status, Gate gate, cudaStream_t stream);
 
+// Key-norm pass of the scoring (score_prune.cu): u[row] = mean over layers
+// of the L2 norm of the row's keys concatenated over KV heads.
+int keynorm_launch(const void *K, const int32_t *prefix_off, int S, int total_rows, int NL,
+                   int row_elems, int dtype, float *u, int32_t *status, cudaStream_t stream);
+
 // Orderable unsigned key of a float: a > b  <=>  key(a) > key(b); -0 == +0.
 __device__ __forceinline__ uint32_t float_key(float f) {
   if (f == 0.0f) f = 0.0f;

@@ -415,6 +415,26 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
   }
 }
 
+int keynorm_launch(const void *K, const int32_t *prefix_off, int S, int total_rows, int NL,
+                   int row_elems, int dtype, float *u, int32_t *status, cudaStream_t stream) {
+  if (total_rows <= 0) return SPRINT_OK;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // One wave: two 256-thread CTAs per SM (register-limited), each warp
+  // striding over rows.
+  int blocks = (total_rows + 7) / 8;
+  blocks = blocks < sms * 2 ? blocks : sms * 2;
+  if (dtype == SPRINT_BF16)
+    keynorm_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(K), prefix_off, S, total_rows, NL, row_elems, u,
+        status);
+  else
+    keynorm_kernel<float><<<blocks, 256, 0, stream>>>(static_cast<const float *>(K), prefix_off,
+                                                      S, total_rows, NL, row_elems, u, status);
+  return launch_status();
+}
+
 }  // namespace sprint
 
 using namespace sprint;
@@ -447,23 +467,9 @@ extern "C" int sprint_score_prune(const void *K, int S, const int32_t *prefix_of
   float *u = static_cast<float *>(ws);
   uint32_t *keys = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) +
                                                 align_up((size_t)total_rows * 4, 256));
-  if (total_rows > 0) {
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // One wave: two 256-thread CTAs per SM (register-limited), each warp
-    // striding over rows.
-    int blocks = (total_rows + 7) / 8;
-    blocks = blocks < sms * 2 ? blocks : sms * 2;
-    if (dtype == SPRINT_BF16)
-      keynorm_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
-          static_cast<const __nv_bfloat16 *>(K), prefix_off, S, total_rows, NL, row_elems, u,
-          status);
-    else
-      keynorm_kernel<float><<<blocks, 256, 0, stream>>>(
-          static_cast<const float *>(K), prefix_off, S, total_rows, NL, row_elems, u, status);
-    if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
-  }
+  if (keynorm_launch(K, prefix_off, S, total_rows, NL, row_elems, dtype, u, status, stream) !=
+      SPRINT_OK)
+    return SPRINT_ERR_CUDA;
   // Stage up to kStageMax positions per sequence in shared memory (5 bytes
   // each); the capacity follows the longest sequence the call can hold.
   const int stage_cap = total_rows < kStageMax ? total_rows : kStageMax;

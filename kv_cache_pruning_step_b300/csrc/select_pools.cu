@@ -1,0 +1,362 @@
+// Selection with keep pools: the top positions of every pool, each pool with
+// its own keep count.
+//
+// LLaDA2.0-Uni paper (arXiv 2604.20796), Inference section, "Sparse Prefix
+// Retention" paragraph: positions are scored by s_i = alpha I_i + (1 -
+// alpha) c_i and, within each group, the top positions by s_i are retained.
+// The paper's groups are the two modalities (sprint_score_prune); here every
+// position carries a pool id (text, one pool per image, or one pool for the
+// whole prefix) and the caller gives each pool's keep count.
+//
+// Kernels (all latency-bound; the key norms come from keynorm_kernel):
+//   pool_score_kernel    one 1024-thread CTA per sequence: the mean of u and
+//                        s_i with exactly the arithmetic of select_kernel
+//                        (so the two modality pools reproduce its kept set
+//                        bit for bit), the orderable key of every s_i, and
+//                        each pool's size and smallest / largest key
+//                        (warp-aggregated shared-memory atomics).  Checks
+//                        the keep counts against the pool sizes and the
+//                        kept offsets.
+//   pool_select_kernel   one 1024-thread CTA per (sequence, pool): radix
+//                        select of the pool's keep-th largest key T on keys
+//                        reduced to the pool's range, 12 bits per pass, then
+//                        the position of the last tie at T that is kept
+//                        (ties go by ascending position).
+//   pool_compact_kernel  one 1024-thread CTA per sequence: stable compaction
+//                        of the kept positions in ascending order (warp
+//                        ballots, a scan of the 32 warp totals, coalesced
+//                        stores).
+#include <limits.h>
+#include <math.h>
+
+#include "common.cuh"
+
+namespace sprint {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kDigit = 12, kBins = 1 << kDigit;
+constexpr int kMaxPools = 256;
+
+// Per (sequence, pool) record in the workspace.
+struct PoolRec {
+  int size;        // members
+  int keep;        // keep count
+  uint32_t kmin;   // smallest and largest key of the pool
+  uint32_t kmax;
+  int mode;        // 0 keep none, 1 keep all, 2 threshold
+  uint32_t thresh; // threshold key T (mode 2)
+  int tie_cut;     // keys equal to T are kept at positions <= tie_cut
+  int ok;          // the sequence passed its checks
+};
+
+__global__ void __launch_bounds__(kThreads)
+pool_score_kernel(const float *__restrict__ u, const float *__restrict__ conf,
+                  const uint8_t *__restrict__ pool, int n_pools,
+                  const int32_t *__restrict__ keep, const int32_t *__restrict__ prefix_off,
+                  const int32_t *__restrict__ kept_off, int total_rows, int total_kept,
+                  float alpha, uint32_t *__restrict__ keys, float *__restrict__ score_out,
+                  PoolRec *__restrict__ rec, int32_t *status) {
+  __shared__ double dsum_sh[32];
+  __shared__ float mean_sh;
+  __shared__ int cnt_sh[kMaxPools];
+  __shared__ uint32_t kmin_sh[kMaxPools], kmax_sh[kMaxPools];
+  __shared__ int bad_sh, ok_sh;
+  const int s = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  PoolRec *r = rec + (size_t)s * n_pools;
+  const int p0 = prefix_off[s], p1 = prefix_off[s + 1];
+  const int k0 = kept_off[s], k1 = kept_off[s + 1];
+  if (p0 < 0 || p1 < p0 || p1 > total_rows || k0 < 0 || k1 < k0 || k1 > total_kept) {
+    if (tid == 0) report(status, SPRINT_STATUS_BAD_OFFSETS);
+    for (int p = tid; p < n_pools; p += kThreads) r[p].ok = 0;
+    return;
+  }
+  const int n = p1 - p0;
+  for (int p = tid; p < kMaxPools; p += kThreads) {
+    cnt_sh[p] = 0;
+    kmin_sh[p] = 0xffffffffu;
+    kmax_sh[p] = 0u;
+  }
+  if (tid == 0) bad_sh = 0;
+
+  // Mean of u: per-thread fp32 sums in select_kernel's order, fp64 across
+  // threads.
+  constexpr int kB = 8;
+  float su_f = 0.f;
+  for (int i0 = tid; i0 < n; i0 += kB * kThreads) {
+    float ub[kB];
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int i = i0 + j * kThreads;
+      ub[j] = i < n ? __ldg(u + p0 + i) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kB; ++j) su_f += ub[j];
+  }
+  const double su = warp_sum((double)su_f);
+  if (lane == 0) dsum_sh[warp] = su;
+  __syncthreads();
+  if (warp == 0) {
+    const double v = warp_sum(dsum_sh[lane]);
+    if (lane == 0) mean_sh = n > 0 ? (float)(v / (double)n) : 0.f;
+  }
+  __syncthreads();
+  const float mean_f = mean_sh;
+
+  // s_i, its key, and per-pool size and key range.
+  const float one_m_alpha = 1.0f - alpha;
+  for (int i0 = 0; i0 < n; i0 += kThreads) {
+    const int i = i0 + tid;
+    const bool in = i < n;
+    const int pid = in ? (int)__ldg(pool + p0 + i) : -1;
+    uint32_t key = 0u;
+    if (in) {
+      const float ui = __ldg(u + p0 + i), ci = __ldg(conf + p0 + i);
+      const float imp = mean_f > 0.0f ? ui / mean_f : 0.0f;
+      const float sc = fmaf(alpha, imp, one_m_alpha * ci);
+      key = float_key(sc);
+      keys[p0 + i] = key;
+      if (score_out) score_out[p0 + i] = sc;
+    }
+    const bool member = in && pid < n_pools;
+    if (in && !member) bad_sh = 1;
+    // Lanes of one pool combine their count and key range; their lowest
+    // lane updates the pool's shared entries.
+    const unsigned grp = __match_any_sync(0xffffffffu, member ? pid : -1);
+    const uint32_t lo = __reduce_min_sync(grp, key), hi = __reduce_max_sync(grp, key);
+    if (member && lane == __ffs(grp) - 1) {
+      atomicAdd(&cnt_sh[pid], __popc(grp));
+      atomicMin(&kmin_sh[pid], lo);
+      atomicMax(&kmax_sh[pid], hi);
+    }
+  }
+  __syncthreads();
+  // Keep counts: each within its pool, and together the sequence's kept rows.
+  int sum = 0, bad = 0;
+  for (int p = tid; p < n_pools; p += kThreads) {
+    const int k = keep[(size_t)s * n_pools + p];
+    bad |= k < 0 || k > cnt_sh[p];
+    sum += k;
+  }
+  sum = warp_sum(sum);
+  bad = __any_sync(0xffffffffu, bad);
+  __shared__ int wsum_sh[32], wbad_sh[32];
+  if (lane == 0) { wsum_sh[warp] = sum; wbad_sh[warp] = bad; }
+  __syncthreads();
+  if (warp == 0) {
+    const int t = warp_sum(wsum_sh[lane]);
+    const int b = __any_sync(0xffffffffu, wbad_sh[lane]);
+    if (lane == 0) {
+      ok_sh = !b && t == k1 - k0 && !bad_sh;
+      if (b || t != k1 - k0) report(status, SPRINT_STATUS_KEPT_MISMATCH);
+      if (bad_sh) report(status, SPRINT_STATUS_BAD_INDEX);
+    }
+  }
+  __syncthreads();
+  for (int p = tid; p < n_pools; p += kThreads) {
+    const int k = keep[(size_t)s * n_pools + p];
+    r[p].size = cnt_sh[p];
+    r[p].keep = k;
+    r[p].kmin = kmin_sh[p];
+    r[p].kmax = kmax_sh[p];
+    r[p].mode = k <= 0 ? 0 : (k >= cnt_sh[p] ? 1 : 2);
+    r[p].thresh = 0u;
+    r[p].tie_cut = INT_MAX;
+    r[p].ok = ok_sh;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+pool_select_kernel(const uint8_t *__restrict__ pool, int n_pools,
+                   const int32_t *__restrict__ prefix_off, const uint32_t *__restrict__ keys,
+                   PoolRec *__restrict__ rec) {
+  __shared__ uint32_t hist[kBins];
+  __shared__ int scan_sh[33];
+  __shared__ uint32_t prefix_sh;
+  __shared__ int shift_sh, need_sh, last_cnt_sh, cut_sh;
+  const int s = blockIdx.x, p = blockIdx.y, tid = threadIdx.x;
+  PoolRec &r = rec[(size_t)s * n_pools + p];
+  if (!r.ok || r.mode != 2) return;
+  const int p0 = prefix_off[s], n = prefix_off[s + 1] - p0;
+  const uint8_t *pl = pool + p0;
+  const uint32_t *ky = keys + p0;
+  const uint32_t base = r.kmin, range = r.kmax - r.kmin;
+  if (tid == 0) {
+    prefix_sh = 0u;
+    shift_sh = range ? 32 - __clz(range) : 0;
+    need_sh = r.keep;
+    last_cnt_sh = r.size;  // all keys equal: every member ties at T
+  }
+  __syncthreads();
+  // Radix select on d = key - base, kDigit bits at a time from the top:
+  // the keep-th largest key T, and need = how many keys equal to T are kept.
+  while (shift_sh > 0) {
+    const int sh = shift_sh, w = sh < kDigit ? sh : kDigit;
+    const uint32_t pre = prefix_sh;
+    const uint32_t need = (uint32_t)need_sh;
+    for (int b = tid; b < kBins; b += kThreads) hist[b] = 0u;
+    __syncthreads();
+#pragma unroll 4
+    for (int i = tid; i < n; i += kThreads) {
+      if (__ldg(pl + i) != p) continue;
+      const uint64_t d = (uint64_t)(__ldg(ky + i) - base);
+      if ((uint32_t)(d >> sh) == pre)
+        atomicAdd(&hist[(uint32_t)(d >> (sh - w)) & ((1u << w) - 1u)], 1u);
+    }
+    __syncthreads();
+    uint32_t c[4];
+    int mine = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      c[q] = hist[kBins - 1 - 4 * tid - q];
+      mine += (int)c[q];
+    }
+    int total;
+    uint32_t run = (uint32_t)block_excl_scan(mine, scan_sh, &total);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (run < need && run + c[q] >= need) {  // the keep-th largest is in this bin
+        prefix_sh = (pre << w) | (uint32_t)(kBins - 1 - 4 * tid - q);
+        need_sh = (int)(need - run);
+        shift_sh = sh - w;
+        last_cnt_sh = (int)c[q];
+      }
+      run += c[q];
+    }
+    __syncthreads();
+  }
+  const uint32_t T = base + prefix_sh;
+  const int need = need_sh;
+  // Ties: when fewer than all keys equal to T are kept, find the position of
+  // the need-th of them in ascending order.
+  if (need < last_cnt_sh) {
+    int before = 0;
+    if (tid == 0) cut_sh = INT_MAX;
+    __syncthreads();
+    for (int i0 = 0; i0 < n; i0 += kThreads) {
+      const int i = i0 + tid;
+      const int t = i < n && __ldg(pl + i) == p && __ldg(ky + i) == T;
+      int total;
+      const int excl = block_excl_scan(t, scan_sh, &total);
+      if (before + total >= need) {
+        if (t && before + excl + 1 == need) cut_sh = i;
+        break;  // uniform: every thread sees the same totals
+      }
+      before += total;
+    }
+    __syncthreads();
+  } else if (tid == 0) {
+    cut_sh = INT_MAX;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    r.thresh = T;
+    r.tie_cut = cut_sh;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+pool_compact_kernel(const uint8_t *__restrict__ pool, int n_pools,
+                    const int32_t *__restrict__ prefix_off, const int32_t *__restrict__ kept_off,
+                    const uint32_t *__restrict__ keys, const PoolRec *__restrict__ rec,
+                    int32_t *__restrict__ kept_idx, int32_t *status) {
+  __shared__ int mode_sh[kMaxPools], cut_sh[kMaxPools];
+  __shared__ uint32_t thr_sh[kMaxPools];
+  __shared__ int wcnt[32];
+  const int s = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const PoolRec *r = rec + (size_t)s * n_pools;
+  if (!r[0].ok) return;
+  for (int p = tid; p < n_pools; p += kThreads) {
+    mode_sh[p] = r[p].mode;
+    thr_sh[p] = r[p].thresh;
+    cut_sh[p] = r[p].tie_cut;
+  }
+  __syncthreads();
+  const int p0 = prefix_off[s], n = prefix_off[s + 1] - p0;
+  const int k0 = kept_off[s], k_all = kept_off[s + 1] - k0;
+  const int per_warp = ((n + 32 * 32 - 1) / (32 * 32)) * 32;  // multiple of 32
+  const int w_lo = warp * per_warp, w_hi = min(n, w_lo + per_warp);
+  auto kept = [&](int i) {
+    if (i >= w_hi) return false;
+    const int pid = __ldg(pool + p0 + i);
+    if (pid >= n_pools) return false;
+    const int m = mode_sh[pid];
+    if (m != 2) return m == 1;
+    const uint32_t key = __ldg(keys + p0 + i), T = thr_sh[pid];
+    return key > T || (key == T && i <= cut_sh[pid]);
+  };
+  int c = 0;
+  for (int i0 = w_lo; i0 < w_hi; i0 += 32) c += __popc(__ballot_sync(0xffffffffu, kept(i0 + lane)));
+  if (lane == 0) wcnt[warp] = c;
+  __syncthreads();
+  if (warp == 0) {
+    const int a = wcnt[lane];
+    wcnt[lane] = warp_incl_scan(a) - a;
+  }
+  __syncthreads();
+  int out = wcnt[warp];
+  const unsigned lt = (1u << lane) - 1u;
+  for (int i0 = w_lo; i0 < w_hi; i0 += 32) {
+    const bool k = kept(i0 + lane);
+    const unsigned b = __ballot_sync(0xffffffffu, k);
+    if (k) {
+      const int o = out + __popc(b & lt);
+      if (o < k_all) kept_idx[k0 + o] = i0 + lane;
+      else report(status, SPRINT_STATUS_KEPT_MISMATCH);
+    }
+    out += __popc(b);
+  }
+}
+
+}  // namespace
+}  // namespace sprint
+
+using namespace sprint;
+
+extern "C" size_t sprint_score_prune_pools_workspace_bytes(int S, int total_rows, int n_pools) {
+  if (S < 0 || total_rows < 0 || n_pools < 1 || n_pools > kMaxPools) return 0;
+  return align_up((size_t)total_rows * sizeof(float), 256) +
+         align_up((size_t)total_rows * sizeof(uint32_t), 256) +
+         align_up((size_t)S * n_pools * sizeof(PoolRec), 256);
+}
+
+extern "C" int sprint_score_prune_pools(const void *K, int S, const int32_t *prefix_off,
+                                        int total_rows, int NL, int Hkv, int d, int dtype,
+                                        const float *conf, const uint8_t *pool, int n_pools,
+                                        const int32_t *keep, float alpha, int32_t *kept_idx,
+                                        const int32_t *kept_off, int total_kept,
+                                        float *score_out, void *ws, size_t ws_bytes,
+                                        int32_t *status, cudaStream_t stream) {
+  if (S < 0 || total_rows < 0 || total_kept < 0 || NL < 1 || Hkv < 1 || d < 1)
+    return SPRINT_ERR_INVALID_ARG;
+  if (n_pools < 1 || n_pools > kMaxPools) return SPRINT_ERR_INVALID_ARG;
+  if (dtype != SPRINT_F32 && dtype != SPRINT_BF16) return SPRINT_ERR_INVALID_ARG;
+  if (!(alpha == alpha)) return SPRINT_ERR_INVALID_ARG;
+  if (S == 0) return SPRINT_OK;
+  if (!prefix_off || !kept_off || !keep || !status || !ws) return SPRINT_ERR_INVALID_ARG;
+  if (total_rows > 0 && (!K || !conf || !pool)) return SPRINT_ERR_INVALID_ARG;
+  if (total_kept > 0 && !kept_idx) return SPRINT_ERR_INVALID_ARG;
+  const int row_elems = Hkv * d;
+  if (row_elems % 8 != 0 || (K && !aligned16(K))) return SPRINT_ERR_UNSUPPORTED;
+  if (ws_bytes < sprint_score_prune_pools_workspace_bytes(S, total_rows, n_pools))
+    return SPRINT_ERR_WORKSPACE;
+  char *w = static_cast<char *>(ws);
+  float *u = reinterpret_cast<float *>(w);
+  w += align_up((size_t)total_rows * 4, 256);
+  uint32_t *keys = reinterpret_cast<uint32_t *>(w);
+  w += align_up((size_t)total_rows * 4, 256);
+  PoolRec *rec = reinterpret_cast<PoolRec *>(w);
+  if (keynorm_launch(K, prefix_off, S, total_rows, NL, row_elems, dtype, u, status, stream) !=
+      SPRINT_OK)
+    return SPRINT_ERR_CUDA;
+  pool_score_kernel<<<S, kThreads, 0, stream>>>(u, conf, pool, n_pools, keep, prefix_off,
+                                                kept_off, total_rows, total_kept, alpha, keys,
+                                                score_out, rec, status);
+  if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
+  pool_select_kernel<<<dim3(S, n_pools), kThreads, 0, stream>>>(pool, n_pools, prefix_off, keys,
+                                                                rec);
+  if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
+  pool_compact_kernel<<<S, kThreads, 0, stream>>>(pool, n_pools, prefix_off, kept_off, keys, rec,
+                                                  kept_idx, status);
+  return launch_status();
+}

@@ -57,10 +57,18 @@ class BlockDecoder:
     indexed=True: no pruned copy of the cache is made; the steps after the
     first read the kept rows of the full cache through the kept indices
     (sprint_block_attn_indexed), with the same result.
+
+    selection picks the keep pools (sprint_score_prune_pools for the last
+    two): "modality" (the paper's: floor(r_text n) of the text and
+    floor(r_img n) of the image positions), "per_image" (text at r_text and
+    every image at r_img; pool_sizes[s] = [n_text, n_image_1, ...] and the
+    prefix dict's "image" tensor gives each position's image number), or
+    "global" (one pool, floor(r_global n) of all positions).
     """
 
     def __init__(self, W, *, NL, Hq, Hkv, d, LB, T, tau, r_text, r_img, alpha=0.5,
-                 mode=sp.UNMASK_ADAPTIVE, modality_counts, want_logits=False, indexed=False):
+                 mode=sp.UNMASK_ADAPTIVE, modality_counts, want_logits=False, indexed=False,
+                 selection="modality", r_global=0.5, pool_sizes=None):
         self.W = W
         self.dev = W.device
         self.dtype = W.dtype
@@ -68,11 +76,14 @@ class BlockDecoder:
         self.LB, self.T, self.tau, self.mode = LB, T, tau, mode
         self.r_text, self.r_img, self.alpha = r_text, r_img, alpha
         self.indexed = bool(indexed)
+        if selection not in ("modality", "per_image", "global"):
+            raise ValueError(f"unknown selection {selection!r}")
+        self.selection, self.r_global = selection, r_global
         self.V, self.D = W.shape
         self.S = S = len(modality_counts)
         self.status = sp.new_status(self.dev)
         self._cap = {}  # capacity tensors of the prefix-sized buffers
-        self.set_prefix(modality_counts)
+        self.set_prefix(modality_counts, pool_sizes)
         dt = self._dt
         i32 = dict(dtype=torch.int32, device=self.dev)
         f32 = dict(dtype=torch.float32, device=self.dev)
@@ -119,7 +130,7 @@ class BlockDecoder:
             self._cap[name] = t
         return t[:numel]
 
-    def set_prefix(self, modality_counts):
+    def set_prefix(self, modality_counts, pool_sizes=None):
         """(Re)target the decoder to prefixes with these (n_text, n_image)
         counts per sequence (the number of sequences is fixed).  Buffers
         sized by the prefix grow when needed and are otherwise reused, so a
@@ -130,8 +141,25 @@ class BlockDecoder:
         S, NL, Hkv, d = self.S, self.NL, self.Hkv, self.d
         self.modality_counts = [tuple(c) for c in modality_counts]
         lens = [nt + ni for nt, ni in modality_counts]
-        kept = [sp.sprint_keep_count(nt, self.r_text) + sp.sprint_keep_count(ni, self.r_img)
-                for nt, ni in modality_counts]
+        self.keep = None  # per-pool keep counts (pool selections)
+        if self.selection == "modality":
+            kept = [sp.sprint_keep_count(nt, self.r_text) + sp.sprint_keep_count(ni, self.r_img)
+                    for nt, ni in modality_counts]
+        else:
+            if self.selection == "global":
+                table = [[sp.sprint_keep_count(n, self.r_global)] for n in lens]
+            else:
+                if pool_sizes is None or len(pool_sizes) != S:
+                    raise ValueError("per_image selection needs pool_sizes per sequence")
+                if any(sum(ps) != n for ps, n in zip(pool_sizes, lens)):
+                    raise ValueError("pool_sizes must add up to the prefix lengths")
+                self.n_pools = max(len(ps) for ps in pool_sizes)
+                table = [[sp.sprint_keep_count(int(c), self.r_text if p == 0 else self.r_img)
+                          for p, c in enumerate(list(ps) + [0] * (self.n_pools - len(ps)))]
+                         for ps in pool_sizes]
+            self.n_pools = len(table[0])
+            kept = [sum(row) for row in table]
+            self.keep = torch.tensor(table, dtype=torch.int32, device=self.dev).reshape(-1)
         self.prefix_off_host = [0]
         self.kept_off_host = [0]
         for n, k in zip(lens, kept):
@@ -154,8 +182,13 @@ class BlockDecoder:
             max(16, sp.sprint_lmhead_workspace_bytes(self.total_rows, self.D, self.V, dt)), u8)
         self.kept_idx = self._buf("kept_idx", self.total_kept, torch.int32)
         self.score = self._buf("score", self.total_rows, torch.float32)
-        self.ws_score = self._buf(
-            "ws_score", max(16, sp.sprint_score_prune_workspace_bytes(S, self.total_rows)), u8)
+        ws_bytes = (sp.sprint_score_prune_workspace_bytes(S, self.total_rows)
+                    if self.keep is None else
+                    sp.sprint_score_prune_pools_workspace_bytes(S, self.total_rows, self.n_pools))
+        self.ws_score = self._buf("ws_score", max(16, ws_bytes), u8)
+        if self.selection == "global":
+            self.zero_pool = self._buf("zero_pool", self.total_rows, u8)
+            self.zero_pool.zero_()
         row = NL * Hkv * d
         if self.indexed:
             self.Kp = self.Vp = None
@@ -197,7 +230,7 @@ class BlockDecoder:
         return self._step_events[slot]
 
     # -- the individual stages (each is one or two library calls) --------
-    def prefix_pass(self, K, V, H, theta, modality, conf_from=0):
+    def prefix_pass(self, K, V, H, theta, modality, conf_from=0, image=None):
         """Step-0 scoring and pruning: confidences of every prefix row, the
         kept set, and the pruned cache (self.Kp / self.Vp; not made when the
         decoder reads the kept rows through their indices).
@@ -220,11 +253,22 @@ class BlockDecoder:
                     H[r0:], self.W, theta[r0:], conf=self.conf_prefix[r0:],
                     argmax=self.argmax_prefix[r0:], ws=self.ws_lm_prefix, status=self.status)
         with self._stage("score_prune"):
-            sp.sprint_score_prune(K, self.prefix_off, self.total_rows, self.NL, self.Hkv,
-                                  self.d, self.conf_prefix, modality, self.alpha, self.r_text,
-                                  self.r_img, self.kept_off, self.total_kept,
-                                  kept_idx=self.kept_idx, score=self.score, ws=self.ws_score,
-                                  status=self.status)
+            if self.keep is None:
+                sp.sprint_score_prune(K, self.prefix_off, self.total_rows, self.NL, self.Hkv,
+                                      self.d, self.conf_prefix, modality, self.alpha,
+                                      self.r_text, self.r_img, self.kept_off, self.total_kept,
+                                      kept_idx=self.kept_idx, score=self.score,
+                                      ws=self.ws_score, status=self.status)
+            else:
+                pool = self.zero_pool if self.selection == "global" else image
+                if pool is None:
+                    raise ValueError("per_image selection needs the prefix's image numbers")
+                sp.sprint_score_prune_pools(K, self.prefix_off, self.total_rows, self.NL,
+                                            self.Hkv, self.d, self.conf_prefix, pool,
+                                            self.n_pools, self.keep, self.alpha, self.kept_off,
+                                            self.total_kept, kept_idx=self.kept_idx,
+                                            score=self.score, ws=self.ws_score,
+                                            status=self.status)
         if self.indexed:
             return
         with self._stage("compact"):
@@ -284,7 +328,7 @@ class BlockDecoder:
         if self._slots[slot] is not None:  # at most two blocks in flight
             self.finish(self._slots[slot])
         self.prefix_pass(prefix["K"], prefix["V"], prefix["H"], prefix["theta"],
-                         prefix["modality"], conf_from=conf_from)
+                         prefix["modality"], conf_from=conf_from, image=prefix.get("image"))
         xs = [steps(t) for t in range(self.T)]
         events = self._events_for_steps(slot) if self.timing is not None else None
         sp.sprint_decode_steps(
@@ -340,7 +384,7 @@ class BlockDecoder:
         self.mask.fill_(1)
         self.tokens.fill_(-1)
         self.prefix_pass(prefix["K"], prefix["V"], prefix["H"], prefix["theta"],
-                         prefix["modality"], conf_from=conf_from)
+                         prefix["modality"], conf_from=conf_from, image=prefix.get("image"))
         accepted = []
         prev = [self.LB] * self.S
         n_steps = 0

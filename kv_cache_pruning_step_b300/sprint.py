@@ -40,6 +40,9 @@ SIGNATURES = {
     "sprint_score_prune_workspace_bytes": (_Z, [_I, _I]),
     "sprint_score_prune": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _F, _D, _D, _P, _P,
                                 _P, _P, _Z, _P, _P]),
+    "sprint_score_prune_pools_workspace_bytes": (_Z, [_I, _I, _I]),
+    "sprint_score_prune_pools": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _F, _P,
+                                      _P, _I, _P, _P, _Z, _P, _P]),
     "sprint_compact_kv": (_I, [_P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P]),
     "sprint_block_attn_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I, _I, _I]),
     "sprint_block_attn": (_I, [_P, _P, _P, _P, _I, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
@@ -223,6 +226,35 @@ def sprint_score_prune(K, prefix_off, total_rows, NL, Hkv, d, conf, modality, al
         _ptr(score, torch.float32, "score"), _ptr(ws), ws.numel(),
         _ptr(status, torch.int32, "status"), _stream(stream))
     _check(rc, "sprint_score_prune")
+    return kept_idx, score
+
+
+def sprint_score_prune_pools_workspace_bytes(S, total_rows, n_pools) -> int:
+    return lib.sprint_score_prune_pools_workspace_bytes(S, total_rows, n_pools)
+
+
+def sprint_score_prune_pools(K, prefix_off, total_rows, NL, Hkv, d, conf, pool, n_pools, keep,
+                             alpha, kept_off, total_kept, *, kept_idx=None, want_score=False,
+                             score=None, ws=None, status=None, stream=None):
+    """Kept positions with a keep count per pool (keep: int32 [S][n_pools]
+    on the device).  Returns (kept_idx int32 [total_kept], score or None)."""
+    S = prefix_off.numel() - 1
+    dev = K.device
+    dt = _dtype_code(K)
+    kept_idx = (torch.empty(total_kept, dtype=torch.int32, device=dev)
+                if kept_idx is None else kept_idx)
+    if want_score and score is None:
+        score = torch.empty(total_rows, dtype=torch.float32, device=dev)
+    status = new_status(dev) if status is None else status
+    ws = _ws(ws, sprint_score_prune_pools_workspace_bytes(S, total_rows, n_pools), dev)
+    rc = lib.sprint_score_prune_pools(
+        _ptr(K, K.dtype, "K"), S, _ptr(prefix_off, torch.int32, "prefix_off"), int(total_rows),
+        NL, Hkv, d, dt, _ptr(conf, torch.float32, "conf"), _ptr(pool, torch.uint8, "pool"),
+        int(n_pools), _ptr(keep, torch.int32, "keep"), float(alpha),
+        _ptr(kept_idx, torch.int32, "kept_idx"), _ptr(kept_off, torch.int32, "kept_off"),
+        int(total_kept), _ptr(score, torch.float32, "score"), _ptr(ws), ws.numel(),
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "sprint_score_prune_pools")
     return kept_idx, score
 
 

@@ -77,6 +77,18 @@ def test_invalid_arguments_rejected_without_launch(sp):
     # LB * group > 128 rows is not supported
     assert lib.sprint_block_attn(None, None, None, None, 4, 4, None, None, 1, 1, 64, 8, 2, 64,
                                  0, None, None, 0, None, None) == -2
+    # keep pools: pool count out of range; null keep counts
+    assert lib.sprint_score_prune_pools(None, 1, P(16), 8, 1, 1, 8, 1, P(16), P(16), 0, P(16),
+                                        0.5, P(16), P(16), 4, None, P(16), 1 << 20, P(16),
+                                        None) == -1
+    assert lib.sprint_score_prune_pools(None, 1, P(16), 8, 1, 1, 8, 1, P(16), P(16), 257, P(16),
+                                        0.5, P(16), P(16), 4, None, P(16), 1 << 20, P(16),
+                                        None) == -1
+    assert lib.sprint_score_prune_pools(P(16), 1, P(16), 8, 1, 1, 8, 1, P(16), P(16), 3, None,
+                                        0.5, P(16), P(16), 4, None, P(16), 1 << 20, P(16),
+                                        None) == -1
+    assert sp.sprint_score_prune_pools_workspace_bytes(2, 100, 300) == 0
+    assert sp.sprint_score_prune_pools_workspace_bytes(2, 100, 17) >= 2 * 100 * 4 + 2 * 17 * 32
     # indexed attention: no kept indices / more kept rows than prefix rows
     assert lib.sprint_block_attn_indexed(None, None, None, None, 8, None, None, 4, 4, None, None,
                                          1, 1, 32, 4, 2, 64, 1, None, None, 0, None, None) == -1

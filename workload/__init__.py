@@ -20,7 +20,9 @@ bf16 workloads round once, at generation.
 Modality layouts follow the image-token counts of the LLaDA2.0-Uni paper,
 Stage 0 paragraph (about 256 tokens for a 256x256 image, about 1024 for a
 512x512 one): image spans are runs of 1024 tokens, or of 256-token slots.
-Tag 0 = text, 1 = image.
+Tag 0 = text, 1 = image.  Each image of a layout also has a number (1, 2,
+... in position order; 0 for text): a 1024-token span is one 512x512 image,
+every 256-token image slot one 256x256 image.
 """
 from __future__ import annotations
 
@@ -147,6 +149,26 @@ def prefix_layout(w: Workload, seq: int = 0, block: int = 0) -> torch.Tensor:
     return torch.tensor(tags, dtype=torch.uint8)
 
 
+def image_layout(w: Workload, seq: int = 0, block: int = 0) -> torch.Tensor:
+    """Image number of every prefix position (uint8): 0 for text, j for the
+    j-th image of the layout in position order (an image is a 1024-token
+    span, or a 256-token slot in the batched workload's layout)."""
+    tags = prefix_layout(w, seq, block)
+    ids = torch.zeros(tags.numel(), dtype=torch.uint8)
+    span = {"batch-16x8k": 256, "prefix-4k": 1024, "prefix-32k": 1024,
+            "sequential-64-blocks": 1024}.get(w.name)
+    j, start, prev = 0, 0, TEXT
+    for i, t in enumerate(tags.tolist()):
+        if t == IMAGE:
+            if prev != IMAGE:
+                start = i
+            if prev != IMAGE or (span is not None and (i - start) % span == 0):
+                j += 1
+            ids[i] = j
+        prev = t
+    return ids
+
+
 def _scaled_normal(shape, pos_dim, g, device):
     """z * exp(0.5*y): z ~ N(0,1) per element, y ~ N(0,1) per position."""
     z = torch.randn(shape, generator=g, device=device)
@@ -160,13 +182,14 @@ def prefix_inputs(w: Workload, seq: int = 0, block: int = 0, device="cpu",
                   n: int | None = None):
     """Prefix tensors of one sequence at one block's first step.
 
-    Returns a dict with K, V [NL][n][Hkv][d], H [n][D], theta [n] (f32) and
-    modality [n] (uint8).  For the sequential workload the cache grows by
+    Returns a dict with K, V [NL][n][Hkv][d], H [n][D], theta [n] (f32),
+    modality [n] (uint8) and image [n] (uint8 image numbers, 0 for text).  For the sequential workload the cache grows by
     appending: block b sees the first 2048 + 32 b rows of one fixed cache.
     """
     modality = prefix_layout(w, seq, block)
     n = modality.numel() if n is None else n
     modality = modality[:n]
+    image = image_layout(w, seq, block)[:n]
     full = n
     blk_key = block
     if w.name == "sequential-64-blocks":
@@ -178,7 +201,8 @@ def prefix_inputs(w: Workload, seq: int = 0, block: int = 0, device="cpu",
     V = _scaled_normal((w.NL, full, w.Hkv, w.d), 1, g, device)[:, :n].to(dt).contiguous()
     H = torch.randn((full, w.D), generator=g, device=device)[:n].to(dt).contiguous()
     theta = (0.5 + 3.5 * torch.rand(full, generator=g, device=device))[:n].contiguous()
-    return {"K": K, "V": V, "H": H, "theta": theta, "modality": modality.to(device)}
+    return {"K": K, "V": V, "H": H, "theta": theta, "modality": modality.to(device),
+            "image": image.to(device)}
 
 
 def step_inputs(w: Workload, seq: int, block: int, step: int, device="cpu"):
