@@ -35,10 +35,15 @@ extraction:
   R13 keep pools (selection variants beyond the paper's two modality pools):
       positions are grouped into pools, each with its own keep count, and
       each pool keeps its top positions as in R4.  'modality' is the paper's
-      keep (text pool, image pool); 'per_image' gives every image (maximal
-      run of image positions) its own pool at r_img; 'global' is one pool
+      keep (text pool, image pool); 'per_image' gives every image its own
+      pool at r_img (which positions form an image is an input;
+      image_pool_ids numbers maximal image runs); 'global' is one pool
       over the whole prefix at one ratio r (the paper's "global keep ratio
-      r = 0.5" sentence read as a budget for the whole prefix).
+      r = 0.5" sentence read as a budget for the whole prefix);
+  R14 residual chain (optional): the block LM head reads h = H + O, the
+      step's own hidden state plus the last layer's attention output with
+      its heads concatenated (Hq d = D), so the attention output reaches
+      the confidences; off by default (h is then an independent input).
 """
 from __future__ import annotations
 
@@ -300,8 +305,18 @@ def unmask_step(conf, argmax, mask, tokens, t, T, tau, mode=UNMASK_ADAPTIVE):
 # --------------------------------------------------------------------------
 # One block, end to end
 # --------------------------------------------------------------------------
+def residual_hidden(h, O):
+    """h + O of the last layer, heads concatenated (reading R14).
+
+    h: [LB, D]; O: [NL, LB, Hq, d] with Hq d = D.  Returns [LB, D] (fp64).
+    """
+    O = _f64(O)
+    NL, LB, Hq, d = O.shape
+    return _f64(h) + O[NL - 1].reshape(LB, Hq * d)
+
+
 def decode_block(prefix, steps, W, *, LB, T, tau, r_text, r_img, alpha=0.5,
-                 mode=UNMASK_ADAPTIVE):
+                 mode=UNMASK_ADAPTIVE, residual=False):
     """Decode one block of LB masked tokens in at most T steps.
 
     Paper, SPRINT paragraphs: the block's first step is a full forward pass
@@ -311,6 +326,7 @@ def decode_block(prefix, steps, W, *, LB, T, tau, r_text, r_img, alpha=0.5,
 
     prefix: dict K, V [NL][n][Hkv][d], H [n][D], theta [n], modality [n].
     steps:  callable t -> dict Q, Kb, Vb, h, theta (the step's inputs).
+    residual: the LM head reads h + O of the last layer (reading R14).
     Returns a dict with the kept set, scores and the per-step trajectory.
     """
     c_pre, am_pre, _ = lm_confidence(prefix["H"], W, prefix["theta"])
@@ -331,7 +347,8 @@ def decode_block(prefix, steps, W, *, LB, T, tau, r_text, r_img, alpha=0.5,
             O = block_attention(x["Q"], prefix["K"], prefix["V"], x["Kb"], x["Vb"])
         else:
             O = block_attention(x["Q"], Kp, Vp, x["Kb"], x["Vb"])
-        conf, am, _ = lm_confidence(x["h"], W, x["theta"])
+        h = residual_hidden(x["h"], O) if residual else x["h"]
+        conf, am, _ = lm_confidence(h, W, x["theta"])
         mask, tokens, acc = unmask_step(conf, am, mask, tokens, t, T, tau, mode)
         traj.append({"t": t, "O": O, "conf": conf, "argmax": am,
                      "accepted": acc, "mask": mask.copy(),

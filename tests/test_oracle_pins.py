@@ -338,6 +338,25 @@ def test_pool_ids_and_counts_golden():
         assert orc.pool_keep_counts([n], "global", r=r) == [k]
 
 
+def test_residual_hidden_closed_forms():
+    """h + O of the last layer: O = 0 gives h; h = 0 gives the last layer's
+    heads laid side by side; earlier layers do not matter; a hand case."""
+    rng = np.random.default_rng(18)
+    NL, LB, Hq, d = 3, 4, 2, 3
+    h = rng.normal(size=(LB, Hq * d))
+    O = rng.normal(size=(NL, LB, Hq, d))
+    np.testing.assert_array_equal(orc.residual_hidden(h, np.zeros_like(O)), h)
+    z = orc.residual_hidden(np.zeros_like(h), O)
+    for j in range(LB):
+        np.testing.assert_array_equal(z[j], np.concatenate([O[NL - 1, j, 0], O[NL - 1, j, 1]]))
+    O2 = O.copy()
+    O2[:NL - 1] = 7.0
+    np.testing.assert_array_equal(orc.residual_hidden(h, O2), orc.residual_hidden(h, O))
+    hand = orc.residual_hidden(np.array([[1.0, 2.0, 3.0, 4.0]]),
+                               np.array([[[[10.0, 20.0], [30.0, 40.0]]]]))
+    np.testing.assert_array_equal(hand, [[11.0, 22.0, 33.0, 44.0]])
+
+
 def test_compact_identity_and_gather():
     rng = np.random.default_rng(8)
     K = rng.normal(size=(2, 10, 3, 4))
