@@ -49,6 +49,8 @@ def parse_args(argv=None):
                     help="keep pools: the two modalities (the paper's), text plus one pool per "
                          "image, or one pool over the whole prefix at --r-global")
     ap.add_argument("--r-global", type=float, default=0.5)
+    ap.add_argument("--residual", action="store_true",
+                    help="the block LM head reads h + O of the last layer (residual chain)")
     ap.add_argument("--prefix-layout", default="compacted", choices=["compacted", "indexed"],
                     help="later steps read a compacted copy of the kept rows, or the kept "
                          "rows of the full cache through their indices")
@@ -228,7 +230,7 @@ def build_inputs(w, seqs, device):
 
 def selection_args(args, prefix, pres=None):
     """BlockDecoder keywords for the --selection keep pools."""
-    out = {"selection": args.selection, "r_global": args.r_global}
+    out = {"selection": args.selection, "r_global": args.r_global, "residual": args.residual}
     if args.selection == "per_image":
         import torch
         if pres is None:
@@ -603,6 +605,7 @@ def run_ours(args):
                    "alpha": w.alpha, "NL": w.NL, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "D": w.D,
                    "V": w.V, "bench_step": "one block decoded to completion",
                    "prefix_layout": args.prefix_layout, "selection": args.selection,
+                   "residual_chain": args.residual,
                    **({"r_global": args.r_global} if args.selection == "global" else {}),
                    "l2": "inputs larger than L2 (K+V+W+H well above 126 MB)",
                    "parallelism": f"replicas x{world}, one sequence set per GPU"},

@@ -325,6 +325,21 @@ int sprint_block_attn_indexed(const void *Q, const void *K, const void *V,
                               cudaStream_t stream);
 
 /*
+ * sprint_residual_hidden -- h_out = h_in + O of the last layer, the heads
+ * concatenated: h_out[s*LB + j][h*d + c] = h_in[...] + O[s][NL-1][j][h][c]
+ * (added in fp32 and stored in dtype).  An optional link of the decode
+ * step, not part of the LLaDA2.0-Uni paper's method (whose backbone is not
+ * reproduced here): it makes the block LM head read the step's attention
+ * output.
+ *
+ *   h_in, h_out  [S*LB][Hq*d] (dtype); h_out may alias h_in
+ *   O            [S][NL][LB][Hq][d] (dtype), as sprint_block_attn writes it
+ */
+int sprint_residual_hidden(const void *h_in, const void *O, int S, int NL,
+                           int LB, int Hq, int d, int dtype, void *h_out,
+                           cudaStream_t stream);
+
+/*
  * sprint_unmask -- one unmask decision per sequence.  LLaDA2.0-Uni paper,
  * Non-uniform Token Unmasking paragraph:
  *   ADAPTIVE  accept every masked position whose confidence exceeds tau
@@ -397,6 +412,12 @@ int sprint_unmask(const float *conf, const int32_t *argmax, uint8_t *mask,
  *                                            end of attention, LM head, unmask
  *   kept_idx                                 NULL, or int32 [total_kept]: the
  *                                            indexed pruned prefix (t >= 1)
+ *   residual, h_res                          residual != 0: every step's LM
+ *                                            head reads h_res = h[t] + O of
+ *                                            the last layer (heads
+ *                                            concatenated; needs Hq d = D),
+ *                                            written by the attention;
+ *                                            h_res is [S*LB][D] (dtype)
  * Returns the first non-zero code of the enqueued calls (nothing after it
  * is enqueued), SPRINT_ERR_INVALID_ARG for a missing field.
  */
@@ -427,6 +448,8 @@ typedef struct sprint_steps_args {
   int32_t *status;
   void *const *events;
   const int32_t *kept_idx;
+  int residual;
+  void *h_res;
 } sprint_steps_args;
 
 int sprint_decode_steps(const sprint_steps_args *args, cudaStream_t stream);

@@ -152,7 +152,7 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ Kp, const T *__r
 // chunk partials in ascending chunk order and normalise.
 template <typename T>
 __global__ void attn_combine_kernel(AttnWs ws, int S, int NL, int LB, int Hq, int Hkv, int D,
-                                    T *__restrict__ O, Gate gate) {
+                                    T *__restrict__ O, AttnResidual res, Gate gate) {
   if (gate_closed(gate)) return;
   const int G = Hq / Hkv, R = LB * G;
   const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -177,9 +177,34 @@ __global__ void attn_combine_kernel(AttnWs ws, int S, int NL, int LB, int Hq, in
     for (int q = 0; q * 32 < D; ++q) acc[q] = fmaf(w, oc[lane + 32 * q], acc[q]);
   }
   const int j = r / G, hh = r % G;
-  T *dst = O + ((size_t)sl * LB + j) * Hq * D + (size_t)(g * G + hh) * D;
+  const size_t at = ((size_t)sl * LB + j) * Hq * D + (size_t)(g * G + hh) * D;
+  T *dst = O + at;
   const float inv = 1.0f / den;
-  for (int q = 0; q * 32 < D; ++q) dst[lane + 32 * q] = from_f32<T>(acc[q] * inv);
+  // Residual epilogue on the last layer: h_out[s][j] = h_in[s][j] + O (heads
+  // concatenated), from O as stored.
+  const bool last = res.h_out && (int)(sl % NL) == NL - 1;
+  const size_t hat = ((size_t)(sl / NL) * LB + j) * Hq * D + (size_t)(g * G + hh) * D;
+  for (int q = 0; q * 32 < D; ++q) {
+    const T o = from_f32<T>(acc[q] * inv);
+    dst[lane + 32 * q] = o;
+    if (last)
+      static_cast<T *>(res.h_out)[hat + lane + 32 * q] =
+          from_f32<T>(to_f32(static_cast<const T *>(res.h_in)[hat + lane + 32 * q]) + to_f32(o));
+  }
+}
+
+// h_out = h_in + O of the last layer, heads concatenated: one thread per
+// element of h ([S * LB][Hq * d]).
+template <typename T>
+__global__ void residual_kernel(const T *__restrict__ h_in, const T *__restrict__ O, int NL,
+                                int LB, int width, long long total, T *__restrict__ h_out) {
+  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
+       e += (long long)gridDim.x * blockDim.x) {
+    const long long row = e / width, c = e % width;  // row = s * LB + j
+    const long long s = row / LB, j = row % LB;
+    const T o = O[((s * NL + (NL - 1)) * LB + j) * width + c];
+    h_out[e] = from_f32<T>(to_f32(h_in[e]) + to_f32(o));
+  }
 }
 
 int attn_chunk_keys(int S, int NL, int Hkv, int LB, int max_kv_rows, int target_units) {
@@ -231,7 +256,8 @@ int sprint::block_attn_impl(const void *Q, const void *Kp, const void *Vp,
                             const int32_t *kv_off, int max_kv_rows, int total_kv_rows,
                             const void *Kb, const void *Vb, int S, int NL, int LB, int Hq,
                             int Hkv, int d, int dtype, void *O, void *ws, size_t ws_bytes,
-                            int32_t *status, KvIndex kvi, Gate gate, cudaStream_t stream) {
+                            int32_t *status, KvIndex kvi, AttnResidual res, Gate gate,
+                            cudaStream_t stream) {
   if (S < 0 || NL < 1 || LB < 1 || Hq < 1 || Hkv < 1 || max_kv_rows < 0 || total_kv_rows < 0)
     return SPRINT_ERR_INVALID_ARG;
   if (dtype != SPRINT_F32 && dtype != SPRINT_BF16) return SPRINT_ERR_INVALID_ARG;
@@ -243,6 +269,7 @@ int sprint::block_attn_impl(const void *Q, const void *Kp, const void *Vp,
   if (total_kv_rows > 0 && (!Kp || !Vp)) return SPRINT_ERR_INVALID_ARG;
   if (kvi.idx && (!kvi.prefix_off || kvi.total_prefix_rows < total_kv_rows))
     return SPRINT_ERR_INVALID_ARG;
+  if (res.h_out && !res.h_in) return SPRINT_ERR_INVALID_ARG;
   if (ws_bytes < sprint_block_attn_workspace_bytes(S, NL, LB, Hq, Hkv, d, max_kv_rows, dtype))
     return SPRINT_ERR_WORKSPACE;
   if (dtype == SPRINT_BF16) {
@@ -254,7 +281,7 @@ int sprint::block_attn_impl(const void *Q, const void *Kp, const void *Vp,
                            static_cast<const __nv_bfloat16 *>(Vp), kv_off, total_kv_rows,
                            static_cast<const __nv_bfloat16 *>(Kb),
                            static_cast<const __nv_bfloat16 *>(Vb), S, NL, LB, Hq, Hkv, d, O, ws,
-                           status, kvi, gate, stream);
+                           status, kvi, res, gate, stream);
   }
   const int ck = attn_chunk_policy(S, NL, Hkv, LB, max_kv_rows);
   const AttnWs w = attn_ws_layout(ws, S, NL, LB, Hq, Hkv, d, max_kv_rows, ck);
@@ -282,7 +309,7 @@ int sprint::block_attn_impl(const void *Q, const void *Kp, const void *Vp,
   const long long rows = (long long)S * NL * Hkv * R;
   const int blocks = (int)((rows * 32 + 255) / 256);
   attn_combine_kernel<float><<<blocks, 256, 0, stream>>>(w, S, NL, LB, Hq, Hkv, d,
-                                                         static_cast<float *>(O), gate);
+                                                         static_cast<float *>(O), res, gate);
   return launch_status();
 }
 
@@ -293,7 +320,7 @@ extern "C" int sprint_block_attn(const void *Q, const void *Kp, const void *Vp,
                                  int32_t *status, cudaStream_t stream) {
   return block_attn_impl(Q, Kp, Vp, kv_off, max_kv_rows, total_kv_rows, Kb, Vb, S, NL, LB, Hq,
                          Hkv, d, dtype, O, ws, ws_bytes, status, KvIndex{nullptr, nullptr, 0},
-                         Gate{nullptr, 0}, stream);
+                         AttnResidual{nullptr, nullptr}, Gate{nullptr, 0}, stream);
 }
 
 extern "C" int sprint_block_attn_indexed(const void *Q, const void *K, const void *V,
@@ -309,5 +336,27 @@ extern "C" int sprint_block_attn_indexed(const void *Q, const void *K, const voi
   const KvIndex kvi = total_kept > 0 ? KvIndex{kept_idx, prefix_off, total_rows}
                                      : KvIndex{nullptr, nullptr, 0};
   return block_attn_impl(Q, K, V, kept_off, max_kept, total_kept, Kb, Vb, S, NL, LB, Hq, Hkv, d,
-                         dtype, O, ws, ws_bytes, status, kvi, Gate{nullptr, 0}, stream);
+                         dtype, O, ws, ws_bytes, status, kvi, AttnResidual{nullptr, nullptr},
+                         Gate{nullptr, 0}, stream);
+}
+
+extern "C" int sprint_residual_hidden(const void *h_in, const void *O, int S, int NL, int LB,
+                                      int Hq, int d, int dtype, void *h_out,
+                                      cudaStream_t stream) {
+  if (S < 0 || NL < 1 || LB < 1 || Hq < 1 || d < 1) return SPRINT_ERR_INVALID_ARG;
+  if (dtype != SPRINT_F32 && dtype != SPRINT_BF16) return SPRINT_ERR_INVALID_ARG;
+  if (S == 0) return SPRINT_OK;
+  if (!h_in || !O || !h_out) return SPRINT_ERR_INVALID_ARG;
+  const long long total = (long long)S * LB * Hq * d;
+  const int blocks = (int)((total + 255) / 256 < 148 * 16 ? (total + 255) / 256 : 148 * 16);
+  if (dtype == SPRINT_BF16)
+    residual_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(h_in), static_cast<const __nv_bfloat16 *>(O), NL, LB,
+        Hq * d, total, static_cast<__nv_bfloat16 *>(h_out));
+  else
+    residual_kernel<float><<<blocks, 256, 0, stream>>>(static_cast<const float *>(h_in),
+                                                       static_cast<const float *>(O), NL, LB,
+                                                       Hq * d, total,
+                                                       static_cast<float *>(h_out));
+  return launch_status();
 }

@@ -30,7 +30,7 @@ size_t attn_tc_workspace_bytes(int S, int NL, int Hkv, int d);
 int attn_tc_forward(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 *Vp,
                     const int32_t *kv_off, int total_kv_rows, const __nv_bfloat16 *Kb,
                     const __nv_bfloat16 *Vb, int S, int NL, int LB, int Hq, int Hkv, int d,
-                    void *O, void *ws, int32_t *status, KvIndex kvi, Gate gate,
-                    cudaStream_t stream);
+                    void *O, void *ws, int32_t *status, KvIndex kvi, AttnResidual res,
+                    Gate gate, cudaStream_t stream);
 
 }  // namespace sprint

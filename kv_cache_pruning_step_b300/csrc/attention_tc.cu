@@ -710,7 +710,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 // weighted sums).
 template <int D>
 __global__ void __launch_bounds__(256)
-attn_tc_combine_kernel(Problem pb, int G, __nv_bfloat16 *__restrict__ O) {
+attn_tc_combine_kernel(Problem pb, int G, __nv_bfloat16 *__restrict__ O, AttnResidual res) {
   if (gate_closed(pb.gate)) return;
   __shared__ int ts[MAX_SEQ + 1], nt[MAX_SEQ + 1], ks[MAX_SEQ + 1], k0[MAX_SEQ + 1];
   build_seq_tables(pb, ts, nt, ks, k0, nullptr);
@@ -769,8 +769,19 @@ attn_tc_combine_kernel(Problem pb, int G, __nv_bfloat16 *__restrict__ O) {
   __nv_bfloat16 *dst =
       O + (((size_t)(s * pb.NL + l) * pb.LB + j) * pb.Hq + (size_t)(g * GQ + hh)) * D;
   const float inv = 1.0f / den;
+  // Residual epilogue on the last layer: h_out[s][j] = h_in[s][j] + O (heads
+  // concatenated), from O as stored (bf16).
+  const bool last = res.h_out && l == pb.NL - 1;
+  const size_t hat = (((size_t)s * pb.LB + j) * pb.Hq + (size_t)(g * GQ + hh)) * D;
 #pragma unroll
-  for (int q = 0; q < D / 32; ++q) dst[lane + 32 * q] = __float2bfloat16_rn(acc[q] * inv);
+  for (int q = 0; q < D / 32; ++q) {
+    const __nv_bfloat16 o = __float2bfloat16_rn(acc[q] * inv);
+    dst[lane + 32 * q] = o;
+    if (last)
+      static_cast<__nv_bfloat16 *>(res.h_out)[hat + lane + 32 * q] = __float2bfloat16_rn(
+          __bfloat162float(static_cast<const __nv_bfloat16 *>(res.h_in)[hat + lane + 32 * q]) +
+          __bfloat162float(o));
+  }
 }
 
 EncodeTiledFn encode3() {
@@ -804,7 +815,7 @@ template <int D>
 int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 *Vp,
            const int32_t *kv_off, int total_kv_rows, const __nv_bfloat16 *Kb,
            const __nv_bfloat16 *Vb, int S, int NL, int LB, int Hq, int Hkv, void *O, void *ws,
-           int32_t *status, KvIndex kvi, Gate gate, cudaStream_t stream) {
+           int32_t *status, KvIndex kvi, AttnResidual res, Gate gate, cudaStream_t stream) {
   using Lt = Layout<D>;
   const int GQ = Hq / Hkv;
   CUtensorMap tq, tkp, tvp, tkb, tvb;
@@ -867,7 +878,7 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
   if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   const long long warps = (long long)pairs * LB * GQ;
   attn_tc_combine_kernel<D><<<(int)((warps * 32 + 255) / 256), 256, 0, stream>>>(
-      pb, G, static_cast<__nv_bfloat16 *>(O));
+      pb, G, static_cast<__nv_bfloat16 *>(O), res);
   return launch_status();
 }
 
@@ -881,13 +892,13 @@ size_t attn_tc_workspace_bytes(int S, int NL, int Hkv, int d) {
 int attn_tc_forward(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 *Vp,
                     const int32_t *kv_off, int total_kv_rows, const __nv_bfloat16 *Kb,
                     const __nv_bfloat16 *Vb, int S, int NL, int LB, int Hq, int Hkv, int d,
-                    void *O, void *ws, int32_t *status, KvIndex kvi, Gate gate,
-                    cudaStream_t stream) {
+                    void *O, void *ws, int32_t *status, KvIndex kvi, AttnResidual res,
+                    Gate gate, cudaStream_t stream) {
   if (S > MAX_SEQ) return SPRINT_ERR_UNSUPPORTED;
   return d == 64 ? launch<64>(Q, Kp, Vp, kv_off, total_kv_rows, Kb, Vb, S, NL, LB, Hq, Hkv, O,
-                              ws, status, kvi, gate, stream)
+                              ws, status, kvi, res, gate, stream)
                  : launch<128>(Q, Kp, Vp, kv_off, total_kv_rows, Kb, Vb, S, NL, LB, Hq, Hkv, O,
-                               ws, status, kvi, gate, stream);
+                               ws, status, kvi, res, gate, stream);
 }
 
 }  // namespace sprint

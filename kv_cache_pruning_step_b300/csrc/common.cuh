@@ -164,6 +164,15 @@ struct KvIndex {
   int total_prefix_rows;
 };
 
+// Residual epilogue of the attention (optional): for the last layer, also
+// write h_out = h_in + O with the heads concatenated ([S * LB][Hq * d], the
+// storage type of O), O rounded to its storage type first.  h_out ==
+// nullptr: off.
+struct AttnResidual {
+  const void *h_in;
+  void *h_out;
+};
+
 // Entry points with a step gate, shared by the C ABI (gate open) and the
 // native block driver.
 int lmhead_confidence_impl(const void *h, const void *W, const float *temp, int M, int D, int V,
@@ -173,8 +182,8 @@ int lmhead_confidence_impl(const void *h, const void *W, const float *temp, int 
 int block_attn_impl(const void *Q, const void *Kp, const void *Vp, const int32_t *kv_off,
                     int max_kv_rows, int total_kv_rows, const void *Kb, const void *Vb, int S,
                     int NL, int LB, int Hq, int Hkv, int d, int dtype, void *O, void *ws,
-                    size_t ws_bytes, int32_t *status, KvIndex kvi, Gate gate,
-                    cudaStream_t stream);
+                    size_t ws_bytes, int32_t *status, KvIndex kvi, AttnResidual res,
+                    Gate gate, cudaStream_t stream);
 int unmask_impl(const float *conf, const int32_t *argmax, uint8_t *mask, int32_t *tokens,
                 int32_t *m_out, int S, int LB, int t, int T, float tau, int mode,
                 uint8_t *accepted_out, int32_t *status, Gate gate, cudaStream_t stream);

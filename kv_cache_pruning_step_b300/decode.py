@@ -64,11 +64,17 @@ class BlockDecoder:
     every image at r_img; pool_sizes[s] = [n_text, n_image_1, ...] and the
     prefix dict's "image" tensor gives each position's image number), or
     "global" (one pool, floor(r_global n) of all positions).
+
+    residual=True: each step's LM head reads h + O of the last layer (heads
+    concatenated, Hq d = D) instead of h alone, so the attention output
+    reaches the confidences; the native driver fuses the sum into the
+    attention's combine kernel, the stepwise path calls
+    sprint_residual_hidden.
     """
 
     def __init__(self, W, *, NL, Hq, Hkv, d, LB, T, tau, r_text, r_img, alpha=0.5,
                  mode=sp.UNMASK_ADAPTIVE, modality_counts, want_logits=False, indexed=False,
-                 selection="modality", r_global=0.5, pool_sizes=None):
+                 selection="modality", r_global=0.5, pool_sizes=None, residual=False):
         self.W = W
         self.dev = W.device
         self.dtype = W.dtype
@@ -79,6 +85,9 @@ class BlockDecoder:
         if selection not in ("modality", "per_image", "global"):
             raise ValueError(f"unknown selection {selection!r}")
         self.selection, self.r_global = selection, r_global
+        self.residual = bool(residual)
+        if self.residual and Hq * d != W.shape[1]:
+            raise ValueError("the residual chain needs Hq * d == D")
         self.V, self.D = W.shape
         self.S = S = len(modality_counts)
         self.status = sp.new_status(self.dev)
@@ -97,6 +106,8 @@ class BlockDecoder:
         self.ws_lm_blk = torch.empty(
             max(16, sp.sprint_lmhead_workspace_bytes(S * LB, self.D, self.V, dt)),
             dtype=torch.uint8, device=self.dev)
+        self.h_res = (torch.empty((S * LB, self.D), dtype=self.dtype, device=self.dev)
+                      if self.residual else None)
         self.mask = torch.empty((S, LB), dtype=torch.uint8, device=self.dev)
         self.tokens = torch.empty((S, LB), **i32)
         self.m_out = torch.empty(S, **i32)
@@ -296,8 +307,12 @@ class BlockDecoder:
                 sp.sprint_block_attn(x["Q"], self.Kp, self.Vp, self.kept_off, self.max_kept,
                                      self.total_kept, x["Kb"], x["Vb"], O=self.O,
                                      ws=self.ws_attn, status=self.status)
+        h = x["h"]
+        if self.residual:
+            with self._stage("residual"):
+                h = sp.sprint_residual_hidden(x["h"], self.O, h_out=self.h_res)
         with self._stage("lmhead_block"):
-            sp.sprint_lmhead_confidence(x["h"], self.W, x["theta"], conf=self.conf_blk,
+            sp.sprint_lmhead_confidence(h, self.W, x["theta"], conf=self.conf_blk,
                                         argmax=self.argmax_blk, logits=self.logits,
                                         ws=self.ws_lm_blk, status=self.status)
         with self._stage("unmask"):
@@ -341,7 +356,7 @@ class BlockDecoder:
             argmax=self.argmax_blk, mask=self.mask, tokens=self.tokens, m_hist=self.m_hist,
             ws_attn=self.ws_attn, ws_lm=self.ws_lm_blk, status=self.status,
             logits=self.logits, events=events,
-            kept_idx=self.kept_idx if self.indexed else None)
+            kept_idx=self.kept_idx if self.indexed else None, h_res=self.h_res)
         m_host = self._m_hist_host[slot]
         m_host.copy_(self.m_hist, non_blocking=True)
         done = self._done[slot]

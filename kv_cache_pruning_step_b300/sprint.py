@@ -49,6 +49,7 @@ SIGNATURES = {
                                _P, _Z, _P, _P]),
     "sprint_block_attn_indexed": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _P, _P, _I, _I, _I,
                                        _I, _I, _I, _I, _P, _P, _Z, _P, _P]),
+    "sprint_residual_hidden": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
     "sprint_unmask": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
     "sprint_decode_steps": (_I, [_P, _P]),
 }
@@ -69,6 +70,7 @@ class StepsArgs(ctypes.Structure):
         ("ws_attn", _P), ("ws_attn_bytes", ctypes.c_size_t),
         ("ws_lm", _P), ("ws_lm_bytes", ctypes.c_size_t),
         ("status", _P), ("events", _P), ("kept_idx", _P),
+        ("residual", ctypes.c_int), ("h_res", _P),
     ]
 
 
@@ -326,6 +328,18 @@ def sprint_block_attn_indexed(Q, K, V, prefix_off, total_rows, kept_idx, kept_of
     return O
 
 
+def sprint_residual_hidden(h_in, O, *, h_out=None, stream=None):
+    """h_out = h_in + O of the last layer, heads concatenated; O is
+    [S][NL][LB][Hq][d], h_in [S*LB][Hq*d]."""
+    S, NL, LB, Hq, d = O.shape
+    h_out = torch.empty_like(h_in) if h_out is None else h_out
+    rc = lib.sprint_residual_hidden(_ptr(h_in, O.dtype, "h_in"), _ptr(O, O.dtype, "O"), S, NL,
+                                    LB, Hq, d, _dtype_code(O), _ptr(h_out, O.dtype, "h_out"),
+                                    _stream(stream))
+    _check(rc, "sprint_residual_hidden")
+    return h_out
+
+
 def sprint_unmask(conf, argmax, mask, tokens, t, T, tau, mode=UNMASK_ADAPTIVE, *, m_out=None,
                   accepted=None, status=None, stream=None):
     """One unmask step in place on mask/tokens ([S][LB]); returns (m_out, accepted)."""
@@ -354,13 +368,15 @@ def _ptr_array(tensors, dtype, name):
 def sprint_decode_steps(*, Q, Kb, Vb, h, theta, Kf, Vf, prefix_off, max_rows, total_rows,
                         Kp, Vp, kept_off, max_kept, total_kept, W, T, tau, mode, O, conf,
                         argmax, mask, tokens, m_hist, ws_attn, ws_lm, status, accepted=None,
-                        logits=None, events=None, kept_idx=None, stream=None):
+                        logits=None, events=None, kept_idx=None, h_res=None, stream=None):
     """Every denoising step of one block in one call (see include/sprint.h).
 
     Q, Kb, Vb: lists of T tensors [S][NL][LB][*][d]; h: list of T [S*LB][D];
     theta: list of T [S*LB] fp32 or None.  m_hist: int32 [T][S] (out);
     events: list of 6*T torch.cuda.Event or None; kept_idx: steps t >= 1
-    read the kept rows of Kf / Vf through it (Kp / Vp unused)."""
+    read the kept rows of Kf / Vf through it (Kp / Vp unused); h_res: the
+    LM head reads h_res = h[t] + O of the last layer (written by the
+    attention)."""
     S, NL, LB, Hq, d = Q[0].shape
     Hkv = Kb[0].shape[3]
     dt = _dtype_code(Q[0])
@@ -388,6 +404,8 @@ def sprint_decode_steps(*, Q, Kb, Vb, h, theta, Kf, Vf, prefix_off, max_rows, to
     a.ws_lm, a.ws_lm_bytes = _ptr(ws_lm), ws_lm.numel()
     a.status = _ptr(status, torch.int32, "status")
     a.kept_idx = _ptr(kept_idx, torch.int32, "kept_idx")
+    a.residual = 1 if h_res is not None else 0
+    a.h_res = _ptr(h_res, Q[0].dtype, "h_res")
     ev = None
     if events is not None:
         ev = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])

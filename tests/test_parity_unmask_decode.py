@@ -207,3 +207,78 @@ def test_indexed_layout_matches_compacted(sp, name):
     assert torch.equal(ra.tokens, rb.tokens) and torch.equal(ra.tokens, rc.tokens)
     assert torch.equal(a.O, b.O) and torch.equal(a.O, outs[-1])
     assert torch.equal(a.conf_blk, b.conf_blk)
+
+
+def test_tiny_block_residual_chain_end_to_end(sp):
+    """Residual chain on the fp32 tiny workload: the LM head reads h + O of
+    the last layer; every step's attention output, confidences and unmask
+    decisions are compared with the oracle's chained decode."""
+    from kv_cache_pruning_step_b300 import BlockDecoder
+    w = WORKLOADS["tiny-256"]
+    W = lm_head_weight(w, device=DEV)
+    pre = prefix_inputs(w, device=DEV)
+    steps = [step_inputs(w, 0, 0, t, device=DEV) for t in range(w.T)]
+    mod = pre["modality"].cpu().numpy()
+    counts = [(int((mod == 0).sum()), int((mod == 1).sum()))]
+    dec = BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
+                       r_text=w.r_text, r_img=w.r_img, alpha=w.alpha, modality_counts=counts,
+                       residual=True)
+    seen = []
+
+    def on_step(t, d):
+        seen.append({"O": gc.host(d.O[0]), "conf": d.conf_blk.cpu().numpy(),
+                     "acc": d.accepted[0].cpu().numpy(), "h": gc.host(d.h_res)})
+
+    def step_fn(t):
+        x = steps[t]
+        return {"Q": x["Q"][None].contiguous(), "Kb": x["Kb"][None].contiguous(),
+                "Vb": x["Vb"][None].contiguous(), "h": x["h"], "theta": x["theta"]}
+
+    res = dec.decode(pre, step_fn, on_step=on_step)
+    torch.cuda.synchronize()
+    assert dec.status.item() == 0
+    ref = orc.decode_block(pre, lambda t: steps[t], W, LB=w.LB, T=w.T, tau=w.tau,
+                           r_text=w.r_text, r_img=w.r_img, alpha=w.alpha, residual=True)
+    assert res.steps == len(ref["steps"])
+    for t, (g, r) in enumerate(zip(seen, ref["steps"])):
+        gc.assert_close(g["O"], r["O"], torch.float32, f"step {t} O")
+        # h = h_in + O from the GPU's own O, and the chain changes the input
+        want_h = orc.residual_hidden(steps[t]["h"], g["O"])
+        np.testing.assert_allclose(g["h"], want_h, rtol=1e-6, atol=1e-6)
+        assert np.abs(g["h"] - gc.host(steps[t]["h"])).max() > 1e-3
+        assert np.abs(g["conf"] - r["conf"]).max() <= gc.CONF_ATOL
+        if g["acc"].astype(bool).tolist() != r["accepted"].tolist():
+            near = np.abs(r["conf"] - w.tau) <= gc.CONF_ATOL
+            assert near.any(), f"step {t}: unmask decisions differ"
+            return
+    assert res.tokens[0].cpu().numpy().tolist() == ref["tokens"].tolist()
+
+
+@pytest.mark.parametrize("name", ["tiny-256", "prefix-4k"])
+def test_residual_chain_native_matches_stepwise(sp, name):
+    """The native driver's fused residual (in the attention's combine
+    kernel) and the stepwise sprint_residual_hidden give the same block, bit
+    for bit; the fused h equals h_in + O within one rounding of its type."""
+    from kv_cache_pruning_step_b300 import BlockDecoder
+    w, pre, steps, _ = _decoder_and_steps(name)
+    W = lm_head_weight(w, device=DEV)
+    mod = pre["modality"].cpu().numpy()
+    counts = [(int((mod == 0).sum()), int((mod == 1).sum()))]
+
+    def make():
+        return BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
+                            r_text=w.r_text, r_img=w.r_img, alpha=w.alpha,
+                            modality_counts=counts, residual=True)
+    a, b = make(), make()
+    ra = a.decode(pre, lambda t: steps[t])
+    rb = b.decode_stepwise(pre, lambda t: steps[t])
+    torch.cuda.synchronize()
+    assert a.status.item() == 0 and b.status.item() == 0
+    assert ra.steps == rb.steps and ra.accepted_per_step == rb.accepted_per_step
+    assert torch.equal(ra.tokens, rb.tokens)
+    assert torch.equal(a.O, b.O) and torch.equal(a.h_res, b.h_res)
+    assert torch.equal(a.conf_blk, b.conf_blk)
+    last = ra.steps - 1
+    want = orc.residual_hidden(steps[last]["h"], a.O[0])
+    rtol = 1e-6 if w.dtype == "f32" else 2.0 ** -8
+    np.testing.assert_allclose(gc.host(a.h_res), want, rtol=rtol, atol=1e-6)
