@@ -20,9 +20,11 @@
 //   warps 2-5   epilogue: each thread owns one accumulator row (TMEM lane),
 //               reads its BN columns 32 at a time with tcgen05.ld, and folds
 //               them into (max of raw dot products, first column reaching it,
-//               sum of exp2((acc - max) * log2(e) / theta)); optional logits
-//               (acc / theta in bf16).  The second accumulator lets the MMA of
-//               the next tile overlap this epilogue.
+//               sum of exp2((acc - max) * log2(e) / theta), one FMA and one
+//               ex2.approx per element); optional logits (acc / theta in
+//               bf16).  Warps whose rows all lie past M skip the reduction.
+//               The second accumulator lets the MMA of the next tile overlap
+//               this epilogue.
 // Output tiles are visited in bands of 32 column tiles so that a band of W
 // (32 x 256 rows) stays in L2 while all row tiles stream past it.
 #include <cuda.h>
@@ -53,6 +55,15 @@ template <int BN> struct Tiles {
   static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
   static_assert(BN % 32 == 0 && BN <= 256, "epilogue reads 32 columns at a time");
 };
+
+// 2^x with the hardware approximation (relative error about 2^-22);
+// results below 2^-126 flush to zero (terms that small do not change a sum
+// that contains 2^0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 
 __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &m, int &n) {
   const int per_band = BAND * num_m;
@@ -216,29 +227,38 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       int arg = 0;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)buf * ACC_STRIDE;
       const int col0 = n * BN;
+      // A warp whose 32 rows all lie past M (a call with few rows) has
+      // nothing to reduce: it only hands the accumulator back.
+      const bool live = m * BM + q * 32 < M;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; live && c < BN / 32; ++c) {
         const int cb = col0 + c * 32;
         const int ncol = min(32, V - cb);
         if (ncol <= 0) break;  // uniform across the warp
         float v[32];
         tc::tmem_ld32(taddr + (uint32_t)(c * 32), v);
         tc::tmem_wait_ld();
+        if (ncol < 32) {  // past the vocabulary: no maximum, no probability
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i >= ncol) v[i] = -INFINITY;
+        }
         float cm = v[0];
         int ca = 0;
 #pragma unroll
         for (int i = 1; i < 32; ++i)
-          if (i < ncol && v[i] > cm) { cm = v[i]; ca = i; }
+          if (v[i] > cm) { cm = v[i]; ca = i; }
         if (cm > run_max) {
-          run_sum *= exp2f((run_max - cm) * sc);
+          run_sum *= fast_exp2((run_max - cm) * sc);
           run_max = cm;
           arg = cb + ca;
         }
-        float sum = 0.f;
+        // exp2((v - max) * log2(e) / theta) as one FMA each, four partial sums
+        const float nb = -run_max * sc;
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i < ncol) sum += exp2f((v[i] - run_max) * sc);
-        run_sum += sum;
+        for (int i = 0; i < 32; ++i) s4[i & 3] += fast_exp2(fmaf(v[i], sc, nb));
+        run_sum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
         if (logits && vrow) {
           __nv_bfloat16 *dst = logits + (size_t)row * V + cb;
 #pragma unroll
