@@ -114,7 +114,9 @@ int sprint_keep_count(int n, double r);
  *   temp       [M] fp32 per-row logit temperature, > 0; NULL means 1
  *   logits_out [M][V]  (dtype) temperature-scaled logits, or NULL
  *   conf_out   [M] fp32  c = 1 / sum_v exp(z_v - max_v z)
- *   argmax_out [M] int32 smallest v attaining max_v z
+ *   argmax_out [M] int32 smallest v attaining max_v z, or NULL when only
+ *              the confidence is wanted (the scoring of prefix rows): the
+ *              kernels then skip tracking the greedy token
  *   ws         workspace of sprint_lmhead_workspace_bytes(M, D, V, dtype)
  *
  * M >= 0, D >= 1, V >= 1; bf16 needs D % 8 == 0 and 16-byte aligned h, W.

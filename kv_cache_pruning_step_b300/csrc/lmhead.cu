@@ -111,7 +111,7 @@ lmhead_simt_kernel(const T *__restrict__ h, const T *__restrict__ W,
     const size_t at = (size_t)strip * M + m0 + tid;
     pmax[at] = r_max[tid];
     psum[at] = r_sum[tid];
-    parg[at] = r_arg[tid];
+    if (parg) parg[at] = r_arg[tid];
   }
 }
 
@@ -155,7 +155,7 @@ lmhead_combine_kernel(const float *__restrict__ pmax, const float *__restrict__ 
 #pragma unroll 4
     for (int t = y; t < strips; t += kCombGroups) {
       const size_t at = (size_t)t * M + row;
-      acc = fold(acc, Part{pmax[at], psum[at], parg[at]}, sc);
+      acc = fold(acc, Part{pmax[at], psum[at], parg ? parg[at] : 0}, sc);
     }
   }
   sh[y][x] = acc;
@@ -165,7 +165,7 @@ lmhead_combine_kernel(const float *__restrict__ pmax, const float *__restrict__ 
 #pragma unroll
     for (int g = 1; g < kCombGroups; ++g) r = fold(r, sh[g][x], sc);
     conf[row] = 1.0f / r.s;
-    argmax[row] = r.a;
+    if (argmax) argmax[row] = r.a;
   }
 }
 
@@ -185,7 +185,7 @@ lmhead_combine_rows_kernel(const float *__restrict__ pmax, const float *__restri
   Part acc{-INFINITY, 0.f, 0};
   for (int t = tid; t < strips; t += 128) {
     const size_t at = (size_t)t * M + row;
-    acc = fold(acc, Part{pmax[at], psum[at], parg[at]}, sc);
+    acc = fold(acc, Part{pmax[at], psum[at], parg ? parg[at] : 0}, sc);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -198,7 +198,7 @@ lmhead_combine_rows_kernel(const float *__restrict__ pmax, const float *__restri
   if (tid == 0) {
     Part r = fold(fold(sh[0], sh[1], sc), fold(sh[2], sh[3], sc), sc);
     conf[row] = 1.0f / r.s;
-    argmax[row] = r.a;
+    if (argmax) argmax[row] = r.a;
   }
 }
 
@@ -229,9 +229,10 @@ int sprint::lmhead_confidence_impl(const void *h, const void *W, const float *te
   if (M < 0 || D < 1 || V < 1) return SPRINT_ERR_INVALID_ARG;
   if (dtype != SPRINT_F32 && dtype != SPRINT_BF16) return SPRINT_ERR_INVALID_ARG;
   if (M == 0) return SPRINT_OK;
-  if (!h || !W || !conf_out || !argmax_out || !ws || !status) return SPRINT_ERR_INVALID_ARG;
+  if (!h || !W || !conf_out || !ws || !status) return SPRINT_ERR_INVALID_ARG;
   if (ws_bytes < sprint_lmhead_workspace_bytes(M, D, V, dtype)) return SPRINT_ERR_WORKSPACE;
-  const LmheadWs p = lmhead_ws_layout(ws, M, V, lmhead_strip_cols(M, dtype));
+  LmheadWs p = lmhead_ws_layout(ws, M, V, lmhead_strip_cols(M, dtype));
+  if (!argmax_out) p.parg = nullptr;  // no greedy token wanted: skip its tracking
   if (dtype == SPRINT_BF16) {
     if (D % 8 != 0 || !aligned16(h) || !aligned16(W)) return SPRINT_ERR_UNSUPPORTED;
     const int rc = lmhead_tc_tiles(static_cast<const __nv_bfloat16 *>(h),

@@ -26,6 +26,7 @@ struct LmheadWs {
   float *pmax;    // [strips][M] max of the raw fp32 dot products in the strip
   float *psum;    // [strips][M] sum of exp(z - z_stripmax) over the strip
   int32_t *parg;  // [strips][M] first column attaining the strip max
+                  // (nullptr: the caller wants no greedy token)
   int strips;     // ceil(V / cols)
   int cols;       // vocabulary columns per strip
 };

@@ -19,10 +19,10 @@
 //               one of two fp32 accumulators (TMEM columns 0 and 256);
 //   warps 2-5   epilogue: each thread owns one accumulator row (TMEM lane),
 //               reads its BN columns 32 at a time with tcgen05.ld, and folds
-//               them into (max of raw dot products, first column reaching it,
-//               sum of exp2((acc - max) * log2(e) / theta), one FMA and one
-//               ex2.approx per element); optional logits (acc / theta in
-//               bf16).  Warps whose rows all lie past M skip the reduction.
+//               them into (max of raw dot products, first column reaching it
+//               when the caller wants the greedy token, sum of exp2((acc -
+//               max) * log2(e) / theta), one FMA and one ex2.approx per
+//               element); optional logits (acc / theta in bf16).  Warps whose rows all lie past M skip the reduction.
 //               The second accumulator lets the MMA of the next tile overlap
 //               this epilogue.
 // Output tiles are visited in bands of 32 column tiles so that a band of W
@@ -56,6 +56,13 @@ template <int BN> struct Tiles {
   static_assert(BN % 32 == 0 && BN <= 256, "epilogue reads 32 columns at a time");
 };
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 2^x with the hardware approximation (relative error about 2^-22);
 // results below 2^-126 flush to zero (terms that small do not change a sum
 // that contains 2^0).
@@ -74,7 +81,9 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &m,
   n = band * BAND + idx % bw;
 }
 
-template <int BN>
+// kArg: also track the first column reaching each row's maximum (the
+// greedy token).  Without it the chunk maximum is a three-input max tree.
+template <int BN, bool kArg>
 __global__ void __launch_bounds__(THREADS, 1)
 lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                  const float *__restrict__ temp, int M, int D, int V,
@@ -243,11 +252,21 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
           for (int i = 0; i < 32; ++i)
             if (i >= ncol) v[i] = -INFINITY;
         }
-        float cm = v[0];
+        float cm;
         int ca = 0;
+        if (kArg) {
+          cm = v[0];
 #pragma unroll
-        for (int i = 1; i < 32; ++i)
-          if (v[i] > cm) { cm = v[i]; ca = i; }
+          for (int i = 1; i < 32; ++i)
+            if (v[i] > cm) { cm = v[i]; ca = i; }
+        } else {
+          float t[11];
+#pragma unroll
+          for (int i = 0; i < 10; ++i) t[i] = max3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+          t[10] = fmaxf(v[30], v[31]);
+          cm = max3(max3(t[0], t[1], t[2]), max3(t[3], t[4], t[5]),
+                    max3(max3(t[6], t[7], t[8]), t[9], t[10]));
+        }
         if (cm > run_max) {
           run_sum *= fast_exp2((run_max - cm) * sc);
           run_max = cm;
@@ -273,7 +292,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
         const size_t at = (size_t)n * M + row;
         pmax[at] = run_max;
         psum[at] = run_sum;
-        parg[at] = arg;
+        if (kArg) parg[at] = arg;
       }
     }
   }
@@ -357,16 +376,25 @@ int launch_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *te
     return SPRINT_ERR_CUDA;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(lmhead_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(lmhead_tc_kernel<BN, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(lmhead_tc_kernel<BN, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess)
       return SPRINT_ERR_CUDA;
     attr_set = true;
   }
   const int tiles = ((M + BM - 1) / BM) * ((V + BN - 1) / BN);
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  lmhead_tc_kernel<BN><<<grid, THREADS, SMEM_BYTES, stream>>>(
-      tm_h, tm_w, temp, M, D, V, logits, p.pmax, p.psum, p.parg, status, wait_cap_ns(),
-      stall_test_enabled(), gate);
+  if (p.parg)
+    lmhead_tc_kernel<BN, true><<<grid, THREADS, SMEM_BYTES, stream>>>(
+        tm_h, tm_w, temp, M, D, V, logits, p.pmax, p.psum, p.parg, status, wait_cap_ns(),
+        stall_test_enabled(), gate);
+  else
+    lmhead_tc_kernel<BN, false><<<grid, THREADS, SMEM_BYTES, stream>>>(
+        tm_h, tm_w, temp, M, D, V, logits, p.pmax, p.psum, nullptr, status, wait_cap_ns(),
+        stall_test_enabled(), gate);
   return launch_status();
 }
 

@@ -65,6 +65,10 @@ class BlockDecoder:
     prefix dict's "image" tensor gives each position's image number), or
     "global" (one pool, floor(r_global n) of all positions).
 
+    prefix_argmax=True also stores the greedy token of every prefix row
+    (self.argmax_prefix); scoring needs only the confidences, so by default
+    the prefix LM head skips it.
+
     residual=True: each step's LM head reads h + O of the last layer (heads
     concatenated, Hq d = D) instead of h alone, so the attention output
     reaches the confidences; the native driver fuses the sum into the
@@ -74,7 +78,8 @@ class BlockDecoder:
 
     def __init__(self, W, *, NL, Hq, Hkv, d, LB, T, tau, r_text, r_img, alpha=0.5,
                  mode=sp.UNMASK_ADAPTIVE, modality_counts, want_logits=False, indexed=False,
-                 selection="modality", r_global=0.5, pool_sizes=None, residual=False):
+                 selection="modality", r_global=0.5, pool_sizes=None, residual=False,
+                 prefix_argmax=False):
         self.W = W
         self.dev = W.device
         self.dtype = W.dtype
@@ -82,6 +87,7 @@ class BlockDecoder:
         self.LB, self.T, self.tau, self.mode = LB, T, tau, mode
         self.r_text, self.r_img, self.alpha = r_text, r_img, alpha
         self.indexed = bool(indexed)
+        self.prefix_argmax = bool(prefix_argmax)
         if selection not in ("modality", "per_image", "global"):
             raise ValueError(f"unknown selection {selection!r}")
         self.selection, self.r_global = selection, r_global
@@ -187,7 +193,8 @@ class BlockDecoder:
         u8 = torch.uint8
         # step-0 prefix pass
         self.conf_prefix = self._buf("conf_prefix", self.total_rows, torch.float32)
-        self.argmax_prefix = self._buf("argmax_prefix", self.total_rows, torch.int32)
+        self.argmax_prefix = (self._buf("argmax_prefix", self.total_rows, torch.int32)
+                              if self.prefix_argmax else None)
         self.ws_lm_prefix = self._buf(
             "ws_lm_prefix",
             max(16, sp.sprint_lmhead_workspace_bytes(self.total_rows, self.D, self.V, dt)), u8)
@@ -262,7 +269,8 @@ class BlockDecoder:
             if r0 < self.total_rows:
                 sp.sprint_lmhead_confidence(
                     H[r0:], self.W, theta[r0:], conf=self.conf_prefix[r0:],
-                    argmax=self.argmax_prefix[r0:], ws=self.ws_lm_prefix, status=self.status)
+                    argmax=self.argmax_prefix[r0:] if self.prefix_argmax else None,
+                    want_argmax=self.prefix_argmax, ws=self.ws_lm_prefix, status=self.status)
         with self._stage("score_prune"):
             if self.keep is None:
                 sp.sprint_score_prune(K, self.prefix_off, self.total_rows, self.NL, self.Hkv,

@@ -154,16 +154,20 @@ def sprint_lmhead_workspace_bytes(M, D, V, dtype) -> int:
 
 
 def sprint_lmhead_confidence(h, W, temp=None, *, want_logits=False, conf=None, argmax=None,
-                             logits=None, ws=None, status=None, stream=None):
+                             logits=None, ws=None, status=None, stream=None, want_argmax=True):
     """c = top-1 softmax confidence and argmax token of every row of h @ W^T / temp.
 
-    Returns (conf fp32 [M], argmax int32 [M], logits [M][V] or None)."""
+    Returns (conf fp32 [M], argmax int32 [M] or None, logits [M][V] or None);
+    want_argmax=False computes the confidence alone."""
     M, D = h.shape
     V = W.shape[0]
     dt = _dtype_code(h)
     dev = h.device
     conf = torch.empty(M, dtype=torch.float32, device=dev) if conf is None else conf
-    argmax = torch.empty(M, dtype=torch.int32, device=dev) if argmax is None else argmax
+    if not want_argmax:
+        argmax = None
+    elif argmax is None:
+        argmax = torch.empty(M, dtype=torch.int32, device=dev)
     if want_logits and logits is None:
         logits = torch.empty((M, V), dtype=h.dtype, device=dev)
     status = new_status(dev) if status is None else status

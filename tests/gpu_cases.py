@@ -48,12 +48,15 @@ def host(t):
 
 
 def check_confidence(c_gpu, am_gpu, h, W, theta, rows, what=""):
-    """c within CONF_ATOL; argmax exact or a near-tie in the oracle."""
+    """c within CONF_ATOL; argmax exact or a near-tie in the oracle
+    (am_gpu None: the confidences alone)."""
     c_o, am_o, z = orc.lm_confidence(h, W, theta, rows=rows, want_logits=True)
     c_gpu = np.asarray(c_gpu, dtype=np.float64)
-    am_gpu = np.asarray(am_gpu).astype(np.int64)
     err = np.abs(c_gpu - c_o)
     assert err.max() <= CONF_ATOL, f"{what}: conf max err {err.max():.3e}"
+    if am_gpu is None:
+        return z, 0
+    am_gpu = np.asarray(am_gpu).astype(np.int64)
     mism = np.nonzero(am_gpu != am_o)[0]
     for i in mism:
         gap = z[i, am_o[i]] - z[i, am_gpu[i]]

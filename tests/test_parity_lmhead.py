@@ -123,3 +123,20 @@ def test_prefix_rows_sampled_bf16(sp, big_weight, M):
     # every confidence is a probability no smaller than 1/V
     cc = c.cpu().numpy()
     assert np.all(cc >= 1.0 / big_weight.shape[0] * (1 - 1e-5)) and np.all(cc <= 1.0 + 1e-6)
+
+
+@pytest.mark.parametrize("M", [4096, 32, 700])
+def test_confidence_without_argmax_bf16(sp, big_weight, M):
+    """argmax_out = NULL (prefix scoring): the kernels skip the greedy token;
+    the confidences are those of the call with it, bit for bit (the same
+    maximum and sum per strip), and match the oracle."""
+    w = WORKLOADS["prefix-4k"]
+    pre = prefix_inputs(w, device=DEV)
+    H, theta = pre["H"][:M].contiguous(), pre["theta"][:M].contiguous()
+    c1, am1, _ = sp.sprint_lmhead_confidence(H, big_weight, theta)
+    c0, am0, _ = sp.sprint_lmhead_confidence(H, big_weight, theta, want_argmax=False)
+    torch.cuda.synchronize()
+    assert am0 is None
+    assert torch.equal(c0, c1)
+    rows = np.unique(np.random.default_rng(M).choice(M, min(M, 40), replace=False))
+    gc.check_confidence(c0.cpu().numpy()[rows], None, H, big_weight, theta, rows, "no argmax")
