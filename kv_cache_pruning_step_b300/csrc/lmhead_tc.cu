@@ -83,7 +83,12 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &m,
 
 // kArg: also track the first column reaching each row's maximum (the
 // greedy token).  Without it the chunk maximum is a three-input max tree.
-template <int BN, bool kArg>
+// kPair: the grid is made of clusters of two CTAs that take row tiles 2i
+// and 2i+1 of the same column tile; rank 0 loads the W tile once for both
+// (TMA multicast), each CTA loads its own h tile, and a stage is reloaded
+// only once the MMAs of both CTAs have read it (each CTA's MMA issuer
+// commits to the empty barrier of both).  This halves the W traffic from L2.
+template <int BN, bool kArg, bool kPair>
 __global__ void __launch_bounds__(THREADS, 1)
 lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                  const float *__restrict__ temp, int M, int D, int V,
@@ -108,12 +113,23 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_m = (M + BM - 1) / BM, num_n = (V + BN - 1) / BN;
-  const int tiles = num_m * num_n, nk = (D + BK - 1) / BK;
+  // Scheduling units: one CTA, or one pair of CTAs (rank 0 / 1 take row
+  // tiles 2 mu and 2 mu + 1).
+  const uint32_t rank = kPair ? tc::cluster_ctarank() : 0u;
+  const int unit = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int units = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int num_mu = kPair ? (num_m + 1) / 2 : num_m;
+  const int tiles = num_mu * num_n, nk = (D + BK - 1) / BK;
+  auto coords = [&](int t, int &m, int &n) {
+    int mu;
+    tile_coords(t, num_mu, num_n, mu, n);
+    m = kPair ? 2 * mu + (int)rank : mu;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(tc::smem_u32(full + s), 1);
-      tc::mbar_init(tc::smem_u32(empty + s), 1);
+      tc::mbar_init(tc::smem_u32(empty + s), kPair ? 2 : 1);  // one commit per CTA
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(tc::smem_u32(tfull + b), 1);
@@ -134,6 +150,8 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
   }
   tc::fence_before_sync();
   __syncthreads();
+  // The peer CTA signals this CTA's barriers: both must be initialised.
+  if (kPair) tc::cluster_sync();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
@@ -143,17 +161,20 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, last_parity = 0;  // bit s: stage s has a load issued
-      for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+      for (int t = unit; t < tiles; t += units) {
         int m, n;
-        tile_coords(t, num_m, num_n, m, n);
+        coords(t, m, n);
         for (int kb = 0; kb < nk; ++kb) {
           if (!tc::mbar_wait(tc::smem_u32(empty + stage), phase ^ 1, cap_ns, abort_flag))
             goto producer_done;
           const uint32_t fb = tc::smem_u32(full + stage);
-          tc::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          tc::mbar_arrive_expect_tx(fb, STAGE_BYTES);  // h tile + W tile (own or multicast)
           const uint32_t sa = tc::smem_u32(smem + stage * STAGE_BYTES);
           tc::tma_load_2d(sa, &tm_h, fb, kb * BK, m * BM);
-          tc::tma_load_2d(sa + A_BYTES, &tm_w, fb, kb * BK, n * BN);
+          if (!kPair)
+            tc::tma_load_2d(sa + A_BYTES, &tm_w, fb, kb * BK, n * BN);
+          else if (rank == 0)
+            tc::tma_load_2d_multicast(sa + A_BYTES, &tm_w, fb, kb * BK, n * BN, 0x3);
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -178,7 +199,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       // Failure-path test: wait on a barrier no one arrives on, so the
       // bounded wait expires and the CTA takes its abort path.
       if (stall_test) tc::mbar_wait(tc::smem_u32(never), 0, cap_ns, abort_flag);
-      for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x, ++it) {
+      for (int t = unit; t < tiles && !*abort_flag; t += units, ++it) {
         const int buf = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
         if (!tc::mbar_wait(tc::smem_u32(tempty + buf), (use & 1u) ^ 1u, cap_ns, abort_flag))
@@ -198,7 +219,10 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)  // +32 bytes along K per step
             tc::mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
-          tc::mma_commit(tc::smem_u32(empty + stage));
+          if (kPair)
+            tc::mma_commit_multicast(tc::smem_u32(empty + stage), 0x3);
+          else
+            tc::mma_commit(tc::smem_u32(empty + stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -214,11 +238,11 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int r_tile = q * 32 + lane;
     int it = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+    for (int t = unit; t < tiles; t += units, ++it) {
       const int buf = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       int m, n;
-      tile_coords(t, num_m, num_n, m, n);
+      coords(t, m, n);
       if (!tc::mbar_wait(tc::smem_u32(tfull + buf), use & 1u, cap_ns, abort_flag)) break;
       tc::fence_after_sync();
       const int row = m * BM + r_tile;
@@ -299,6 +323,9 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
 
   tc::fence_before_sync();
   __syncthreads();
+  // Neither CTA of a pair leaves while the other may still signal it (its
+  // MMAs' commits are done once its drain wait above has completed).
+  if (kPair) tc::cluster_sync();
   tc::fence_after_sync();
   if (threadIdx.x == 0 && *abort_flag) report(status, SPRINT_STATUS_TIMEOUT);
   if (warp == 1) tc::tmem_dealloc(tmem, TMEM_COLS);
@@ -365,37 +392,76 @@ int sm_count() {
   return sms;
 }
 
-template <int BN>
-int launch_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *temp, int M, int D,
-                 int V, __nv_bfloat16 *logits, const LmheadWs &p, int32_t *status, Gate gate,
-                 cudaStream_t stream) {
+template <int BN, bool kArg, bool kPair>
+int launch_kernel(const CUtensorMap &tm_h, const CUtensorMap &tm_w, const float *temp, int M,
+                  int D, int V, __nv_bfloat16 *logits, const LmheadWs &p, int32_t *status,
+                  Gate gate, int units, cudaStream_t stream) {
   constexpr size_t SMEM_BYTES = Tiles<BN>::SMEM_BYTES;
-  CUtensorMap tm_h, tm_w;
-  if (!make_tmap_bf16_2d(&tm_h, h, D, M, D, BK, BM) ||
-      !make_tmap_bf16_2d(&tm_w, W, D, V, D, BK, BN))
-    return SPRINT_ERR_CUDA;
+  auto kern = lmhead_tc_kernel<BN, kArg, kPair>;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(lmhead_tc_kernel<BN, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(lmhead_tc_kernel<BN, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess)
       return SPRINT_ERR_CUDA;
     attr_set = true;
   }
-  const int tiles = ((M + BM - 1) / BM) * ((V + BN - 1) / BN);
-  const int grid = tiles < sm_count() ? tiles : sm_count();
-  if (p.parg)
-    lmhead_tc_kernel<BN, true><<<grid, THREADS, SMEM_BYTES, stream>>>(
-        tm_h, tm_w, temp, M, D, V, logits, p.pmax, p.psum, p.parg, status, wait_cap_ns(),
-        stall_test_enabled(), gate);
-  else
-    lmhead_tc_kernel<BN, false><<<grid, THREADS, SMEM_BYTES, stream>>>(
-        tm_h, tm_w, temp, M, D, V, logits, p.pmax, p.psum, nullptr, status, wait_cap_ns(),
-        stall_test_enabled(), gate);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  int grid = units;
+  if (kPair) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // Clusters resident at once (pairs of SMs in a GPC); every pair keeps
+    // its tiles, so more pairs than fit would only run later.
+    static int max_pairs = 0;
+    if (!max_pairs) {
+      cfg.gridDim = dim3(2 * units);
+      if (cudaOccupancyMaxActiveClusters(&max_pairs, kern, &cfg) != cudaSuccess ||
+          max_pairs < 1)
+        max_pairs = 1;
+    }
+    grid = 2 * (units < max_pairs ? units : max_pairs);
+  }
+  cfg.gridDim = dim3(grid);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tm_h, tm_w, temp, M, D, V, logits,
+                                           p.pmax, p.psum, p.parg, status, wait_cap_ns(),
+                                           stall_test_enabled(), gate);
+  if (e != cudaSuccess) return SPRINT_ERR_CUDA;
   return launch_status();
+}
+
+template <int BN>
+int launch_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *temp, int M, int D,
+                 int V, __nv_bfloat16 *logits, const LmheadWs &p, int32_t *status, Gate gate,
+                 cudaStream_t stream) {
+  CUtensorMap tm_h, tm_w;
+  if (!make_tmap_bf16_2d(&tm_h, h, D, M, D, BK, BM) ||
+      !make_tmap_bf16_2d(&tm_w, W, D, V, D, BK, BN))
+    return SPRINT_ERR_CUDA;
+  const int num_m = (M + BM - 1) / BM, num_n = (V + BN - 1) / BN;
+  const int sms = sm_count();
+  // Calls with two or more row tiles run as CTA pairs sharing each W tile.
+  if (num_m >= 2) {
+    const int pair_tiles = ((num_m + 1) / 2) * num_n;
+    const int pairs = pair_tiles < sms / 2 ? pair_tiles : sms / 2;
+    return p.parg ? launch_kernel<BN, true, true>(tm_h, tm_w, temp, M, D, V, logits, p, status,
+                                                   gate, pairs, stream)
+                  : launch_kernel<BN, false, true>(tm_h, tm_w, temp, M, D, V, logits, p, status,
+                                                    gate, pairs, stream);
+  }
+  const int tiles = num_m * num_n;
+  const int grid = tiles < sms ? tiles : sms;
+  return p.parg ? launch_kernel<BN, true, false>(tm_h, tm_w, temp, M, D, V, logits, p, status,
+                                                  gate, grid, stream)
+                : launch_kernel<BN, false, false>(tm_h, tm_w, temp, M, D, V, logits, p, status,
+                                                   gate, grid, stream);
 }
 
 int lmhead_tc_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *temp, int M,
