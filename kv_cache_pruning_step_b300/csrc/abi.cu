@@ -15,7 +15,7 @@ extern "C" const char *sprint_strerror(int code) {
   switch (code) {
     case SPRINT_OK: return "ok";
     case SPRINT_ERR_INVALID_ARG: return "invalid argument (null pointer, size or alignment)";
-    case SPRINT_ERR_UNSUPPORTED: return "unsupported shape or layout for this build";
+    case SPRINT_ERR_UNSUPPORTED: return "unsupported shape or layout";
     case SPRINT_ERR_CUDA: return "a CUDA call or kernel launch failed";
     case SPRINT_ERR_WORKSPACE: return "workspace smaller than the *_workspace_bytes() size";
     case SPRINT_ERR_TOO_LARGE: return "request larger than the library's fixed scratch array";
