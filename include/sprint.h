@@ -412,6 +412,9 @@ int sprint_unmask(const float *conf, const int32_t *argmax, uint8_t *mask,
  *   events                                   NULL or a HOST array of 6*T
  *                                            cudaEvent_t: per step, start and
  *                                            end of attention, LM head, unmask
+ *                                            (NULL entries are not recorded;
+ *                                            an event between two kernels
+ *                                            keeps them from overlapping)
  *   kept_idx                                 NULL, or int32 [total_kept]: the
  *                                            indexed pruned prefix (t >= 1)
  *   residual, h_res                          residual != 0: every step's LM

@@ -15,7 +15,7 @@ using namespace sprint;
 namespace {
 
 int record(void *const *events, int i, cudaStream_t stream) {
-  if (!events) return SPRINT_OK;
+  if (!events || !events[i]) return SPRINT_OK;
   return cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) == cudaSuccess
              ? SPRINT_OK
              : SPRINT_ERR_CUDA;

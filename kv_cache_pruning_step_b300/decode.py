@@ -123,8 +123,11 @@ class BlockDecoder:
         self.ev = torch.cuda.Event()
         # When a dict, every stage records (start, end) CUDA events on the
         # current stream; after the block the durations (ms) are appended to
-        # timing[stage] (used by the benchmark).
+        # timing[stage] (used by the benchmark).  timing_stages, when a set,
+        # limits the events to those stages: an event between two kernels
+        # keeps the second from launching before the first ends.
         self.timing = None
+        self.timing_stages = None
         self._pending = []
         # Two slots for blocks decoded without waiting (decode(wait=False)).
         self._step_events = [None, None]
@@ -217,9 +220,13 @@ class BlockDecoder:
             "ws_attn", max(16, sp.sprint_block_attn_workspace_bytes(
                 S, NL, self.LB, self.Hq, Hkv, d, self.max_rows, dt)), u8)
 
+    def _timed(self, name):
+        return self.timing is not None and (self.timing_stages is None
+                                            or name in self.timing_stages)
+
     @contextlib.contextmanager
     def _stage(self, name):
-        if self.timing is None:
+        if not self._timed(name):
             yield
             return
         a = torch.cuda.Event(enable_timing=True)
@@ -236,16 +243,24 @@ class BlockDecoder:
                 self.timing.setdefault(name, []).append(a.elapsed_time(b))
         self._pending = []
 
+    _STEP_STAGES = ("attn", "lmhead_block", "unmask")
+
     def _events_for_steps(self, slot):
         """6 * T timing events for the native step driver (one set per
         pending-block slot), created once; each is recorded once here so that
-        its CUDA event exists."""
+        its CUDA event exists.  Entries of stages not timed are None."""
         if self._step_events[slot] is None:
             evs = [torch.cuda.Event(enable_timing=True) for _ in range(6 * self.T)]
             for e in evs:
                 e.record()
             self._step_events[slot] = evs
-        return self._step_events[slot]
+        evs = list(self._step_events[slot])
+        for t in range(self.T):
+            for k, name in enumerate(self._STEP_STAGES):
+                full = "attn_full" if t == 0 else "attn_pruned"
+                if not self._timed(full if name == "attn" else name):
+                    evs[6 * t + 2 * k] = evs[6 * t + 2 * k + 1] = None
+        return evs
 
     # -- the individual stages (each is one or two library calls) --------
     def prefix_pass(self, K, V, H, theta, modality, conf_from=0, image=None):
@@ -392,7 +407,8 @@ class BlockDecoder:
                 ev = pending.step_events
                 for k, name in enumerate(("attn_full" if t == 0 else "attn_pruned",
                                           "lmhead_block", "unmask")):
-                    timing.append((name, ev[6 * t + 2 * k], ev[6 * t + 2 * k + 1]))
+                    if ev[6 * t + 2 * k] is not None:
+                        timing.append((name, ev[6 * t + 2 * k], ev[6 * t + 2 * k + 1]))
         if self.timing is not None:
             for name, a, b in timing:
                 self.timing.setdefault(name, []).append(a.elapsed_time(b))

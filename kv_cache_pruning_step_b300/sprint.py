@@ -377,7 +377,7 @@ def sprint_decode_steps(*, Q, Kb, Vb, h, theta, Kf, Vf, prefix_off, max_rows, to
 
     Q, Kb, Vb: lists of T tensors [S][NL][LB][*][d]; h: list of T [S*LB][D];
     theta: list of T [S*LB] fp32 or None.  m_hist: int32 [T][S] (out);
-    events: list of 6*T torch.cuda.Event or None; kept_idx: steps t >= 1
+    events: list of 6*T torch.cuda.Event (or None entries) or None; kept_idx: steps t >= 1
     read the kept rows of Kf / Vf through it (Kp / Vp unused); h_res: the
     LM head reads h_res = h[t] + O of the last layer (written by the
     attention)."""
@@ -412,7 +412,8 @@ def sprint_decode_steps(*, Q, Kb, Vb, h, theta, Kf, Vf, prefix_off, max_rows, to
     a.h_res = _ptr(h_res, Q[0].dtype, "h_res")
     ev = None
     if events is not None:
-        ev = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+        ev = (ctypes.c_void_p * len(events))(*[e.cuda_event if e is not None else None
+                                                for e in events])
         a.events = ctypes.cast(ev, ctypes.c_void_p)
     rc = lib.sprint_decode_steps(ctypes.byref(a), _stream(stream))
     _check(rc, "sprint_decode_steps")

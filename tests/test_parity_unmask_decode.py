@@ -282,3 +282,17 @@ def test_residual_chain_native_matches_stepwise(sp, name):
     want = orc.residual_hidden(steps[last]["h"], a.O[0])
     rtol = 1e-6 if w.dtype == "f32" else 2.0 ** -8
     np.testing.assert_allclose(gc.host(a.h_res), want, rtol=rtol, atol=1e-6)
+
+
+def test_timing_of_selected_stages_only(sp):
+    """timing_stages limits the recorded events (the native driver skips the
+    others); the block decodes the same."""
+    w, pre, steps, make = _decoder_and_steps("prefix-4k")
+    a, b = make(), make()
+    a.timing, a.timing_stages = {}, {"lmhead_block", "lmhead_prefix"}
+    ra = a.decode(pre, lambda t: steps[t])
+    rb = b.decode(pre, lambda t: steps[t])
+    torch.cuda.synchronize()
+    assert set(a.timing) == {"lmhead_block", "lmhead_prefix"}
+    assert len(a.timing["lmhead_block"]) == ra.steps
+    assert ra.steps == rb.steps and torch.equal(ra.tokens, rb.tokens)
