@@ -28,7 +28,7 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ Kp, const T *__r
                  const T *__restrict__ Kb, const T *__restrict__ Vb, int NL, int LB, int Hq,
                  int Hkv, AttnWs ws, int32_t *status, KvIndex kvi, Gate gate) {
   constexpr int TK = 32;
-  if (step_begin(gate)) return;
+  if (gate_closed(gate)) return;
   extern __shared__ float smem[];
   const int G = Hq / Hkv, R = LB * G;
   float *Qs = smem;                  // [R][D]
@@ -153,7 +153,7 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ Kp, const T *__r
 template <typename T>
 __global__ void attn_combine_kernel(AttnWs ws, int S, int NL, int LB, int Hq, int Hkv, int D,
                                     T *__restrict__ O, AttnResidual res, Gate gate) {
-  if (step_begin(gate)) return;
+  if (gate_closed(gate)) return;
   const int G = Hq / Hkv, R = LB * G;
   const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -292,26 +292,24 @@ int sprint::block_attn_impl(const void *Q, const void *Kp, const void *Vp,
     if (d == 64) {
       cudaFuncSetAttribute(attn_simt_kernel<float, 64>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      launch_pdl(attn_simt_kernel<float, 64>, grid, dim3(256), sm, stream,
-                 static_cast<const float *>(Q), static_cast<const float *>(Kp),
-                 static_cast<const float *>(Vp), kv_off, total_kv_rows,
-                 static_cast<const float *>(Kb), static_cast<const float *>(Vb), NL, LB, Hq, Hkv,
-                 w, status, kvi, gate);
+      attn_simt_kernel<float, 64><<<grid, 256, sm, stream>>>(
+          static_cast<const float *>(Q), static_cast<const float *>(Kp),
+          static_cast<const float *>(Vp), kv_off, total_kv_rows, static_cast<const float *>(Kb),
+          static_cast<const float *>(Vb), NL, LB, Hq, Hkv, w, status, kvi, gate);
     } else {
       cudaFuncSetAttribute(attn_simt_kernel<float, 128>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      launch_pdl(attn_simt_kernel<float, 128>, grid, dim3(256), sm, stream,
-                 static_cast<const float *>(Q), static_cast<const float *>(Kp),
-                 static_cast<const float *>(Vp), kv_off, total_kv_rows,
-                 static_cast<const float *>(Kb), static_cast<const float *>(Vb), NL, LB, Hq, Hkv,
-                 w, status, kvi, gate);
+      attn_simt_kernel<float, 128><<<grid, 256, sm, stream>>>(
+          static_cast<const float *>(Q), static_cast<const float *>(Kp),
+          static_cast<const float *>(Vp), kv_off, total_kv_rows, static_cast<const float *>(Kb),
+          static_cast<const float *>(Vb), NL, LB, Hq, Hkv, w, status, kvi, gate);
     }
     if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   }
   const long long rows = (long long)S * NL * Hkv * R;
   const int blocks = (int)((rows * 32 + 255) / 256);
-  launch_pdl(attn_combine_kernel<float>, dim3(blocks), dim3(256), 0, stream, w, S, NL, LB, Hq,
-             Hkv, d, static_cast<float *>(O), res, gate);
+  attn_combine_kernel<float><<<blocks, 256, 0, stream>>>(w, S, NL, LB, Hq, Hkv, d,
+                                                         static_cast<float *>(O), res, gate);
   return launch_status();
 }
 

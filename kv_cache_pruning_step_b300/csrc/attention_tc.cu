@@ -250,7 +250,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                const __grid_constant__ CUtensorMap tm_kb,
                const __grid_constant__ CUtensorMap tm_vb, Problem pb) {
   using L = Layout<D>;
-  if (step_begin(pb.gate)) return;
+  if (gate_closed(pb.gate)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -711,7 +711,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 template <int D>
 __global__ void __launch_bounds__(256)
 attn_tc_combine_kernel(Problem pb, int G, __nv_bfloat16 *__restrict__ O, AttnResidual res) {
-  if (step_begin(pb.gate)) return;
+  if (gate_closed(pb.gate)) return;
   __shared__ int ts[MAX_SEQ + 1], nt[MAX_SEQ + 1], ks[MAX_SEQ + 1], k0[MAX_SEQ + 1];
   build_seq_tables(pb, ts, nt, ks, k0, nullptr);
   __syncthreads();
@@ -872,15 +872,13 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
   pb.Kf = kvi.idx ? Kp : nullptr;
   pb.Vf = kvi.idx ? Vp : nullptr;
   if (kvi.idx)
-    launch_pdl(attn_tc_kernel<D, true>, dim3(G), dim3(THREADS_INDEXED), smem, stream, tq, tkp,
-               tvp, tkb, tvb, pb);
+    attn_tc_kernel<D, true><<<G, THREADS_INDEXED, smem, stream>>>(tq, tkp, tvp, tkb, tvb, pb);
   else
-    launch_pdl(attn_tc_kernel<D, false>, dim3(G), dim3(THREADS), smem, stream, tq, tkp, tvp, tkb,
-               tvb, pb);
+    attn_tc_kernel<D, false><<<G, THREADS, smem, stream>>>(tq, tkp, tvp, tkb, tvb, pb);
   if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   const long long warps = (long long)pairs * LB * GQ;
-  launch_pdl(attn_tc_combine_kernel<D>, dim3((unsigned)((warps * 32 + 255) / 256)), dim3(256), 0,
-             stream, pb, G, static_cast<__nv_bfloat16 *>(O), res);
+  attn_tc_combine_kernel<D><<<(int)((warps * 32 + 255) / 256), 256, 0, stream>>>(
+      pb, G, static_cast<__nv_bfloat16 *>(O), res);
   return launch_status();
 }
 

@@ -139,34 +139,6 @@ struct Gate {
   int S;
 };
 
-// Programmatic dependent launch of the per-step kernels: each one lets the
-// next kernel on the stream be launched as soon as all of its own CTAs are
-// running, and waits for the previous kernel's completion (and memory)
-// before reading anything.  The next kernel's launch then overlaps this
-// one instead of following its exit.
-__device__ __forceinline__ void pdl_begin() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-// Launch with programmatic stream serialisation allowed (kernels that start
-// with pdl_begin()).
-template <typename... KArgs, typename... Args>
-static inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                                     cudaStream_t stream, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
-}
-
 // Block-uniform test; every thread of the block must call it, before any
 // other barrier of the kernel.
 __device__ __forceinline__ bool gate_closed(const Gate &g) {
@@ -179,13 +151,6 @@ __device__ __forceinline__ bool gate_closed(const Gate &g) {
   }
   __syncthreads();
   return closed_sh != 0;
-}
-
-// Start of every per-step kernel: the dependent-launch wait, then the step
-// gate.
-__device__ __forceinline__ bool step_begin(const Gate &g) {
-  pdl_begin();
-  return gate_closed(g);
 }
 
 // Prefix keys read through an index instead of a compacted copy: key i of

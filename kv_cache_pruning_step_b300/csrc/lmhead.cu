@@ -29,7 +29,7 @@ lmhead_simt_kernel(const T *__restrict__ h, const T *__restrict__ W,
                    T *__restrict__ logits, float *__restrict__ pmax,
                    float *__restrict__ psum, int32_t *__restrict__ parg,
                    int32_t *status, Gate gate) {
-  if (step_begin(gate)) return;
+  if (gate_closed(gate)) return;
   constexpr int BM = 64, BN = 64, BK = 16;
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
@@ -142,7 +142,7 @@ lmhead_combine_kernel(const float *__restrict__ pmax, const float *__restrict__ 
                       const int32_t *__restrict__ parg, const float *__restrict__ temp, int M,
                       int strips, float *__restrict__ conf, int32_t *__restrict__ argmax,
                       Gate gate) {
-  if (step_begin(gate)) return;
+  if (gate_closed(gate)) return;
   __shared__ Part sh[kCombGroups][kCombRows];
   const int x = threadIdx.x, y = threadIdx.y;
   const int row = blockIdx.x * kCombRows + x;
@@ -176,7 +176,7 @@ lmhead_combine_rows_kernel(const float *__restrict__ pmax, const float *__restri
                            const int32_t *__restrict__ parg, const float *__restrict__ temp,
                            int M, int strips, float *__restrict__ conf,
                            int32_t *__restrict__ argmax, Gate gate) {
-  if (step_begin(gate)) return;
+  if (gate_closed(gate)) return;
   __shared__ Part sh[4];
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float th = temp ? temp[row] : 1.0f;
@@ -242,18 +242,18 @@ int sprint::lmhead_confidence_impl(const void *h, const void *W, const float *te
     if (rc != SPRINT_OK) return rc;
   } else {
     dim3 grid(p.strips, (M + 63) / 64);
-    launch_pdl(lmhead_simt_kernel<float>, grid, dim3(256), 0, stream,
-               static_cast<const float *>(h), static_cast<const float *>(W), temp, M, D, V,
-               static_cast<float *>(logits_out), p.pmax, p.psum, p.parg, status, gate);
+    lmhead_simt_kernel<float><<<grid, 256, 0, stream>>>(
+        static_cast<const float *>(h), static_cast<const float *>(W), temp, M, D, V,
+        static_cast<float *>(logits_out), p.pmax, p.psum, p.parg, status, gate);
     if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   }
   if (M < 4096)
-    launch_pdl(lmhead_combine_rows_kernel, dim3(M), dim3(128), 0, stream, p.pmax, p.psum,
-               p.parg, temp, M, p.strips, conf_out, argmax_out, gate);
+    lmhead_combine_rows_kernel<<<M, 128, 0, stream>>>(p.pmax, p.psum, p.parg, temp, M, p.strips,
+                                                      conf_out, argmax_out, gate);
   else
-    launch_pdl(lmhead_combine_kernel, dim3((M + kCombRows - 1) / kCombRows),
-               dim3(kCombRows, kCombGroups), 0, stream, p.pmax, p.psum, p.parg, temp, M,
-               p.strips, conf_out, argmax_out, gate);
+    lmhead_combine_kernel<<<(M + kCombRows - 1) / kCombRows, dim3(kCombRows, kCombGroups), 0,
+                            stream>>>(p.pmax, p.psum, p.parg, temp, M, p.strips, conf_out,
+                                      argmax_out, gate);
   return launch_status();
 }
 

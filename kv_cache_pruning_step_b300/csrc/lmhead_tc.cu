@@ -95,7 +95,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
                  __nv_bfloat16 *__restrict__ logits, float *__restrict__ pmax,
                  float *__restrict__ psum, int32_t *__restrict__ parg, int32_t *status,
                  unsigned long long cap_ns, int stall_test, Gate gate) {
-  if (step_begin(gate)) return;
+  if (gate_closed(gate)) return;
   // The final waits for in-flight copies and MMAs ignore the abort flag and
   // get at least one second.
   const unsigned long long drain_ns = cap_ns > 1000000000ull ? cap_ns : 1000000000ull;
@@ -406,22 +406,18 @@ int launch_kernel(const CUtensorMap &tm_h, const CUtensorMap &tm_w, const float 
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
-  // Programmatic dependent launch (the kernel starts with step_begin).
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   int grid = units;
   if (kPair) {
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 2;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.numAttrs = 2;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     // Clusters resident at once (pairs of SMs in a GPC); every pair keeps
     // its tiles, so more pairs than fit would only run later.
     static int max_pairs = 0;

@@ -20,7 +20,7 @@ __global__ void unmask_kernel(const float *__restrict__ conf,
                               int32_t *__restrict__ m_out, int LB, int t, int T,
                               float tau, int mode, uint8_t *__restrict__ accepted_out,
                               Gate gate) {
-  if (step_begin(gate)) {  // the block finished earlier: nothing left to unmask
+  if (gate_closed(gate)) {  // the block finished earlier: nothing left to unmask
     const size_t at = (size_t)blockIdx.x * LB + threadIdx.x;
     if (accepted_out && (int)threadIdx.x < LB) accepted_out[at] = 0;
     if (threadIdx.x == 0) m_out[blockIdx.x] = 0;
@@ -78,8 +78,8 @@ int sprint::unmask_impl(const float *conf, const int32_t *argmax, uint8_t *mask,
   if (S == 0) return SPRINT_OK;
   if (!conf || !argmax || !mask || !tokens || !m_out) return SPRINT_ERR_INVALID_ARG;
   const int threads = (LB + 31) / 32 * 32;
-  launch_pdl(unmask_kernel, dim3(S), dim3(threads), 0, stream, conf, argmax, mask, tokens, m_out,
-             LB, t, T, tau, mode, accepted_out, gate);
+  unmask_kernel<<<S, threads, 0, stream>>>(conf, argmax, mask, tokens, m_out, LB, t, T, tau,
+                                           mode, accepted_out, gate);
   return launch_status();
 }
 
