@@ -569,7 +569,12 @@ def run_ours(args):
         "compact": ("hbm", 2 * 2 * kept * row_b),
         "attn_full": ("hbm", 2 * (n_rows + w.S * w.LB) * row_b),
         "attn_pruned": ("hbm", 2 * (kept + w.S * w.LB) * row_b),
-        "lmhead_block": ("hbm", w.V * w.D * 2),
+        # the block LM head streams W once: HBM-bound for few rows, tensor-bound
+        # once its arithmetic intensity (about S * LB flop per byte) passes
+        # the machine's ridge (peak flop/s over copy bytes/s)
+        "lmhead_block": (("tensor", 2.0 * w.S * w.LB * w.D * w.V)
+                         if w.S * w.LB > peaks["bf16_tflops"] * 1e3 / peaks["hbm_gbs"]
+                         else ("hbm", w.V * w.D * 2)),
     }
     kernels = {}
     for k, (bound, amount) in work.items():
