@@ -417,6 +417,12 @@ int sprint_unmask(const float *conf, const int32_t *argmax, uint8_t *mask,
  *                                            keeps them from overlapping)
  *   kept_idx                                 NULL, or int32 [total_kept]: the
  *                                            indexed pruned prefix (t >= 1)
+ *   step0_given                              != 0: conf and argmax already
+ *                                            hold step 0's block confidences
+ *                                            (computed by the caller, e.g.
+ *                                            with the prefix rows in one LM-
+ *                                            head call); step 0 skips its LM
+ *                                            head (not with residual)
  *   residual, h_res                          residual != 0: every step's LM
  *                                            head reads h_res = h[t] + O of
  *                                            the last layer (heads
@@ -455,6 +461,7 @@ typedef struct sprint_steps_args {
   const int32_t *kept_idx;
   int residual;
   void *h_res;
+  int step0_given;
 } sprint_steps_args;
 
 int sprint_decode_steps(const sprint_steps_args *args, cudaStream_t stream);

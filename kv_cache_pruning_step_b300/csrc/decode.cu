@@ -32,6 +32,7 @@ extern "C" int sprint_decode_steps(const sprint_steps_args *a, cudaStream_t stre
   for (int t = 0; t < a->T; ++t)
     if (!a->Q[t] || !a->Kb[t] || !a->Vb[t] || !a->h[t]) return SPRINT_ERR_INVALID_ARG;
   if (a->residual && (!a->h_res || a->Hq * a->d != a->D)) return SPRINT_ERR_INVALID_ARG;
+  if (a->residual && a->step0_given) return SPRINT_ERR_INVALID_ARG;
   const int S = a->S, LB = a->LB, M = S * LB;
   if (cudaMemsetAsync(a->mask, 1, (size_t)M, stream) != cudaSuccess ||
       cudaMemsetAsync(a->tokens, 0xff, (size_t)M * sizeof(int32_t), stream) != cudaSuccess)
@@ -54,7 +55,7 @@ extern "C" int sprint_decode_steps(const sprint_steps_args *a, cudaStream_t stre
                            gate, stream);
     if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 1, stream);
     if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 2, stream);
-    if (rc == SPRINT_OK)
+    if (rc == SPRINT_OK && !(t == 0 && a->step0_given))
       rc = lmhead_confidence_impl(a->residual ? a->h_res : a->h[t], a->W, a->theta ? a->theta[t] : nullptr, M, a->D,
                                   a->vocab, a->dtype, a->logits, a->conf, a->argmax, a->ws_lm,
                                   a->ws_lm_bytes, a->status, gate, stream);

@@ -44,6 +44,7 @@ class PendingBlock:
     stage_events: list         # (stage, start, end) of the prefix pass
     tokens: torch.Tensor       # live device token buffer of the decoder
     result: BlockResult = None
+    step0_given: bool = False  # step 0's block LM head ran with the prefix rows
 
 
 class BlockDecoder:
@@ -263,7 +264,7 @@ class BlockDecoder:
         return evs
 
     # -- the individual stages (each is one or two library calls) --------
-    def prefix_pass(self, K, V, H, theta, modality, conf_from=0, image=None):
+    def prefix_pass(self, K, V, H, theta, modality, conf_from=0, image=None, step0=None):
         """Step-0 scoring and pruning: confidences of every prefix row, the
         kept set, and the pruned cache (self.Kp / self.Vp; not made when the
         decoder reads the kept rows through their indices).
@@ -275,13 +276,21 @@ class BlockDecoder:
         prefix stays below 4096 rows both ways of computing it use the same
         vocabulary strips and fold order, so the result is bit-identical;
         above that the full-prefix call folds wider strips and the two agree
-        to rounding."""
+        to rounding.
+
+        step0 (with conf_from > 0): the block's step-0 inputs; the new prefix
+        rows and the block's step-0 rows then go through one LM-head call
+        (one pass over W instead of two), which fills self.conf_blk and
+        self.argmax_blk for step 0 as well.  Returns True when it did."""
         r0 = int(conf_from)
         if r0:
             if self.S != 1 or not 0 < r0 <= self.total_rows:
                 raise ValueError("conf_from needs one sequence and 0 < conf_from <= rows")
+        merged = False
         with self._stage("lmhead_prefix"):
-            if r0 < self.total_rows:
+            if r0 and step0 is not None and r0 < self.total_rows:
+                merged = self._merged_lmhead(H, theta, r0, step0)
+            if not merged and r0 < self.total_rows:
                 sp.sprint_lmhead_confidence(
                     H[r0:], self.W, theta[r0:], conf=self.conf_prefix[r0:],
                     argmax=self.argmax_prefix[r0:] if self.prefix_argmax else None,
@@ -304,11 +313,44 @@ class BlockDecoder:
                                             score=self.score, ws=self.ws_score,
                                             status=self.status)
         if self.indexed:
-            return
+            return merged
         with self._stage("compact"):
             sp.sprint_compact_kv(K, V, self.prefix_off, self.total_rows, self.NL, self.Hkv,
                                  self.d, self.kept_idx, self.kept_off, self.total_kept,
                                  Kp=self.Kp, Vp=self.Vp, status=self.status)
+        return merged
+
+    def _merged_lmhead(self, H, theta, r0, step0):
+        """One LM-head call over the new prefix rows [r0, n) and the block's
+        step-0 rows, laid side by side (device copies); its outputs are
+        copied back to the prefix and block buffers.  A row's result does
+        not depend on the other rows of the call, so this equals the two
+        separate calls bit for bit while both stay below 4096 rows."""
+        if step0.get("theta") is None:
+            return False
+        n_new, M_blk = self.total_rows - r0, self.S * self.LB
+        rows = n_new + M_blk
+        if rows >= 4096 or self.total_rows >= 4096:  # keep both calls on the same strips
+            return False
+        dt = self._dt
+        if sp.sprint_lmhead_workspace_bytes(rows, self.D, self.V, dt) > self.ws_lm_prefix.numel():
+            return False
+        hm = self._buf("h_merge", rows * self.D, self.dtype).view(rows, self.D)
+        tm = self._buf("theta_merge", rows, torch.float32)
+        cm = self._buf("conf_merge", rows, torch.float32)
+        am = self._buf("argmax_merge", rows, torch.int32)
+        hm[:n_new].copy_(H[r0:])
+        hm[n_new:].copy_(step0["h"])
+        tm[:n_new].copy_(theta[r0:])
+        tm[n_new:].copy_(step0["theta"])
+        sp.sprint_lmhead_confidence(hm, self.W, tm, conf=cm, argmax=am, ws=self.ws_lm_prefix,
+                                    status=self.status)
+        self.conf_prefix[r0:].copy_(cm[:n_new])
+        if self.prefix_argmax:
+            self.argmax_prefix[r0:].copy_(am[:n_new])
+        self.conf_blk.copy_(cm[n_new:])
+        self.argmax_blk.copy_(am[n_new:])
+        return True
 
     def step(self, t, x, K, V):
         """One denoising step.  K, V: the full prefix cache; step 0 attends
@@ -365,9 +407,14 @@ class BlockDecoder:
         self._next_slot ^= 1
         if self._slots[slot] is not None:  # at most two blocks in flight
             self.finish(self._slots[slot])
-        self.prefix_pass(prefix["K"], prefix["V"], prefix["H"], prefix["theta"],
-                         prefix["modality"], conf_from=conf_from, image=prefix.get("image"))
         xs = [steps(t) for t in range(self.T)]
+        # With the prefix-confidence cache, step 0's block rows share the
+        # prefix LM-head call (not with the residual chain: there step 0's
+        # h depends on its attention).
+        step0_given = self.prefix_pass(
+            prefix["K"], prefix["V"], prefix["H"], prefix["theta"], prefix["modality"],
+            conf_from=conf_from, image=prefix.get("image"),
+            step0=xs[0] if conf_from and not self.residual and not self.want_logits else None)
         events = self._events_for_steps(slot) if self.timing is not None else None
         sp.sprint_decode_steps(
             Q=[x["Q"] for x in xs], Kb=[x["Kb"] for x in xs], Vb=[x["Vb"] for x in xs],
@@ -379,12 +426,14 @@ class BlockDecoder:
             argmax=self.argmax_blk, mask=self.mask, tokens=self.tokens, m_hist=self.m_hist,
             ws_attn=self.ws_attn, ws_lm=self.ws_lm_blk, status=self.status,
             logits=self.logits, events=events,
-            kept_idx=self.kept_idx if self.indexed else None, h_res=self.h_res)
+            kept_idx=self.kept_idx if self.indexed else None, h_res=self.h_res,
+            step0_given=step0_given)
         m_host = self._m_hist_host[slot]
         m_host.copy_(self.m_hist, non_blocking=True)
         done = self._done[slot]
         done.record()
-        pending = PendingBlock(slot, done, m_host, events, self._pending, self.tokens)
+        pending = PendingBlock(slot, done, m_host, events, self._pending, self.tokens,
+                               step0_given=step0_given)
         self._pending = []
         self._slots[slot] = pending
         return self.finish(pending) if wait else pending
@@ -407,6 +456,8 @@ class BlockDecoder:
                 ev = pending.step_events
                 for k, name in enumerate(("attn_full" if t == 0 else "attn_pruned",
                                           "lmhead_block", "unmask")):
+                    if t == 0 and name == "lmhead_block" and pending.step0_given:
+                        continue  # computed within the prefix LM-head stage
                     if ev[6 * t + 2 * k] is not None:
                         timing.append((name, ev[6 * t + 2 * k], ev[6 * t + 2 * k + 1]))
         if self.timing is not None:

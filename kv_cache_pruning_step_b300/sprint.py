@@ -70,7 +70,7 @@ class StepsArgs(ctypes.Structure):
         ("ws_attn", _P), ("ws_attn_bytes", ctypes.c_size_t),
         ("ws_lm", _P), ("ws_lm_bytes", ctypes.c_size_t),
         ("status", _P), ("events", _P), ("kept_idx", _P),
-        ("residual", ctypes.c_int), ("h_res", _P),
+        ("residual", ctypes.c_int), ("h_res", _P), ("step0_given", ctypes.c_int),
     ]
 
 
@@ -372,7 +372,8 @@ def _ptr_array(tensors, dtype, name):
 def sprint_decode_steps(*, Q, Kb, Vb, h, theta, Kf, Vf, prefix_off, max_rows, total_rows,
                         Kp, Vp, kept_off, max_kept, total_kept, W, T, tau, mode, O, conf,
                         argmax, mask, tokens, m_hist, ws_attn, ws_lm, status, accepted=None,
-                        logits=None, events=None, kept_idx=None, h_res=None, stream=None):
+                        logits=None, events=None, kept_idx=None, h_res=None,
+                        step0_given=False, stream=None):
     """Every denoising step of one block in one call (see include/sprint.h).
 
     Q, Kb, Vb: lists of T tensors [S][NL][LB][*][d]; h: list of T [S*LB][D];
@@ -410,6 +411,7 @@ def sprint_decode_steps(*, Q, Kb, Vb, h, theta, Kf, Vf, prefix_off, max_rows, to
     a.kept_idx = _ptr(kept_idx, torch.int32, "kept_idx")
     a.residual = 1 if h_res is not None else 0
     a.h_res = _ptr(h_res, Q[0].dtype, "h_res")
+    a.step0_given = 1 if step0_given else 0
     ev = None
     if events is not None:
         ev = (ctypes.c_void_p * len(events))(*[e.cuda_event if e is not None else None

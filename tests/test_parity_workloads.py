@@ -146,8 +146,8 @@ def test_sequential_blocks(sp, block):
 def test_sequential_prefix_confidence_cache_is_bit_exact(sp):
     """Block b+1's prefix is block b's plus the rows generated in between:
     reusing block b's prefix confidences and sending only the new rows
-    through the LM head gives bit-identical confidences, kept set and
-    decoded tokens."""
+    through the LM head (together with the block's step-0 rows) gives
+    bit-identical confidences, kept set and decoded tokens."""
     from kv_cache_pruning_step_b300 import BlockDecoder
     w = WORKLOADS["sequential-64-blocks"]
     W, _ = weights_of(w.name)
@@ -181,3 +181,5 @@ def test_sequential_prefix_confidence_cache_is_bit_exact(sp):
     assert torch.equal(dec.conf_prefix, fresh_dec.conf_prefix)
     assert torch.equal(dec.kept_idx, fresh_dec.kept_idx)
     assert cached.steps == fresh.steps and torch.equal(cached.tokens, fresh.tokens)
+    # the cached decode ran step 0's block LM head within the prefix call
+    assert cached.accepted_per_step == fresh.accepted_per_step
