@@ -131,15 +131,6 @@ def lm_confidence(h, W, theta=None, rows=None, chunk=64, want_logits=False):
     return c, am, z_all
 
 
-def logits_rows(h, W, theta=None, rows=None):
-    """Temperature-scaled logits z = (h . W_v) / theta for selected rows."""
-    h = _f64(h)
-    W = _f64(W)
-    rows = np.arange(h.shape[0]) if rows is None else np.asarray(rows)
-    th = np.ones(h.shape[0]) if theta is None else _f64(theta)
-    return (h[rows] @ W.T) / th[rows][:, None]
-
-
 # --------------------------------------------------------------------------
 # Composite score and modality-aware keep (paper: Sparse Prefix Retention)
 # --------------------------------------------------------------------------

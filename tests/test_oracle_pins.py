@@ -77,8 +77,9 @@ def test_importance_degenerate():
 # -------------------------------------------------------------- confidence
 def brute_confidence(h, W, theta):
     """Softmax written the textbook way with explicit loops: p_v = e^{z_v} /
-    sum_u e^{z_u}, no max-subtraction; argmax by first strict improvement."""
-    out_c, out_a = [], []
+    sum_u e^{z_u}, no max-subtraction; argmax by first strict improvement.
+    Also returns the loop-computed logits z."""
+    out_c, out_a, out_z = [], [], []
     for i in range(len(h)):
         z = []
         for v in range(len(W)):
@@ -94,14 +95,17 @@ def brute_confidence(h, W, theta):
                 best = v
         out_c.append(max(p))
         out_a.append(best)
-    return np.array(out_c), np.array(out_a)
+        out_z.append(z)
+    return np.array(out_c), np.array(out_a), np.array(out_z)
 
 
 def check_confidence_golden(fn):
     for case in load("confidence_hand.json")["cases"]:
-        c, am, _ = fn(np.array(case["h"]), np.array(case["W"]), np.array(case["theta"]))
+        c, am, z = fn(np.array(case["h"]), np.array(case["W"]), np.array(case["theta"]),
+                      want_logits=True)
         np.testing.assert_allclose(c, case["expected_c"], rtol=1e-14)
         np.testing.assert_array_equal(am, case["expected_argmax"])
+        np.testing.assert_allclose(z, case["expected_logits"], rtol=1e-14, atol=1e-15)
 
 
 def check_confidence_brute(fn):
@@ -110,10 +114,11 @@ def check_confidence_brute(fn):
     h = rng.normal(size=(M, D))
     W = rng.normal(size=(V, D)) * 0.7
     theta = rng.uniform(0.5, 4.0, size=M)
-    c, am, _ = fn(h, W, theta)
-    bc, ba = brute_confidence(h, W, theta)
+    c, am, z = fn(h, W, theta, want_logits=True)
+    bc, ba, bz = brute_confidence(h, W, theta)
     np.testing.assert_allclose(c, bc, rtol=1e-12)
     np.testing.assert_array_equal(am, ba)
+    np.testing.assert_allclose(z, bz, rtol=1e-12, atol=1e-14)
 
 
 def test_confidence_golden():
@@ -169,7 +174,10 @@ def test_confidence_rows_subset_and_logits():
     cs, ams, _ = orc.lm_confidence(h, W, th, rows=[7, 2])
     np.testing.assert_allclose(cs, c[[7, 2]], rtol=1e-14)
     np.testing.assert_array_equal(ams, am[[7, 2]])
-    np.testing.assert_allclose(z, orc.logits_rows(h, W, th), rtol=1e-14, atol=1e-15)
+    # logits of a row subset are those rows of the full logits, and chunking
+    # does not change them
+    _, _, zs = orc.lm_confidence(h, W, th, rows=[7, 2], want_logits=True, chunk=1)
+    np.testing.assert_allclose(zs, z[[7, 2]], rtol=1e-14, atol=1e-15)
 
 
 # ------------------------------------------------------------ keep / select
@@ -579,9 +587,23 @@ def test_planted_mistakes_are_caught():
         c, am, z = orc.lm_confidence(h, W, th, want_logits=True)
         am = z.shape[1] - 1 - np.argmax(z[:, ::-1], axis=1)
         return c, am, z
+    # logits offset by their maximum: c and argmax are blind to the shift,
+    # the hand-worked logits are not
+    def shifted_logits(h, W, th, **kw):
+        c, am, z = orc.lm_confidence(h, W, th, want_logits=True)
+        return c, am, z - z.max(axis=1, keepdims=True)
+
+    # logits left without the temperature while c keeps it
+    def logits_no_temp(h, W, th, **kw):
+        c, am, _ = orc.lm_confidence(h, W, th)
+        _, _, z = orc.lm_confidence(h, W, None, want_logits=True)
+        return c, am, z
     _fails(check_confidence_brute, no_temp)
     _fails(check_confidence_brute, mul_temp)
     _fails(check_confidence_golden, last_argmax)
+    _fails(check_confidence_golden, shifted_logits)
+    _fails(check_confidence_brute, shifted_logits)
+    _fails(check_confidence_golden, logits_no_temp)
 
     # selection: ties to the higher index / one pooled ranking / ceil for floor
     def ties_high(s, mod, rt, ri):
