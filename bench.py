@@ -248,14 +248,52 @@ def nbytes(d):
 
 
 # ---------------------------------------------------------------- oracle timing
-def cpu_baseline(w, pres, steps_host, W, steps_per_block, sample_rows=128,
+# Prefix rows whose LM-head confidences the CPU legs compute per sample; the
+# cpu_baseline leg and the reference arm use the same sample.
+CPU_SAMPLE_ROWS = 128
+
+
+def host_f64(t):
+    """fp64 numpy copy of a host tensor (bf16 widened exactly)."""
+    import numpy as np
+    if hasattr(t, "detach"):
+        t = t.detach().cpu()
+        if str(t.dtype) in ("torch.bfloat16", "torch.float16"):
+            t = t.float()
+        t = t.numpy()
+    return np.asarray(t, dtype=np.float64)
+
+
+def cpu_inputs(pres, steps_host, W):
+    """Inputs of the CPU legs, widened to fp64 once, before any timing.
+
+    The oracle expands what it is given to fp64 on entry.  Handing it
+    bf16 tensors would charge every call the widening of all of W (2.6 GB
+    in fp64) or of every layer's keys, and the sample's scale factors would
+    then multiply that fixed cost as if it were per-row work."""
+    p = pres[0]
+    x = steps_host[0]
+    one = lambda a: host_f64(a[0])  # noqa: E731  (first sequence of the stacked inputs)
+    return {
+        "K": host_f64(p["K"]), "V": host_f64(p["V"]), "H": host_f64(p["H"]),
+        "theta": host_f64(p["theta"]), "modality": p["modality"].numpy(),
+        "image": p["image"].numpy() if "image" in p else None,
+        "W": host_f64(W),
+        "Q": one(x["Q"]), "Kb": one(x["Kb"]), "Vb": one(x["Vb"]),
+        "h": host_f64(x["h"]), "theta_b": host_f64(x["theta"]),
+    }
+
+
+def cpu_baseline(w, ci, steps_per_block, sample_rows=CPU_SAMPLE_ROWS,
                  selection="modality", r_global=0.5):
     """The oracle, as it stands, on a bounded sample of one block.
 
+    `ci` are the fp64 inputs of cpu_inputs (widened before this call).
     Measured: key-norm importance, selection and compaction of the whole
-    prefix; prefix confidences of `sample_rows` rows (scaled to all rows);
-    block attention of layer 0 at the full and at the pruned prefix (scaled
-    to all layers); the block LM head and unmask of one step (whole)."""
+    prefix; prefix confidences of `sample_rows` rows (scaled to all rows:
+    the work per row is one row of the logits and its softmax); block
+    attention of layer 0 at the full and at the pruned prefix (scaled to
+    all layers); the block LM head and unmask of one step (whole)."""
     import numpy as np
 
     from oracle import sprint_oracle as orc
@@ -264,46 +302,44 @@ def cpu_baseline(w, pres, steps_host, W, steps_per_block, sample_rows=128,
         cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
     except Exception:  # noqa: BLE001
         cores = os.cpu_count()
-    p = pres[0]
-    n = p["modality"].numel()
+    n = ci["modality"].size
     t0 = time.perf_counter()
-    imp = orc.key_norm_importance(p["K"])
+    imp = orc.key_norm_importance(ci["K"])
     t_imp = time.perf_counter() - t0
     rows = np.linspace(0, n - 1, min(sample_rows, n)).astype(np.int64)
     t0 = time.perf_counter()
-    c_s, _, _ = orc.lm_confidence(p["H"], W, p["theta"], rows=rows)
-    t_conf = (time.perf_counter() - t0) * n / len(rows)
+    c_s, _, _ = orc.lm_confidence(ci["H"], ci["W"], ci["theta"], rows=rows)
+    t_conf_sample = time.perf_counter() - t0
+    t_conf = t_conf_sample * n / len(rows)
     conf_all = np.full(n, float(np.mean(c_s)))
     conf_all[rows] = c_s
     t0 = time.perf_counter()
     score = orc.composite_score(imp, conf_all, w.alpha)
     if selection == "modality":
-        kept = orc.select_kept(score, p["modality"].numpy(), w.r_text, w.r_img)
+        kept = orc.select_kept(score, ci["modality"], w.r_text, w.r_img)
     else:
-        pool = p["image"].numpy() if selection == "per_image" else np.zeros(n, np.int64)
+        pool = ci["image"] if selection == "per_image" else np.zeros(n, np.int64)
         sizes = np.bincount(pool).tolist()
         keep = orc.pool_keep_counts(sizes, selection, w.r_text, w.r_img, r_global)
         kept = orc.select_kept_pools(score, pool, keep)
-    Kp = orc.compact(p["K"], kept)
-    Vp = orc.compact(p["V"], kept)
+    Kp = orc.compact(ci["K"], kept)
+    Vp = orc.compact(ci["V"], kept)
     t_sel = time.perf_counter() - t0
-    x = steps_host[0]
-    one = lambda a: a[0]  # noqa: E731  (first sequence of the stacked inputs)
     t0 = time.perf_counter()
-    orc.block_attention(one(x["Q"]), p["K"], p["V"], one(x["Kb"]), one(x["Vb"]), layers=[0])
-    t_attn_full = (time.perf_counter() - t0) * w.NL
+    orc.block_attention(ci["Q"], ci["K"], ci["V"], ci["Kb"], ci["Vb"], layers=[0])
+    t_attn_full_l0 = time.perf_counter() - t0
     t0 = time.perf_counter()
-    orc.block_attention(one(x["Q"]), Kp, Vp, one(x["Kb"]), one(x["Vb"]), layers=[0])
-    t_attn_pruned = (time.perf_counter() - t0) * w.NL
+    orc.block_attention(ci["Q"], Kp, Vp, ci["Kb"], ci["Vb"], layers=[0])
+    t_attn_pruned_l0 = time.perf_counter() - t0
     t0 = time.perf_counter()
-    c_b, am_b, _ = orc.lm_confidence(x["h"][:w.LB], W, x["theta"][:w.LB])
+    c_b, am_b, _ = orc.lm_confidence(ci["h"][:w.LB], ci["W"], ci["theta_b"][:w.LB])
     orc.unmask_step(c_b, am_b, np.ones(w.LB, bool), np.full(w.LB, -1), 0, w.T, w.tau)
     t_step_head = time.perf_counter() - t0
     extra = max(steps_per_block - 1, 0)
-    t_block = (t_imp + t_conf + t_sel + t_attn_full + t_step_head
-               + extra * (t_attn_pruned + t_step_head))
-    measured = t_imp + t_conf * len(rows) / n + t_sel + (t_attn_full + t_attn_pruned) / w.NL \
-        + t_step_head
+    t_block = (t_imp + t_conf + t_sel + t_attn_full_l0 * w.NL + t_step_head
+               + extra * (t_attn_pruned_l0 * w.NL + t_step_head))
+    measured = (t_imp + t_conf_sample + t_sel + t_attn_full_l0 + t_attn_pruned_l0
+                + t_step_head)
     return {
         "value": steps_per_block / t_block,
         "unit": "steps/s",
@@ -312,7 +348,9 @@ def cpu_baseline(w, pres, steps_host, W, steps_per_block, sample_rows=128,
         "tokens_per_s": w.LB / t_block,
         "block_s_extrapolated": t_block,
         "measured_s": measured,
-        "sample": (f"one block of sequence 0 ({n}-row prefix): key norms, selection and "
+        "extrapolation": round(t_block / measured, 2),
+        "sample": (f"one block of sequence 0 ({n}-row prefix), inputs widened to fp64 once "
+                   f"before timing (widening excluded): key norms, selection and "
                    f"compaction of the whole prefix; LM-head confidences of {len(rows)} of "
                    f"{n} prefix rows scaled x{n / len(rows):.0f}; attention of layer 0 of "
                    f"{w.NL} scaled x{w.NL} (full prefix, then pruned); one step's block LM "
@@ -638,8 +676,9 @@ def run_ours(args):
         "e2e": e2e, "full_retention_comparison": compare,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, pres, steps_h, W_h, n_steps / args.steps,
-                                           selection=args.selection, r_global=args.r_global)
+        out["cpu_baseline"] = cpu_baseline(w, cpu_inputs(pres, steps_h, W_h),
+                                           n_steps / args.steps, selection=args.selection,
+                                           r_global=args.r_global)
     if rank == 0:
         print(json.dumps(out))
     if world > 1:
@@ -761,31 +800,39 @@ def run_sequential(args):
 # ---------------------------------------------------------------- reference arm
 def run_reference(args):
     """The CPU oracle as the reference arm: each bench step is one bounded
-    sample of a block (see cpu_baseline), timed on the host cores."""
+    sample of a block (the cpu_baseline sample), timed on the host cores;
+    the line's value is the block rate extrapolated from the samples."""
     rank, world, local = rank_info()
     if rank != 0:
         return
     from workload import WORKLOADS
     w = WORKLOADS[args.workload]
     prefix_h, steps_h, W_h, counts, pres = build_inputs(w, [0], "cpu")
+    ci = cpu_inputs(pres, steps_h, W_h)
     for _ in range(args.warmup):
-        cpu_baseline(w, pres, steps_h, W_h, w.T, sample_rows=32)
+        cpu_baseline(w, ci, w.T)
     vals = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        vals.append(cpu_baseline(w, pres, steps_h, W_h, w.T, sample_rows=32))
+        vals.append(cpu_baseline(w, ci, w.T))
     wall = time.perf_counter() - t0
     block_s = statistics.mean(v["block_s_extrapolated"] for v in vals)
     value = w.T / block_s
     cb = dict(vals[-1])
     cb["value"] = value
+    cb["block_s_extrapolated"] = block_s
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
         "tokens_per_s": w.LB / block_s, "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": 1e3 * block_s, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
         "config": {"workload": w.name, "description": w.description,
-                   "bench_step": "one block, oracle on a bounded sample, extrapolated"},
+                   "bench_step": ("one bounded sample of a block (the oracle on the sample "
+                                  "cpu_baseline describes); ms_per_step is the measured time "
+                                  "of one sample, value the block rate extrapolated from it")},
+        "samples": args.steps, "measured_s": wall,
+        "extrapolated_ms_per_block": 1e3 * block_s,
         "cpu_baseline": cb, "wall_s": wall,
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

@@ -785,15 +785,16 @@ attn_tc_combine_kernel(Problem pb, int G, __nv_bfloat16 *__restrict__ O, AttnRes
 }
 
 EncodeTiledFn encode3() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
+  // Looked up once per process (a thread-safe static initialisation).
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     cudaDriverEntryPointQueryResult q;
     void *p = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+      return reinterpret_cast<EncodeTiledFn>(p);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -833,22 +834,19 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
     tvp = tvb;
   }
   // As many ring stages as fit next to Q, the barriers and the tables.
-  static int optin = 0;
-  if (!optin) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(attn_tc_kernel<D, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             optin - 256) != cudaSuccess ||
-        cudaFuncSetAttribute(attn_tc_kernel<D, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             optin - 256) != cudaSuccess) {
-      optin = 0;
-      return SPRINT_ERR_CUDA;
-    }
-  }
+  static PerDevice optin_cache;
+  int optin = 0;
+  if (!optin_cache.get(&optin, [](int dev, int *v) {
+        return cudaDeviceGetAttribute(v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ==
+                   cudaSuccess &&
+               cudaFuncSetAttribute(attn_tc_kernel<D, false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    *v - 256) == cudaSuccess &&
+               cudaFuncSetAttribute(attn_tc_kernel<D, true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    *v - 256) == cudaSuccess;
+      }))
+    return SPRINT_ERR_CUDA;
   int stages = MAX_STAGES;
   while (stages > 2 && Lt::smem_bytes(stages, S) > (size_t)(optin - 256)) --stages;
   const size_t smem = Lt::smem_bytes(stages, S);

@@ -6,9 +6,38 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/sprint.h"
 
 namespace sprint {
+
+// Host: one int per device ordinal, computed once per device under a lock.
+// Function attributes and occupancy belong to one device's context, so a
+// process that calls the library on several devices (or from several host
+// threads) needs them per device.
+struct PerDevice {
+  static constexpr int kMax = 64;
+  std::mutex mu;
+  int value[kMax] = {};
+  bool ready[kMax] = {};
+  // *out = the current device's value; init(dev, &v) computes it the first
+  // time.  False when the device cannot be read or init fails (init is then
+  // tried again on the next call).
+  template <typename F> bool get(int *out, F init) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMax) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ready[dev]) {
+      int v = 0;
+      if (!init(dev, &v)) return false;
+      value[dev] = v;
+      ready[dev] = true;
+    }
+    *out = value[dev];
+    return true;
+  }
+};
 
 // Host: kernel launches made by this library in this process.
 void count_launches(int n);

@@ -10,23 +10,29 @@
 // Design (one persistent CTA per SM, 192 threads, 1 CTA/SM):
 //   warp 0      TMA producer: 128x64 tiles of h and BNx64 tiles of W (bf16,
 //               128-byte swizzle) into a shared-memory ring of as many
-//               stages as fit in 227 KB; BN = 256 (4 stages), or 224 (5
-//               stages) when the call has few rows: the column tiles are
-//               then all the work, and 702 of them spread over 148 SMs more
-//               evenly than 614;
+//               stages as fit in 227 KB; BN = 256, or 224 when the call has
+//               few rows: the column tiles are then all the work, and 702
+//               of them spread over 148 SMs more evenly than 614;
 //   warp 1      allocates 512 TMEM columns; one lane issues
-//               tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16) into
-//               one of two fp32 accumulators (TMEM columns 0 and 256);
+//               tcgen05.mma.kind::f16 (K=16) into one of two fp32
+//               accumulators (TMEM columns 0 and 256);
 //   warps 2-5   epilogue: each thread owns one accumulator row (TMEM lane),
 //               reads its BN columns 32 at a time with tcgen05.ld, and folds
 //               them into (max of raw dot products, first column reaching it
 //               when the caller wants the greedy token, sum of exp2((acc -
 //               max) * log2(e) / theta), one FMA and one ex2.approx per
-//               element); optional logits (acc / theta in bf16).  Warps whose rows all lie past M skip the reduction.
-//               The second accumulator lets the MMA of the next tile overlap
-//               this epilogue.
+//               element); optional logits (acc / theta in bf16).  Warps
+//               whose rows all lie past M skip the reduction.  The second
+//               accumulator lets the MMA of the next tile overlap this
+//               epilogue.
+// Calls with one row tile (block steps) run one CTA per tile with
+// cta_group::1 MMAs of M=128, N=BN.  Calls with two or more row tiles (the
+// prefix) run clusters of two CTAs whose MMAs are one cta_group::2 product
+// of M=256, N=BN: each CTA loads its own h tile and half of the W tile, so
+// W crosses from L2 into the SMs once per pair and each SM's tensor core
+// reads half as much W from shared memory per MMA.
 // Output tiles are visited in bands of 32 column tiles so that a band of W
-// (32 x 256 rows) stays in L2 while all row tiles stream past it.
+// (32 x BN rows) stays in L2 while all row tiles stream past it.
 #include <cuda.h>
 #include <math.h>
 #include <stdlib.h>
@@ -45,15 +51,19 @@ constexpr uint32_t ACC_STRIDE = 256;  // TMEM columns between the two accumulato
 constexpr int THREADS = 192;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Tile shape per column width BN (256, or 224 for calls with few rows).
-template <int BN> struct Tiles {
-  static constexpr int B_BYTES = BN * BK * 2;
+// Tile shape per column width BN (256, or 224 for calls with few rows).  A
+// CTA of a pair (kPair) loads half of each W tile: BN/2 rows.
+template <int BN, bool kPair> struct Tiles {
+  static constexpr int B_ROWS = kPair ? BN / 2 : BN;
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  // As many stages as fit in 227 KB: 5 of 44 KB at BN = 224, 4 of 48 KB at 256.
+  // As many stages as fit in 227 KB: 5 of 44 KB at BN = 224, 4 of 48 KB at
+  // 256; 7 of 30 or 32 KB per CTA of a pair.
   static constexpr int STAGES = (227 * 1024 - 1024 - 256) / STAGE_BYTES;
   static constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
   static_assert(STAGE_BYTES % 1024 == 0, "stages must stay 1024-byte aligned");
   static_assert(BN % 32 == 0 && BN <= 256, "epilogue reads 32 columns at a time");
+  static_assert(8 * (2 * STAGES + 7) <= 256, "barriers, TMEM slot and abort flag fit in 256 bytes");
 };
 
 // max(a, b, c) in one instruction.
@@ -83,11 +93,16 @@ __device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &m,
 
 // kArg: also track the first column reaching each row's maximum (the
 // greedy token).  Without it the chunk maximum is a three-input max tree.
-// kPair: the grid is made of clusters of two CTAs that take row tiles 2i
-// and 2i+1 of the same column tile; rank 0 loads the W tile once for both
-// (TMA multicast), each CTA loads its own h tile, and a stage is reloaded
-// only once the MMAs of both CTAs have read it (each CTA's MMA issuer
-// commits to the empty barrier of both).  This halves the W traffic from L2.
+// kPair: the grid is made of clusters of two CTAs that run their MMAs as
+// one cta_group::2 product of M = 256 rows: rank 0 and rank 1 take row
+// tiles 2i and 2i+1 of the same column tile, and each loads its own h tile
+// and its own half (BN/2 rows) of the W tile, so W is read once per pair.
+// Rank 0 issues the MMAs; both CTAs' copies complete on rank 0's full
+// barrier, its commits arrive on both CTAs' empty and accumulator-full
+// barriers, and rank 1's epilogue hands the accumulator back on rank 0's
+// accumulator-empty barrier.  Each CTA's tensor memory holds its own 128
+// rows of the 128 x BN product: columns [0, BN/2) from rank 0's W half,
+// [BN/2, BN) from rank 1's.
 template <int BN, bool kArg, bool kPair>
 __global__ void __launch_bounds__(THREADS, 1)
 lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
@@ -99,8 +114,9 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
   // The final waits for in-flight copies and MMAs ignore the abort flag and
   // get at least one second.
   const unsigned long long drain_ns = cap_ns > 1000000000ull ? cap_ns : 1000000000ull;
-  constexpr int STAGE_BYTES = Tiles<BN>::STAGE_BYTES;
-  constexpr int STAGES = Tiles<BN>::STAGES;
+  constexpr int STAGE_BYTES = Tiles<BN, kPair>::STAGE_BYTES;
+  constexpr int STAGES = Tiles<BN, kPair>::STAGES;
+  constexpr int B_ROWS = Tiles<BN, kPair>::B_ROWS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -128,12 +144,12 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      tc::mbar_init(tc::smem_u32(full + s), 1);
-      tc::mbar_init(tc::smem_u32(empty + s), kPair ? 2 : 1);  // one commit per CTA
+      tc::mbar_init(tc::smem_u32(full + s), 1);   // the expect-tx arrive (rank 0 of a pair)
+      tc::mbar_init(tc::smem_u32(empty + s), 1);  // one MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(tc::smem_u32(tfull + b), 1);
-      tc::mbar_init(tc::smem_u32(tempty + b), 4);
+      tc::mbar_init(tc::smem_u32(tempty + b), kPair ? 8 : 4);  // epilogue warps (of both CTAs)
     }
     tc::mbar_init(tc::smem_u32(drain), 1);
     tc::mbar_init(tc::smem_u32(never), 1);
@@ -141,8 +157,13 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
     tc::fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
-    tc::tmem_relinquish();
+    if (kPair) {
+      tc::tmem_alloc_pair(tc::smem_u32(tmem_slot), TMEM_COLS);
+      tc::tmem_relinquish_pair();
+    } else {
+      tc::tmem_alloc(tc::smem_u32(tmem_slot), TMEM_COLS);
+      tc::tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
     tc::prefetch_tmap(&tm_h);
@@ -157,7 +178,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer (both CTAs of a pair)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, last_parity = 0;  // bit s: stage s has a load issued
@@ -168,13 +189,20 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
           if (!tc::mbar_wait(tc::smem_u32(empty + stage), phase ^ 1, cap_ns, abort_flag))
             goto producer_done;
           const uint32_t fb = tc::smem_u32(full + stage);
-          tc::mbar_arrive_expect_tx(fb, STAGE_BYTES);  // h tile + W tile (own or multicast)
           const uint32_t sa = tc::smem_u32(smem + stage * STAGE_BYTES);
-          tc::tma_load_2d(sa, &tm_h, fb, kb * BK, m * BM);
-          if (!kPair)
+          if (kPair) {
+            // Both CTAs' tiles complete on rank 0's full barrier, armed by
+            // rank 0 for the two CTAs' bytes.
+            const uint32_t fb0 = tc::map_to_rank(fb, 0);
+            if (rank == 0) tc::mbar_arrive_expect_tx(fb, 2 * STAGE_BYTES);
+            tc::tma_load_2d_pair(sa, &tm_h, fb0, kb * BK, m * BM);
+            tc::tma_load_2d_pair(sa + A_BYTES, &tm_w, fb0, kb * BK,
+                                 n * BN + (int)rank * B_ROWS);
+          } else {
+            tc::mbar_arrive_expect_tx(fb, STAGE_BYTES);  // h tile + W tile
+            tc::tma_load_2d(sa, &tm_h, fb, kb * BK, m * BM);
             tc::tma_load_2d(sa + A_BYTES, &tm_w, fb, kb * BK, n * BN);
-          else if (rank == 0)
-            tc::tma_load_2d_multicast(sa + A_BYTES, &tm_w, fb, kb * BK, n * BN, 0x3);
+          }
           issued |= 1u << stage;
           last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -182,17 +210,20 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       }
     producer_done:
       // Never leave with a copy in flight: wait (bounded) for the last load
-      // issued into every stage.
-      for (int s = 0; s < STAGES; ++s)
-        if (issued >> s & 1u) {
-          volatile int no_abort = 0;
-          tc::mbar_wait(tc::smem_u32(full + s), last_parity >> s & 1u, drain_ns, &no_abort);
-        }
+      // issued into every stage.  Rank 0's full barriers also count rank
+      // 1's copies; rank 1 stays resident until rank 0 has drained (the
+      // cluster barrier before exit).
+      if (!kPair || rank == 0)
+        for (int s = 0; s < STAGES; ++s)
+          if (issued >> s & 1u) {
+            volatile int no_abort = 0;
+            tc::mbar_wait(tc::smem_u32(full + s), last_parity >> s & 1u, drain_ns, &no_abort);
+          }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN, false, false);
+    if (lane == 0 && (!kPair || rank == 0)) {
+      // ---------------- MMA issuer (rank 0 of a pair)
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(kPair ? 2 * BM : BM, BN, false, false);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
@@ -217,19 +248,29 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
           const uint64_t adesc = tc::desc_kmajor_sw128(sa);
           const uint64_t bdesc = tc::desc_kmajor_sw128(sa + A_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)  // +32 bytes along K per step
-            tc::mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+          for (int k = 0; k < BK / 16; ++k) {  // +32 bytes along K per step
+            if (kPair)
+              tc::mma_bf16_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+            else
+              tc::mma_bf16(d, adesc + 2 * k, bdesc + 2 * k, idesc, (kb | k) != 0);
+          }
           if (kPair)
-            tc::mma_commit_multicast(tc::smem_u32(empty + stage), 0x3);
+            tc::mma_commit_pair_multicast(tc::smem_u32(empty + stage), 0x3);
           else
             tc::mma_commit(tc::smem_u32(empty + stage));
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        tc::mma_commit(tc::smem_u32(tfull + buf));
+        if (kPair)
+          tc::mma_commit_pair_multicast(tc::smem_u32(tfull + buf), 0x3);
+        else
+          tc::mma_commit(tc::smem_u32(tfull + buf));
       }
       // Every MMA this thread issued has finished once `drain` completes.
-      tc::mma_commit(tc::smem_u32(drain));
+      if (kPair)
+        tc::mma_commit_pair(tc::smem_u32(drain));
+      else
+        tc::mma_commit(tc::smem_u32(drain));
       volatile int no_abort = 0;
       tc::mbar_wait(tc::smem_u32(drain), 0, drain_ns, &no_abort);
     }
@@ -311,7 +352,14 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
       }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(tempty + buf));
+      if (lane == 0) {
+        // Rank 0's MMA issuer reuses the buffer once every epilogue warp of
+        // the pair has read it.
+        if (kPair)
+          tc::mbar_arrive_cluster(tc::map_to_rank(tc::smem_u32(tempty + buf), 0));
+        else
+          tc::mbar_arrive(tc::smem_u32(tempty + buf));
+      }
       if (vrow) {
         const size_t at = (size_t)n * M + row;
         pmax[at] = run_max;
@@ -323,12 +371,18 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
 
   tc::fence_before_sync();
   __syncthreads();
-  // Neither CTA of a pair leaves while the other may still signal it (its
-  // MMAs' commits are done once its drain wait above has completed).
+  // Neither CTA of a pair leaves, or frees its tensor memory, while the
+  // other may still signal it or write into it (rank 0's MMAs are done once
+  // its drain wait above has completed).
   if (kPair) tc::cluster_sync();
   tc::fence_after_sync();
   if (threadIdx.x == 0 && *abort_flag) report(status, SPRINT_STATUS_TIMEOUT);
-  if (warp == 1) tc::tmem_dealloc(tmem, TMEM_COLS);
+  if (warp == 1) {
+    if (kPair)
+      tc::tmem_dealloc_pair(tmem, TMEM_COLS);
+    else
+      tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -339,15 +393,16 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 }  // namespace
 
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
+  // Looked up once per process (a thread-safe static initialisation).
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     cudaDriverEntryPointQueryResult q;
     void *p = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+      return reinterpret_cast<EncodeTiledFn>(p);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -367,21 +422,19 @@ bool make_tmap_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_
 }
 
 int stall_test_enabled() {
-  static int v = -1;
-  if (v < 0) {
+  static const int v = [] {
     const char *e = getenv("SPRINT_TEST_STALL");
-    v = (e && e[0] == '1') ? 1 : 0;
-  }
+    return (e && e[0] == '1') ? 1 : 0;
+  }();
   return v;
 }
 
 unsigned long long wait_cap_ns() {
-  static unsigned long long cap = 0;
-  if (!cap) {
+  static const unsigned long long cap = [] {
     const char *e = getenv("SPRINT_WAIT_CAP_NS");
-    cap = e ? strtoull(e, nullptr, 10) : 2000000000ull;
-    if (!cap) cap = 1;
-  }
+    const unsigned long long c = e ? strtoull(e, nullptr, 10) : 2000000000ull;
+    return c ? c : 1ull;
+  }();
   return cap;
 }
 
@@ -396,15 +449,16 @@ template <int BN, bool kArg, bool kPair>
 int launch_kernel(const CUtensorMap &tm_h, const CUtensorMap &tm_w, const float *temp, int M,
                   int D, int V, __nv_bfloat16 *logits, const LmheadWs &p, int32_t *status,
                   Gate gate, int units, cudaStream_t stream) {
-  constexpr size_t SMEM_BYTES = Tiles<BN>::SMEM_BYTES;
+  constexpr size_t SMEM_BYTES = Tiles<BN, kPair>::SMEM_BYTES;
   auto kern = lmhead_tc_kernel<BN, kArg, kPair>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES) != cudaSuccess)
-      return SPRINT_ERR_CUDA;
-    attr_set = true;
-  }
+  static PerDevice attr_set;
+  int set = 0;
+  if (!attr_set.get(&set, [&](int, int *v) {
+        *v = 1;
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)SMEM_BYTES) == cudaSuccess;
+      }))
+    return SPRINT_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(THREADS);
@@ -420,13 +474,19 @@ int launch_kernel(const CUtensorMap &tm_h, const CUtensorMap &tm_w, const float 
     cfg.numAttrs = 1;
     // Clusters resident at once (pairs of SMs in a GPC); every pair keeps
     // its tiles, so more pairs than fit would only run later.
-    static int max_pairs = 0;
-    if (!max_pairs) {
-      cfg.gridDim = dim3(2 * units);
-      if (cudaOccupancyMaxActiveClusters(&max_pairs, kern, &cfg) != cudaSuccess ||
-          max_pairs < 1)
-        max_pairs = 1;
-    }
+    static PerDevice pairs_cache;
+    int max_pairs = 1;
+    if (!pairs_cache.get(&max_pairs, [&](int, int *v) {
+          cfg.gridDim = dim3(2 * units);
+          int mp = 0;
+          if (cudaOccupancyMaxActiveClusters(&mp, kern, &cfg) != cudaSuccess || mp < 1) {
+            (void)cudaGetLastError();  // not a launch error: fall back to one pair
+            mp = 1;
+          }
+          *v = mp;
+          return true;
+        }))
+      return SPRINT_ERR_CUDA;
     grid = 2 * (units < max_pairs ? units : max_pairs);
   }
   cfg.gridDim = dim3(grid);
@@ -442,13 +502,15 @@ int launch_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *te
                  int V, __nv_bfloat16 *logits, const LmheadWs &p, int32_t *status, Gate gate,
                  cudaStream_t stream) {
   CUtensorMap tm_h, tm_w;
-  if (!make_tmap_bf16_2d(&tm_h, h, D, M, D, BK, BM) ||
-      !make_tmap_bf16_2d(&tm_w, W, D, V, D, BK, BN))
-    return SPRINT_ERR_CUDA;
   const int num_m = (M + BM - 1) / BM, num_n = (V + BN - 1) / BN;
+  // Calls with two or more row tiles run as CTA pairs; a CTA of a pair
+  // loads BN/2 rows of each W tile.
+  const bool pair = num_m >= 2;
+  if (!make_tmap_bf16_2d(&tm_h, h, D, M, D, BK, BM) ||
+      !make_tmap_bf16_2d(&tm_w, W, D, V, D, BK, pair ? BN / 2 : BN))
+    return SPRINT_ERR_CUDA;
   const int sms = sm_count();
-  // Calls with two or more row tiles run as CTA pairs sharing each W tile.
-  if (num_m >= 2) {
+  if (pair) {
     const int pair_tiles = ((num_m + 1) / 2) * num_n;
     const int pairs = pair_tiles < sms / 2 ? pair_tiles : sms / 2;
     return p.parg ? launch_kernel<BN, true, true>(tm_h, tm_w, temp, M, D, V, logits, p, status,

@@ -474,13 +474,14 @@ extern "C" int sprint_score_prune(const void *K, int S, const int32_t *prefix_of
   // each); the capacity follows the longest sequence the call can hold.
   const int stage_cap = total_rows < kStageMax ? total_rows : kStageMax;
   const size_t stage_bytes = (size_t)((stage_cap + 3) & ~3) * 4 + (size_t)stage_cap + 16;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)((size_t)kStageMax * 5 + 16)) != cudaSuccess)
-      return SPRINT_ERR_CUDA;
-    attr_set = true;
-  }
+  static PerDevice attr_set;
+  int set = 0;
+  if (!attr_set.get(&set, [](int, int *v) {
+        *v = 1;
+        return cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)((size_t)kStageMax * 5 + 16)) == cudaSuccess;
+      }))
+    return SPRINT_ERR_CUDA;
   select_kernel<<<S, kSelThreads, stage_bytes, stream>>>(u, conf, modality, prefix_off,
                                                          kept_off, S, total_rows, alpha, r_text,
                                                          r_img, keys, kept_idx, score_out,
