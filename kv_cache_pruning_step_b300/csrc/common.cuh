@@ -149,6 +149,69 @@ __device__ __forceinline__ int block_excl_scan(int v, int *sh, int *total) {
   return out;
 }
 
+// Canonical sum of the key-norm means u over the n positions of one
+// sequence, the numerator of the mean in I_i.  Its bits do not depend on
+// how a launch divides the work, so kernels that split the positions
+// differently (the two-modality selection in clusters of CTAs, the keep
+// pools in one CTA) reach the same mean:
+//   * a leaf is kLeaf = 1024 consecutive positions; lane j of a warp adds
+//     positions j, j + 32, ..., j + 992 of the leaf in fp32 in that order,
+//     and the 32 lane sums are added in fp64 by an xor butterfly;
+//   * the leaves are added by a complete binary tree over the leaf index,
+//     padded with zero leaves to a power of two.
+// Any division of that tree into aligned power-of-two blocks of leaves
+// (adding +0 changes nothing) gives the same result.
+constexpr int kLeaf = 1024;
+
+__device__ __forceinline__ int next_pow2(int x) { return x <= 1 ? 1 : 1 << (32 - __clz(x - 1)); }
+
+// Sum of leaf g; the same value in every lane.
+__device__ __forceinline__ double u_leaf_sum(const float *__restrict__ u, int n, int g,
+                                             int lane) {
+  const int base = g * kLeaf;
+  float acc = 0.f;
+#pragma unroll
+  for (int i0 = 0; i0 < 32; i0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int p = base + (i0 + i) * 32 + lane;
+      v[i] = p < n ? __ldg(u + p) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc += v[i];
+  }
+  return warp_sum((double)acc);
+}
+
+// Tree sum of the aligned block of `count` leaves (a power of two) that
+// starts at leaf `first`; leaves at or past G are zero.  Whole warp.
+__device__ __forceinline__ double u_subtree_sum(const float *__restrict__ u, int n, int G,
+                                                int first, int count, int lane) {
+  if (first >= G) return 0.0;
+  double stack[32];
+  int level_top = 0;
+  for (int j = 0; j < count; ++j) {
+    const int g = first + j;
+    double v = g < G ? u_leaf_sum(u, n, g, lane) : 0.0;
+    int level = 0;
+    while ((j >> level) & 1) {  // merge complete left subtrees (binary carry)
+      v = stack[level] + v;
+      ++level;
+    }
+    stack[level] = v;
+    level_top = level;
+  }
+  return stack[level_top];
+}
+
+// In-place complete binary tree over v[0..cnt) (cnt a power of two); the
+// sum lands in v[0].
+__device__ __forceinline__ void tree_fold(double *v, int cnt) {
+  for (int step = 1; step < cnt; step <<= 1)
+    for (int q = 0; q + step < cnt; q += 2 * step) v[q] = v[q] + v[q + step];
+}
+
 // Sequence that owns global row `row` under CSR offsets off[0..S].
 __device__ __forceinline__ int csr_owner(const int32_t *off, int S, int row) {
   int lo = 0, hi = S - 1;

@@ -27,9 +27,12 @@
 //                   staged in shared memory (5 bytes per position) when they
 //                   fit, so global memory is read once; longer sequences
 //                   keep them in the workspace.
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace sprint {
 
@@ -122,144 +125,193 @@ keynorm_kernel(const T *__restrict__ K, const int32_t *__restrict__ prefix_off,
 
 constexpr int kSelThreads = 1024;
 constexpr int kDigit = 12, kBins = 1 << kDigit;  // radix digit of the selection
-// Longest sequence whose keys and tags are staged in shared memory:
-// 36,864 x 5 bytes = 180 KB, next to 34 KB of histograms and scan space.
-constexpr int kStageMax = 36864;
+constexpr int kMaxCluster = 8;                     // CTAs per sequence, at most
+// Positions a CTA's slice aims at when the cluster size is chosen, and the
+// longest slice whose keys and tags are staged in shared memory (5 bytes
+// per position); longer slices keep their keys in the workspace.
+constexpr int kSliceTarget = 2048;
+constexpr int kStageCta = 16384;
 
 __device__ __forceinline__ int keep_count_dev(int n, double r) {
   return (int)floor(r * (double)n + 1e-9);
 }
 
-__global__ void __launch_bounds__(kSelThreads)
-select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
-              const uint8_t *__restrict__ modality,
-              const int32_t *__restrict__ prefix_off,
-              const int32_t *__restrict__ kept_off, int S, int total_rows,
-              float alpha, double r_text, double r_img,
-              uint32_t *__restrict__ keys_ws, int32_t *__restrict__ kept_idx,
-              float *__restrict__ score_out, int32_t *status, int stage_cap) {
-  extern __shared__ uint4 stage_raw[];  // [stage_cap rounded up to 4] keys, then tags
-  uint32_t *stage_sh = reinterpret_cast<uint32_t *>(stage_raw);
-  __shared__ uint32_t hist[2][kBins];
-  __shared__ uint32_t kmin_sh[2], kmax_sh[2], prefix_sh[2];
-  __shared__ int shift_sh[2];
-  __shared__ int scan_sh[33];
-  __shared__ double dsum_sh[32];
-  __shared__ int cnt_sh[32];
-  __shared__ float mean_sh;
-  __shared__ uint32_t thresh_sh[2];
-  __shared__ int need_sh[2];
-  __shared__ int mode_sh[2];  // 0 keep none, 1 keep all, 2 threshold
+// What each CTA of a sequence's cluster publishes to the others (read
+// through distributed shared memory after a cluster barrier).
+struct SelXchg {
+  double tree;        // this CTA's block of the canonical sum of u
+  int nimg;           // image positions in the slice
+  uint32_t lo[2];     // smallest / largest key per modality in the slice
+  uint32_t hi[2];
+  uint32_t tot[2];    // keys of the current radix pass in the digits this CTA owns
+  uint32_t digit[2];  // the threshold digit, from the CTA that owns it
+  int need[2];        // keys still to keep inside that digit
+  int cnt[3];         // definite keeps, text ties, image ties in the slice
+};
 
-  const int s = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// Dynamic shared memory: histograms [2][kBins], the cluster sums of the
+// digits this CTA owns [2][kBins / cl] (cl > 1), then the staged keys and
+// tags of the slice.
+__host__ __device__ inline size_t select_smem_bytes(int cl, int cap) {
+  return (size_t)2 * kBins * 4 + (cl > 1 ? (size_t)2 * (kBins / cl) * 4 : 0) + (size_t)cap * 5;
+}
+
+// One cluster of cl CTAs per sequence (cl = 1, 2, 4 or 8, the same for the
+// whole launch); CTA `rank` owns the slice [rank L, rank L + L) of the
+// sequence's positions and the radix digits [rank kBins/cl, ...).
+//   1. the canonical sum of u (common.cuh), the image count, the mean and
+//      the keep counts; every CTA folds the cluster's partials in rank order;
+//   2. s_i = alpha I_i + (1 - alpha) c_i in fp32 with I_i = u_i / mean (an
+//      fp32 division by the fp32-rounded mean), its orderable key, and each
+//      modality's smallest and largest key;
+//   3. radix select of each modality's k-th largest key on keys reduced to
+//      the modality's range, 12 bits per pass from the top: every CTA
+//      histograms its slice, each CTA sums its own digits over the cluster,
+//      and the CTA whose digits hold the k-th key finds the digit;
+//   4. stable compaction in ascending position order: warps count their
+//      definite keeps and threshold ties with ballots, counts are scanned
+//      over the warps and over the cluster's CTAs, and every warp writes its
+//      kept positions to consecutive output slots (ties by ascending
+//      position).
+__global__ void __launch_bounds__(kSelThreads, 1)
+select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
+              const uint8_t *__restrict__ modality, const int32_t *__restrict__ prefix_off,
+              const int32_t *__restrict__ kept_off, int total_rows, float alpha,
+              double r_text, double r_img, uint32_t *__restrict__ keys_ws,
+              int32_t *__restrict__ kept_idx, float *__restrict__ score_out, int32_t *status,
+              int stage_cap) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int cl = (int)cluster.num_blocks(), rank = (int)cluster.block_rank();
+  const int s = blockIdx.x / cl;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  extern __shared__ __align__(16) uint8_t sel_smem[];
+  const int W = kBins / cl;  // digits this CTA owns
+  uint32_t *hist = reinterpret_cast<uint32_t *>(sel_smem);
+  uint32_t *hsum = cl > 1 ? hist + 2 * kBins : hist;  // [2][W]
+  uint32_t *stage_keys = hist + 2 * kBins + (cl > 1 ? 2 * W : 0);
+  uint8_t *stage_tags = reinterpret_cast<uint8_t *>(stage_keys + stage_cap);
+  __shared__ SelXchg xc;
+  __shared__ double wtree[32];
+  __shared__ int scan_sh[33];
+  __shared__ int wcnt[3][32];
+  __shared__ float mean_sh;
+  __shared__ int info_sh[4];  // image count, text keep, image keep, counts consistent
+  __shared__ uint32_t lmin_sh[2], lmax_sh[2], kmin_sh[2], prefix_sh[2];
+  __shared__ int shift_sh[2], need_sh[2], mode_sh[2], qstar_sh[2], above_sh[2];
+
   const int p0 = prefix_off[s], p1 = prefix_off[s + 1];
   const int k0 = kept_off[s], k1 = kept_off[s + 1];
+  // Every CTA of the cluster reads the same offsets, so all of them return
+  // here or none does (before any cluster barrier).
   if (p0 < 0 || p1 < p0 || p1 > total_rows || k0 < 0 || k1 < k0) {
-    if (tid == 0) report(status, SPRINT_STATUS_BAD_OFFSETS);
+    if (rank == 0 && tid == 0) report(status, SPRINT_STATUS_BAD_OFFSETS);
     return;
   }
   const int n = p1 - p0;
-  // Keys and modality tags of this sequence: staged in shared memory when
-  // they fit, else read from the workspace / the caller's array.
-  const bool staged = n <= stage_cap;
-  uint32_t *keys = staged ? stage_sh : keys_ws + p0;
-  // The tags start 16-byte aligned (the key area is rounded up to 4 keys):
-  // the compaction reads 8 tags at a time with one 8-byte load.
-  uint8_t *mod_sh = reinterpret_cast<uint8_t *>(stage_sh + ((stage_cap + 3) & ~3));
-  const uint8_t *mods = staged ? mod_sh : modality + p0;
+  const int L = ((n + cl - 1) / cl + 31) & ~31;
+  const int lo_i = min(n, rank * L), m = min(n, lo_i + L) - lo_i;
+  const int g0 = p0 + lo_i;  // first global row of the slice
+  const bool staged = L <= stage_cap;
+  uint32_t *keys = staged ? stage_keys : keys_ws + g0;
+  const uint8_t *tags = staged ? stage_tags : modality + g0;
+  if (tid < 2) {
+    lmin_sh[tid] = 0xffffffffu;
+    lmax_sh[tid] = 0u;
+  }
 
-  // Pass 1: sum of u and the image count; u is kept (as raw bits) where the
-  // keys will go.  Each thread sums its positions in fp32; the 1024 thread
-  // sums are added in fp64 (FP64 throughput is low on this GPU, so fp64 is
-  // kept off the per-position path).  Loads come in batches of kB per
-  // thread, all issued before any store (stores through `keys` might alias
-  // the byte-typed tag loads, so the compiler would not reorder them).
-  constexpr int kB = 8;
-  float su_f = 0.f;
+  // ---- 1. canonical sum of u; image count; staging of u bits and tags
+  {
+    const int G = (n + kLeaf - 1) / kLeaf, P = next_pow2(G);
+    const int workers = cl * 32, B = P > workers ? P / workers : 1;
+    const int wk = rank * 32 + warp;
+    const double v = wk * B < P ? u_subtree_sum(u + p0, n, G, wk * B, B, lane) : 0.0;
+    if (lane == 0) wtree[warp] = v;
+  }
+  constexpr int kB = 4;
   int nimg = 0;
-  for (int i0 = tid; i0 < n; i0 += kB * kSelThreads) {
+  for (int j0 = tid; j0 < m; j0 += kB * kSelThreads) {
     float ub[kB];
     uint8_t mb[kB];
 #pragma unroll
-    for (int j = 0; j < kB; ++j) {
-      const int i = i0 + j * kSelThreads;
-      ub[j] = i < n ? __ldg(u + p0 + i) : 0.f;
-      mb[j] = i < n ? (__ldg(modality + p0 + i) != 0) : 0;
+    for (int q = 0; q < kB; ++q) {
+      const int j = j0 + q * kSelThreads;
+      ub[q] = j < m ? __ldg(u + g0 + j) : 0.f;
+      mb[q] = j < m ? (__ldg(modality + g0 + j) != 0) : 0;
     }
 #pragma unroll
-    for (int j = 0; j < kB; ++j) {
-      const int i = i0 + j * kSelThreads;
-      su_f += ub[j];
-      nimg += mb[j];
-      if (staged && i < n) {
-        keys[i] = __float_as_uint(ub[j]);
-        mod_sh[i] = mb[j];
+    for (int q = 0; q < kB; ++q) {
+      const int j = j0 + q * kSelThreads;
+      nimg += mb[q];
+      if (staged && j < m) {
+        stage_keys[j] = __float_as_uint(ub[q]);
+        stage_tags[j] = mb[q];
       }
     }
   }
-  double su = warp_sum((double)su_f);
   nimg = warp_sum(nimg);
-  if (lane == 0) { dsum_sh[warp] = su; cnt_sh[warp] = nimg; }
+  if (lane == 0) wcnt[0][warp] = nimg;
   __syncthreads();
-  if (warp == 0) {
-    double v = dsum_sh[lane];
-    int c = cnt_sh[lane];
-    v = warp_sum(v);
-    c = warp_sum(c);
-    if (lane == 0) {
-      // One thread does the fp64 division and the keep counts.
-      const int ni = c, nt = n - c;
-      mean_sh = n > 0 ? (float)(v / (double)n) : 0.f;
-      cnt_sh[0] = ni;
-      cnt_sh[1] = keep_count_dev(nt, r_text);
-      cnt_sh[2] = keep_count_dev(ni, r_img);
+  if (tid == 0) {
+    double v[32];
+    int t = 0;
+    for (int i = 0; i < 32; ++i) {
+      v[i] = wtree[i];
+      t += wcnt[0][i];
     }
+    tree_fold(v, 32);
+    xc.tree = v[0];
+    xc.nimg = t;
+  }
+  cluster.sync();
+  if (tid == 0) {
+    double v[kMaxCluster];
+    int ni = 0;
+    for (int q = 0; q < cl; ++q) {
+      const SelXchg *r = cluster.map_shared_rank(&xc, q);
+      v[q] = r->tree;
+      ni += r->nimg;
+    }
+    tree_fold(v, cl);
+    mean_sh = n > 0 ? (float)(v[0] / (double)n) : 0.f;
+    info_sh[0] = ni;
+    info_sh[1] = keep_count_dev(n - ni, r_text);
+    info_sh[2] = keep_count_dev(ni, r_img);
+    info_sh[3] = k1 - k0 == info_sh[1] + info_sh[2];
   }
   __syncthreads();
   const float mean_f = mean_sh;
-  const int n_img = cnt_sh[0], n_txt = n - n_img;
-  const int k_txt = cnt_sh[1], k_img = cnt_sh[2];
-  if (k1 - k0 != k_txt + k_img) {
-    if (tid == 0) report(status, SPRINT_STATUS_KEPT_MISMATCH);
-    return;
-  }
+  const int n_img = info_sh[0], n_txt = n - n_img;
+  const int k_txt = info_sh[1], k_img = info_sh[2];
 
-  // Pass 2: composite score s_i = alpha I_i + (1 - alpha) c_i in fp32
-  // (I_i = u_i / mean, an fp32 division by the fp32-rounded mean), its
-  // orderable key, and the smallest and largest key of each modality.
-  if (tid < 2) {
-    kmin_sh[tid] = 0xffffffffu;
-    kmax_sh[tid] = 0u;
-  }
-  __syncthreads();
+  // ---- 2. scores, keys, key range per modality
   const float one_m_alpha = 1.0f - alpha;
   uint32_t lo0 = 0xffffffffu, lo1 = 0xffffffffu, hi0 = 0u, hi1 = 0u;
-  for (int i0 = tid; i0 < n; i0 += kB * kSelThreads) {
+  for (int j0 = tid; j0 < m; j0 += kB * kSelThreads) {
     float ub[kB], cb[kB];
     bool ib[kB];
 #pragma unroll
-    for (int j = 0; j < kB; ++j) {
-      const int i = i0 + j * kSelThreads;
-      ub[j] = i < n ? (staged ? __uint_as_float(keys[i]) : __ldg(u + p0 + i)) : 0.f;
-      cb[j] = i < n ? __ldg(conf + p0 + i) : 0.f;
-      ib[j] = i < n && mods[i] != 0;
+    for (int q = 0; q < kB; ++q) {
+      const int j = j0 + q * kSelThreads;
+      ub[q] = j < m ? (staged ? __uint_as_float(stage_keys[j]) : __ldg(u + g0 + j)) : 0.f;
+      cb[q] = j < m ? __ldg(conf + g0 + j) : 0.f;
+      ib[q] = j < m && tags[j] != 0;
     }
 #pragma unroll
-    for (int j = 0; j < kB; ++j) {
-      const int i = i0 + j * kSelThreads;
-      if (i >= n) continue;
-      const float imp = mean_f > 0.0f ? ub[j] / mean_f : 0.0f;
-      const float sc = fmaf(alpha, imp, one_m_alpha * cb[j]);
+    for (int q = 0; q < kB; ++q) {
+      const int j = j0 + q * kSelThreads;
+      if (j >= m) continue;
+      const float imp = mean_f > 0.0f ? ub[q] / mean_f : 0.0f;
+      const float sc = fmaf(alpha, imp, one_m_alpha * cb[q]);
       const uint32_t key = float_key(sc);
-      keys[i] = key;
-      if (ib[j]) {
+      keys[j] = key;
+      if (ib[q]) {
         lo1 = min(lo1, key);
         hi1 = max(hi1, key);
       } else {
         lo0 = min(lo0, key);
         hi0 = max(hi0, key);
       }
-      if (score_out) score_out[p0 + i] = sc;
+      if (score_out) score_out[g0 + j] = sc;
     }
   }
   lo0 = __reduce_min_sync(0xffffffffu, lo0);
@@ -267,103 +319,168 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
   hi0 = __reduce_max_sync(0xffffffffu, hi0);
   hi1 = __reduce_max_sync(0xffffffffu, hi1);
   if (lane == 0) {
-    atomicMin(&kmin_sh[0], lo0);
-    atomicMin(&kmin_sh[1], lo1);
-    atomicMax(&kmax_sh[0], hi0);
-    atomicMax(&kmax_sh[1], hi1);
+    atomicMin(&lmin_sh[0], lo0);
+    atomicMin(&lmin_sh[1], lo1);
+    atomicMax(&lmax_sh[0], hi0);
+    atomicMax(&lmax_sh[1], hi1);
   }
   __syncthreads();
   if (tid < 2) {
-    const int k = tid == 0 ? k_txt : k_img, nm = tid == 0 ? n_txt : n_img;
-    mode_sh[tid] = k <= 0 ? 0 : (k >= nm ? 1 : 2);
-    need_sh[tid] = k;
+    xc.lo[tid] = lmin_sh[tid];
+    xc.hi[tid] = lmax_sh[tid];
+  }
+  cluster.sync();
+  if (!info_sh[3]) {  // the same decision in every CTA of the cluster
+    if (rank == 0 && tid == 0) report(status, SPRINT_STATUS_KEPT_MISMATCH);
+    cluster.sync();  // nobody leaves while another CTA may still read its xc
+    return;
+  }
+  if (tid < 2) {
+    const int mu = tid;
+    uint32_t kmn = 0xffffffffu, kmx = 0u;
+    for (int q = 0; q < cl; ++q) {
+      const SelXchg *r = cluster.map_shared_rank(&xc, q);
+      kmn = min(kmn, r->lo[mu]);
+      kmx = max(kmx, r->hi[mu]);
+    }
+    const int k = mu ? k_img : k_txt, nm = mu ? n_img : n_txt;
+    mode_sh[mu] = k <= 0 ? 0 : (k >= nm ? 1 : 2);
+    need_sh[mu] = k;
+    kmin_sh[mu] = kmn;
+    prefix_sh[mu] = 0u;
     // Keys of the modality relative to its smallest key span `shift` bits;
     // the selection resolves them kDigit bits at a time from the top.
-    const uint32_t range = kmax_sh[tid] - kmin_sh[tid];
-    shift_sh[tid] = mode_sh[tid] == 2 && range ? 32 - __clz(range) : 0;
-    prefix_sh[tid] = 0u;
+    const uint32_t range = kmx - kmn;
+    shift_sh[mu] = mode_sh[mu] == 2 && range ? 32 - __clz(range) : 0;
   }
   __syncthreads();
 
-  // Radix select on d = key - (smallest key of the modality), kDigit bits at
-  // a time from the top, both modalities together: find the k-th largest
-  // key T and how many keys equal to T are kept (ties then go by position).
-  // Range reduction and 4096 bins keep atomic collisions rare.
-  while (__syncthreads_or(tid < 2 && shift_sh[tid] > 0)) {
-    for (int b = tid; b < 2 * kBins; b += kSelThreads) (&hist[0][0])[b] = 0u;
+  // ---- 3. radix select, both modalities together.  The loop condition and
+  // every decision below come from values that are identical in all CTAs
+  // of the cluster, so they pass the same cluster barriers.
+  while (shift_sh[0] > 0 || shift_sh[1] > 0) {
+    for (int b = tid; b < 2 * kBins; b += kSelThreads) hist[b] = 0u;
     __syncthreads();
     const int sh0 = shift_sh[0], sh1 = shift_sh[1];
     const int w0 = sh0 < kDigit ? sh0 : kDigit, w1 = sh1 < kDigit ? sh1 : kDigit;
     const uint32_t pre0 = prefix_sh[0], pre1 = prefix_sh[1];
     const uint32_t base0 = kmin_sh[0], base1 = kmin_sh[1];
-    // Read before the scans below: one thread rewrites need_sh after them.
-    const uint32_t needv0 = (uint32_t)need_sh[0], needv1 = (uint32_t)need_sh[1];
 #pragma unroll 4
-    for (int i = tid; i < n; i += kSelThreads) {
-      const bool img = mods[i] != 0;
+    for (int j = tid; j < m; j += kSelThreads) {
+      const bool img = tags[j] != 0;
       const int sh = img ? sh1 : sh0, w = img ? w1 : w0;
       if (sh == 0) continue;
-      const uint64_t d = (uint64_t)(keys[i] - (img ? base1 : base0));
+      const uint64_t d = (uint64_t)(keys[j] - (img ? base1 : base0));
       if ((uint32_t)(d >> sh) == (img ? pre1 : pre0))
-        atomicAdd(&hist[img][(uint32_t)(d >> (sh - w)) & ((1u << w) - 1u)], 1u);
+        atomicAdd(&hist[(img ? kBins : 0) + ((uint32_t)(d >> (sh - w)) & ((1u << w) - 1u))], 1u);
+    }
+    cluster.sync();  // every CTA's histogram is complete
+    if (cl > 1) {
+      for (int idx = tid; idx < 2 * W; idx += kSelThreads) {
+        const int mu = idx >= W, b = rank * W + (idx - mu * W);
+        uint32_t t = 0u;
+        for (int q = 0; q < cl; ++q) t += cluster.map_shared_rank(hist, q)[mu * kBins + b];
+        hsum[idx] = t;
+      }
+      __syncthreads();
+    }
+    uint32_t t0 = 0u, t1 = 0u;
+    for (int b = tid; b < W; b += kSelThreads) {
+      t0 += hsum[b];
+      t1 += hsum[W + b];
+    }
+    t0 = __reduce_add_sync(0xffffffffu, t0);
+    t1 = __reduce_add_sync(0xffffffffu, t1);
+    if (lane == 0) {
+      wcnt[0][warp] = (int)t0;
+      wcnt[1][warp] = (int)t1;
     }
     __syncthreads();
-    // Counts above each thread's 4 bins (bins in descending order), one
-    // block scan per modality.
-    uint32_t c0[4], c1[4];
-    int mine0 = 0, mine1 = 0;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int bin = kBins - 1 - 4 * tid - q;
-      c0[q] = hist[0][bin];
-      c1[q] = hist[1][bin];
-      mine0 += (int)c0[q];
-      mine1 += (int)c1[q];
+    if (tid < 2) {
+      uint32_t t = 0u;
+      for (int i = 0; i < 32; ++i) t += (uint32_t)wcnt[tid][i];
+      xc.tot[tid] = t;
     }
-    int total;
-    const int above0 = block_excl_scan(mine0, scan_sh, &total);
-    const int above1 = block_excl_scan(mine1, scan_sh, &total);
-#pragma unroll
+    cluster.sync();  // every CTA's digit totals are published
+    if (tid < 2) {
+      const int mu = tid;
+      int qs = -1;
+      uint32_t above = 0u, run = 0u;
+      const uint32_t need = (uint32_t)need_sh[mu];
+      if (shift_sh[mu] > 0)
+        for (int q = cl - 1; q >= 0; --q) {  // higher ranks own larger digits
+          const uint32_t tq = cluster.map_shared_rank(&xc, q)->tot[mu];
+          if (qs < 0 && run < need && run + tq >= need) {
+            qs = q;
+            above = run;
+          }
+          run += tq;
+        }
+      qstar_sh[mu] = qs;
+      above_sh[mu] = (int)above;
+    }
+    __syncthreads();
     for (int mu = 0; mu < 2; ++mu) {
-      const int sh = mu ? sh1 : sh0, w = mu ? w1 : w0;
-      if (sh == 0) continue;
-      const uint32_t need = mu ? needv1 : needv0;
-      uint32_t run = (uint32_t)(mu ? above1 : above0);
+      if (qstar_sh[mu] != rank) continue;  // uniform in the CTA
+      // Digits of this CTA in descending order, bpt per thread; counts above
+      // each thread's digits by one block scan.
+      const int bpt = (W + kSelThreads - 1) / kSelThreads;  // 1, 2 or 4
+      uint32_t c[4];
+      int mine = 0;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint32_t cq = mu ? c1[q] : c0[q];
-        if (run < need && run + cq >= need) {  // the k-th largest lies in this bin
-          const uint32_t digit = (uint32_t)(kBins - 1 - 4 * tid - q);
-          prefix_sh[mu] = ((mu ? pre1 : pre0) << w) | digit;
-          need_sh[mu] = (int)(need - run);
-          shift_sh[mu] = sh - w;
+        const int jd = tid * bpt + q;
+        c[q] = (q < bpt && jd < W) ? hsum[mu * W + (W - 1 - jd)] : 0u;
+        mine += (int)c[q];
+      }
+      int total;
+      const int above_in = block_excl_scan(mine, scan_sh, &total);
+      const uint32_t need = (uint32_t)need_sh[mu];
+      uint32_t run = (uint32_t)above_sh[mu] + (uint32_t)above_in;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int jd = tid * bpt + q;
+        if (q < bpt && jd < W) {
+          if (run < need && run + c[q] >= need) {  // the k-th largest lies in this digit
+            xc.digit[mu] = (uint32_t)(rank * W + (W - 1 - jd));
+            xc.need[mu] = (int)(need - run);
+          }
+          run += c[q];
         }
-        run += cq;
+      }
+    }
+    cluster.sync();  // the threshold digits are published
+    if (tid < 2 && shift_sh[tid] > 0) {
+      const int mu = tid, sh = shift_sh[mu], w = sh < kDigit ? sh : kDigit;
+      if (qstar_sh[mu] >= 0) {
+        const SelXchg *r = cluster.map_shared_rank(&xc, qstar_sh[mu]);
+        prefix_sh[mu] = (prefix_sh[mu] << w) | r->digit[mu];
+        need_sh[mu] = r->need[mu];
+        shift_sh[mu] = sh - w;
+      } else {  // counts inconsistent with the keep count: cannot happen
+        report(status, SPRINT_STATUS_KEPT_MISMATCH);
+        shift_sh[mu] = 0;
       }
     }
     __syncthreads();
   }
-  if (tid < 2) thresh_sh[tid] = kmin_sh[tid] + prefix_sh[tid];
-  __syncthreads();
 
-  // Pass 3: stable compaction in ascending position order.  A position is
+  // ---- 4. stable compaction in ascending position order.  A position is
   // kept if its key exceeds its modality's threshold (or the modality keeps
   // everything), or equals the threshold and is among the first need_sh
-  // such ties by position.  Warp w owns positions [w R, (w+1) R): it counts
-  // its definite keeps and ties with ballots, the 32 warp totals are
-  // scanned, then every warp walks its range again and writes its kept
-  // positions at consecutive output slots (coalesced stores).
-  const uint32_t T0 = thresh_sh[0], T1 = thresh_sh[1];
+  // such ties by position.  Warp w owns positions [w R, (w+1) R) of the
+  // slice.
+  const uint32_t T0 = kmin_sh[0] + prefix_sh[0], T1 = kmin_sh[1] + prefix_sh[1];
   const int m0 = mode_sh[0], m1 = mode_sh[1];
   const int need0 = need_sh[0], need1 = need_sh[1];
   const int k_all = k1 - k0;
-  const int per_warp = ((n + 32 * 32 - 1) / (32 * 32)) * 32;  // multiple of 32
-  const int w_lo = warp * per_warp, w_hi = min(n, w_lo + per_warp);
-  auto classify = [&](int i, bool &def, bool &tie0, bool &tie1) {
+  const int per_warp = ((m + 32 * 32 - 1) / (32 * 32)) * 32;  // multiple of 32
+  const int w_lo = warp * per_warp, w_hi = min(m, w_lo + per_warp);
+  auto classify = [&](int j, bool &def, bool &tie0, bool &tie1) {
     def = tie0 = tie1 = false;
-    if (i >= w_hi) return;
-    const uint32_t key = keys[i];
-    if (mods[i] != 0) {
+    if (j >= w_hi) return;
+    const uint32_t key = keys[j];
+    if (tags[j] != 0) {
       def = m1 == 1 || (m1 == 2 && key > T1);
       tie1 = m1 == 2 && key == T1;
     } else {
@@ -372,30 +489,45 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
     }
   };
   int c_def = 0, c_t0 = 0, c_t1 = 0;
-  for (int i0 = w_lo; i0 < w_hi; i0 += 32) {
+  for (int j0 = w_lo; j0 < w_hi; j0 += 32) {
     bool d, t0, t1;
-    classify(i0 + lane, d, t0, t1);
+    classify(j0 + lane, d, t0, t1);
     c_def += __popc(__ballot_sync(0xffffffffu, d));
     c_t0 += __popc(__ballot_sync(0xffffffffu, t0));
     c_t1 += __popc(__ballot_sync(0xffffffffu, t1));
   }
-  // Exclusive scan of the warp totals (thread w of warp 0 handles warp w).
-  __shared__ int wdef[32], wt0[32], wt1[32];
-  if (lane == 0) { wdef[warp] = c_def; wt0[warp] = c_t0; wt1[warp] = c_t1; }
-  __syncthreads();
-  if (warp == 0) {
-    const int a = wdef[lane], b = wt0[lane], c = wt1[lane];
-    const int ia = warp_incl_scan(a), ib = warp_incl_scan(b), ic = warp_incl_scan(c);
-    wdef[lane] = ia - a;
-    wt0[lane] = ib - b;
-    wt1[lane] = ic - c;
+  if (lane == 0) {
+    wcnt[0][warp] = c_def;
+    wcnt[1][warp] = c_t0;
+    wcnt[2][warp] = c_t1;
   }
   __syncthreads();
-  int r_def = wdef[warp], r_t0 = wt0[warp], r_t1 = wt1[warp];
+  if (warp == 0) {  // exclusive scans of the warp totals; the CTA's totals
+    const int a = wcnt[0][lane], b = wcnt[1][lane], c = wcnt[2][lane];
+    const int ia = warp_incl_scan(a), ib = warp_incl_scan(b), ic = warp_incl_scan(c);
+    wcnt[0][lane] = ia - a;
+    wcnt[1][lane] = ib - b;
+    wcnt[2][lane] = ic - c;
+    if (lane == 31) {
+      xc.cnt[0] = ia;
+      xc.cnt[1] = ib;
+      xc.cnt[2] = ic;
+    }
+  }
+  cluster.sync();  // every CTA's totals are published
+  __shared__ int cbase_sh[3];
+  if (tid < 3) {
+    int t = 0;
+    for (int q = 0; q < rank; ++q) t += cluster.map_shared_rank(&xc, q)->cnt[tid];
+    cbase_sh[tid] = t;
+  }
+  __syncthreads();
+  int r_def = cbase_sh[0] + wcnt[0][warp], r_t0 = cbase_sh[1] + wcnt[1][warp],
+      r_t1 = cbase_sh[2] + wcnt[2][warp];
   const unsigned lt = (1u << lane) - 1u;
-  for (int i0 = w_lo; i0 < w_hi; i0 += 32) {
+  for (int j0 = w_lo; j0 < w_hi; j0 += 32) {
     bool d, t0, t1;
-    classify(i0 + lane, d, t0, t1);
+    classify(j0 + lane, d, t0, t1);
     const unsigned bd = __ballot_sync(0xffffffffu, d);
     const unsigned b0 = __ballot_sync(0xffffffffu, t0);
     const unsigned b1 = __ballot_sync(0xffffffffu, t1);
@@ -406,13 +538,14 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
     const int base = r_def + min(r_t0, need0) + min(r_t1, need1);
     if (keep) {
       const int out = base + __popc(bk & lt);
-      if (out < k_all) kept_idx[k0 + out] = i0 + lane;
+      if (out < k_all) kept_idx[k0 + out] = lo_i + j0 + lane;
       else report(status, SPRINT_STATUS_KEPT_MISMATCH);
     }
     r_def += __popc(bd);
     r_t0 += __popc(b0);
     r_t1 += __popc(b1);
   }
+  cluster.sync();  // nobody leaves while another CTA may still read its counts
 }
 
 int keynorm_launch(const void *K, const int32_t *prefix_off, int S, int total_rows, int NL,
@@ -470,22 +603,43 @@ extern "C" int sprint_score_prune(const void *K, int S, const int32_t *prefix_of
   if (keynorm_launch(K, prefix_off, S, total_rows, NL, row_elems, dtype, u, status, stream) !=
       SPRINT_OK)
     return SPRINT_ERR_CUDA;
-  // Stage up to kStageMax positions per sequence in shared memory (5 bytes
-  // each); the capacity follows the longest sequence the call can hold.
-  const int stage_cap = total_rows < kStageMax ? total_rows : kStageMax;
-  const size_t stage_bytes = (size_t)((stage_cap + 3) & ~3) * 4 + (size_t)stage_cap + 16;
+  // One cluster per sequence, sized so that a CTA's slice is about
+  // kSliceTarget positions of an average sequence; slices up to kStageCta
+  // positions are staged in shared memory.
+  const int avg = total_rows / S;
+  int cl = 1;
+  while (cl < kMaxCluster && cl * kSliceTarget < avg) cl <<= 1;
+  int cap = ((total_rows + cl - 1) / cl + 31) & ~31;
+  if (cap > kStageCta) cap = kStageCta;
   static PerDevice attr_set;
   int set = 0;
   if (!attr_set.get(&set, [](int, int *v) {
         *v = 1;
+        size_t most = 0;
+        for (int c = 1; c <= kMaxCluster; c <<= 1) {
+          const size_t b = select_smem_bytes(c, kStageCta);
+          most = b > most ? b : most;
+        }
         return cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)((size_t)kStageMax * 5 + 16)) == cudaSuccess;
+                                    (int)most) == cudaSuccess;
       }))
     return SPRINT_ERR_CUDA;
-  select_kernel<<<S, kSelThreads, stage_bytes, stream>>>(u, conf, modality, prefix_off,
-                                                         kept_off, S, total_rows, alpha, r_text,
-                                                         r_img, keys, kept_idx, score_out,
-                                                         status, stage_cap);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(S * cl);
+  cfg.blockDim = dim3(kSelThreads);
+  cfg.dynamicSmemBytes = select_smem_bytes(cl, cap);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, select_kernel, u, conf, modality, prefix_off, kept_off,
+                         total_rows, alpha, r_text, r_img, keys, kept_idx, score_out, status,
+                         cap) != cudaSuccess)
+    return SPRINT_ERR_CUDA;
   return launch_status();
 }
 

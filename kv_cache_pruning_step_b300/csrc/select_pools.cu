@@ -79,26 +79,20 @@ pool_score_kernel(const float *__restrict__ u, const float *__restrict__ conf,
   }
   if (tid == 0) bad_sh = 0;
 
-  // Mean of u: per-thread fp32 sums in select_kernel's order, fp64 across
-  // threads.
-  constexpr int kB = 8;
-  float su_f = 0.f;
-  for (int i0 = tid; i0 < n; i0 += kB * kThreads) {
-    float ub[kB];
-#pragma unroll
-    for (int j = 0; j < kB; ++j) {
-      const int i = i0 + j * kThreads;
-      ub[j] = i < n ? __ldg(u + p0 + i) : 0.f;
-    }
-#pragma unroll
-    for (int j = 0; j < kB; ++j) su_f += ub[j];
+  // Mean of u: the canonical sum (common.cuh) with the CTA's 32 warps as
+  // the workers, the same bits as the two-modality selection's clusters.
+  {
+    const int G = (n + kLeaf - 1) / kLeaf, P = next_pow2(G);
+    const int B = P > 32 ? P / 32 : 1;
+    const double v = warp * B < P ? u_subtree_sum(u + p0, n, G, warp * B, B, lane) : 0.0;
+    if (lane == 0) dsum_sh[warp] = v;
   }
-  const double su = warp_sum((double)su_f);
-  if (lane == 0) dsum_sh[warp] = su;
   __syncthreads();
-  if (warp == 0) {
-    const double v = warp_sum(dsum_sh[lane]);
-    if (lane == 0) mean_sh = n > 0 ? (float)(v / (double)n) : 0.f;
+  if (tid == 0) {
+    double v[32];
+    for (int i = 0; i < 32; ++i) v[i] = dsum_sh[i];
+    tree_fold(v, 32);
+    mean_sh = n > 0 ? (float)(v[0] / (double)n) : 0.f;
   }
   __syncthreads();
   const float mean_f = mean_sh;

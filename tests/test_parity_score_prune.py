@@ -75,6 +75,45 @@ def test_fuzz_ragged_sequences(sp, dtype, r_text, r_img):
     check_sequences(w, prefixes, confs, cat, kh, kept, score, r_text, r_img)
 
 
+def _ragged_prefixes(shapes, NL, Hkv, d, dtype, seed0):
+    prefixes, confs = [], []
+    for s, (n, n_img) in enumerate(shapes):
+        w = small_workload(dtype=dtype, NL=NL, Hkv=Hkv, d=d, n=n, n_img=n_img, seed=seed0 + s)
+        p = prefix_inputs(w, seq=s, device=DEV)
+        g = torch.Generator().manual_seed(seed0 + s)
+        p["modality"] = p["modality"][torch.randperm(n, generator=g)].to(DEV)
+        prefixes.append(p)
+        confs.append(random_confidences(n, seed0 + 50 + s, device=DEV))
+    return w, prefixes, confs
+
+
+@pytest.mark.parametrize("shapes", [
+    # average lengths that give clusters of 2, 4 and 8 CTAs per sequence, with
+    # empty sequences, sequences shorter than the cluster, and slices that
+    # end mid-warp
+    [(5000, 1234), (4000, 0), (0, 0), (5, 5)],
+    [(15000, 7001), (7, 3)],
+    [(40000, 20000), (5, 2), (100, 0)],
+])
+@pytest.mark.parametrize("r_text,r_img", [(1.0, 0.8), (0.5, 0.29)])
+def test_cluster_sizes_ragged(sp, shapes, r_text, r_img):
+    w, prefixes, confs = _ragged_prefixes(shapes, 2, 1, 8, "f32", 300)
+    cat, conf_d, kh, ko, kept, score, _ = run_score_prune(sp, w, prefixes, confs, r_text, r_img)
+    check_sequences(w, prefixes, confs, cat, kh, kept, score, r_text, r_img)
+
+
+def test_long_sequence_keys_in_workspace(sp):
+    """A sequence whose slice of the cluster exceeds what shared memory
+    stages (more than 8 x 16384 positions) keeps its keys in the workspace;
+    a short sequence in the same call is staged."""
+    shapes = [(140000, 70001), (300, 100)]
+    w, prefixes, confs = _ragged_prefixes(shapes, 1, 1, 8, "f32", 400)
+    for r_text, r_img in ((1.0, 0.8), (0.37, 0.61)):
+        cat, conf_d, kh, ko, kept, score, _ = run_score_prune(sp, w, prefixes, confs, r_text,
+                                                              r_img)
+        check_sequences(w, prefixes, confs, cat, kh, kept, score, r_text, r_img)
+
+
 def test_ties_go_to_lower_index(sp):
     w = small_workload(dtype="f32", NL=2, Hkv=2, d=64, n=64, n_img=0, seed=3)
     p = prefix_inputs(w, device=DEV)
