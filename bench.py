@@ -839,8 +839,39 @@ def run_reference(args):
     }))
 
 
+def launch_plan(gpus: int, env=None):
+    """How `--gpus N` runs: 'run' in this process, 'spawn' N ranks under
+    torch.distributed.run (N > 1 and no launcher around this process), or
+    an error when a launcher gave a world size other than N."""
+    env = os.environ if env is None else env
+    if gpus < 1:
+        raise SystemExit(f"--gpus must be at least 1, got {gpus}")
+    if "WORLD_SIZE" in env:
+        world = int(env["WORLD_SIZE"])
+        if world != gpus:
+            raise SystemExit(f"--gpus {gpus} but the launcher started {world} rank(s)")
+        return "run"
+    return "spawn" if gpus > 1 else "run"
+
+
+def spawn_ranks(gpus: int, argv) -> int:
+    """Run this script as `gpus` local ranks (one per GPU) and return the
+    launcher's exit code."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={gpus}", "--master-addr", "127.0.0.1", "--master-port",
+           str(port), os.path.abspath(__file__), *argv]
+    return subprocess.run(cmd).returncode
+
+
 def main(argv=None):
+    argv = sys.argv[1:] if argv is None else argv
     args = parse_args(argv)
+    if launch_plan(args.gpus) == "spawn":
+        sys.exit(spawn_ranks(args.gpus, argv))
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -55,3 +55,18 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(3.0, 1) == 3.0
     assert bench.sum_over_ranks(4, 1) == 4.0
+
+
+def test_gpus_flag_matches_the_launch():
+    """--gpus N never silently measures another number of GPUs: without a
+    launcher N > 1 spawns N ranks, and a launcher's world size must be N."""
+    import bench
+    assert bench.launch_plan(1, {}) == "run"
+    assert bench.launch_plan(4, {}) == "spawn"
+    assert bench.launch_plan(2, {"WORLD_SIZE": "2"}) == "run"
+    with pytest.raises(SystemExit):
+        bench.launch_plan(8, {"WORLD_SIZE": "1"})
+    with pytest.raises(SystemExit):
+        bench.launch_plan(1, {"WORLD_SIZE": "2"})
+    with pytest.raises(SystemExit):
+        bench.launch_plan(0, {})

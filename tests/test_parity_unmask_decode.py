@@ -64,6 +64,48 @@ def test_random_trajectories_match_oracle(sp, mode, LB, T):
         assert int(mask.sum()) == 0  # terminates within T
 
 
+def _check_block_stagewise(w, W, pre, steps, seen, ref, gpu_tokens, residual=False):
+    """Compare every step of a GPU block decode stage by stage: the oracle's
+    attention on the step's inputs (full prefix at step 0, the prefix pruned
+    by the GPU's kept set afterwards); the oracle's confidences and greedy
+    tokens on the step's LM-head input (h + the GPU's O with the residual
+    chain); and the oracle's unmask rule applied to the GPU's own
+    confidences, greedy tokens and mask state, which must give the GPU's
+    decisions and state exactly.  The whole-block oracle trajectory is also
+    followed while the decisions agree; the GPU may leave it only at a step
+    where a confidence lies within CONF_ATOL of tau, and then the remaining
+    steps are still compared stage by stage."""
+    kept = seen[0]["kept"]
+    Kp, Vp = orc.compact(pre["K"], kept), orc.compact(pre["V"], kept)
+    mask = np.ones(w.LB, dtype=bool)
+    tokens = np.full(w.LB, -1, dtype=np.int64)
+    follows = True
+    rows = np.arange(w.LB)
+    for t, g in enumerate(seen):
+        x = steps[t]
+        Kt, Vt = (pre["K"], pre["V"]) if t == 0 else (Kp, Vp)
+        O = orc.block_attention(x["Q"], Kt, Vt, x["Kb"], x["Vb"])
+        gc.assert_close(g["O"], O, torch.float32, f"step {t} O")
+        h = orc.residual_hidden(x["h"], g["O"]) if residual else gc.host(x["h"])
+        gc.check_confidence(g["conf"], g["argmax"], h, W, x["theta"], rows, f"step {t}")
+        mask, tokens, acc = orc.unmask_step(g["conf"], g["argmax"], mask, tokens, t, w.T, w.tau)
+        assert acc.tolist() == g["acc"].astype(bool).tolist(), f"step {t}: unmask decisions"
+        assert mask.tolist() == g["mask"].astype(bool).tolist(), f"step {t}: mask"
+        assert tokens.tolist() == g["tokens"].astype(np.int64).tolist(), f"step {t}: tokens"
+        if follows:
+            r = ref["steps"][t]
+            if r["accepted"].tolist() != acc.tolist():
+                near = np.abs(r["conf"] - w.tau) <= gc.CONF_ATOL
+                assert near.any(), f"step {t}: decisions leave the oracle's trajectory"
+                follows = False
+    assert not mask.any(), "the block must be unmasked within T steps"
+    assert np.asarray(gpu_tokens).tolist() == tokens.tolist()
+    if follows:
+        assert len(seen) == len(ref["steps"])
+        assert tokens.tolist() == ref["tokens"].tolist()
+    return follows
+
+
 @pytest.mark.parametrize("indexed", [False, True])
 def test_tiny_block_end_to_end(sp, indexed):
     """Whole block on the fp32 tiny workload, every step compared (later
@@ -84,6 +126,7 @@ def test_tiny_block_end_to_end(sp, indexed):
     def on_step(t, d):
         seen.append({"O": gc.host(d.O[0]), "conf": d.conf_blk.cpu().numpy(),
                      "argmax": d.argmax_blk.cpu().numpy(), "acc": d.accepted[0].cpu().numpy(),
+                     "mask": d.mask[0].cpu().numpy(), "tokens": d.tokens[0].cpu().numpy(),
                      "kept": d.kept_idx.cpu().numpy(), "score": d.score.cpu().numpy(),
                      "conf_prefix": d.conf_prefix.cpu().numpy()})
 
@@ -101,16 +144,8 @@ def test_tiny_block_end_to_end(sp, indexed):
     assert np.abs(seen[0]["conf_prefix"] - ref["prefix_conf"]).max() <= gc.CONF_ATOL
     assert np.abs(seen[0]["score"] - ref["score"]).max() <= gc.SCORE_EXCUSE
     gc.check_kept(seen[0]["kept"], ref["score"], mod, w.r_text, w.r_img, "tiny kept")
-    assert res.steps == len(ref["steps"])
-    for t, (g, r) in enumerate(zip(seen, ref["steps"])):
-        gc.assert_close(g["O"], r["O"], torch.float32, f"step {t} O")
-        assert np.abs(g["conf"] - r["conf"]).max() <= gc.CONF_ATOL
-        # decisions: exact unless a confidence sits within CONF_ATOL of tau
-        if g["acc"].astype(bool).tolist() != r["accepted"].tolist():
-            near = np.abs(r["conf"] - w.tau) <= gc.CONF_ATOL
-            assert near.any(), f"step {t}: unmask decisions differ"
-            return
-    assert res.tokens[0].cpu().numpy().tolist() == ref["tokens"].tolist()
+    assert res.steps == len(seen)
+    _check_block_stagewise(w, W, pre, steps, seen, ref, res.tokens[0].cpu().numpy())
 
 
 def _decoder_and_steps(name, tau=None, mode=0):
@@ -227,7 +262,9 @@ def test_tiny_block_residual_chain_end_to_end(sp):
 
     def on_step(t, d):
         seen.append({"O": gc.host(d.O[0]), "conf": d.conf_blk.cpu().numpy(),
-                     "acc": d.accepted[0].cpu().numpy(), "h": gc.host(d.h_res)})
+                     "argmax": d.argmax_blk.cpu().numpy(), "acc": d.accepted[0].cpu().numpy(),
+                     "mask": d.mask[0].cpu().numpy(), "tokens": d.tokens[0].cpu().numpy(),
+                     "kept": d.kept_idx.cpu().numpy(), "h": gc.host(d.h_res)})
 
     def step_fn(t):
         x = steps[t]
@@ -239,19 +276,14 @@ def test_tiny_block_residual_chain_end_to_end(sp):
     assert dec.status.item() == 0
     ref = orc.decode_block(pre, lambda t: steps[t], W, LB=w.LB, T=w.T, tau=w.tau,
                            r_text=w.r_text, r_img=w.r_img, alpha=w.alpha, residual=True)
-    assert res.steps == len(ref["steps"])
-    for t, (g, r) in enumerate(zip(seen, ref["steps"])):
-        gc.assert_close(g["O"], r["O"], torch.float32, f"step {t} O")
+    assert res.steps == len(seen)
+    for t, g in enumerate(seen):
         # h = h_in + O from the GPU's own O, and the chain changes the input
         want_h = orc.residual_hidden(steps[t]["h"], g["O"])
         np.testing.assert_allclose(g["h"], want_h, rtol=1e-6, atol=1e-6)
         assert np.abs(g["h"] - gc.host(steps[t]["h"])).max() > 1e-3
-        assert np.abs(g["conf"] - r["conf"]).max() <= gc.CONF_ATOL
-        if g["acc"].astype(bool).tolist() != r["accepted"].tolist():
-            near = np.abs(r["conf"] - w.tau) <= gc.CONF_ATOL
-            assert near.any(), f"step {t}: unmask decisions differ"
-            return
-    assert res.tokens[0].cpu().numpy().tolist() == ref["tokens"].tolist()
+    _check_block_stagewise(w, W, pre, steps, seen, ref, res.tokens[0].cpu().numpy(),
+                           residual=True)
 
 
 @pytest.mark.parametrize("name", ["tiny-256", "prefix-4k"])

@@ -29,9 +29,26 @@ def _inputs(M, D, V, dtype, seed):
     return h, W, theta
 
 
+def _largest_rows_that_fit(D, V):
+    """Most bf16 rows whose partials fit the library's scratch array."""
+    from kv_cache_pruning_step_b300 import sprint as sp
+    limit = 4 << 20
+    M = 1
+    while sp.lib.sprint_lmhead_workspace_bytes(M + 1, D, V, sp.BF16) <= limit:
+        M += 1
+    return M
+
+
 @pytest.mark.parametrize("dtype,M,D,V", [(torch.bfloat16, 32, 2048, 157184),
+                                         (torch.bfloat16, 300, 2048, 157184),
+                                         (torch.bfloat16, "largest", 2048, 157184),
                                          (torch.float32, 40, 256, 1000)])
 def test_noalloc_matches_allocating_entry_point_twice(dtype, M, D, V):
+    """Block rows (one row tile), and 300 rows up to the largest call the
+    array holds (row tiles in CTA pairs, partials filling the array)."""
+    if M == "largest":
+        M = _largest_rows_that_fit(D, V)
+        assert M == 497
     from kv_cache_pruning_step_b300 import sprint as sp
     for seed in (1, 2):  # two calls in a row reuse the library's scratch array
         h, W, theta = _inputs(M, D, V, dtype, seed)
@@ -57,3 +74,9 @@ def test_noalloc_rejects_requests_beyond_its_array():
                                               None, None, None, None, None)
     assert rc == -6
     assert "scratch" in sp.sprint_strerror(rc)
+    # one row past the largest call that fits is rejected the same way
+    M = _largest_rows_that_fit(2048, 157184) + 1
+    assert lib.sprint_lmhead_workspace_bytes(M, 2048, 157184, sp.BF16) > (4 << 20)
+    rc = lib.sprint_lmhead_confidence_noalloc(None, None, None, M, 2048, 157184, sp.BF16,
+                                              None, None, None, None, None)
+    assert rc == -6
