@@ -43,7 +43,12 @@ extraction:
   R14 residual chain (optional): the block LM head reads h = H + O, the
       step's own hidden state plus the last layer's attention output with
       its heads concatenated (Hq d = D), so the attention output reaches
-      the confidences; off by default (h is then an independent input).
+      the confidences; off by default (h is then an independent input);
+  R15 the full forward pass of a block's first step recomputes the prefix:
+      every prefix position attends to every prefix position of its
+      sequence (no causal mask, the prefix being one clean context), with
+      scale 1/sqrt(d) and GQA group floor(h Hkv / Hq); the prefix does not
+      attend to the block being decoded.
 """
 from __future__ import annotations
 
@@ -246,6 +251,33 @@ def block_attention(Q, Kp, Vp, Kb, Vb, layers=None):
             p = np.exp(scores - scores.max(axis=1, keepdims=True))
             p = p / p.sum(axis=1, keepdims=True)
             O[l, :, h, :] = p @ vals
+    return O
+
+
+def prefix_attention(Q, K, V, rows=None):
+    """Self-attention of the prefix over itself in the full forward pass of
+    a block's first step (reading R15): every prefix position attends to
+    every prefix position, no causal mask.
+
+    Paper, Sparse Prefix Retention paragraph: the first step of each block
+    performs a full forward pass, which yields the logits and the complete
+    KV cache of the prefix.
+
+    Q: [NL, n, Hq, d]; K, V: [NL, n, Hkv, d]; rows: optional subset of the
+    query positions.  Returns O [NL, m, Hq, d] (fp64), m = len(rows) or n.
+    """
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    NL, n, Hq, d = Q.shape
+    Hkv = K.shape[2]
+    rows = np.arange(n) if rows is None else np.asarray(rows, dtype=np.int64)
+    O = np.zeros((NL, len(rows), Hq, d))
+    for l in range(NL):
+        for h in range(Hq):
+            g = (h * Hkv) // Hq
+            scores = (Q[l, rows, h, :] @ K[l, :, g, :].T) / math.sqrt(d)   # [m, n]
+            p = np.exp(scores - scores.max(axis=1, keepdims=True))
+            p = p / p.sum(axis=1, keepdims=True)
+            O[l, :, h, :] = p @ V[l, :, g, :]
     return O
 
 

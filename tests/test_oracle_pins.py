@@ -408,6 +408,112 @@ def check_attention_brute(fn):
                                rtol=1e-12, atol=1e-13)
 
 
+def brute_prefix_attention(Q, K, V):
+    """Loops over layer, query head, query position and key position; GQA
+    by explicit head groups; softmax as e^x / sum e^x."""
+    NL, n, Hq, d = Q.shape
+    group = Hq // K.shape[2]
+    O = np.zeros(Q.shape)
+    for l in range(NL):
+        for h in range(Hq):
+            g = h // group
+            for r in range(n):
+                w = [math.exp(sum(Q[l, r, h, x] * K[l, j, g, x] for x in range(d)) / math.sqrt(d))
+                     for j in range(n)]
+                tot = sum(w)
+                for x in range(d):
+                    O[l, r, h, x] = sum(w[j] * V[l, j, g, x] for j in range(n)) / tot
+    return O
+
+
+def check_prefix_attention(fn):
+    rng = np.random.default_rng(19)
+    NL, n, Hq, Hkv, d = 2, 7, 4, 2, 5
+    Q = rng.normal(size=(NL, n, Hq, d))
+    K, V = rng.normal(size=(2, NL, n, Hkv, d)) * rng.lognormal(0, 0.5, size=(1, 1, n, 1, 1))
+    np.testing.assert_allclose(fn(Q, K, V), brute_prefix_attention(Q, K, V), rtol=1e-12,
+                               atol=1e-13)
+    # bidirectional: permuting the prefix positions permutes the outputs (a
+    # causal mask would break this)
+    perm = rng.permutation(n)
+    np.testing.assert_allclose(fn(Q[:, perm], K[:, perm], V[:, perm]), fn(Q, K, V)[:, perm],
+                               rtol=1e-12, atol=1e-13)
+
+
+def test_prefix_attention_brute_force_and_bidirectional():
+    check_prefix_attention(orc.prefix_attention)
+
+
+def test_prefix_attention_special_cases():
+    rng = np.random.default_rng(20)
+    NL, Hq, Hkv, d = 2, 4, 2, 6
+    # one position: o = v
+    Q = rng.normal(size=(NL, 1, Hq, d))
+    K, V = rng.normal(size=(2, NL, 1, Hkv, d))
+    O = orc.prefix_attention(Q, K, V)
+    for h in range(Hq):
+        np.testing.assert_allclose(O[:, 0, h], V[:, 0, h // 2], rtol=1e-15)
+    # identical keys: every query gets the mean of the values
+    n = 9
+    Q = rng.normal(size=(NL, n, Hq, d))
+    K = np.broadcast_to(rng.normal(size=d), (NL, n, Hkv, d)).copy()
+    V = rng.normal(size=(NL, n, Hkv, d))
+    O = orc.prefix_attention(Q, K, V)
+    for h in range(Hq):
+        np.testing.assert_allclose(O[:, :, h], np.broadcast_to(V[:, :, h // 2].mean(axis=1)[:, None],
+                                                                (NL, n, d)), rtol=1e-12)
+    # the prefix's own attention equals the block attention with the keys
+    # split anywhere into a "prefix" part and a "block" part (both pinned
+    # separately), for any subset of query rows
+    n = 11
+    Q = rng.normal(size=(NL, n, Hq, d))
+    K, V = rng.normal(size=(2, NL, n, Hkv, d))
+    rows = [0, 4, 10, 7]
+    for split in (0, 3, n - 1, n):
+        want = orc.block_attention(Q[:, rows], K[:, :split], V[:, :split], K[:, split:],
+                                   V[:, split:])
+        np.testing.assert_allclose(orc.prefix_attention(Q, K, V, rows=rows), want, rtol=1e-12,
+                                   atol=1e-13)
+    # GQA equals multi-head attention with every KV head repeated per group
+    rep = lambda a: np.repeat(a, Hq // Hkv, axis=2)  # noqa: E731
+    np.testing.assert_allclose(orc.prefix_attention(Q, K, V),
+                               orc.prefix_attention(Q, rep(K), rep(V)), rtol=1e-13)
+
+
+def test_prefix_attention_planted_mistakes():
+    def causal(Q, K, V):
+        Q, K, V = (np.asarray(a, float) for a in (Q, K, V))
+        NL, n, Hq, d = Q.shape
+        O = np.zeros(Q.shape)
+        for i in range(n):
+            O[:, i] = orc.prefix_attention(Q[:, :i + 1], K[:, :i + 1], V[:, :i + 1])[:, i]
+        return O
+
+    def no_scale(Q, K, V):
+        return orc.prefix_attention(np.asarray(Q) * math.sqrt(np.asarray(Q).shape[-1]), K, V)
+
+    def modulo_group(Q, K, V):
+        Q = np.asarray(Q)
+        Hq, Hkv = Q.shape[2], np.asarray(K).shape[2]
+        order = [(h % Hkv) * (Hq // Hkv) + h // Hkv for h in range(Hq)]
+        return orc.prefix_attention(Q[:, :, order], K, V)[:, :, np.argsort(order)]
+
+    def softmax_over_queries(Q, K, V):
+        Q, K, V = (np.asarray(a, float) for a in (Q, K, V))
+        NL, n, Hq, d = Q.shape
+        O = np.zeros(Q.shape)
+        for l in range(NL):
+            for h in range(Hq):
+                g = h * K.shape[2] // Hq
+                s = Q[l, :, h] @ K[l, :, g].T / math.sqrt(d)
+                p = np.exp(s - s.max(axis=0, keepdims=True))
+                p = p / p.sum(axis=0, keepdims=True)
+                O[l, :, h] = p @ V[l, :, g]
+        return O
+    for bad in (causal, no_scale, modulo_group, softmax_over_queries):
+        _fails(check_prefix_attention, bad)
+
+
 def test_attention_brute_force():
     check_attention_brute(orc.block_attention)
 
