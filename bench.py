@@ -51,6 +51,9 @@ def parse_args(argv=None):
     ap.add_argument("--r-global", type=float, default=0.5)
     ap.add_argument("--residual", action="store_true",
                     help="the block LM head reads h + O of the last layer (residual chain)")
+    ap.add_argument("--prefix-attn", action="store_true",
+                    help="step 0 also runs the prefix's own attention of the full forward "
+                         "pass (sprint_prefix_attn) on seeded prefix queries")
     ap.add_argument("--prefix-layout", default="compacted", choices=["compacted", "indexed"],
                     help="later steps read a compacted copy of the kept rows, or the kept "
                          "rows of the full cache through their indices")
@@ -199,11 +202,12 @@ def load_peaks():
 
 
 # ---------------------------------------------------------------- inputs
-def build_inputs(w, seqs, device):
-    """Seeded prefix and per-step inputs of sequences `seqs` (CSR layout)."""
+def build_inputs(w, seqs, device, prefix_attn=False):
+    """Seeded prefix and per-step inputs of sequences `seqs` (CSR layout);
+    prefix_attn adds the prefix queries Qp of the prefix's own attention."""
     import torch
 
-    from workload import lm_head_weight, prefix_inputs, step_inputs
+    from workload import lm_head_weight, prefix_inputs, prefix_queries, step_inputs
     pres = [prefix_inputs(w, seq=s, device="cpu") for s in seqs]
     prefix = {
         "K": torch.cat([p["K"].reshape(-1) for p in pres]),
@@ -213,6 +217,9 @@ def build_inputs(w, seqs, device):
         "modality": torch.cat([p["modality"] for p in pres]),
         "image": torch.cat([p["image"] for p in pres]),
     }
+    if prefix_attn:
+        prefix["Qp"] = torch.cat([prefix_queries(w, seq=s, device="cpu").reshape(-1)
+                                  for s in seqs])
     counts = [(int((p["modality"] == 0).sum()), int((p["modality"] != 0).sum())) for p in pres]
     steps = []
     for t in range(w.T):
@@ -465,13 +472,15 @@ def run_ours(args):
     dist = init_dist(world, "nccl")
     w = WORKLOADS[args.workload]
     seqs = [rank * w.S + s for s in range(w.S)]
-    prefix_h, steps_h, W_h, counts, pres = build_inputs(w, seqs, "cpu")
+    prefix_h, steps_h, W_h, counts, pres = build_inputs(w, seqs, "cpu",
+                                                        prefix_attn=args.prefix_attn)
     W = W_h.to(dev)
     prefix = to_device(prefix_h, dev)
     steps = [to_device(x, dev) for x in steps_h]
     dec = BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
                        r_text=w.r_text, r_img=w.r_img, alpha=w.alpha, modality_counts=counts,
                        indexed=args.prefix_layout == "indexed",
+                       prefix_attn=args.prefix_attn,
                        **selection_args(args, prefix_h, pres))
     step_fn = lambda t: steps[t]  # noqa: E731
 
@@ -601,8 +610,11 @@ def run_ours(args):
     n_rows = dec.total_rows
     kept = dec.total_kept
     row_b = w.NL * w.Hkv * w.d * 2
+    seq_rows = [dec.prefix_off_host[i + 1] - dec.prefix_off_host[i] for i in range(dec.S)]
     work = {  # algorithmic work per launch of each stage
         "lmhead_prefix": ("tensor", 2.0 * n_rows * w.D * w.V),
+        # QK^T and PV over every (query, key) pair of each prefix, all heads and layers
+        "prefix_attn": ("tensor", sum(4.0 * n * n * w.Hq * w.d * w.NL for n in seq_rows)),
         "score_prune": ("hbm", n_rows * row_b),
         "compact": ("hbm", 2 * 2 * kept * row_b),
         "attn_full": ("hbm", 2 * (n_rows + w.S * w.LB) * row_b),
@@ -658,6 +670,7 @@ def run_ours(args):
         "data": "synthetic (seeded; shapes and modality layout of the workload)",
         "config": {"workload": w.name, "description": w.description,
                    "prefix_rows": n_rows, "kept_rows": kept, "sequences": w.S,
+                   "prefix_attn": bool(args.prefix_attn),
                    "LB": w.LB, "T": w.T, "tau": w.tau, "r_text": w.r_text, "r_img": w.r_img,
                    "alpha": w.alpha, "NL": w.NL, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d, "D": w.D,
                    "V": w.V, "bench_step": "one block decoded to completion",

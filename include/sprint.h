@@ -75,6 +75,8 @@ extern "C" {
 #define SPRINT_STATUS_TIMEOUT 4u       /* a bounded device wait expired      */
 #define SPRINT_STATUS_BAD_INDEX 8u     /* kept index outside its prefix      */
 #define SPRINT_STATUS_BAD_TEMPERATURE 16u /* temperature <= 0 or not finite  */
+#define SPRINT_STATUS_DEBUG_CHECK 32u  /* an invariant checked only by the
+                                          debug build failed (see below)     */
 
 /* Storage types. */
 #define SPRINT_F32 0
@@ -90,6 +92,20 @@ const char *sprint_strerror(int code);
 /* Kernels this library has launched in this process (a diagnostic counter;
  * every successful launch adds one). */
 unsigned long long sprint_kernel_launches(void);
+
+/* 1 when this library is the debug build (compiled with SPRINT_DEBUG_CHECKS,
+ * `python -m kv_cache_pruning_step_b300.build --debug`, libsprint_debug.so),
+ * else 0.  The debug build also checks invariants that the release build
+ * trusts, and reports a failed one as SPRINT_STATUS_DEBUG_CHECK in the
+ * call's status word; no check traps or stops a kernel.  Checked: the kept
+ * indices of every sequence are strictly ascending (sprint_compact_kv, as
+ * sprint_score_prune writes them); the selection wrote exactly the kept
+ * count of every sequence (sprint_score_prune); the still-masked count m
+ * equals the number of set mask bytes after every unmask, and every
+ * unmasked position holds a token (sprint_unmask); every greedy token lies
+ * in [0, V) and every confidence in [1/V, 1] within rounding
+ * (sprint_lmhead_confidence).  Not a counterpart of anything in the paper. */
+int sprint_debug_checks(void);
 
 /*
  * floor(r * n) keep count of one modality.  LLaDA2.0-Uni paper, Sparse
@@ -325,6 +341,33 @@ int sprint_block_attn_indexed(const void *Q, const void *K, const void *V,
                               int Hkv, int d, int dtype, void *O, void *ws,
                               size_t ws_bytes, int32_t *status,
                               cudaStream_t stream);
+
+/*
+ * sprint_prefix_attn -- the prefix's own attention in the full forward pass
+ * of a block's first step.  LLaDA2.0-Uni paper, Sparse Prefix Retention
+ * paragraph: the first step of each block runs a full forward pass that
+ * yields the logits and the complete KV cache of the prefix.  Every prefix
+ * position attends to every prefix position of its sequence (no causal
+ * mask: the prefix is one clean context), softmax scale 1/sqrt(d), query
+ * head h reads KV head floor(h Hkv / Hq):
+ *   Op[l][i][h] = sum_j softmax_j(Qp[l][i][h] . K[l][j][g] / sqrt(d)) V[l][j][g]
+ * over j < n_s.  An optional part of the step (the bench's --prefix-attn):
+ * the pruning itself needs only the cache, not this output.
+ *
+ *   Qp, Op      per sequence [NL][n_s][Hq][d], sequences concatenated
+ *               (dtype; Op written, caller-owned)
+ *   K, V        per sequence [NL][n_s][Hkv][d] (dtype)
+ *   prefix_off  int32 [S+1] (device); total_rows = prefix_off[S] (host)
+ *
+ * bf16 only, on the tcgen05 tensor cores: d in {64, 128}, Hq % Hkv == 0,
+ * S <= 1024, all pointers 16-byte aligned, NL * total_rows < 2^31
+ * (SPRINT_ERR_UNSUPPORTED otherwise, e.g. for fp32).  No workspace.
+ * Device status: SPRINT_STATUS_BAD_OFFSETS, SPRINT_STATUS_TIMEOUT.
+ */
+int sprint_prefix_attn(const void *Qp, const void *K, const void *V,
+                       const int32_t *prefix_off, int total_rows, int S, int NL,
+                       int Hq, int Hkv, int d, int dtype, void *Op, int32_t *status,
+                       cudaStream_t stream);
 
 /*
  * sprint_residual_hidden -- h_out = h_in + O of the last layer, the heads

@@ -340,6 +340,25 @@ extern "C" int sprint_block_attn_indexed(const void *Q, const void *K, const voi
                          Gate{nullptr, 0}, stream);
 }
 
+extern "C" int sprint_prefix_attn(const void *Qp, const void *K, const void *V,
+                                  const int32_t *prefix_off, int total_rows, int S, int NL,
+                                  int Hq, int Hkv, int d, int dtype, void *Op, int32_t *status,
+                                  cudaStream_t stream) {
+  if (S < 0 || total_rows < 0 || NL < 1 || Hq < 1 || Hkv < 1) return SPRINT_ERR_INVALID_ARG;
+  if (dtype != SPRINT_F32 && dtype != SPRINT_BF16) return SPRINT_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return SPRINT_ERR_INVALID_ARG;
+  if (dtype != SPRINT_BF16 || (d != 64 && d != 128)) return SPRINT_ERR_UNSUPPORTED;
+  if (S == 0 || total_rows == 0) return SPRINT_OK;
+  if (!Qp || !K || !V || !prefix_off || !Op || !status) return SPRINT_ERR_INVALID_ARG;
+  if ((long long)NL * total_rows > 0x7fffffffLL) return SPRINT_ERR_UNSUPPORTED;
+  if (!aligned16(Qp) || !aligned16(K) || !aligned16(V) || !aligned16(Op))
+    return SPRINT_ERR_UNSUPPORTED;
+  return attn_tc_prefix(static_cast<const __nv_bfloat16 *>(Qp),
+                        static_cast<const __nv_bfloat16 *>(K),
+                        static_cast<const __nv_bfloat16 *>(V), prefix_off, total_rows, S, NL, Hq,
+                        Hkv, d, static_cast<__nv_bfloat16 *>(Op), status, stream);
+}
+
 extern "C" int sprint_residual_hidden(const void *h_in, const void *O, int S, int NL, int LB,
                                       int Hq, int d, int dtype, void *h_out,
                                       cudaStream_t stream) {

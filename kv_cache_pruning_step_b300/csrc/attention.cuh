@@ -32,5 +32,9 @@ int attn_tc_forward(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_
                     const __nv_bfloat16 *Vb, int S, int NL, int LB, int Hq, int Hkv, int d,
                     void *O, void *ws, int32_t *status, KvIndex kvi, AttnResidual res,
                     Gate gate, cudaStream_t stream);
+// The prefix's own attention (bf16, tcgen05; attention_tc.cu).
+int attn_tc_prefix(const __nv_bfloat16 *Qp, const __nv_bfloat16 *K, const __nv_bfloat16 *V,
+                   const int32_t *prefix_off, int total_rows, int S, int NL, int Hq, int Hkv,
+                   int d, __nv_bfloat16 *Op, int32_t *status, cudaStream_t stream);
 
 }  // namespace sprint

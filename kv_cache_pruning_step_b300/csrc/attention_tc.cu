@@ -114,6 +114,9 @@ struct Problem {
   int stages;                   // K/V ring stages of this launch (2..MAX_STAGES)
   KvIndex kvi;                  // indexed prefix (kvi.idx != nullptr): gathered
   const __nv_bfloat16 *Kf, *Vf; // from these full caches
+  __nv_bfloat16 *Op;            // prefix self-attention: output [NL][n][Hq][d] per sequence
+  bool prefix;                  // prefix self-attention (no block keys, one unit per
+                                // (layer, query head, 128-row query tile), whole key range)
 };
 
 // Per-sequence tables: ts[s] = first global tile of sequence s; nt[s] =
@@ -129,10 +132,17 @@ __device__ void build_seq_tables(const Problem &pb, int *ts, int *nt, int *ks, i
       int k = b - a;
       if (a < 0 || k < 0 || b > pb.total_kv_rows) { bad = true; k = 0; a = 0; }
       ts[s] = acc;
-      nt[s] = (k + TILE - 1) / TILE + (pb.LB + TILE - 1) / TILE;
       ks[s] = k;
       k0[s] = a;
-      acc += pb.NL * pb.Hkv * nt[s];
+      if (pb.prefix) {
+        // units: (layer, KV head, query tile, head of the group); the key
+        // tiles of a unit are all ceil(k / TILE) prefix tiles
+        nt[s] = (k + TILE - 1) / TILE;
+        acc += pb.NL * pb.Hkv * (pb.Hq / pb.Hkv) * nt[s];
+      } else {
+        nt[s] = (k + TILE - 1) / TILE + (pb.LB + TILE - 1) / TILE;
+        acc += pb.NL * pb.Hkv * nt[s];
+      }
     }
     ts[pb.S] = acc;
     if (bad && blockIdx.x == 0) report(status, SPRINT_STATUS_BAD_OFFSETS);
@@ -144,7 +154,9 @@ struct Seg {
   int first_tile, ntile;   // tile index within the pair, tiles in the segment
   int n_pair, k_s, kv0;    // tiles of the pair, prefix keys, kv_off[s]
   int slot;
+  int qt, hh;              // prefix self-attention: query tile, head within the group
 };
+
 
 __device__ __forceinline__ int seq_of(const int *ts, int S, int x) {
   int lo = 0, hi = S - 1;
@@ -180,6 +192,31 @@ __device__ __forceinline__ Seg locate(const Problem &pb, const int *ts, const in
   return sg;
 }
 
+// Unit u of the prefix self-attention: sequence s, then (layer, KV head),
+// then query tile, then the head within the group (fastest, so the heads
+// that share a KV head run at the same time and share its tiles in L2).
+__device__ __forceinline__ Seg locate_prefix(const Problem &pb, const int *ts, const int *nt,
+                                             const int *ks, const int *k0, int u) {
+  Seg sg;
+  sg.s = seq_of(ts, pb.S, u);
+  const int GQ = pb.Hq / pb.Hkv;
+  const int per_pair = nt[sg.s] * GQ;
+  const int y = u - ts[sg.s];
+  const int pis = y / per_pair, rem = y - pis * per_pair;
+  sg.l = pis / pb.Hkv;
+  sg.g = pis - sg.l * pb.Hkv;
+  sg.pair = sg.s * pb.NL * pb.Hkv + pis;
+  sg.qt = rem / GQ;
+  sg.hh = rem - sg.qt * GQ;
+  sg.first_tile = 0;
+  sg.ntile = nt[sg.s];
+  sg.n_pair = nt[sg.s];
+  sg.k_s = ks[sg.s];
+  sg.kv0 = k0[sg.s];
+  sg.slot = 0;
+  return sg;
+}
+
 // 16-byte global -> shared copy (L2 only); src_bytes = 0 writes zeros.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
@@ -208,10 +245,15 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return r;
 }
 
+// Tensor-memory stores, each waited for in the same statement: tcgen05.st
+// reads its source registers asynchronously until tcgen05.wait::st, and the
+// compiler, seeing the registers as read by the store itself, may reuse
+// them for the next values before then.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
       "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
       "r"(v[15])
@@ -222,7 +264,8 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
       "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
       "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
       "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
@@ -243,7 +286,7 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
-template <int D, bool kIndexed>
+template <int D, bool kIndexed, bool kPrefix>
 __global__ void __launch_bounds__(kIndexed ? THREADS_INDEXED : THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kp,
                const __grid_constant__ CUtensorMap tm_vp,
@@ -265,14 +308,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   uint64_t *pv_done = p_ready + 4;               // 2
   uint64_t *o_full = pv_done + 2, *drain = o_full + 1;  // drain[2]: one per issuer
   uint64_t *never = drain + 2;  // no one arrives: the stall test waits on it
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(never + 1);
+  uint64_t *ml_ready = never + 1;  // 2: prefix mode, a warpgroup's (m, l) are published
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ml_ready + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *ts = reinterpret_cast<int *>(smem + off_bar + 256);
   int *nt = ts + (pb.S + 1), *ks = nt + (pb.S + 1), *k0 = ks + (pb.S + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
-  const int GQ = pb.Hq / pb.Hkv, R = pb.LB * GQ;
+  // Query rows of a tile: the block's LB rows of every head of the group,
+  // or (prefix mode) 128 prefix positions of one head.
+  const int GQ = pb.Hq / pb.Hkv, R = kPrefix ? ROWS : pb.LB * GQ;
   const int BR = pb.LB < TILE ? pb.LB : TILE;  // rows of a block-key box
 
   // Zero the query and K/V buffers once: rows TMA never writes (query rows
@@ -297,6 +343,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     tc::mbar_init(tc::smem_u32(drain), 1);
     tc::mbar_init(tc::smem_u32(drain + 1), 1);
     tc::mbar_init(tc::smem_u32(never), 1);
+    tc::mbar_init(tc::smem_u32(ml_ready), 4);      // the 4 warps of warpgroup 0
+    tc::mbar_init(tc::smem_u32(ml_ready + 1), 4);  // and of warpgroup 1
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
@@ -308,9 +356,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // Decode: a contiguous range of the tile list (stream-K).  Prefix mode:
+  // units blockIdx.x, blockIdx.x + G, ... (whole key ranges).
   const int T = ts[pb.S];
-  const int x_begin = (int)((long long)blockIdx.x * T / G);
-  const int x_end = (int)((long long)(blockIdx.x + 1) * T / G);
+  const int x_begin = kPrefix ? (int)blockIdx.x : (int)((long long)blockIdx.x * T / G);
+  const int x_end = kPrefix ? T : (int)((long long)(blockIdx.x + 1) * T / G);
   const uint32_t sQ = tc::smem_u32(smem + L::OFF_Q);
   const uint32_t sKV = tc::smem_u32(smem + L::OFF_KV);
   const float qk_scale = kLog2e * rsqrtf((float)D);
@@ -321,8 +371,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   uint32_t issued = 0, last_par = 0, q_issued = 0, q_par = 0;
 
   for (int x = x_begin; x < x_end; ++seg_no) {
-    const Seg sg = locate(pb, ts, nt, ks, k0, x, x_end, G, T);
-    x += sg.ntile;
+    const Seg sg = kPrefix ? locate_prefix(pb, ts, nt, ks, k0, x)
+                           : locate(pb, ts, nt, ks, k0, x, x_end, G, T);
+    x += kPrefix ? G : sg.ntile;
     const int np = (sg.k_s + TILE - 1) / TILE;  // prefix tiles of the pair
     const bool run = !*abort_flag;
     if (kIndexed && (warp == 0 || warp == GATHER_WARP) && run) {
@@ -446,9 +497,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       // ------------------------------------------------ producer
       const uint32_t qb = tc::smem_u32(q_full);
       tc::mbar_arrive_expect_tx(qb, (uint32_t)((D / 64) * R * 128));
-      const int qrow = (sg.s * pb.NL + sg.l) * pb.LB;
-      for (int b = 0; b < D / 64; ++b)
-        tc::tma_load_3d(sQ + b * L::QBOX, &tm_q, qb, b * 64, sg.g * GQ, qrow);
+      if (kPrefix) {  // 128 prefix positions of head g GQ + hh
+        const int qrow = pb.NL * sg.kv0 + sg.l * sg.k_s + sg.qt * TILE;
+        for (int b = 0; b < D / 64; ++b)
+          tc::tma_load_3d(sQ + b * L::QBOX, &tm_q, qb, b * 64, sg.g * GQ + sg.hh, qrow);
+      } else {
+        const int qrow = (sg.s * pb.NL + sg.l) * pb.LB;
+        for (int b = 0; b < D / 64; ++b)
+          tc::tma_load_3d(sQ + b * L::QBOX, &tm_q, qb, b * 64, sg.g * GQ, qrow);
+      }
       q_issued = 1;
       q_par = seg_no & 1;
       for (int t = 0; t < sg.ntile; ++t) {
@@ -577,13 +634,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           break;
         }
         tc::fence_after_sync();
-        // Pass 1: row max of the raw scores, 32 columns of S at a time.
         float mraw = -INFINITY;
 #pragma unroll
         for (int c = 0; c < TILE / 32; ++c) {
           float v[32];
           tc::tmem_ld32(s_addr + c * 32, v);
-          tc::tmem_wait_ld();
           if (nvalid < TILE) {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
@@ -613,36 +668,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           for (int c = 0; c < D / 32; ++c) {
             float o[32];
             tc::tmem_ld32(o_addr + c * 32, o);
-            tc::tmem_wait_ld();
             uint32_t u[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(o[j] * alpha);
             tmem_st32(o_addr + c * 32, u);
           }
         }
-        // Pass 2: P = exp2(S * scale - m) as bf16 pairs, 32 keys at a time,
-        // written over the first 64 columns of S[h] (P chunk c lands in
-        // columns 16c..16c+15, all read already; masked keys give 0).
         const float nm = -m_used;
         float lsum = 0.f;
 #pragma unroll
         for (int c = 0; c < TILE / 32; ++c) {
           float v[32];
           tc::tmem_ld32(s_addr + c * 32, v);
-          tc::tmem_wait_ld();
           uint32_t pk[16];
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
             const int j = 2 * u;
             const float p0 = c * 32 + j < nvalid ? fast_exp2(fmaf(v[j], qk_scale, nm)) : 0.f;
-            const float p1 = c * 32 + j + 1 < nvalid ? fast_exp2(fmaf(v[j + 1], qk_scale, nm))
-                                                    : 0.f;
+            const float p1 = c * 32 + j + 1 < nvalid ? fast_exp2(fmaf(v[j + 1], qk_scale, nm)) : 0.f;
             lsum += p0 + p1;
             __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
             pk[u] = *reinterpret_cast<uint32_t *>(&h2);
           }
           tmem_st16(s_addr + c * 16, pk);
-          if (c == TILE / 64 - 1 || c == TILE / 32 - 1) {  // a 64-key half of P is written
+          if (c == TILE / 64 - 1 || c == TILE / 32 - 1) {
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             tc::fence_before_sync();
             __syncwarp();
@@ -651,8 +700,63 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         l_sum += lsum;
       }
-      if (ok && __all_sync(0xffffffffu, tc::mbar_wait(tc::smem_u32(o_full), seg_no & 1,
-                                                      pb.cap_ns, abort_flag))) {
+      if (kPrefix && ok &&
+          __all_sync(0xffffffffu, tc::mbar_wait(tc::smem_u32(o_full), seg_no & 1, pb.cap_ns,
+                                                abort_flag))) {
+        // Prefix mode: merge the two warpgroups' accumulators of each row
+        // and write the normalised output.  The warpgroups publish (m, l)
+        // in the Q buffer (no QK of this unit is left to read it) and each
+        // writes half of the row's columns.
+        tc::fence_after_sync();
+        float2 *ml_sh = reinterpret_cast<float2 *>(smem + L::OFF_Q);
+        ml_sh[h * ROWS + r] = mine ? make_float2(m_used, l_sum) : make_float2(-INFINITY, 0.f);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(ml_ready + h));
+        if (__all_sync(0xffffffffu, tc::mbar_wait(tc::smem_u32(ml_ready + (h ^ 1)), seg_no & 1,
+                                                  pb.cap_ns, abort_flag))) {
+          const float2 a = ml_sh[r], b = ml_sh[ROWS + r];
+          const float M = fmaxf(a.x, b.x);
+          const float w0 = a.x == -INFINITY ? 0.f : exp2f(a.x - M);
+          const float w1 = b.x == -INFINITY ? 0.f : exp2f(b.x - M);
+          const float den = (w0 > 0.f ? w0 * a.y : 0.f) + (w1 > 0.f ? w1 * b.y : 0.f);
+          const float inv = 1.0f / den;
+          const int i = sg.qt * TILE + r;
+          __nv_bfloat16 *dst =
+              pb.Op + (((size_t)pb.NL * sg.kv0 + (size_t)sg.l * sg.k_s + i) * pb.Hq +
+                       (size_t)(sg.g * GQ + sg.hh)) * D;
+          const uint32_t o0 = tmem + lane_off + L::TMEM_O, o1 = o0 + D;
+#pragma unroll 1
+          for (int c = h * (D / 64); c < (h + 1) * (D / 64); ++c) {
+            float x0[32], x1[32];
+            tc::tmem_ld32(o0 + c * 32, x0);
+            tc::tmem_ld32(o1 + c * 32, x1);
+            if (i < sg.k_s) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int u = 0; u < 16; ++u) {
+                // a warpgroup without keys in this unit left its
+                // accumulator unwritten: its weight 0 selects nothing of it
+                const float e0 = (w0 > 0.f ? x0[2 * u] * w0 : 0.f) +
+                                 (w1 > 0.f ? x1[2 * u] * w1 : 0.f);
+                const float e1 = (w0 > 0.f ? x0[2 * u + 1] * w0 : 0.f) +
+                                 (w1 > 0.f ? x1[2 * u + 1] * w1 : 0.f);
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(e0 * inv, e1 * inv);
+                pk[u] = *reinterpret_cast<uint32_t *>(&h2);
+              }
+              uint4 *out = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                out[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+          }
+        }
+        // The next unit's Q lands here by TMA (async proxy) after the
+        // generic accesses above.
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tc::fence_before_sync();
+      } else if (!kPrefix && ok &&
+                 __all_sync(0xffffffffu, tc::mbar_wait(tc::smem_u32(o_full), seg_no & 1,
+                                                       pb.cap_ns, abort_flag))) {
         tc::fence_after_sync();
         const size_t part = (size_t)(2 * sg.slot + h) * ROWS + r;
         if (mine) {
@@ -661,7 +765,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           for (int c = 0; c < D / 32; ++c) {
             float o[32];
             tc::tmem_ld32(o_addr + c * 32, o);
-            tc::tmem_wait_ld();
             if (r < R) {
 #pragma unroll
               for (int j = 0; j < 32; j += 4)
@@ -812,6 +915,25 @@ bool make_tmap_3d(CUtensorMap *m, const void *base, int D, int heads, uint64_t r
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Largest dynamic shared memory a CTA may use, with every variant of the
+// kernel opted in to it (once per device).
+template <int D> bool smem_optin(int *optin) {
+  static PerDevice optin_cache;
+  return optin_cache.get(optin, [](int dev, int *v) {
+    return cudaDeviceGetAttribute(v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ==
+               cudaSuccess &&
+           cudaFuncSetAttribute(attn_tc_kernel<D, false, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, *v - 256) ==
+               cudaSuccess &&
+           cudaFuncSetAttribute(attn_tc_kernel<D, true, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, *v - 256) ==
+               cudaSuccess &&
+           cudaFuncSetAttribute(attn_tc_kernel<D, false, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, *v - 256) ==
+               cudaSuccess;
+  });
+}
+
 template <int D>
 int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 *Vp,
            const int32_t *kv_off, int total_kv_rows, const __nv_bfloat16 *Kb,
@@ -834,19 +956,8 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
     tvp = tvb;
   }
   // As many ring stages as fit next to Q, the barriers and the tables.
-  static PerDevice optin_cache;
   int optin = 0;
-  if (!optin_cache.get(&optin, [](int dev, int *v) {
-        return cudaDeviceGetAttribute(v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) ==
-                   cudaSuccess &&
-               cudaFuncSetAttribute(attn_tc_kernel<D, false>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    *v - 256) == cudaSuccess &&
-               cudaFuncSetAttribute(attn_tc_kernel<D, true>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    *v - 256) == cudaSuccess;
-      }))
-    return SPRINT_ERR_CUDA;
+  if (!smem_optin<D>(&optin)) return SPRINT_ERR_CUDA;
   int stages = MAX_STAGES;
   while (stages > 2 && Lt::smem_bytes(stages, S) > (size_t)(optin - 256)) --stages;
   const size_t smem = Lt::smem_bytes(stages, S);
@@ -869,10 +980,13 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
   pb.kvi = kvi;
   pb.Kf = kvi.idx ? Kp : nullptr;
   pb.Vf = kvi.idx ? Vp : nullptr;
+  pb.Op = nullptr;
+  pb.prefix = false;
   if (kvi.idx)
-    attn_tc_kernel<D, true><<<G, THREADS_INDEXED, smem, stream>>>(tq, tkp, tvp, tkb, tvb, pb);
+    attn_tc_kernel<D, true, false><<<G, THREADS_INDEXED, smem, stream>>>(tq, tkp, tvp, tkb, tvb,
+                                                                         pb);
   else
-    attn_tc_kernel<D, false><<<G, THREADS, smem, stream>>>(tq, tkp, tvp, tkb, tvb, pb);
+    attn_tc_kernel<D, false, false><<<G, THREADS, smem, stream>>>(tq, tkp, tvp, tkb, tvb, pb);
   if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   const long long warps = (long long)pairs * LB * GQ;
   attn_tc_combine_kernel<D><<<(int)((warps * 32 + 255) / 256), 256, 0, stream>>>(
@@ -880,7 +994,58 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
   return launch_status();
 }
 
+// Prefix self-attention: one unit per (sequence, layer, query head, 128-row
+// query tile) over all of the sequence's prefix keys; no workspace, no
+// combine (each unit merges its two warpgroups' accumulators and writes
+// its normalised rows).
+template <int D>
+int launch_prefix(const __nv_bfloat16 *Qp, const __nv_bfloat16 *K, const __nv_bfloat16 *V,
+                  const int32_t *prefix_off, int total_rows, int S, int NL, int Hq, int Hkv,
+                  __nv_bfloat16 *Op, int32_t *status, cudaStream_t stream) {
+  using Lt = Layout<D>;
+  CUtensorMap tq, tk, tv;
+  const uint64_t rows = (uint64_t)NL * total_rows;
+  if (!make_tmap_3d(&tq, Qp, D, Hq, rows, 1, TILE) || !make_tmap_3d(&tk, K, D, Hkv, rows, 1, TILE) ||
+      !make_tmap_3d(&tv, V, D, Hkv, rows, 1, TILE))
+    return SPRINT_ERR_CUDA;
+  int optin = 0;
+  if (!smem_optin<D>(&optin)) return SPRINT_ERR_CUDA;
+  int stages = MAX_STAGES;
+  while (stages > 2 && Lt::smem_bytes(stages, S) > (size_t)(optin - 256)) --stages;
+  const size_t smem = Lt::smem_bytes(stages, S);
+  if (smem > (size_t)(optin - 256)) return SPRINT_ERR_UNSUPPORTED;
+  Problem pb;
+  pb.kv_off = prefix_off;
+  pb.total_kv_rows = total_rows;
+  pb.S = S; pb.NL = NL; pb.LB = 0; pb.Hq = Hq; pb.Hkv = Hkv;
+  pb.ws_o = nullptr;
+  pb.ws_ml = nullptr;
+  pb.status = status;
+  pb.cap_ns = wait_cap_ns();
+  pb.drain_ns = pb.cap_ns > 1000000000ull ? pb.cap_ns : 1000000000ull;
+  pb.stall_test = stall_test_enabled();
+  pb.gate = Gate{nullptr, 0};
+  pb.stages = stages;
+  pb.kvi = KvIndex{nullptr, nullptr, 0};
+  pb.Kf = nullptr;
+  pb.Vf = nullptr;
+  pb.Op = Op;
+  pb.prefix = true;
+  attn_tc_kernel<D, false, true><<<sm_count(), THREADS, smem, stream>>>(tq, tk, tv, tk, tv, pb);
+  return launch_status();
+}
+
 }  // namespace
+
+int attn_tc_prefix(const __nv_bfloat16 *Qp, const __nv_bfloat16 *K, const __nv_bfloat16 *V,
+                   const int32_t *prefix_off, int total_rows, int S, int NL, int Hq, int Hkv,
+                   int d, __nv_bfloat16 *Op, int32_t *status, cudaStream_t stream) {
+  if (S > MAX_SEQ) return SPRINT_ERR_UNSUPPORTED;
+  return d == 64 ? launch_prefix<64>(Qp, K, V, prefix_off, total_rows, S, NL, Hq, Hkv, Op, status,
+                                     stream)
+                 : launch_prefix<128>(Qp, K, V, prefix_off, total_rows, S, NL, Hq, Hkv, Op,
+                                      status, stream);
+}
 
 size_t attn_tc_workspace_bytes(int S, int NL, int Hkv, int d) {
   const size_t parts = 2 * ((size_t)S * NL * Hkv + (size_t)sm_count());

@@ -311,7 +311,6 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
         if (ncol <= 0) break;  // uniform across the warp
         float v[32];
         tc::tmem_ld32(taddr + (uint32_t)(c * 32), v);
-        tc::tmem_wait_ld();
         if (ncol < 32) {  // past the vocabulary: no maximum, no probability
 #pragma unroll
           for (int i = 0; i < 32; ++i)

@@ -75,12 +75,18 @@ class BlockDecoder:
     reaches the confidences; the native driver fuses the sum into the
     attention's combine kernel, the stepwise path calls
     sprint_residual_hidden.
+
+    prefix_attn=True: step 0 also runs the prefix's own attention of the full
+    forward pass (sprint_prefix_attn) on the prefix queries prefix["Qp"]
+    ([NL][n][Hq][d] per sequence) into self.O_prefix.  The output feeds
+    nothing downstream here (the backbone around it is not reproduced);
+    the option puts that work into the timed step.
     """
 
     def __init__(self, W, *, NL, Hq, Hkv, d, LB, T, tau, r_text, r_img, alpha=0.5,
                  mode=sp.UNMASK_ADAPTIVE, modality_counts, want_logits=False, indexed=False,
                  selection="modality", r_global=0.5, pool_sizes=None, residual=False,
-                 prefix_argmax=False):
+                 prefix_argmax=False, prefix_attn=False):
         self.W = W
         self.dev = W.device
         self.dtype = W.dtype
@@ -93,6 +99,7 @@ class BlockDecoder:
             raise ValueError(f"unknown selection {selection!r}")
         self.selection, self.r_global = selection, r_global
         self.residual = bool(residual)
+        self.prefix_attn = bool(prefix_attn)
         if self.residual and Hq * d != W.shape[1]:
             raise ValueError("the residual chain needs Hq * d == D")
         self.V, self.D = W.shape
@@ -220,6 +227,8 @@ class BlockDecoder:
         self.ws_attn = self._buf(
             "ws_attn", max(16, sp.sprint_block_attn_workspace_bytes(
                 S, NL, self.LB, self.Hq, Hkv, d, self.max_rows, dt)), u8)
+        self.O_prefix = (self._buf("O_prefix", self.total_rows * NL * self.Hq * d, self.dtype)
+                         if self.prefix_attn else None)
 
     def _timed(self, name):
         return self.timing is not None and (self.timing_stages is None
@@ -264,7 +273,8 @@ class BlockDecoder:
         return evs
 
     # -- the individual stages (each is one or two library calls) --------
-    def prefix_pass(self, K, V, H, theta, modality, conf_from=0, image=None, step0=None):
+    def prefix_pass(self, K, V, H, theta, modality, conf_from=0, image=None, step0=None,
+                    Qp=None):
         """Step-0 scoring and pruning: confidences of every prefix row, the
         kept set, and the pruned cache (self.Kp / self.Vp; not made when the
         decoder reads the kept rows through their indices).
@@ -286,6 +296,13 @@ class BlockDecoder:
         if r0:
             if self.S != 1 or not 0 < r0 <= self.total_rows:
                 raise ValueError("conf_from needs one sequence and 0 < conf_from <= rows")
+        if self.prefix_attn:
+            if Qp is None:
+                raise ValueError("prefix_attn needs the prefix queries prefix['Qp']")
+            with self._stage("prefix_attn"):
+                sp.sprint_prefix_attn(Qp, K, V, self.prefix_off, self.total_rows, self.NL,
+                                      self.Hq, self.Hkv, self.d, Op=self.O_prefix,
+                                      status=self.status)
         merged = False
         with self._stage("lmhead_prefix"):
             if r0 and step0 is not None and r0 < self.total_rows:
@@ -414,7 +431,8 @@ class BlockDecoder:
         step0_given = self.prefix_pass(
             prefix["K"], prefix["V"], prefix["H"], prefix["theta"], prefix["modality"],
             conf_from=conf_from, image=prefix.get("image"),
-            step0=xs[0] if conf_from and not self.residual and not self.want_logits else None)
+            step0=xs[0] if conf_from and not self.residual and not self.want_logits else None,
+            Qp=prefix.get("Qp"))
         events = self._events_for_steps(slot) if self.timing is not None else None
         sp.sprint_decode_steps(
             Q=[x["Q"] for x in xs], Kb=[x["Kb"] for x in xs], Vb=[x["Vb"] for x in xs],
@@ -474,7 +492,8 @@ class BlockDecoder:
         self.mask.fill_(1)
         self.tokens.fill_(-1)
         self.prefix_pass(prefix["K"], prefix["V"], prefix["H"], prefix["theta"],
-                         prefix["modality"], conf_from=conf_from, image=prefix.get("image"))
+                         prefix["modality"], conf_from=conf_from, image=prefix.get("image"),
+                         Qp=prefix.get("Qp"))
         accepted = []
         prev = [self.LB] * self.S
         n_steps = 0

@@ -14,7 +14,10 @@ import os
 
 import torch
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsprint.so")
+# The release library next to this file, or the one SPRINT_LIBRARY names
+# (the debug build, libsprint_debug.so).
+LIB_PATH = os.environ.get("SPRINT_LIBRARY") or os.path.join(
+    os.path.dirname(os.path.abspath(__file__)), "libsprint.so")
 
 F32 = 0
 BF16 = 1
@@ -26,6 +29,7 @@ STATUS_KEPT_MISMATCH = 2
 STATUS_TIMEOUT = 4
 STATUS_BAD_INDEX = 8
 STATUS_BAD_TEMPERATURE = 16
+STATUS_DEBUG_CHECK = 32
 
 # Every symbol include/sprint.h declares, with (restype, argtypes).
 _P, _I, _Z, _F, _D = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float, ctypes.c_double
@@ -33,6 +37,7 @@ SIGNATURES = {
     "sprint_version": (_I, []),
     "sprint_strerror": (ctypes.c_char_p, [_I]),
     "sprint_kernel_launches": (ctypes.c_ulonglong, []),
+    "sprint_debug_checks": (_I, []),
     "sprint_keep_count": (_I, [_I, _D]),
     "sprint_lmhead_workspace_bytes": (_Z, [_I, _I, _I, _I]),
     "sprint_lmhead_confidence": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P, _P]),
@@ -50,6 +55,7 @@ SIGNATURES = {
     "sprint_block_attn_indexed": (_I, [_P, _P, _P, _P, _I, _P, _P, _I, _I, _P, _P, _I, _I, _I,
                                        _I, _I, _I, _I, _P, _P, _Z, _P, _P]),
     "sprint_residual_hidden": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P]),
+    "sprint_prefix_attn": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "sprint_unmask": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _P, _P]),
     "sprint_decode_steps": (_I, [_P, _P]),
 }
@@ -143,6 +149,10 @@ def sprint_strerror(code: int) -> str:
 
 def sprint_kernel_launches() -> int:
     return lib.sprint_kernel_launches()
+
+
+def sprint_debug_checks() -> int:
+    return lib.sprint_debug_checks()
 
 
 def sprint_keep_count(n: int, r: float) -> int:
@@ -342,6 +352,24 @@ def sprint_residual_hidden(h_in, O, *, h_out=None, stream=None):
                                     _stream(stream))
     _check(rc, "sprint_residual_hidden")
     return h_out
+
+
+def sprint_prefix_attn(Qp, K, V, prefix_off, total_rows, NL, Hq, Hkv, d, *, Op=None,
+                       status=None, stream=None):
+    """The prefix's own attention at a block's first step: Op [NL][n_s][Hq][d]
+    per sequence (concatenated like Qp), every position over every position
+    of its sequence's prefix."""
+    S = prefix_off.numel() - 1
+    dev = Qp.device
+    Op = torch.empty_like(Qp) if Op is None else Op
+    status = new_status(dev) if status is None else status
+    rc = lib.sprint_prefix_attn(
+        _ptr(Qp, Qp.dtype, "Qp"), _ptr(K, Qp.dtype, "K"), _ptr(V, Qp.dtype, "V"),
+        _ptr(prefix_off, torch.int32, "prefix_off"), int(total_rows), S, NL, Hq, Hkv, d,
+        _dtype_code(Qp), _ptr(Op, Qp.dtype, "Op"), _ptr(status, torch.int32, "status"),
+        _stream(stream))
+    _check(rc, "sprint_prefix_attn")
+    return Op
 
 
 def sprint_unmask(conf, argmax, mask, tokens, t, T, tau, mode=UNMASK_ADAPTIVE, *, m_out=None,

@@ -205,6 +205,15 @@ def prefix_inputs(w: Workload, seq: int = 0, block: int = 0, device="cpu",
             "image": image.to(device)}
 
 
+def prefix_queries(w: Workload, seq: int = 0, block: int = 0, device="cpu",
+                   n: int | None = None) -> torch.Tensor:
+    """Queries of the prefix positions for the prefix's own attention in a
+    block's first step: Qp [NL][n][Hq][d] ~ N(0, 1), in the storage type."""
+    n = prefix_layout(w, seq, block).numel() if n is None else n
+    g = generator(device, w.seed, "prefix-q", seq, block)
+    return torch.randn((w.NL, n, w.Hq, w.d), generator=g, device=device).to(w.torch_dtype)
+
+
 def step_inputs(w: Workload, seq: int, block: int, step: int, device="cpu"):
     """Per-step block tensors: Q [NL][LB][Hq][d], Kb, Vb [NL][LB][Hkv][d],
     h [LB][D] and theta [LB]."""
