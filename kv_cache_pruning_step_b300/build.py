@@ -3,7 +3,10 @@
     python -m kv_cache_pruning_step_b300.build [--debug]
 
 Objects go to _build/ at the repository root; the shared library is written
-next to this file so that it ships with the package directory.
+next to this file so that it ships with the package directory.  --debug
+builds libsprint_debug.so instead (SPRINT_DEBUG_CHECKS=1: device-side
+invariant checks that report SPRINT_STATUS_DEBUG_CHECK); the binding loads
+it when SPRINT_LIBRARY names it.
 """
 from __future__ import annotations
 
@@ -17,6 +20,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "libsprint.so")
+OUT_DEBUG = os.path.join(PKG, "libsprint_debug.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
@@ -63,12 +67,13 @@ def build(debug: bool = False, verbose: bool = False, force: bool = False) -> st
                 failed.append(cmd[-3])
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(failed))
-    if jobs or not os.path.exists(OUT) or force:
-        link = [NVCC, *ARCH, "-shared", "-o", OUT, *objs]
+    out = OUT_DEBUG if debug else OUT
+    if jobs or not os.path.exists(out) or force:
+        link = [NVCC, *ARCH, "-shared", "-o", out, *objs]
         r = subprocess.run(link, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
-    return OUT
+    return out
 
 
 if __name__ == "__main__":

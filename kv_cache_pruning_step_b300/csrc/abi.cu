@@ -11,6 +11,8 @@ extern "C" unsigned long long sprint_kernel_launches(void) { return g_launches.l
 
 extern "C" int sprint_version(void) { return SPRINT_VERSION; }
 
+extern "C" int sprint_debug_checks(void) { return sprint::kDebugChecks ? 1 : 0; }
+
 extern "C" const char *sprint_strerror(int code) {
   switch (code) {
     case SPRINT_OK: return "ok";

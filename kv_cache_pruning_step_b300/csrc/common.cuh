@@ -60,6 +60,22 @@ __device__ __forceinline__ void report(int32_t *status, uint32_t bit) {
   if (status) atomicOr(reinterpret_cast<unsigned int *>(status), bit);
 }
 
+// Invariant checks compiled into the debug build only (SPRINT_DEBUG_CHECKS
+// defined non-zero): a failed check ORs SPRINT_STATUS_DEBUG_CHECK into the
+// status word and the kernel carries on; nothing traps.
+#if defined(SPRINT_DEBUG_CHECKS) && SPRINT_DEBUG_CHECKS
+constexpr bool kDebugChecks = true;
+#define SPRINT_DCHECK(cond, status)                                      \
+  do {                                                                   \
+    if (!(cond)) ::sprint::report((status), SPRINT_STATUS_DEBUG_CHECK);  \
+  } while (0)
+#else
+constexpr bool kDebugChecks = false;
+#define SPRINT_DCHECK(cond, status) \
+  do {                              \
+  } while (0)
+#endif
+
 // Eight consecutive elements of a row, widened to fp32.
 template <typename T> struct Vec8;
 

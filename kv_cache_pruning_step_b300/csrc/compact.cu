@@ -32,6 +32,8 @@ compact_kernel(const uint4 *__restrict__ K, const uint4 *__restrict__ V,
     }
     const int n = p1 - p0, ks = k1 - k0, j = g - k0;
     const int idx = __ldg(kept_idx + g);
+    // Kept indices are stored in ascending position order.
+    if (kDebugChecks && lane == 0 && j > 0) SPRINT_DCHECK(__ldg(kept_idx + g - 1) < idx, status);
     if (idx < 0 || idx >= n) {
       if (lane == 0) report(status, SPRINT_STATUS_BAD_INDEX);
       continue;

@@ -132,6 +132,14 @@ __device__ __forceinline__ Part fold(Part x, Part y, float sc) {
   return r;
 }
 
+// Debug build: a row's greedy token lies in [0, V) and its confidence, a
+// maximum probability, in [1/V, 1] (with room for rounding).
+__device__ __forceinline__ void debug_check_row(float c, int a, int V, int32_t *status) {
+  (void)c; (void)a; (void)V; (void)status;
+  SPRINT_DCHECK(a >= 0 && a < V, status);
+  SPRINT_DCHECK(c >= (1.0f / (float)V) * (1.0f - 1e-3f) && c <= 1.0f + 1e-5f, status);
+}
+
 // Many rows: a CTA of 32 rows x 8 strip groups.  Thread (x, y) folds strips
 // y, y + 8, ... of row x (loads coalesced over x), then the 8 group partials
 // of each row are folded in ascending y.  Deterministic for given M, V.
@@ -140,8 +148,8 @@ constexpr int kCombRows = 32, kCombGroups = 8;
 __global__ void __launch_bounds__(kCombRows * kCombGroups)
 lmhead_combine_kernel(const float *__restrict__ pmax, const float *__restrict__ psum,
                       const int32_t *__restrict__ parg, const float *__restrict__ temp, int M,
-                      int strips, float *__restrict__ conf, int32_t *__restrict__ argmax,
-                      Gate gate) {
+                      int strips, int V, float *__restrict__ conf, int32_t *__restrict__ argmax,
+                      int32_t *status, Gate gate) {
   if (gate_closed(gate)) return;
   __shared__ Part sh[kCombGroups][kCombRows];
   const int x = threadIdx.x, y = threadIdx.y;
@@ -166,6 +174,7 @@ lmhead_combine_kernel(const float *__restrict__ pmax, const float *__restrict__ 
     for (int g = 1; g < kCombGroups; ++g) r = fold(r, sh[g][x], sc);
     conf[row] = 1.0f / r.s;
     if (argmax) argmax[row] = r.a;
+    debug_check_row(1.0f / r.s, argmax ? r.a : 0, V, status);
   }
 }
 
@@ -174,8 +183,8 @@ lmhead_combine_kernel(const float *__restrict__ pmax, const float *__restrict__ 
 __global__ void __launch_bounds__(128)
 lmhead_combine_rows_kernel(const float *__restrict__ pmax, const float *__restrict__ psum,
                            const int32_t *__restrict__ parg, const float *__restrict__ temp,
-                           int M, int strips, float *__restrict__ conf,
-                           int32_t *__restrict__ argmax, Gate gate) {
+                           int M, int strips, int V, float *__restrict__ conf,
+                           int32_t *__restrict__ argmax, int32_t *status, Gate gate) {
   if (gate_closed(gate)) return;
   __shared__ Part sh[4];
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -199,6 +208,7 @@ lmhead_combine_rows_kernel(const float *__restrict__ pmax, const float *__restri
     Part r = fold(fold(sh[0], sh[1], sc), fold(sh[2], sh[3], sc), sc);
     conf[row] = 1.0f / r.s;
     if (argmax) argmax[row] = r.a;
+    debug_check_row(1.0f / r.s, argmax ? r.a : 0, V, status);
   }
 }
 
@@ -249,11 +259,11 @@ int sprint::lmhead_confidence_impl(const void *h, const void *W, const float *te
   }
   if (M < 4096)
     lmhead_combine_rows_kernel<<<M, 128, 0, stream>>>(p.pmax, p.psum, p.parg, temp, M, p.strips,
-                                                      conf_out, argmax_out, gate);
+                                                      V, conf_out, argmax_out, status, gate);
   else
     lmhead_combine_kernel<<<(M + kCombRows - 1) / kCombRows, dim3(kCombRows, kCombGroups), 0,
-                            stream>>>(p.pmax, p.psum, p.parg, temp, M, p.strips, conf_out,
-                                      argmax_out, gate);
+                            stream>>>(p.pmax, p.psum, p.parg, temp, M, p.strips, V, conf_out,
+                                      argmax_out, status, gate);
   return launch_status();
 }
 

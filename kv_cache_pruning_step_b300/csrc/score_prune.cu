@@ -545,6 +545,12 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
     r_t0 += __popc(b0);
     r_t1 += __popc(b1);
   }
+  if (kDebugChecks && rank == cl - 1 && tid == 0) {
+    // positions written by the whole cluster = the sequence's kept count
+    const int written = cbase_sh[0] + xc.cnt[0] + min(cbase_sh[1] + xc.cnt[1], need0) +
+                        min(cbase_sh[2] + xc.cnt[2], need1);
+    SPRINT_DCHECK(written == k_all, status);
+  }
   cluster.sync();  // nobody leaves while another CTA may still read its counts
 }
 

@@ -19,7 +19,7 @@ __global__ void unmask_kernel(const float *__restrict__ conf,
                               uint8_t *__restrict__ mask, int32_t *__restrict__ tokens,
                               int32_t *__restrict__ m_out, int LB, int t, int T,
                               float tau, int mode, uint8_t *__restrict__ accepted_out,
-                              Gate gate) {
+                              int32_t *status, Gate gate) {
   if (gate_closed(gate)) {  // the block finished earlier: nothing left to unmask
     const size_t at = (size_t)blockIdx.x * LB + threadIdx.x;
     if (accepted_out && (int)threadIdx.x < LB) accepted_out[at] = 0;
@@ -61,6 +61,12 @@ __global__ void unmask_kernel(const float *__restrict__ conf,
   if (active && accepted_out) accepted_out[at] = accept;
   const int n_acc = __syncthreads_count(accept);
   if (j == 0) m_out[s] = m - n_acc;
+  if (kDebugChecks) {  // the count left equals the mask; unmasked positions hold tokens
+    const bool still = active && mask[at] != 0;
+    const int left = __syncthreads_count(still);
+    if (j == 0) SPRINT_DCHECK(left == m - n_acc, status);
+    if (active && !still) SPRINT_DCHECK(tokens[at] >= 0, status);
+  }
 }
 
 }  // namespace sprint
@@ -71,7 +77,6 @@ int sprint::unmask_impl(const float *conf, const int32_t *argmax, uint8_t *mask,
                         int32_t *m_out, int S, int LB, int t, int T, float tau, int mode,
                         uint8_t *accepted_out, int32_t *status, Gate gate,
                         cudaStream_t stream) {
-  (void)status;
   if (S < 0 || LB < 1 || LB > 1024 || T < 1 || t < 0) return SPRINT_ERR_INVALID_ARG;
   if (mode != SPRINT_UNMASK_ADAPTIVE && mode != SPRINT_UNMASK_FIXED)
     return SPRINT_ERR_INVALID_ARG;
@@ -79,7 +84,7 @@ int sprint::unmask_impl(const float *conf, const int32_t *argmax, uint8_t *mask,
   if (!conf || !argmax || !mask || !tokens || !m_out) return SPRINT_ERR_INVALID_ARG;
   const int threads = (LB + 31) / 32 * 32;
   unmask_kernel<<<S, threads, 0, stream>>>(conf, argmax, mask, tokens, m_out, LB, t, T, tau,
-                                           mode, accepted_out, gate);
+                                           mode, accepted_out, status, gate);
   return launch_status();
 }
 
