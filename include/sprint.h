@@ -419,11 +419,15 @@ int sprint_unmask(const float *conf, const int32_t *argmax, uint8_t *mask,
  *
  * For step t = 0 .. T-1 the call enqueues sprint_block_attn, then
  * sprint_lmhead_confidence on the block rows, then sprint_unmask, on
- * `stream`, without any device-to-host synchronisation.  Whether a step
- * runs is decided on the device: the kernels of step t >= 1 read the
- * still-masked counts m_hist[t-1][0..S) written by step t-1 and return at
- * once when all are zero (the block finished earlier).  Before step 0 the
- * call sets mask to 1 and tokens to -1 (cudaMemsetAsync).  The prefix pass
+ * `stream`, without any device-to-host synchronisation.  With fewer than
+ * 4096 block rows (S * LB < 4096) the LM head's strip partials are folded
+ * and the block unmasked by one kernel (the same arithmetic as the two
+ * separate calls, bit for bit).  Whether a step runs is decided on the
+ * device: the kernels of step t >= 1 read the still-masked counts
+ * m_hist[t-1][0..S) written by step t-1 and return at once when all are
+ * zero (the block finished earlier).  Step 0's unmask treats every
+ * position as masked whatever mask holds, and leaves mask and tokens fully
+ * written (1 / -1 where not accepted).  The prefix pass
  * (prefix confidences, sprint_score_prune, sprint_compact_kv) is not part
  * of this call.  With kept_idx set, steps t >= 1 attend as
  * sprint_block_attn_indexed does (kept rows of Kf / Vf read through
@@ -447,7 +451,7 @@ int sprint_unmask(const float *conf, const int32_t *argmax, uint8_t *mask,
  *   O                                        [S][NL][LB][Hq][d] attention out
  *   logits                                   [S*LB][vocab] or NULL
  *   conf, argmax                             [S*LB] last executed step's c
- *   mask, tokens                             [S][LB] state, reset at step 0
+ *   mask, tokens                             [S][LB] state, set at step 0
  *   m_hist                                   int32 [T][S] masked after step t
  *   accepted                                 uint8 [T][S][LB] or NULL
  *   ws_attn / ws_lm (+ bytes)                workspaces of the two calls

@@ -185,18 +185,15 @@ __device__ __forceinline__ int next_pow2(int x) { return x <= 1 ? 1 : 1 << (32 -
 __device__ __forceinline__ double u_leaf_sum(const float *__restrict__ u, int n, int g,
                                              int lane) {
   const int base = g * kLeaf;
+  float v[32];  // all 32 loads in flight before the in-order sum
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int p = base + i * 32 + lane;
+    v[i] = p < n ? __ldg(u + p) : 0.f;
+  }
   float acc = 0.f;
 #pragma unroll
-  for (int i0 = 0; i0 < 32; i0 += 8) {
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int p = base + (i0 + i) * 32 + lane;
-      v[i] = p < n ? __ldg(u + p) : 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc += v[i];
-  }
+  for (int i = 0; i < 32; ++i) acc += v[i];
   return warp_sum((double)acc);
 }
 
@@ -294,7 +291,21 @@ int block_attn_impl(const void *Q, const void *Kp, const void *Vp, const int32_t
                     Gate gate, cudaStream_t stream);
 int unmask_impl(const float *conf, const int32_t *argmax, uint8_t *mask, int32_t *tokens,
                 int32_t *m_out, int S, int LB, int t, int T, float tau, int mode,
-                uint8_t *accepted_out, int32_t *status, Gate gate, cudaStream_t stream);
+                uint8_t *accepted_out, int32_t *status, Gate gate, cudaStream_t stream,
+                int fresh = 0);
+// Native driver, block steps of fewer than 4096 rows and blocks of at most
+// kFusedMaxLB positions: the LM-head tiles only (strip partials in ws), then
+// one kernel that folds each sequence's rows and unmasks its block
+// (lmhead.cu).
+constexpr int kFusedMaxLB = 512;
+int lmhead_tiles_impl(const void *h, const void *W, const float *temp, int M, int D, int V,
+                      int dtype, void *logits_out, bool want_argmax, void *ws, size_t ws_bytes,
+                      int32_t *status, Gate gate, cudaStream_t stream);
+int combine_unmask_impl(void *ws, const float *temp, int S, int LB, int V, int dtype,
+                        float *conf_out, int32_t *argmax_out, uint8_t *mask, int32_t *tokens,
+                        int32_t *m_out, int t, int T, float tau, int mode,
+                        uint8_t *accepted_out, int fresh, int32_t *status, Gate gate,
+                        cudaStream_t stream);
 
 // Key-norm pass of the scoring (score_prune.cu): u[row] = mean over layers
 // of the L2 norm of the row's keys concatenated over KV heads.

@@ -34,9 +34,11 @@ extern "C" int sprint_decode_steps(const sprint_steps_args *a, cudaStream_t stre
   if (a->residual && (!a->h_res || a->Hq * a->d != a->D)) return SPRINT_ERR_INVALID_ARG;
   if (a->residual && a->step0_given) return SPRINT_ERR_INVALID_ARG;
   const int S = a->S, LB = a->LB, M = S * LB;
-  if (cudaMemsetAsync(a->mask, 1, (size_t)M, stream) != cudaSuccess ||
-      cudaMemsetAsync(a->tokens, 0xff, (size_t)M * sizeof(int32_t), stream) != cudaSuccess)
-    return SPRINT_ERR_CUDA;
+  // Fewer than 4096 block rows and blocks of at most kFusedMaxLB positions:
+  // the LM head's strip partials are folded and the block unmasked by one
+  // kernel per step.  Step 0's unmask starts from an all-masked block, so
+  // mask and tokens need no separate initialisation.
+  const bool fused = M < 4096 && LB <= kFusedMaxLB;
   for (int t = 0; t < a->T; ++t) {
     const Gate gate = t == 0 ? Gate{nullptr, 0} : Gate{a->m_hist + (size_t)(t - 1) * S, S};
     const bool full = t == 0, indexed = !full && a->kept_idx;
@@ -55,17 +57,36 @@ extern "C" int sprint_decode_steps(const sprint_steps_args *a, cudaStream_t stre
                            gate, stream);
     if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 1, stream);
     if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 2, stream);
-    if (rc == SPRINT_OK && !(t == 0 && a->step0_given))
-      rc = lmhead_confidence_impl(a->residual ? a->h_res : a->h[t], a->W, a->theta ? a->theta[t] : nullptr, M, a->D,
-                                  a->vocab, a->dtype, a->logits, a->conf, a->argmax, a->ws_lm,
-                                  a->ws_lm_bytes, a->status, gate, stream);
-    if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 3, stream);
-    if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 4, stream);
-    if (rc == SPRINT_OK)
-      rc = unmask_impl(a->conf, a->argmax, a->mask, a->tokens, a->m_hist + (size_t)t * S, S, LB,
-                       t, a->T, a->tau, a->mode,
-                       a->accepted ? a->accepted + (size_t)t * M : nullptr, a->status, gate,
-                       stream);
+    const void *h = a->residual ? a->h_res : a->h[t];
+    const float *theta = a->theta ? a->theta[t] : nullptr;
+    uint8_t *acc = a->accepted ? a->accepted + (size_t)t * M : nullptr;
+    int32_t *m_t = a->m_hist + (size_t)t * S;
+    const int fresh = t == 0;
+    const bool head = !(t == 0 && a->step0_given);
+    if (fused && head) {
+      // the LM-head tiles, then one kernel folding the rows and unmasking
+      // (its time is counted in the LM-head stage; the unmask events mark
+      // an empty interval)
+      if (rc == SPRINT_OK)
+        rc = lmhead_tiles_impl(h, a->W, theta, M, a->D, a->vocab, a->dtype, a->logits, true,
+                               a->ws_lm, a->ws_lm_bytes, a->status, gate, stream);
+      if (rc == SPRINT_OK)
+        rc = combine_unmask_impl(a->ws_lm, theta, S, LB, a->vocab, a->dtype, a->conf, a->argmax,
+                                 a->mask, a->tokens, m_t, t, a->T, a->tau, a->mode, acc, fresh,
+                                 a->status, gate, stream);
+      if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 3, stream);
+      if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 4, stream);
+    } else {
+      if (rc == SPRINT_OK && head)
+        rc = lmhead_confidence_impl(h, a->W, theta, M, a->D, a->vocab, a->dtype, a->logits,
+                                    a->conf, a->argmax, a->ws_lm, a->ws_lm_bytes, a->status,
+                                    gate, stream);
+      if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 3, stream);
+      if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 4, stream);
+      if (rc == SPRINT_OK)
+        rc = unmask_impl(a->conf, a->argmax, a->mask, a->tokens, m_t, S, LB, t, a->T, a->tau,
+                         a->mode, acc, a->status, gate, stream, fresh);
+    }
     if (rc == SPRINT_OK) rc = record(a->events, 6 * t + 5, stream);
     if (rc != SPRINT_OK) return rc;
   }

@@ -14,10 +14,15 @@
 // combine kernel and the entry point.
 #include <math.h>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
+#include "unmask.cuh"
 #include "lmhead.cuh"
 
 namespace sprint {
+
+namespace cg = cooperative_groups;
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -178,38 +183,162 @@ lmhead_combine_kernel(const float *__restrict__ pmax, const float *__restrict__ 
   }
 }
 
-// Few rows: one CTA per row, threads stride over the strips, then a fixed
-// shuffle/shared-memory tree (deterministic).
-__global__ void __launch_bounds__(128)
+__device__ __forceinline__ float row_scale(const float *__restrict__ temp, int row) {
+  float th = temp ? temp[row] : 1.0f;
+  if (!(th > 0.0f) || !isfinite(th)) th = 1.0f;
+  return kLog2e / th;
+}
+
+// Few rows (M < 4096): the strip partials of a tile of up to 32 rows are
+// folded by a cluster of kFoldCtas CTAs.  Strip group g < kFoldGroups folds
+// strips g, g + kFoldGroups, ... of each row in order; the groups' partials
+// are then folded by a complete binary tree over the groups in order, the
+// lower group always the first operand (a fixed tree: deterministic, ties to
+// the lowest column).  CTA r holds groups [r G, r G + G) (G =
+// kGroupsPerCta, one warp per group, lane = row of the tile) and folds their
+// subtree in shared memory; rank 0 folds the CTAs' subtrees, which the other
+// CTAs write into its shared memory.
+constexpr int kFoldCtas = 8, kGroupsPerCta = 16, kFoldGroups = kFoldCtas * kGroupsPerCta;
+constexpr int kFoldThreads = 32 * kGroupsPerCta;
+static_assert(kFoldThreads == kFusedMaxLB, "one unmask thread per block position");
+
+struct FoldSmem {
+  float m[kGroupsPerCta][33], s[kGroupsPerCta][33];
+  int a[kGroupsPerCta][33];
+  float cm[kFoldCtas][32], cs[kFoldCtas][32];  // the CTAs' subtrees (read in rank 0)
+  int ca[kFoldCtas][32];
+};
+
+// Every thread of every CTA of the cluster calls it; warp 0 of rank 0 gets
+// the row's partial (lane = row of the tile).
+__device__ __forceinline__ Part fold_rows_cluster(cg::cluster_group &cluster,
+                                                  const float *__restrict__ pmax,
+                                                  const float *__restrict__ psum,
+                                                  const int32_t *__restrict__ parg, int M,
+                                                  int strips, int row0, int nrows, float sc,
+                                                  FoldSmem &sh) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const unsigned rank = cluster.block_rank();
+  const int g = (int)rank * kGroupsPerCta + w;
+  Part acc{-INFINITY, 0.f, 0};
+  if (lane < nrows) {
+    const int row = row0 + lane;
+#pragma unroll 8
+    for (int t = g; t < strips; t += kFoldGroups) {
+      const size_t at = (size_t)t * M + row;
+      acc = fold(acc, Part{pmax[at], psum[at], parg ? parg[at] : 0}, sc);
+    }
+  }
+  sh.m[w][lane] = acc.m;
+  sh.s[w][lane] = acc.s;
+  sh.a[w][lane] = acc.a;
+  __syncthreads();
+#pragma unroll
+  for (int o = 1; o < kGroupsPerCta; o <<= 1) {
+    if ((w & (2 * o - 1)) == 0) {
+      acc = fold(acc, Part{sh.m[w + o][lane], sh.s[w + o][lane], sh.a[w + o][lane]}, sc);
+      sh.m[w][lane] = acc.m;
+      sh.s[w][lane] = acc.s;
+      sh.a[w][lane] = acc.a;
+    }
+    __syncthreads();
+  }
+  if (w == 0) {
+    FoldSmem *dst = cluster.map_shared_rank(&sh, 0);
+    dst->cm[rank][lane] = acc.m;
+    dst->cs[rank][lane] = acc.s;
+    dst->ca[rank][lane] = acc.a;
+  }
+  cluster.sync();  // rank 0 holds every CTA's subtree
+  if (rank == 0 && w == 0) {
+    Part p[kFoldCtas];
+#pragma unroll
+    for (int c = 0; c < kFoldCtas; ++c) p[c] = Part{sh.cm[c][lane], sh.cs[c][lane], sh.ca[c][lane]};
+#pragma unroll
+    for (int o = 1; o < kFoldCtas; o <<= 1)
+#pragma unroll
+      for (int c = 0; c < kFoldCtas; c += 2 * o) p[c] = fold(p[c], p[c + o], sc);
+    acc = p[0];
+  }
+  return acc;
+}
+
+// One cluster per tile of 32 rows.
+__global__ void __launch_bounds__(kFoldThreads)
 lmhead_combine_rows_kernel(const float *__restrict__ pmax, const float *__restrict__ psum,
                            const int32_t *__restrict__ parg, const float *__restrict__ temp,
                            int M, int strips, int V, float *__restrict__ conf,
                            int32_t *__restrict__ argmax, int32_t *status, Gate gate) {
-  if (gate_closed(gate)) return;
-  __shared__ Part sh[4];
-  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float th = temp ? temp[row] : 1.0f;
-  if (!(th > 0.0f) || !isfinite(th)) th = 1.0f;
-  const float sc = kLog2e / th;
-  Part acc{-INFINITY, 0.f, 0};
-  for (int t = tid; t < strips; t += 128) {
-    const size_t at = (size_t)t * M + row;
-    acc = fold(acc, Part{pmax[at], psum[at], parg ? parg[at] : 0}, sc);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    Part y{__shfl_xor_sync(0xffffffffu, acc.m, o), __shfl_xor_sync(0xffffffffu, acc.s, o),
-           __shfl_xor_sync(0xffffffffu, acc.a, o)};
-    acc = (lane & o) ? fold(y, acc, sc) : fold(acc, y, sc);
-  }
-  if (lane == 0) sh[warp] = acc;
-  __syncthreads();
-  if (tid == 0) {
-    Part r = fold(fold(sh[0], sh[1], sc), fold(sh[2], sh[3], sc), sc);
+  if (gate_closed(gate)) return;  // the same decision in every CTA of the cluster
+  __shared__ FoldSmem sh;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int row0 = (int)(blockIdx.x / kFoldCtas) * 32, nrows = min(32, M - row0);
+  const int row = row0 + min((int)(threadIdx.x & 31), nrows - 1);
+  const Part r = fold_rows_cluster(cluster, pmax, psum, parg, M, strips, row0, nrows,
+                                   row_scale(temp, row), sh);
+  if (cluster.block_rank() == 0 && (int)threadIdx.x < nrows) {
     conf[row] = 1.0f / r.s;
     if (argmax) argmax[row] = r.a;
     debug_check_row(1.0f / r.s, argmax ? r.a : 0, V, status);
   }
+}
+
+// Native block driver: one cluster per sequence folds the strip partials of
+// the sequence's LB rows (32 rows at a time, exactly as
+// lmhead_combine_rows_kernel); rank 0 (blockDim.x = 512 >= LB) then takes
+// the step's unmask decision for the block (exactly as unmask_kernel): one
+// launch instead of two.
+__global__ void __launch_bounds__(kFoldThreads)
+lmhead_combine_unmask_kernel(const float *__restrict__ pmax, const float *__restrict__ psum,
+                             const int32_t *__restrict__ parg, const float *__restrict__ temp,
+                             int LB, int M, int strips, int V, float *__restrict__ conf,
+                             int32_t *__restrict__ argmax, uint8_t *__restrict__ mask,
+                             int32_t *__restrict__ tokens, int32_t *__restrict__ m_out, int t,
+                             int T, float tau, int mode, uint8_t *__restrict__ accepted_out,
+                             int fresh, int32_t *status, Gate gate) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const bool lead = cluster.block_rank() == 0;
+  const int s = (int)(blockIdx.x / kFoldCtas);
+  if (gate_closed(gate)) {
+    if (lead) unmask_gated(m_out, s, LB, accepted_out);
+    return;
+  }
+  __shared__ FoldSmem sh;
+  const int lane = threadIdx.x & 31;
+  for (int j0 = 0; j0 < LB; j0 += 32) {
+    if (j0) cluster.sync();  // rank 0 has read the previous tile's subtrees
+    const int row0 = s * LB + j0, nrows = min(32, LB - j0);
+    const int row = row0 + min(lane, nrows - 1);
+    const Part r = fold_rows_cluster(cluster, pmax, psum, parg, M, strips, row0, nrows,
+                                     row_scale(temp, row), sh);
+    if (lead && (int)threadIdx.x < nrows) {
+      conf[row] = 1.0f / r.s;
+      argmax[row] = r.a;
+      debug_check_row(1.0f / r.s, r.a, V, status);
+    }
+  }
+  if (!lead) return;
+  __syncthreads();  // the block's confidences are written (read back from global below)
+  unmask_body(conf, argmax, mask, tokens, m_out, s, LB, t, T, tau, mode, accepted_out, fresh,
+              status);
+}
+
+template <typename... KArgs, typename... Args>
+int launch_fold(void (*kern)(KArgs...), int clusters, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kFoldCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(clusters * kFoldCtas);
+  cfg.blockDim = dim3(kFoldThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, args...) != cudaSuccess) return SPRINT_ERR_CUDA;
+  return launch_status();
 }
 
 LmheadWs lmhead_ws_layout(void *ws, int M, int V, int cols) {
@@ -258,13 +387,50 @@ int sprint::lmhead_confidence_impl(const void *h, const void *W, const float *te
     if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   }
   if (M < 4096)
-    lmhead_combine_rows_kernel<<<M, 128, 0, stream>>>(p.pmax, p.psum, p.parg, temp, M, p.strips,
-                                                      V, conf_out, argmax_out, status, gate);
-  else
-    lmhead_combine_kernel<<<(M + kCombRows - 1) / kCombRows, dim3(kCombRows, kCombGroups), 0,
+    return launch_fold(lmhead_combine_rows_kernel, (M + 31) / 32, stream, (const float *)p.pmax,
+                       (const float *)p.psum, (const int32_t *)p.parg, temp, M, p.strips, V,
+                       conf_out, argmax_out, status, gate);
+  lmhead_combine_kernel<<<(M + kCombRows - 1) / kCombRows, dim3(kCombRows, kCombGroups), 0,
                             stream>>>(p.pmax, p.psum, p.parg, temp, M, p.strips, V, conf_out,
                                       argmax_out, status, gate);
   return launch_status();
+}
+
+int sprint::lmhead_tiles_impl(const void *h, const void *W, const float *temp, int M, int D,
+                              int V, int dtype, void *logits_out, bool want_argmax, void *ws,
+                              size_t ws_bytes, int32_t *status, Gate gate, cudaStream_t stream) {
+  if (M < 1 || M >= 4096 || D < 1 || V < 1 || !h || !W || !ws || !status)
+    return SPRINT_ERR_INVALID_ARG;
+  if (ws_bytes < sprint_lmhead_workspace_bytes(M, D, V, dtype)) return SPRINT_ERR_WORKSPACE;
+  LmheadWs p = lmhead_ws_layout(ws, M, V, lmhead_strip_cols(M, dtype));
+  if (!want_argmax) p.parg = nullptr;
+  if (dtype == SPRINT_BF16) {
+    if (D % 8 != 0 || !aligned16(h) || !aligned16(W)) return SPRINT_ERR_UNSUPPORTED;
+    return lmhead_tc_tiles(static_cast<const __nv_bfloat16 *>(h),
+                           static_cast<const __nv_bfloat16 *>(W), temp, M, D, V,
+                           static_cast<__nv_bfloat16 *>(logits_out), p, status, gate, stream);
+  }
+  dim3 grid(p.strips, (M + 63) / 64);
+  lmhead_simt_kernel<float><<<grid, 256, 0, stream>>>(
+      static_cast<const float *>(h), static_cast<const float *>(W), temp, M, D, V,
+      static_cast<float *>(logits_out), p.pmax, p.psum, p.parg, status, gate);
+  return launch_status();
+}
+
+int sprint::combine_unmask_impl(void *ws, const float *temp, int S, int LB, int V, int dtype,
+                                float *conf_out, int32_t *argmax_out, uint8_t *mask,
+                                int32_t *tokens, int32_t *m_out, int t, int T, float tau,
+                                int mode, uint8_t *accepted_out, int fresh, int32_t *status,
+                                Gate gate, cudaStream_t stream) {
+  const int M = S * LB;
+  if (S < 1 || LB < 1 || LB > kFusedMaxLB || M >= 4096 || !ws || !conf_out || !argmax_out || !mask ||
+      !tokens || !m_out)
+    return SPRINT_ERR_INVALID_ARG;
+  const LmheadWs p = lmhead_ws_layout(ws, M, V, lmhead_strip_cols(M, dtype));
+  return launch_fold(lmhead_combine_unmask_kernel, S, stream, (const float *)p.pmax,
+                     (const float *)p.psum, (const int32_t *)p.parg, temp, LB, M, p.strips, V,
+                     conf_out, argmax_out, mask, tokens, m_out, t, T, tau, mode, accepted_out,
+                     fresh, status, gate);
 }
 
 extern "C" int sprint_lmhead_confidence(const void *h, const void *W, const float *temp,

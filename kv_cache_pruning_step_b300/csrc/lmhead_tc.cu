@@ -31,11 +31,14 @@
 // of M=256, N=BN: each CTA loads its own h tile and half of the W tile, so
 // W crosses from L2 into the SMs once per pair and each SM's tensor core
 // reads half as much W from shared memory per MMA.
-// Output tiles are visited in bands of 32 column tiles so that a band of W
-// (32 x BN rows) stays in L2 while all row tiles stream past it.
+// Output tiles are visited in bands along one operand (at most 32 MB of h
+// rows, or of W columns) that stays in L2 while the other operand's tiles
+// stream past it once per band.
 #include <cuda.h>
 #include <math.h>
 #include <stdlib.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "lmhead.cuh"
@@ -44,7 +47,7 @@
 namespace sprint {
 namespace {
 
-constexpr int BM = 128, BK = 64, BAND = 32;
+constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_STRIDE = 256;  // TMEM columns between the two accumulators
@@ -82,13 +85,28 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return r;
 }
 
-__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, int &m, int &n) {
-  const int per_band = BAND * num_m;
-  const int band = t / per_band;
-  const int idx = t - band * per_band;
-  const int bw = min(BAND, num_n - band * BAND);
-  m = idx / bw;
-  n = band * BAND + idx % bw;
+// Tile order for L2 reuse: tiles are visited in bands of `band` consecutive
+// tiles along the kept operand's axis (row units of h, or column tiles of
+// W); inside a band the other operand's tiles are the outer loop, so each
+// of them streams from DRAM once per band while the band's tiles of the
+// kept operand stay in L2 (every one is touched again after about one band
+// of reads).  Consecutive tile numbers run on concurrent CTAs, which
+// therefore share the streamed tile.
+struct TileOrder {
+  int keep_h;  // 1: bands of h row units, 0: bands of W column tiles
+  int band;    // tiles of the kept operand per band
+};
+
+__device__ __forceinline__ void tile_coords(int t, int num_m, int num_n, TileOrder o, int &m,
+                                            int &n) {
+  const int kept = o.keep_h ? num_m : num_n, streamed = o.keep_h ? num_n : num_m;
+  const int per_band = o.band * streamed;
+  const int b = t / per_band;
+  const int idx = t - b * per_band;
+  const int bw = min(o.band, kept - b * o.band);
+  const int k = b * o.band + idx % bw, q = idx / bw;
+  m = o.keep_h ? k : q;
+  n = o.keep_h ? q : k;
 }
 
 // kArg: also track the first column reaching each row's maximum (the
@@ -109,7 +127,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
                  const float *__restrict__ temp, int M, int D, int V,
                  __nv_bfloat16 *__restrict__ logits, float *__restrict__ pmax,
                  float *__restrict__ psum, int32_t *__restrict__ parg, int32_t *status,
-                 unsigned long long cap_ns, int stall_test, Gate gate) {
+                 unsigned long long cap_ns, int stall_test, TileOrder order, Gate gate) {
   if (gate_closed(gate)) return;
   // The final waits for in-flight copies and MMAs ignore the abort flag and
   // get at least one second.
@@ -138,7 +156,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
   const int tiles = num_mu * num_n, nk = (D + BK - 1) / BK;
   auto coords = [&](int t, int &m, int &n) {
     int mu;
-    tile_coords(t, num_mu, num_n, mu, n);
+    tile_coords(t, num_mu, num_n, order, mu, n);
     m = kPair ? 2 * mu + (int)rank : mu;
   };
 
@@ -196,8 +214,7 @@ lmhead_tc_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant
             const uint32_t fb0 = tc::map_to_rank(fb, 0);
             if (rank == 0) tc::mbar_arrive_expect_tx(fb, 2 * STAGE_BYTES);
             tc::tma_load_2d_pair(sa, &tm_h, fb0, kb * BK, m * BM);
-            tc::tma_load_2d_pair(sa + A_BYTES, &tm_w, fb0, kb * BK,
-                                 n * BN + (int)rank * B_ROWS);
+            tc::tma_load_2d_pair(sa + A_BYTES, &tm_w, fb0, kb * BK, n * BN + (int)rank * B_ROWS);
           } else {
             tc::mbar_arrive_expect_tx(fb, STAGE_BYTES);  // h tile + W tile
             tc::tma_load_2d(sa, &tm_h, fb, kb * BK, m * BM);
@@ -447,7 +464,7 @@ int sm_count() {
 template <int BN, bool kArg, bool kPair>
 int launch_kernel(const CUtensorMap &tm_h, const CUtensorMap &tm_w, const float *temp, int M,
                   int D, int V, __nv_bfloat16 *logits, const LmheadWs &p, int32_t *status,
-                  Gate gate, int units, cudaStream_t stream) {
+                  Gate gate, int units, TileOrder order, cudaStream_t stream) {
   constexpr size_t SMEM_BYTES = Tiles<BN, kPair>::SMEM_BYTES;
   auto kern = lmhead_tc_kernel<BN, kArg, kPair>;
   static PerDevice attr_set;
@@ -491,9 +508,31 @@ int launch_kernel(const CUtensorMap &tm_h, const CUtensorMap &tm_w, const float 
   cfg.gridDim = dim3(grid);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tm_h, tm_w, temp, M, D, V, logits,
                                            p.pmax, p.psum, p.parg, status, wait_cap_ns(),
-                                           stall_test_enabled(), gate);
+                                           stall_test_enabled(), order, gate);
   if (e != cudaSuccess) return SPRINT_ERR_CUDA;
   return launch_status();
+}
+
+// The kept operand's band is at most kKeepBytes; the order with the smaller
+// estimate of DRAM reads wins: keeping h reads h once and W once per band of
+// rows, keeping W the other way round.  32 MB is what measured best at the
+// 32K-row prefix (both orders, bands of 16 to 64 MB, with and without L2
+// eviction hints): far less than the 126 MB L2 stays useful to tiles that
+// all 148 SMs read.
+constexpr size_t kKeepBytes = size_t(32) << 20;
+
+TileOrder tile_order(int num_m, int num_n, size_t m_tile_bytes, size_t n_tile_bytes) {
+  auto banding = [](int tiles, size_t tile_bytes, int &band) {
+    const int most = (int)std::max<size_t>(1, kKeepBytes / tile_bytes);
+    const int bands = (tiles + most - 1) / most;
+    band = (tiles + bands - 1) / bands;
+    return bands;
+  };
+  int band_m, band_n;
+  const double h = (double)num_m * m_tile_bytes, w = (double)num_n * n_tile_bytes;
+  const double keep_h = h + w * banding(num_m, m_tile_bytes, band_m);
+  const double keep_w = w + h * banding(num_n, n_tile_bytes, band_n);
+  return keep_h <= keep_w ? TileOrder{1, band_m} : TileOrder{0, band_n};
 }
 
 template <int BN>
@@ -509,20 +548,23 @@ int launch_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *te
       !make_tmap_bf16_2d(&tm_w, W, D, V, D, BK, pair ? BN / 2 : BN))
     return SPRINT_ERR_CUDA;
   const int sms = sm_count();
+  const int num_mu = pair ? (num_m + 1) / 2 : num_m;
+  const TileOrder order = tile_order(num_mu, num_n, (size_t)(pair ? 2 * BM : BM) * D * 2,
+                                     (size_t)BN * D * 2);
   if (pair) {
-    const int pair_tiles = ((num_m + 1) / 2) * num_n;
+    const int pair_tiles = num_mu * num_n;
     const int pairs = pair_tiles < sms / 2 ? pair_tiles : sms / 2;
     return p.parg ? launch_kernel<BN, true, true>(tm_h, tm_w, temp, M, D, V, logits, p, status,
-                                                   gate, pairs, stream)
+                                                   gate, pairs, order, stream)
                   : launch_kernel<BN, false, true>(tm_h, tm_w, temp, M, D, V, logits, p, status,
-                                                    gate, pairs, stream);
+                                                    gate, pairs, order, stream);
   }
   const int tiles = num_m * num_n;
   const int grid = tiles < sms ? tiles : sms;
   return p.parg ? launch_kernel<BN, true, false>(tm_h, tm_w, temp, M, D, V, logits, p, status,
-                                                  gate, grid, stream)
+                                                  gate, grid, order, stream)
                 : launch_kernel<BN, false, false>(tm_h, tm_w, temp, M, D, V, logits, p, status,
-                                                   gate, grid, stream);
+                                                   gate, grid, order, stream);
 }
 
 int lmhead_tc_tiles(const __nv_bfloat16 *h, const __nv_bfloat16 *W, const float *temp, int M,

@@ -123,7 +123,9 @@ keynorm_kernel(const T *__restrict__ K, const int32_t *__restrict__ prefix_off,
   }
 }
 
-constexpr int kSelThreads = 1024;
+constexpr int kSelThreads = 512;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kMaxBpt = (1 << 12) / kSelThreads;  // digits per thread in a scan, at most
 constexpr int kDigit = 12, kBins = 1 << kDigit;  // radix digit of the selection
 constexpr int kMaxCluster = 8;                     // CTAs per sequence, at most
 // Positions a CTA's slice aims at when the cluster size is chosen, and the
@@ -191,7 +193,7 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
   uint32_t *stage_keys = hist + 2 * kBins + (cl > 1 ? 2 * W : 0);
   uint8_t *stage_tags = reinterpret_cast<uint8_t *>(stage_keys + stage_cap);
   __shared__ SelXchg xc;
-  __shared__ double wtree[32];
+  __shared__ double wtree[kSelWarps];
   __shared__ int scan_sh[33];
   __shared__ int wcnt[3][32];
   __shared__ float mean_sh;
@@ -222,8 +224,8 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
   // ---- 1. canonical sum of u; image count; staging of u bits and tags
   {
     const int G = (n + kLeaf - 1) / kLeaf, P = next_pow2(G);
-    const int workers = cl * 32, B = P > workers ? P / workers : 1;
-    const int wk = rank * 32 + warp;
+    const int workers = cl * kSelWarps, B = P > workers ? P / workers : 1;
+    const int wk = rank * kSelWarps + warp;
     const double v = wk * B < P ? u_subtree_sum(u + p0, n, G, wk * B, B, lane) : 0.0;
     if (lane == 0) wtree[warp] = v;
   }
@@ -252,25 +254,29 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
   if (lane == 0) wcnt[0][warp] = nimg;
   __syncthreads();
   if (tid == 0) {
-    double v[32];
+    double v[kSelWarps];
     int t = 0;
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < kSelWarps; ++i) {
       v[i] = wtree[i];
       t += wcnt[0][i];
     }
-    tree_fold(v, 32);
+    tree_fold(v, kSelWarps);
     xc.tree = v[0];
     xc.nimg = t;
   }
   cluster.sync();
   if (tid == 0) {
     double v[kMaxCluster];
-    int ni = 0;
-    for (int q = 0; q < cl; ++q) {
-      const SelXchg *r = cluster.map_shared_rank(&xc, q);
-      v[q] = r->tree;
-      ni += r->nimg;
+    int nq[kMaxCluster];
+#pragma unroll
+    for (int q = 0; q < kMaxCluster; ++q) {  // all remote loads in flight
+      const SelXchg *r = cluster.map_shared_rank(&xc, q < cl ? q : 0);
+      v[q] = q < cl ? r->tree : 0.0;
+      nq[q] = q < cl ? r->nimg : 0;
     }
+    int ni = 0;
+#pragma unroll
+    for (int q = 0; q < kMaxCluster; ++q) ni += nq[q];
     tree_fold(v, cl);
     mean_sh = n > 0 ? (float)(v[0] / (double)n) : 0.f;
     info_sh[0] = ni;
@@ -337,11 +343,18 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
   }
   if (tid < 2) {
     const int mu = tid;
+    uint32_t lo[kMaxCluster], hi[kMaxCluster];
+#pragma unroll
+    for (int q = 0; q < kMaxCluster; ++q) {
+      const SelXchg *r = cluster.map_shared_rank(&xc, q < cl ? q : 0);
+      lo[q] = r->lo[mu];
+      hi[q] = r->hi[mu];
+    }
     uint32_t kmn = 0xffffffffu, kmx = 0u;
-    for (int q = 0; q < cl; ++q) {
-      const SelXchg *r = cluster.map_shared_rank(&xc, q);
-      kmn = min(kmn, r->lo[mu]);
-      kmx = max(kmx, r->hi[mu]);
+#pragma unroll
+    for (int q = 0; q < kMaxCluster; ++q) {
+      kmn = min(kmn, lo[q]);
+      kmx = max(kmx, hi[q]);
     }
     const int k = mu ? k_img : k_txt, nm = mu ? n_img : n_txt;
     mode_sh[mu] = k <= 0 ? 0 : (k >= nm ? 1 : 2);
@@ -376,10 +389,16 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
     }
     cluster.sync();  // every CTA's histogram is complete
     if (cl > 1) {
+      // all cl remote loads of a digit in flight at once
       for (int idx = tid; idx < 2 * W; idx += kSelThreads) {
         const int mu = idx >= W, b = rank * W + (idx - mu * W);
+        uint32_t c[kMaxCluster];
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; ++q)
+          c[q] = q < cl ? cluster.map_shared_rank(hist, q)[mu * kBins + b] : 0u;
         uint32_t t = 0u;
-        for (int q = 0; q < cl; ++q) t += cluster.map_shared_rank(hist, q)[mu * kBins + b];
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; ++q) t += c[q];
         hsum[idx] = t;
       }
       __syncthreads();
@@ -398,7 +417,7 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
     __syncthreads();
     if (tid < 2) {
       uint32_t t = 0u;
-      for (int i = 0; i < 32; ++i) t += (uint32_t)wcnt[tid][i];
+      for (int i = 0; i < kSelWarps; ++i) t += (uint32_t)wcnt[tid][i];
       xc.tot[tid] = t;
     }
     cluster.sync();  // every CTA's digit totals are published
@@ -407,15 +426,20 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
       int qs = -1;
       uint32_t above = 0u, run = 0u;
       const uint32_t need = (uint32_t)need_sh[mu];
-      if (shift_sh[mu] > 0)
+      if (shift_sh[mu] > 0) {
+        uint32_t tot[kMaxCluster];
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; ++q)
+          tot[q] = q < cl ? cluster.map_shared_rank(&xc, q)->tot[mu] : 0u;
         for (int q = cl - 1; q >= 0; --q) {  // higher ranks own larger digits
-          const uint32_t tq = cluster.map_shared_rank(&xc, q)->tot[mu];
+          const uint32_t tq = tot[q];
           if (qs < 0 && run < need && run + tq >= need) {
             qs = q;
             above = run;
           }
           run += tq;
         }
+      }
       qstar_sh[mu] = qs;
       above_sh[mu] = (int)above;
     }
@@ -424,11 +448,11 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
       if (qstar_sh[mu] != rank) continue;  // uniform in the CTA
       // Digits of this CTA in descending order, bpt per thread; counts above
       // each thread's digits by one block scan.
-      const int bpt = (W + kSelThreads - 1) / kSelThreads;  // 1, 2 or 4
-      uint32_t c[4];
+      const int bpt = (W + kSelThreads - 1) / kSelThreads;
+      uint32_t c[kMaxBpt];
       int mine = 0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < kMaxBpt; ++q) {
         const int jd = tid * bpt + q;
         c[q] = (q < bpt && jd < W) ? hsum[mu * W + (W - 1 - jd)] : 0u;
         mine += (int)c[q];
@@ -438,7 +462,7 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
       const uint32_t need = (uint32_t)need_sh[mu];
       uint32_t run = (uint32_t)above_sh[mu] + (uint32_t)above_in;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < kMaxBpt; ++q) {
         const int jd = tid * bpt + q;
         if (q < bpt && jd < W) {
           if (run < need && run + c[q] >= need) {  // the k-th largest lies in this digit
@@ -474,7 +498,7 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
   const int m0 = mode_sh[0], m1 = mode_sh[1];
   const int need0 = need_sh[0], need1 = need_sh[1];
   const int k_all = k1 - k0;
-  const int per_warp = ((m + 32 * 32 - 1) / (32 * 32)) * 32;  // multiple of 32
+  const int per_warp = ((m + kSelWarps * 32 - 1) / (kSelWarps * 32)) * 32;  // multiple of 32
   const int w_lo = warp * per_warp, w_hi = min(m, w_lo + per_warp);
   auto classify = [&](int j, bool &def, bool &tie0, bool &tie1) {
     def = tie0 = tie1 = false;
@@ -503,7 +527,9 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
   }
   __syncthreads();
   if (warp == 0) {  // exclusive scans of the warp totals; the CTA's totals
-    const int a = wcnt[0][lane], b = wcnt[1][lane], c = wcnt[2][lane];
+    const bool w_ok = lane < kSelWarps;
+    const int a = w_ok ? wcnt[0][lane] : 0, b = w_ok ? wcnt[1][lane] : 0,
+              c = w_ok ? wcnt[2][lane] : 0;
     const int ia = warp_incl_scan(a), ib = warp_incl_scan(b), ic = warp_incl_scan(c);
     wcnt[0][lane] = ia - a;
     wcnt[1][lane] = ib - b;
@@ -517,8 +543,13 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
   cluster.sync();  // every CTA's totals are published
   __shared__ int cbase_sh[3];
   if (tid < 3) {
+    int c[kMaxCluster];
+#pragma unroll
+    for (int q = 0; q < kMaxCluster; ++q)
+      c[q] = q < rank ? cluster.map_shared_rank(&xc, q)->cnt[tid] : 0;
     int t = 0;
-    for (int q = 0; q < rank; ++q) t += cluster.map_shared_rank(&xc, q)->cnt[tid];
+#pragma unroll
+    for (int q = 0; q < kMaxCluster; ++q) t += c[q];
     cbase_sh[tid] = t;
   }
   __syncthreads();

@@ -140,3 +140,25 @@ def test_confidence_without_argmax_bf16(sp, big_weight, M):
     assert torch.equal(c0, c1)
     rows = np.unique(np.random.default_rng(M).choice(M, min(M, 40), replace=False))
     gc.check_confidence(c0.cpu().numpy()[rows], None, H, big_weight, theta, rows, "no argmax")
+
+
+@pytest.mark.parametrize("M,V", [(20000, 2000), (40000, 30000), (20000, 40000)])
+def test_tile_orders_bf16(sp, M, V):
+    """h above the 32 MB band: (20000, 2000) keeps W in L2 in one band,
+    (40000, 30000) keeps W in four bands, (20000, 40000) keeps h in three
+    bands of 27 row units (6912 rows).  Each order must cover every output
+    tile exactly once: sampled rows (among them both sides of a band edge)
+    match the oracle, and every confidence is a probability of at least
+    1/V."""
+    D = 2048
+    h, W, theta = draw(M, D, V, torch.bfloat16, M + V)
+    c, am, _ = run(sp, h, W, theta, want_logits=False)
+    rng = np.random.default_rng(V)
+    edges = [0, M - 1, 6911, 6912, M // 2]
+    rows = np.unique(np.concatenate([edges, rng.choice(M, 24, replace=False)]))
+    rows = rows[rows < M]
+    _, nmis = gc.check_confidence(c.cpu().numpy()[rows], am.cpu().numpy()[rows], h, W, theta,
+                                  rows, f"order {M}x{V}")
+    assert nmis <= 1
+    cc = c.cpu().numpy()
+    assert np.all(cc >= 1.0 / V * (1 - 1e-5)) and np.all(cc <= 1.0 + 1e-6)

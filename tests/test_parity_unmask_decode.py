@@ -8,7 +8,7 @@ import torch
 
 from oracle import sprint_oracle as orc
 from tests import gpu_cases as gc
-from workload import WORKLOADS, lm_head_weight, prefix_inputs, step_inputs
+from workload import WORKLOADS, lm_head_weight, prefix_inputs, small_workload, step_inputs
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -150,7 +150,7 @@ def test_tiny_block_end_to_end(sp, indexed):
 
 def _decoder_and_steps(name, tau=None, mode=0):
     from kv_cache_pruning_step_b300 import BlockDecoder
-    w = WORKLOADS[name]
+    w = WORKLOADS[name] if isinstance(name, str) else name
     W = lm_head_weight(w, device=DEV)
     pre = prefix_inputs(w, device=DEV)
     mod = pre["modality"].cpu().numpy()
@@ -186,6 +186,59 @@ def test_native_step_driver_matches_stepwise(sp, name, mode):
     assert ra.accepted_per_step == rb.accepted_per_step
     assert torch.equal(ra.tokens, rb.tokens)
     assert torch.equal(a.O, b.O)
+    assert torch.equal(a.conf_blk, b.conf_blk)
+
+
+def test_native_step_driver_block_of_several_row_tiles(sp):
+    """A block of 100 positions: the fused fold-and-unmask kernel (one
+    cluster per sequence) loops over four tiles of 32 rows; the trajectory
+    equals the stepwise one bit for bit."""
+    w = small_workload("lb-fuzz", dtype="bf16", NL=2, Hq=2, Hkv=2, d=64, D=256, V=3000, LB=100,
+                       T=5, n=300, n_img=100, seed=100)
+    w, pre, steps, make = _decoder_and_steps(w)
+    a, b = make(), make()
+    ra = a.decode(pre, lambda t: steps[t])
+    rb = b.decode_stepwise(pre, lambda t: steps[t])
+    torch.cuda.synchronize()
+    assert a.status.item() == 0 and b.status.item() == 0
+    assert ra.steps == rb.steps and ra.accepted_per_step == rb.accepted_per_step
+    assert sum(int(x[0]) for x in ra.accepted_per_step) == w.LB
+    assert torch.equal(ra.tokens, rb.tokens)
+    assert torch.equal(a.conf_blk, b.conf_blk)
+
+
+def test_native_step_driver_4096_block_rows(sp):
+    """128 sequences of 32 positions, 4096 block rows: above the fused
+    kernel's row limit the driver runs the LM head's own combine and then
+    the unmask kernel.  The trajectory equals the stepwise one bit for bit."""
+    from kv_cache_pruning_step_b300 import BlockDecoder
+    S = 128
+    w = small_workload("rows-4096", dtype="bf16", NL=2, Hq=4, Hkv=2, d=64, D=256, V=3000, LB=32,
+                       T=4, n=64, n_img=16, seed=3, S=S)
+    W = lm_head_weight(w, device=DEV)
+    prefixes = [prefix_inputs(w, seq=s, device=DEV) for s in range(S)]
+    cat = gc.concat_prefixes(prefixes)
+    counts = [(int((p["modality"] == 0).sum()), int((p["modality"] != 0).sum()))
+              for p in prefixes]
+    steps = []
+    for t in range(w.T):
+        xs = [step_inputs(w, s, 0, t, device=DEV) for s in range(S)]
+        steps.append({k: (torch.stack([x[k] for x in xs]) if k in ("Q", "Kb", "Vb")
+                          else torch.cat([x[k] for x in xs])).contiguous()
+                      for k in ("Q", "Kb", "Vb", "h", "theta")})
+
+    def make():
+        return BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
+                            r_text=w.r_text, r_img=w.r_img, alpha=w.alpha,
+                            modality_counts=counts)
+    a, b = make(), make()
+    ra = a.decode(cat, lambda t: steps[t])
+    rb = b.decode_stepwise(cat, lambda t: steps[t])
+    torch.cuda.synchronize()
+    assert a.status.item() == 0 and b.status.item() == 0
+    assert ra.steps == rb.steps and ra.accepted_per_step == rb.accepted_per_step
+    assert all(sum(int(x[s]) for x in ra.accepted_per_step) == w.LB for s in range(S))
+    assert torch.equal(ra.tokens, rb.tokens)
     assert torch.equal(a.conf_blk, b.conf_blk)
 
 
