@@ -159,7 +159,8 @@ class ClockSampler:
 # bench reports that traffic only while the sources are unchanged.
 TRAFFIC_SOURCES = {
     "lmhead_prefix": ["lmhead_tc.cu", "lmhead.cu", "lmhead.cuh", "tc_ptx.cuh", "common.cuh"],
-    "lmhead_block": ["lmhead_tc.cu", "lmhead.cu", "lmhead.cuh", "tc_ptx.cuh", "common.cuh"],
+    "lmhead_block": ["lmhead_tc.cu", "lmhead.cu", "lmhead.cuh", "unmask.cuh", "tc_ptx.cuh",
+                     "common.cuh"],
     "attn_full": ["attention_tc.cu", "attention.cu", "attention.cuh", "tc_ptx.cuh", "common.cuh"],
     "attn_pruned": ["attention_tc.cu", "attention.cu", "attention.cuh", "tc_ptx.cuh",
                     "common.cuh"],

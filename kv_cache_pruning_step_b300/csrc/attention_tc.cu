@@ -676,7 +676,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         const float nm = -m_used;
         float lsum = 0.f;
-#pragma unroll
+        // Unrolled by two, not four: at the 168-register cap of three warps
+        // per sub-partition the full unroll spilled registers.
+#pragma unroll 2
         for (int c = 0; c < TILE / 32; ++c) {
           float v[32];
           tc::tmem_ld32(s_addr + c * 32, v);

@@ -146,8 +146,6 @@ struct SelXchg {
   uint32_t lo[2];     // smallest / largest key per modality in the slice
   uint32_t hi[2];
   uint32_t tot[2];    // keys of the current radix pass in the digits this CTA owns
-  uint32_t digit[2];  // the threshold digit, from the CTA that owns it
-  int need[2];        // keys still to keep inside that digit
   int cnt[3];         // definite keeps, text ties, image ties in the slice
 };
 
@@ -199,7 +197,8 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
   __shared__ float mean_sh;
   __shared__ int info_sh[4];  // image count, text keep, image keep, counts consistent
   __shared__ uint32_t lmin_sh[2], lmax_sh[2], kmin_sh[2], prefix_sh[2];
-  __shared__ int shift_sh[2], need_sh[2], mode_sh[2], qstar_sh[2], above_sh[2];
+  __shared__ int shift_sh[2], need_sh[2], mode_sh[2], qstar_sh[2], above_sh[2], dneed_sh[2];
+  __shared__ uint32_t digit_sh[2];
 
   const int p0 = prefix_off[s], p1 = prefix_off[s + 1];
   const int k0 = kept_off[s], k1 = kept_off[s + 1];
@@ -444,9 +443,16 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
       above_sh[mu] = (int)above;
     }
     __syncthreads();
+    // Every CTA finds the threshold digit itself from the digit totals of
+    // the CTA that owns it (read through distributed shared memory), so no
+    // barrier publishes it.  That CTA rewrites its totals only after the
+    // next pass's first cluster barrier, which every reader reaches after
+    // these reads.
     for (int mu = 0; mu < 2; ++mu) {
-      if (qstar_sh[mu] != rank) continue;  // uniform in the CTA
-      // Digits of this CTA in descending order, bpt per thread; counts above
+      const int qs = qstar_sh[mu];
+      if (shift_sh[mu] <= 0 || qs < 0) continue;  // uniform in the CTA
+      const uint32_t *src = cl > 1 ? cluster.map_shared_rank(hsum, qs) : hsum;
+      // Digits of CTA qs in descending order, bpt per thread; counts above
       // each thread's digits by one block scan.
       const int bpt = (W + kSelThreads - 1) / kSelThreads;
       uint32_t c[kMaxBpt];
@@ -454,7 +460,7 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
 #pragma unroll
       for (int q = 0; q < kMaxBpt; ++q) {
         const int jd = tid * bpt + q;
-        c[q] = (q < bpt && jd < W) ? hsum[mu * W + (W - 1 - jd)] : 0u;
+        c[q] = (q < bpt && jd < W) ? src[mu * W + (W - 1 - jd)] : 0u;
         mine += (int)c[q];
       }
       int total;
@@ -466,20 +472,19 @@ select_kernel(const float *__restrict__ u, const float *__restrict__ conf,
         const int jd = tid * bpt + q;
         if (q < bpt && jd < W) {
           if (run < need && run + c[q] >= need) {  // the k-th largest lies in this digit
-            xc.digit[mu] = (uint32_t)(rank * W + (W - 1 - jd));
-            xc.need[mu] = (int)(need - run);
+            digit_sh[mu] = (uint32_t)(qs * W + (W - 1 - jd));
+            dneed_sh[mu] = (int)(need - run);
           }
           run += c[q];
         }
       }
     }
-    cluster.sync();  // the threshold digits are published
+    __syncthreads();
     if (tid < 2 && shift_sh[tid] > 0) {
       const int mu = tid, sh = shift_sh[mu], w = sh < kDigit ? sh : kDigit;
       if (qstar_sh[mu] >= 0) {
-        const SelXchg *r = cluster.map_shared_rank(&xc, qstar_sh[mu]);
-        prefix_sh[mu] = (prefix_sh[mu] << w) | r->digit[mu];
-        need_sh[mu] = r->need[mu];
+        prefix_sh[mu] = (prefix_sh[mu] << w) | digit_sh[mu];
+        need_sh[mu] = dneed_sh[mu];
         shift_sh[mu] = sh - w;
       } else {  // counts inconsistent with the keep count: cannot happen
         report(status, SPRINT_STATUS_KEPT_MISMATCH);

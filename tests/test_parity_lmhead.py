@@ -162,3 +162,18 @@ def test_tile_orders_bf16(sp, M, V):
     assert nmis <= 1
     cc = c.cpu().numpy()
     assert np.all(cc >= 1.0 / V * (1 - 1e-5)) and np.all(cc <= 1.0 + 1e-6)
+
+
+def test_logit_error_is_within_the_argmax_excuse(sp):
+    """The argmax excuse rests on the computed logits' error: at D = 2048
+    (the model width) with temperatures down to 0.5 the fp32 logits stay
+    within ARGMAX_EXCUSE / 4 of the fp64 oracle, so a greedy token can
+    differ only on a near-tie of two logits."""
+    g = generator(DEV, "logit-error", 2048)
+    h = torch.randn((256, 2048), generator=g, device=DEV)
+    W = torch.randn((8192, 2048), generator=g, device=DEV) / 16
+    theta = 0.5 + 3.5 * torch.rand(256, generator=g, device=DEV)
+    _, _, lg = run(sp, h, W, theta)
+    _, _, z = orc.lm_confidence(h, W, theta, want_logits=True)
+    err = np.abs(gc.host(lg).astype(np.float64) - z).max()
+    assert err <= gc.ARGMAX_EXCUSE / 4, f"logit error {err:.3e}"
