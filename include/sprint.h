@@ -436,6 +436,15 @@ int sprint_unmask(const float *conf, const int32_t *argmax, uint8_t *mask,
  * Steps executed = 1 + the number of t in [1, T) with some m_hist[t-1][s]
  * > 0; the caller reads m_hist after synchronising.
  *
+ * bf16 without the residual chain: each step's attention combine (which
+ * only writes O) runs on an internal stream of the library, one per
+ * device, forked from `stream` by an event after the step's attention and
+ * joined back before the next step's attention and before the call
+ * returns, so all work of the call is ordered before later work on
+ * `stream` (and the call can be captured into a CUDA graph from `stream`).
+ * Calls from several host threads on one device are serialised while they
+ * enqueue.
+ *
  * Every step's inputs (Q, Kb, Vb, h, theta) are given up front: this
  * driver suits step inputs that are already resident (for example produced
  * by device work enqueued earlier on the same stream).

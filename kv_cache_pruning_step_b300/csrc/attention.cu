@@ -257,7 +257,7 @@ int sprint::block_attn_impl(const void *Q, const void *Kp, const void *Vp,
                             const void *Kb, const void *Vb, int S, int NL, int LB, int Hq,
                             int Hkv, int d, int dtype, void *O, void *ws, size_t ws_bytes,
                             int32_t *status, KvIndex kvi, AttnResidual res, Gate gate,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, SideStream side) {
   if (S < 0 || NL < 1 || LB < 1 || Hq < 1 || Hkv < 1 || max_kv_rows < 0 || total_kv_rows < 0)
     return SPRINT_ERR_INVALID_ARG;
   if (dtype != SPRINT_F32 && dtype != SPRINT_BF16) return SPRINT_ERR_INVALID_ARG;
@@ -281,7 +281,7 @@ int sprint::block_attn_impl(const void *Q, const void *Kp, const void *Vp,
                            static_cast<const __nv_bfloat16 *>(Vp), kv_off, total_kv_rows,
                            static_cast<const __nv_bfloat16 *>(Kb),
                            static_cast<const __nv_bfloat16 *>(Vb), S, NL, LB, Hq, Hkv, d, O, ws,
-                           status, kvi, res, gate, stream);
+                           status, kvi, res, gate, stream, side);
   }
   const int ck = attn_chunk_policy(S, NL, Hkv, LB, max_kv_rows);
   const AttnWs w = attn_ws_layout(ws, S, NL, LB, Hq, Hkv, d, max_kv_rows, ck);

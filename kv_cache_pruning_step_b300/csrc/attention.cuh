@@ -31,7 +31,7 @@ int attn_tc_forward(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_
                     const int32_t *kv_off, int total_kv_rows, const __nv_bfloat16 *Kb,
                     const __nv_bfloat16 *Vb, int S, int NL, int LB, int Hq, int Hkv, int d,
                     void *O, void *ws, int32_t *status, KvIndex kvi, AttnResidual res,
-                    Gate gate, cudaStream_t stream);
+                    Gate gate, cudaStream_t stream, SideStream side);
 // The prefix's own attention (bf16, tcgen05; attention_tc.cu).
 int attn_tc_prefix(const __nv_bfloat16 *Qp, const __nv_bfloat16 *K, const __nv_bfloat16 *V,
                    const int32_t *prefix_off, int total_rows, int S, int NL, int Hq, int Hkv,

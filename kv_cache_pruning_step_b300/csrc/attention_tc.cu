@@ -940,7 +940,8 @@ template <int D>
 int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 *Vp,
            const int32_t *kv_off, int total_kv_rows, const __nv_bfloat16 *Kb,
            const __nv_bfloat16 *Vb, int S, int NL, int LB, int Hq, int Hkv, void *O, void *ws,
-           int32_t *status, KvIndex kvi, AttnResidual res, Gate gate, cudaStream_t stream) {
+           int32_t *status, KvIndex kvi, AttnResidual res, Gate gate, cudaStream_t stream,
+           SideStream side) {
   using Lt = Layout<D>;
   const int GQ = Hq / Hkv;
   CUtensorMap tq, tkp, tvp, tkb, tvb;
@@ -991,9 +992,19 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
     attn_tc_kernel<D, false, false><<<G, THREADS, smem, stream>>>(tq, tkp, tvp, tkb, tvb, pb);
   if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
   const long long warps = (long long)pairs * LB * GQ;
-  attn_tc_combine_kernel<D><<<(int)((warps * 32 + 255) / 256), 256, 0, stream>>>(
+  cudaStream_t cs = stream;
+  if (side.side) {  // the combine on the side stream, after the chunk kernel
+    if (cudaEventRecord(side.fork, stream) != cudaSuccess ||
+        cudaStreamWaitEvent(side.side, side.fork, 0) != cudaSuccess)
+      return SPRINT_ERR_CUDA;
+    cs = side.side;
+  }
+  attn_tc_combine_kernel<D><<<(int)((warps * 32 + 255) / 256), 256, 0, cs>>>(
       pb, G, static_cast<__nv_bfloat16 *>(O), res);
-  return launch_status();
+  const int rc = launch_status();
+  if (rc == SPRINT_OK && side.side && cudaEventRecord(side.join, side.side) != cudaSuccess)
+    return SPRINT_ERR_CUDA;
+  return rc;
 }
 
 // Prefix self-attention: one unit per (sequence, layer, query head, 128-row
@@ -1058,12 +1069,12 @@ int attn_tc_forward(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_
                     const int32_t *kv_off, int total_kv_rows, const __nv_bfloat16 *Kb,
                     const __nv_bfloat16 *Vb, int S, int NL, int LB, int Hq, int Hkv, int d,
                     void *O, void *ws, int32_t *status, KvIndex kvi, AttnResidual res,
-                    Gate gate, cudaStream_t stream) {
+                    Gate gate, cudaStream_t stream, SideStream side) {
   if (S > MAX_SEQ) return SPRINT_ERR_UNSUPPORTED;
   return d == 64 ? launch<64>(Q, Kp, Vp, kv_off, total_kv_rows, Kb, Vb, S, NL, LB, Hq, Hkv, O,
-                              ws, status, kvi, res, gate, stream)
+                              ws, status, kvi, res, gate, stream, side)
                  : launch<128>(Q, Kp, Vp, kv_off, total_kv_rows, Kb, Vb, S, NL, LB, Hq, Hkv, O,
-                               ws, status, kvi, res, gate, stream);
+                               ws, status, kvi, res, gate, stream, side);
 }
 
 }  // namespace sprint

@@ -284,11 +284,18 @@ int lmhead_confidence_impl(const void *h, const void *W, const float *temp, int 
                            int dtype, void *logits_out, float *conf_out, int32_t *argmax_out,
                            void *ws, size_t ws_bytes, int32_t *status, Gate gate,
                            cudaStream_t stream);
+// Native driver: the bf16 attention's combine kernel may run on a side
+// stream (forked after the chunk kernel with `fork`, joined through `join`,
+// which the caller waits on before the workspace or O is touched again).
+struct SideStream {
+  cudaStream_t side;  // nullptr: the combine runs on the call's stream
+  cudaEvent_t fork, join;
+};
 int block_attn_impl(const void *Q, const void *Kp, const void *Vp, const int32_t *kv_off,
                     int max_kv_rows, int total_kv_rows, const void *Kb, const void *Vb, int S,
                     int NL, int LB, int Hq, int Hkv, int d, int dtype, void *O, void *ws,
                     size_t ws_bytes, int32_t *status, KvIndex kvi, AttnResidual res,
-                    Gate gate, cudaStream_t stream);
+                    Gate gate, cudaStream_t stream, SideStream side = {nullptr, nullptr, nullptr});
 int unmask_impl(const float *conf, const int32_t *argmax, uint8_t *mask, int32_t *tokens,
                 int32_t *m_out, int S, int LB, int t, int T, float tau, int mode,
                 uint8_t *accepted_out, int32_t *status, Gate gate, cudaStream_t stream,

@@ -153,6 +153,37 @@ def test_ragged_random_pools_and_ties(sp):
         assert np.array_equal(ks[pools[5][ks] == p], members[:keep[5][p]])
 
 
+def test_ragged_pools_in_clusters(sp):
+    """Sequences long enough on average for clusters of 4 CTAs per
+    sequence, among them sequences shorter than one CTA's slice (empty
+    slices in their clusters) and one with every score equal: pool sizes,
+    key ranges, ties and the compaction's cross-CTA offsets must hold."""
+    lens = [0, 3, 40000, 9000, 1, 20000]
+    prefixes, confs, pools, keep = [], [], [], []
+    g = np.random.default_rng(9)
+    for s, n in enumerate(lens):
+        w = small_workload(dtype="bf16", NL=2, Hq=4, Hkv=2, d=64, n=n, n_img=n // 2,
+                           seed=140 + s)
+        p = prefix_inputs(w, seq=s, device=DEV)
+        c = random_confidences(n, seed=150 + s)
+        if s == 5:  # identical keys and confidences: all scores equal
+            p["K"][:] = 0.5
+            c[:] = 0.25
+        prefixes.append(p)
+        confs.append(c)
+        pl = g.integers(0, 7, size=n)
+        pools.append(pl)
+        sizes = np.bincount(pl, minlength=7)
+        keep.append([int(g.integers(0, sz + 1)) for sz in sizes])
+    kept, score, koff, off, st = run_pools(sp, w, prefixes, confs, pools, 7, keep)
+    assert st == 0
+    check_against_oracle(w, prefixes, confs, pools, keep, kept, score, koff, off, "clusters")
+    ks = kept[koff[5]:koff[6]]
+    for p in range(7):
+        members = np.nonzero(pools[5] == p)[0]
+        assert np.array_equal(ks[pools[5][ks] == p], members[:keep[5][p]])
+
+
 def test_bad_counts_and_pool_ids_reported(sp):
     w = small_workload(dtype="bf16", NL=1, Hq=4, Hkv=2, d=64, n=300, n_img=100, seed=3)
     pre = prefix_inputs(w, device=DEV)
