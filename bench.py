@@ -164,6 +164,7 @@ TRAFFIC_SOURCES = {
     "attn_full": ["attention_tc.cu", "attention.cu", "attention.cuh", "tc_ptx.cuh", "common.cuh"],
     "attn_pruned": ["attention_tc.cu", "attention.cu", "attention.cuh", "tc_ptx.cuh",
                     "common.cuh"],
+    "keynorm": ["score_prune.cu", "common.cuh"],
     "score_prune": ["score_prune.cu", "common.cuh"],
     "compact": ["compact.cu", "common.cuh"],
 }
@@ -616,7 +617,10 @@ def run_ours(args):
         "lmhead_prefix": ("tensor", 2.0 * n_rows * w.D * w.V),
         # QK^T and PV over every (query, key) pair of each prefix, all heads and layers
         "prefix_attn": ("tensor", sum(4.0 * n * n * w.Hq * w.d * w.NL for n in seq_rows)),
-        "score_prune": ("hbm", n_rows * row_b),
+        "keynorm": ("hbm", n_rows * row_b),
+        # with the key norms on a side stream under the prefix LM head, the
+        # stage is the selection alone: a chain of cluster barriers
+        "score_prune": (("latency", None) if "keynorm" in stage_ms else ("hbm", n_rows * row_b)),
         "compact": ("hbm", 2 * 2 * kept * row_b),
         "attn_full": ("hbm", 2 * (n_rows + w.S * w.LB) * row_b),
         "attn_pruned": ("hbm", 2 * (kept + w.S * w.LB) * row_b),
@@ -633,7 +637,9 @@ def run_ours(args):
             continue
         sec = stage_ms[k] / 1e3
         traffic = profiled_traffic(k, w.name)
-        if bound == "tensor":
+        if bound == "latency":
+            kernels[k] = {"bound": "latency", "ms": stage_ms[k], "traffic": traffic}
+        elif bound == "tensor":
             ach = amount / sec / 1e12
             pk = peaks["bf16_tflops"]
             kernels[k] = {"bound": "tensor", "achieved": ach, "peak": pk, "unit": "TFLOP/s",

@@ -15,6 +15,8 @@
  *                             per-modality top-floor(r n) kept set
  *   sprint_score_prune_pools  the same scores, kept set with one keep count
  *                             per pool (per-image or whole-prefix pools)
+ *   sprint_key_norms,         the two halves of the above as separate calls
+ *   sprint_select_kept(_pools) (key norms; scores and kept set)
  *   sprint_compact_kv         gather of the kept rows of K and V
  *   sprint_block_attn         bidirectional block attention over
  *                             [pruned prefix ; block]
@@ -251,6 +253,46 @@ int sprint_score_prune_pools(const void *K, int S, const int32_t *prefix_off,
                              const int32_t *kept_off, int total_kept,
                              float *score_out, void *ws, size_t ws_bytes,
                              int32_t *status, cudaStream_t stream);
+
+/*
+ * The two halves of sprint_score_prune / sprint_score_prune_pools as
+ * separate calls, so that the key norms (HBM-bound, they read every prefix
+ * key once) can run on another stream while the prefix LM head (tensor-
+ * bound) computes the confidences the selection needs.  The pair gives the
+ * combined call's kept set and scores bit for bit.
+ *
+ * sprint_key_norms -- u_out[i] = (1/NL) sum_l ||k_i^(l)||, the numerator of
+ * the key-norm importance I_i (Sparse Prefix Retention paragraph): the L2
+ * norm of position i's keys concatenated over the KV heads, averaged over
+ * the layers.
+ *   K, S, prefix_off, total_rows, NL, Hkv, d, dtype   as for sprint_score_prune
+ *   u_out        fp32 [total_rows] OUT
+ * Device status: SPRINT_STATUS_BAD_OFFSETS.
+ *
+ * sprint_select_kept -- the composite scores and the per-modality kept set
+ * of sprint_score_prune, from key norms u (fp32 [total_rows], as written by
+ * sprint_key_norms); the other arguments as for sprint_score_prune, ws of
+ * sprint_select_kept_workspace_bytes(S, total_rows) bytes.
+ *
+ * sprint_select_kept_pools -- the same for sprint_score_prune_pools, ws of
+ * sprint_select_kept_pools_workspace_bytes(S, total_rows, n_pools) bytes.
+ */
+int sprint_key_norms(const void *K, int S, const int32_t *prefix_off, int total_rows, int NL,
+                     int Hkv, int d, int dtype, float *u_out, int32_t *status,
+                     cudaStream_t stream);
+size_t sprint_select_kept_workspace_bytes(int S, int total_rows);
+int sprint_select_kept(const float *u, int S, const int32_t *prefix_off, int total_rows,
+                       const float *conf, const uint8_t *modality, float alpha,
+                       double r_text, double r_img, int32_t *kept_idx,
+                       const int32_t *kept_off, float *score_out, void *ws,
+                       size_t ws_bytes, int32_t *status, cudaStream_t stream);
+size_t sprint_select_kept_pools_workspace_bytes(int S, int total_rows, int n_pools);
+int sprint_select_kept_pools(const float *u, int S, const int32_t *prefix_off,
+                             int total_rows, const float *conf, const uint8_t *pool,
+                             int n_pools, const int32_t *keep, float alpha,
+                             int32_t *kept_idx, const int32_t *kept_off, int total_kept,
+                             float *score_out, void *ws, size_t ws_bytes, int32_t *status,
+                             cudaStream_t stream);
 
 /*
  * sprint_compact_kv -- pruned prefix cache: Kp[l][j] = K[l][kept_idx[j]],

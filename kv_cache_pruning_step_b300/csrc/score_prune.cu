@@ -620,31 +620,14 @@ extern "C" size_t sprint_score_prune_workspace_bytes(int S, int total_rows) {
          align_up((size_t)total_rows * sizeof(uint32_t), 256);
 }
 
-extern "C" int sprint_score_prune(const void *K, int S, const int32_t *prefix_off,
-                                  int total_rows, int NL, int Hkv, int d, int dtype,
-                                  const float *conf, const uint8_t *modality,
-                                  float alpha, double r_text, double r_img,
-                                  int32_t *kept_idx, const int32_t *kept_off,
-                                  float *score_out, void *ws, size_t ws_bytes,
-                                  int32_t *status, cudaStream_t stream) {
-  if (S < 0 || total_rows < 0 || NL < 1 || Hkv < 1 || d < 1) return SPRINT_ERR_INVALID_ARG;
-  if (dtype != SPRINT_F32 && dtype != SPRINT_BF16) return SPRINT_ERR_INVALID_ARG;
-  if (!(r_text >= 0.0 && r_text <= 1.0 && r_img >= 0.0 && r_img <= 1.0))
-    return SPRINT_ERR_INVALID_ARG;
-  if (!(alpha == alpha)) return SPRINT_ERR_INVALID_ARG;
-  if (S == 0) return SPRINT_OK;
-  if (!prefix_off || !kept_off || !status) return SPRINT_ERR_INVALID_ARG;
-  if (total_rows > 0 && (!K || !conf || !modality || !ws)) return SPRINT_ERR_INVALID_ARG;
-  const int row_elems = Hkv * d;
-  if (row_elems % 8 != 0 || (K && !aligned16(K))) return SPRINT_ERR_UNSUPPORTED;
-  if (ws_bytes < sprint_score_prune_workspace_bytes(S, total_rows)) return SPRINT_ERR_WORKSPACE;
+namespace {
 
-  float *u = static_cast<float *>(ws);
-  uint32_t *keys = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) +
-                                                align_up((size_t)total_rows * 4, 256));
-  if (keynorm_launch(K, prefix_off, S, total_rows, NL, row_elems, dtype, u, status, stream) !=
-      SPRINT_OK)
-    return SPRINT_ERR_CUDA;
+// select_kernel over every sequence, on key norms u already in memory; keys
+// is the [total_rows] key scratch.
+int select_launch(const float *u, int S, const int32_t *prefix_off, int total_rows,
+                  const float *conf, const uint8_t *modality, float alpha, double r_text,
+                  double r_img, int32_t *kept_idx, const int32_t *kept_off, float *score_out,
+                  uint32_t *keys, int32_t *status, cudaStream_t stream) {
   // One cluster per sequence, sized so that a CTA's slice is about
   // kSliceTarget positions of an average sequence; slices up to kStageCta
   // positions are staged in shared memory.
@@ -683,6 +666,77 @@ extern "C" int sprint_score_prune(const void *K, int S, const int32_t *prefix_of
                          cap) != cudaSuccess)
     return SPRINT_ERR_CUDA;
   return launch_status();
+}
+
+
+bool select_args_ok(int S, int total_rows, float alpha, double r_text, double r_img) {
+  return S >= 0 && total_rows >= 0 && r_text >= 0.0 && r_text <= 1.0 && r_img >= 0.0 &&
+         r_img <= 1.0 && alpha == alpha;
+}
+
+}  // namespace
+
+extern "C" int sprint_key_norms(const void *K, int S, const int32_t *prefix_off, int total_rows,
+                                int NL, int Hkv, int d, int dtype, float *u_out,
+                                int32_t *status, cudaStream_t stream) {
+  if (S < 0 || total_rows < 0 || NL < 1 || Hkv < 1 || d < 1) return SPRINT_ERR_INVALID_ARG;
+  if (dtype != SPRINT_F32 && dtype != SPRINT_BF16) return SPRINT_ERR_INVALID_ARG;
+  if (S == 0 || total_rows == 0) return SPRINT_OK;
+  if (!prefix_off || !status || !K || !u_out) return SPRINT_ERR_INVALID_ARG;
+  const int row_elems = Hkv * d;
+  if (row_elems % 8 != 0 || !aligned16(K)) return SPRINT_ERR_UNSUPPORTED;
+  return keynorm_launch(K, prefix_off, S, total_rows, NL, row_elems, dtype, u_out, status,
+                        stream) == SPRINT_OK
+             ? SPRINT_OK
+             : SPRINT_ERR_CUDA;
+}
+
+extern "C" size_t sprint_select_kept_workspace_bytes(int S, int total_rows) {
+  if (S < 0 || total_rows < 0) return 0;
+  return align_up((size_t)total_rows * sizeof(uint32_t), 256);
+}
+
+extern "C" int sprint_select_kept(const float *u, int S, const int32_t *prefix_off,
+                                  int total_rows, const float *conf, const uint8_t *modality,
+                                  float alpha, double r_text, double r_img, int32_t *kept_idx,
+                                  const int32_t *kept_off, float *score_out, void *ws,
+                                  size_t ws_bytes, int32_t *status, cudaStream_t stream) {
+  if (!select_args_ok(S, total_rows, alpha, r_text, r_img)) return SPRINT_ERR_INVALID_ARG;
+  if (S == 0) return SPRINT_OK;
+  if (!prefix_off || !kept_off || !status) return SPRINT_ERR_INVALID_ARG;
+  if (total_rows > 0 && (!u || !conf || !modality || !ws)) return SPRINT_ERR_INVALID_ARG;
+  if (ws_bytes < sprint_select_kept_workspace_bytes(S, total_rows)) return SPRINT_ERR_WORKSPACE;
+  return select_launch(u, S, prefix_off, total_rows, conf, modality, alpha, r_text, r_img,
+                       kept_idx, kept_off, score_out, static_cast<uint32_t *>(ws), status,
+                       stream);
+}
+
+extern "C" int sprint_score_prune(const void *K, int S, const int32_t *prefix_off,
+                                  int total_rows, int NL, int Hkv, int d, int dtype,
+                                  const float *conf, const uint8_t *modality,
+                                  float alpha, double r_text, double r_img,
+                                  int32_t *kept_idx, const int32_t *kept_off,
+                                  float *score_out, void *ws, size_t ws_bytes,
+                                  int32_t *status, cudaStream_t stream) {
+  if (NL < 1 || Hkv < 1 || d < 1) return SPRINT_ERR_INVALID_ARG;
+  if (dtype != SPRINT_F32 && dtype != SPRINT_BF16) return SPRINT_ERR_INVALID_ARG;
+  if (!select_args_ok(S, total_rows, alpha, r_text, r_img)) return SPRINT_ERR_INVALID_ARG;
+  if (S == 0) return SPRINT_OK;
+  if (!prefix_off || !kept_off || !status) return SPRINT_ERR_INVALID_ARG;
+  if (total_rows > 0 && (!K || !conf || !modality || !ws)) return SPRINT_ERR_INVALID_ARG;
+  const int row_elems = Hkv * d;
+  if (row_elems % 8 != 0 || (K && !aligned16(K))) return SPRINT_ERR_UNSUPPORTED;
+  if (ws_bytes < sprint_score_prune_workspace_bytes(S, total_rows)) return SPRINT_ERR_WORKSPACE;
+  // The key norms, then the selection on them: sprint_key_norms followed by
+  // sprint_select_kept.
+  float *u = static_cast<float *>(ws);
+  uint32_t *keys = reinterpret_cast<uint32_t *>(static_cast<char *>(ws) +
+                                                align_up((size_t)total_rows * 4, 256));
+  if (keynorm_launch(K, prefix_off, S, total_rows, NL, row_elems, dtype, u, status, stream) !=
+      SPRINT_OK)
+    return SPRINT_ERR_CUDA;
+  return select_launch(u, S, prefix_off, total_rows, conf, modality, alpha, r_text, r_img,
+                       kept_idx, kept_off, score_out, keys, status, stream);
 }
 
 extern "C" int sprint_keep_count(int n, double r) {

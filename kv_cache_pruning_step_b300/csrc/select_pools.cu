@@ -397,42 +397,35 @@ pool_compact_kernel(const uint8_t *__restrict__ pool, int n_pools,
 
 using namespace sprint;
 
-extern "C" size_t sprint_score_prune_pools_workspace_bytes(int S, int total_rows, int n_pools) {
+extern "C" size_t sprint_select_kept_pools_workspace_bytes(int S, int total_rows, int n_pools) {
   if (S < 0 || total_rows < 0 || n_pools < 1 || n_pools > kMaxPools) return 0;
-  return align_up((size_t)total_rows * sizeof(float), 256) +
-         align_up((size_t)total_rows * sizeof(uint32_t), 256) +
+  return align_up((size_t)total_rows * sizeof(uint32_t), 256) +
          align_up((size_t)S * n_pools * sizeof(PoolRec), 256);
 }
 
-extern "C" int sprint_score_prune_pools(const void *K, int S, const int32_t *prefix_off,
-                                        int total_rows, int NL, int Hkv, int d, int dtype,
-                                        const float *conf, const uint8_t *pool, int n_pools,
-                                        const int32_t *keep, float alpha, int32_t *kept_idx,
-                                        const int32_t *kept_off, int total_kept,
-                                        float *score_out, void *ws, size_t ws_bytes,
-                                        int32_t *status, cudaStream_t stream) {
-  if (S < 0 || total_rows < 0 || total_kept < 0 || NL < 1 || Hkv < 1 || d < 1)
-    return SPRINT_ERR_INVALID_ARG;
-  if (n_pools < 1 || n_pools > kMaxPools) return SPRINT_ERR_INVALID_ARG;
-  if (dtype != SPRINT_F32 && dtype != SPRINT_BF16) return SPRINT_ERR_INVALID_ARG;
-  if (!(alpha == alpha)) return SPRINT_ERR_INVALID_ARG;
-  if (S == 0) return SPRINT_OK;
-  if (!prefix_off || !kept_off || !keep || !status || !ws) return SPRINT_ERR_INVALID_ARG;
-  if (total_rows > 0 && (!K || !conf || !pool)) return SPRINT_ERR_INVALID_ARG;
-  if (total_kept > 0 && !kept_idx) return SPRINT_ERR_INVALID_ARG;
-  const int row_elems = Hkv * d;
-  if (row_elems % 8 != 0 || (K && !aligned16(K))) return SPRINT_ERR_UNSUPPORTED;
-  if (ws_bytes < sprint_score_prune_pools_workspace_bytes(S, total_rows, n_pools))
-    return SPRINT_ERR_WORKSPACE;
+extern "C" size_t sprint_score_prune_pools_workspace_bytes(int S, int total_rows, int n_pools) {
+  if (S < 0 || total_rows < 0 || n_pools < 1 || n_pools > kMaxPools) return 0;
+  return align_up((size_t)total_rows * sizeof(float), 256) +
+         sprint_select_kept_pools_workspace_bytes(S, total_rows, n_pools);
+}
+
+namespace {
+
+int pools_args_ok(int S, int total_rows, int total_kept, int n_pools, float alpha) {
+  return S >= 0 && total_rows >= 0 && total_kept >= 0 && n_pools >= 1 && n_pools <= kMaxPools &&
+         alpha == alpha;
+}
+
+// The three pool kernels on key norms u already in memory; ws holds the
+// keys and the pool records.
+int pools_launch(const float *u, int S, const int32_t *prefix_off, int total_rows,
+                 const float *conf, const uint8_t *pool, int n_pools, const int32_t *keep,
+                 float alpha, int32_t *kept_idx, const int32_t *kept_off, int total_kept,
+                 float *score_out, void *ws, int32_t *status, cudaStream_t stream) {
   char *w = static_cast<char *>(ws);
-  float *u = reinterpret_cast<float *>(w);
-  w += align_up((size_t)total_rows * 4, 256);
   uint32_t *keys = reinterpret_cast<uint32_t *>(w);
   w += align_up((size_t)total_rows * 4, 256);
   PoolRec *rec = reinterpret_cast<PoolRec *>(w);
-  if (keynorm_launch(K, prefix_off, S, total_rows, NL, row_elems, dtype, u, status, stream) !=
-      SPRINT_OK)
-    return SPRINT_ERR_CUDA;
   // One cluster per sequence for scoring and compaction, sized so that a
   // CTA's slice is about kPoolSlice positions of an average sequence.
   const int avg = total_rows / S;
@@ -449,9 +442,9 @@ extern "C" int sprint_score_prune_pools(const void *K, int S, const int32_t *pre
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, pool_score_kernel, (const float *)u, conf, pool, n_pools, keep,
-                         prefix_off, kept_off, total_rows, total_kept, alpha, keys, score_out,
-                         rec, status) != cudaSuccess ||
+  if (cudaLaunchKernelEx(&cfg, pool_score_kernel, u, conf, pool, n_pools, keep, prefix_off,
+                         kept_off, total_rows, total_kept, alpha, keys, score_out, rec,
+                         status) != cudaSuccess ||
       launch_status() != SPRINT_OK)
     return SPRINT_ERR_CUDA;
   pool_select_kernel<<<dim3(S, n_pools), kThreads, 0, stream>>>(pool, n_pools, prefix_off, keys,
@@ -462,4 +455,52 @@ extern "C" int sprint_score_prune_pools(const void *K, int S, const int32_t *pre
                          status) != cudaSuccess)
     return SPRINT_ERR_CUDA;
   return launch_status();
+}
+
+}  // namespace
+
+extern "C" int sprint_select_kept_pools(const float *u, int S, const int32_t *prefix_off,
+                                        int total_rows, const float *conf, const uint8_t *pool,
+                                        int n_pools, const int32_t *keep, float alpha,
+                                        int32_t *kept_idx, const int32_t *kept_off,
+                                        int total_kept, float *score_out, void *ws,
+                                        size_t ws_bytes, int32_t *status, cudaStream_t stream) {
+  if (!pools_args_ok(S, total_rows, total_kept, n_pools, alpha)) return SPRINT_ERR_INVALID_ARG;
+  if (S == 0) return SPRINT_OK;
+  if (!prefix_off || !kept_off || !keep || !status || !ws) return SPRINT_ERR_INVALID_ARG;
+  if (total_rows > 0 && (!u || !conf || !pool)) return SPRINT_ERR_INVALID_ARG;
+  if (total_kept > 0 && !kept_idx) return SPRINT_ERR_INVALID_ARG;
+  if (ws_bytes < sprint_select_kept_pools_workspace_bytes(S, total_rows, n_pools))
+    return SPRINT_ERR_WORKSPACE;
+  return pools_launch(u, S, prefix_off, total_rows, conf, pool, n_pools, keep, alpha, kept_idx,
+                      kept_off, total_kept, score_out, ws, status, stream);
+}
+
+extern "C" int sprint_score_prune_pools(const void *K, int S, const int32_t *prefix_off,
+                                        int total_rows, int NL, int Hkv, int d, int dtype,
+                                        const float *conf, const uint8_t *pool, int n_pools,
+                                        const int32_t *keep, float alpha, int32_t *kept_idx,
+                                        const int32_t *kept_off, int total_kept,
+                                        float *score_out, void *ws, size_t ws_bytes,
+                                        int32_t *status, cudaStream_t stream) {
+  if (!pools_args_ok(S, total_rows, total_kept, n_pools, alpha) || NL < 1 || Hkv < 1 || d < 1)
+    return SPRINT_ERR_INVALID_ARG;
+  if (dtype != SPRINT_F32 && dtype != SPRINT_BF16) return SPRINT_ERR_INVALID_ARG;
+  if (S == 0) return SPRINT_OK;
+  if (!prefix_off || !kept_off || !keep || !status || !ws) return SPRINT_ERR_INVALID_ARG;
+  if (total_rows > 0 && (!K || !conf || !pool)) return SPRINT_ERR_INVALID_ARG;
+  if (total_kept > 0 && !kept_idx) return SPRINT_ERR_INVALID_ARG;
+  const int row_elems = Hkv * d;
+  if (row_elems % 8 != 0 || (K && !aligned16(K))) return SPRINT_ERR_UNSUPPORTED;
+  if (ws_bytes < sprint_score_prune_pools_workspace_bytes(S, total_rows, n_pools))
+    return SPRINT_ERR_WORKSPACE;
+  // The key norms, then the pool selection on them: sprint_key_norms
+  // followed by sprint_select_kept_pools.
+  float *u = static_cast<float *>(ws);
+  void *rest = static_cast<char *>(ws) + align_up((size_t)total_rows * 4, 256);
+  if (keynorm_launch(K, prefix_off, S, total_rows, NL, row_elems, dtype, u, status, stream) !=
+      SPRINT_OK)
+    return SPRINT_ERR_CUDA;
+  return pools_launch(u, S, prefix_off, total_rows, conf, pool, n_pools, keep, alpha, kept_idx,
+                      kept_off, total_kept, score_out, rest, status, stream);
 }

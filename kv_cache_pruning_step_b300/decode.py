@@ -76,6 +76,13 @@ class BlockDecoder:
     attention's combine kernel, the stepwise path calls
     sprint_residual_hidden.
 
+    overlap_keynorm=True (default): the key norms of the scoring, which read
+    every prefix key once (HBM-bound), run on a side stream while the prefix
+    LM head (tensor-bound) computes the confidences, and the selection then
+    runs on the key norms (sprint_key_norms + sprint_select_kept, the same
+    bits as sprint_score_prune).  False: one sprint_score_prune call after
+    the LM head.
+
     prefix_attn=True: step 0 also runs the prefix's own attention of the full
     forward pass (sprint_prefix_attn) on the prefix queries prefix["Qp"]
     ([NL][n][Hq][d] per sequence) into self.O_prefix.  The output feeds
@@ -86,7 +93,7 @@ class BlockDecoder:
     def __init__(self, W, *, NL, Hq, Hkv, d, LB, T, tau, r_text, r_img, alpha=0.5,
                  mode=sp.UNMASK_ADAPTIVE, modality_counts, want_logits=False, indexed=False,
                  selection="modality", r_global=0.5, pool_sizes=None, residual=False,
-                 prefix_argmax=False, prefix_attn=False):
+                 prefix_argmax=False, prefix_attn=False, overlap_keynorm=True):
         self.W = W
         self.dev = W.device
         self.dtype = W.dtype
@@ -100,6 +107,11 @@ class BlockDecoder:
         self.selection, self.r_global = selection, r_global
         self.residual = bool(residual)
         self.prefix_attn = bool(prefix_attn)
+        self.overlap_keynorm = bool(overlap_keynorm)
+        if self.overlap_keynorm:
+            self.side = torch.cuda.Stream(device=W.device)
+            self._k_ready = torch.cuda.Event()
+            self._u_ready = torch.cuda.Event()
         if self.residual and Hq * d != W.shape[1]:
             raise ValueError("the residual chain needs Hq * d == D")
         self.V, self.D = W.shape
@@ -211,6 +223,7 @@ class BlockDecoder:
             max(16, sp.sprint_lmhead_workspace_bytes(self.total_rows, self.D, self.V, dt)), u8)
         self.kept_idx = self._buf("kept_idx", self.total_kept, torch.int32)
         self.score = self._buf("score", self.total_rows, torch.float32)
+        self.u = self._buf("u", self.total_rows, torch.float32)
         ws_bytes = (sp.sprint_score_prune_workspace_bytes(S, self.total_rows)
                     if self.keep is None else
                     sp.sprint_score_prune_pools_workspace_bytes(S, self.total_rows, self.n_pools))
@@ -303,6 +316,9 @@ class BlockDecoder:
                 sp.sprint_prefix_attn(Qp, K, V, self.prefix_off, self.total_rows, self.NL,
                                       self.Hq, self.Hkv, self.d, Op=self.O_prefix,
                                       status=self.status)
+        overlap = self.overlap_keynorm and self.total_rows > 0
+        if overlap:
+            self._k_ready.record()  # the prefix keys are ready on the current stream
         merged = False
         with self._stage("lmhead_prefix"):
             if r0 and step0 is not None and r0 < self.total_rows:
@@ -312,17 +328,41 @@ class BlockDecoder:
                     H[r0:], self.W, theta[r0:], conf=self.conf_prefix[r0:],
                     argmax=self.argmax_prefix[r0:] if self.prefix_argmax else None,
                     want_argmax=self.prefix_argmax, ws=self.ws_lm_prefix, status=self.status)
+        if overlap:
+            # launched after the LM head, so its CTAs find the GEMM's already
+            # resident and fill the room beside them
+            with torch.cuda.stream(self.side):
+                self.side.wait_event(self._k_ready)
+                with self._stage("keynorm"):
+                    sp.sprint_key_norms(K, self.prefix_off, self.total_rows, self.NL,
+                                        self.Hkv, self.d, u=self.u, status=self.status)
+                self._u_ready.record(self.side)
+            torch.cuda.current_stream().wait_event(self._u_ready)
         with self._stage("score_prune"):
-            if self.keep is None:
+            pool = None
+            if self.keep is not None:
+                pool = self.zero_pool if self.selection == "global" else image
+                if pool is None:
+                    raise ValueError("per_image selection needs the prefix's image numbers")
+            if self.keep is None and overlap:
+                sp.sprint_select_kept(self.u, self.prefix_off, self.total_rows,
+                                      self.conf_prefix, modality, self.alpha, self.r_text,
+                                      self.r_img, self.kept_off, self.total_kept,
+                                      kept_idx=self.kept_idx, score=self.score,
+                                      ws=self.ws_score, status=self.status)
+            elif self.keep is None:
                 sp.sprint_score_prune(K, self.prefix_off, self.total_rows, self.NL, self.Hkv,
                                       self.d, self.conf_prefix, modality, self.alpha,
                                       self.r_text, self.r_img, self.kept_off, self.total_kept,
                                       kept_idx=self.kept_idx, score=self.score,
                                       ws=self.ws_score, status=self.status)
+            elif overlap:
+                sp.sprint_select_kept_pools(self.u, self.prefix_off, self.total_rows,
+                                            self.conf_prefix, pool, self.n_pools, self.keep,
+                                            self.alpha, self.kept_off, self.total_kept,
+                                            kept_idx=self.kept_idx, score=self.score,
+                                            ws=self.ws_score, status=self.status)
             else:
-                pool = self.zero_pool if self.selection == "global" else image
-                if pool is None:
-                    raise ValueError("per_image selection needs the prefix's image numbers")
                 sp.sprint_score_prune_pools(K, self.prefix_off, self.total_rows, self.NL,
                                             self.Hkv, self.d, self.conf_prefix, pool,
                                             self.n_pools, self.keep, self.alpha, self.kept_off,

@@ -45,6 +45,13 @@ SIGNATURES = {
     "sprint_score_prune_workspace_bytes": (_Z, [_I, _I]),
     "sprint_score_prune": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _F, _D, _D, _P, _P,
                                 _P, _P, _Z, _P, _P]),
+    "sprint_key_norms": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "sprint_select_kept_workspace_bytes": (_Z, [_I, _I]),
+    "sprint_select_kept": (_I, [_P, _I, _P, _I, _P, _P, _F, _D, _D, _P, _P, _P, _P, _Z, _P,
+                                _P]),
+    "sprint_select_kept_pools_workspace_bytes": (_Z, [_I, _I, _I]),
+    "sprint_select_kept_pools": (_I, [_P, _I, _P, _I, _P, _P, _I, _P, _F, _P, _P, _I, _P, _P,
+                                      _Z, _P, _P]),
     "sprint_score_prune_pools_workspace_bytes": (_Z, [_I, _I, _I]),
     "sprint_score_prune_pools": (_I, [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _F, _P,
                                       _P, _I, _P, _P, _Z, _P, _P]),
@@ -242,6 +249,77 @@ def sprint_score_prune(K, prefix_off, total_rows, NL, Hkv, d, conf, modality, al
         _ptr(score, torch.float32, "score"), _ptr(ws), ws.numel(),
         _ptr(status, torch.int32, "status"), _stream(stream))
     _check(rc, "sprint_score_prune")
+    return kept_idx, score
+
+
+def sprint_key_norms(K, prefix_off, total_rows, NL, Hkv, d, *, u=None, status=None,
+                     stream=None):
+    """u fp32 [total_rows]: mean over layers of the L2 norm of every prefix
+    position's keys (concatenated over the KV heads)."""
+    S = prefix_off.numel() - 1
+    dev = K.device
+    u = torch.empty(total_rows, dtype=torch.float32, device=dev) if u is None else u
+    status = new_status(dev) if status is None else status
+    rc = lib.sprint_key_norms(
+        _ptr(K, K.dtype, "K"), S, _ptr(prefix_off, torch.int32, "prefix_off"), int(total_rows),
+        NL, Hkv, d, _dtype_code(K), _ptr(u, torch.float32, "u"),
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "sprint_key_norms")
+    return u
+
+
+def sprint_select_kept_workspace_bytes(S, total_rows) -> int:
+    return lib.sprint_select_kept_workspace_bytes(S, total_rows)
+
+
+def sprint_select_kept(u, prefix_off, total_rows, conf, modality, alpha, r_text, r_img,
+                       kept_off, total_kept, *, kept_idx=None, want_score=False, score=None,
+                       ws=None, status=None, stream=None):
+    """sprint_score_prune's scores and kept set from key norms u.  Returns
+    (kept_idx int32 [total_kept], score fp32 [total_rows] or None)."""
+    S = prefix_off.numel() - 1
+    dev = u.device
+    kept_idx = (torch.empty(total_kept, dtype=torch.int32, device=dev)
+                if kept_idx is None else kept_idx)
+    if want_score and score is None:
+        score = torch.empty(total_rows, dtype=torch.float32, device=dev)
+    status = new_status(dev) if status is None else status
+    ws = _ws(ws, sprint_select_kept_workspace_bytes(S, total_rows), dev)
+    rc = lib.sprint_select_kept(
+        _ptr(u, torch.float32, "u"), S, _ptr(prefix_off, torch.int32, "prefix_off"),
+        int(total_rows), _ptr(conf, torch.float32, "conf"),
+        _ptr(modality, torch.uint8, "modality"), float(alpha), float(r_text), float(r_img),
+        _ptr(kept_idx, torch.int32, "kept_idx"), _ptr(kept_off, torch.int32, "kept_off"),
+        _ptr(score, torch.float32, "score"), _ptr(ws), ws.numel(),
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "sprint_select_kept")
+    return kept_idx, score
+
+
+def sprint_select_kept_pools_workspace_bytes(S, total_rows, n_pools) -> int:
+    return lib.sprint_select_kept_pools_workspace_bytes(S, total_rows, n_pools)
+
+
+def sprint_select_kept_pools(u, prefix_off, total_rows, conf, pool, n_pools, keep, alpha,
+                             kept_off, total_kept, *, kept_idx=None, want_score=False,
+                             score=None, ws=None, status=None, stream=None):
+    """sprint_score_prune_pools' scores and kept set from key norms u."""
+    S = prefix_off.numel() - 1
+    dev = u.device
+    kept_idx = (torch.empty(total_kept, dtype=torch.int32, device=dev)
+                if kept_idx is None else kept_idx)
+    if want_score and score is None:
+        score = torch.empty(total_rows, dtype=torch.float32, device=dev)
+    status = new_status(dev) if status is None else status
+    ws = _ws(ws, sprint_select_kept_pools_workspace_bytes(S, total_rows, n_pools), dev)
+    rc = lib.sprint_select_kept_pools(
+        _ptr(u, torch.float32, "u"), S, _ptr(prefix_off, torch.int32, "prefix_off"),
+        int(total_rows), _ptr(conf, torch.float32, "conf"), _ptr(pool, torch.uint8, "pool"),
+        int(n_pools), _ptr(keep, torch.int32, "keep"), float(alpha),
+        _ptr(kept_idx, torch.int32, "kept_idx"), _ptr(kept_off, torch.int32, "kept_off"),
+        int(total_kept), _ptr(score, torch.float32, "score"), _ptr(ws), ws.numel(),
+        _ptr(status, torch.int32, "status"), _stream(stream))
+    _check(rc, "sprint_select_kept_pools")
     return kept_idx, score
 
 

@@ -215,3 +215,32 @@ def test_compaction_identity_and_bad_index(sp):
                          Kp=Kp, Vp=Vp, status=status)
     torch.cuda.synchronize()
     assert status.item() & sp.STATUS_BAD_INDEX
+
+
+@pytest.mark.parametrize("dtype,shapes", [
+    ("bf16", [(4096, 3072)]),
+    ("f32", [(5000, 1234), (4000, 0), (0, 0), (5, 5)]),
+    ("bf16", [(40000, 20000), (5, 2), (100, 0)]),
+])
+def test_key_norms_then_select_equals_score_prune(sp, dtype, shapes):
+    """sprint_key_norms followed by sprint_select_kept (the split the
+    decoder overlaps with the prefix LM head) gives sprint_score_prune's
+    kept set and scores bit for bit, and the key norms are the oracle's."""
+    w, prefixes, confs = _ragged_prefixes(shapes, 2, 2, 64, dtype, 500)
+    r_text, r_img = 1.0, 0.8
+    cat, conf, kh, ko, kept, score, _ = run_score_prune(sp, w, prefixes, confs, r_text, r_img)
+    n = cat["off_host"][-1]
+    status = sp.new_status(DEV)
+    u = sp.sprint_key_norms(cat["K"], cat["off"], n, w.NL, w.Hkv, w.d, status=status)
+    kept2, score2 = sp.sprint_select_kept(u, cat["off"], n, conf, cat["modality"], 0.5, r_text,
+                                          r_img, ko, kh[-1], want_score=True, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.equal(kept, kept2)
+    assert torch.equal(score, score2)
+    for s, p in enumerate(prefixes):
+        a, b = cat["off_host"][s], cat["off_host"][s + 1]
+        if b > a:  # u over its mean is the oracle's importance
+            us = u[a:b].cpu().numpy().astype(np.float64)
+            np.testing.assert_allclose(us / us.mean(), orc.key_norm_importance(p["K"]),
+                                       rtol=1e-5)

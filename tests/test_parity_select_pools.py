@@ -237,3 +237,36 @@ def test_decoder_selection_variants(sp, selection, name):
     want = orc.select_kept_pools(a.score.cpu().numpy(), pool, keep)
     assert a.kept_idx.cpu().numpy().tolist() == want.tolist()
     assert a.total_kept == sum(keep)
+
+
+def test_key_norms_then_select_pools_equals_score_prune_pools(sp):
+    """sprint_key_norms followed by sprint_select_kept_pools gives
+    sprint_score_prune_pools' kept set and scores bit for bit."""
+    lens = [0, 3, 40000, 9000, 1, 700]
+    prefixes, confs, pools, keep = [], [], [], []
+    g = np.random.default_rng(13)
+    for s, n in enumerate(lens):
+        w = small_workload(dtype="bf16", NL=2, Hq=4, Hkv=2, d=64, n=n, n_img=n // 2,
+                           seed=170 + s)
+        prefixes.append(prefix_inputs(w, seq=s, device=DEV))
+        confs.append(random_confidences(n, seed=180 + s))
+        pl = g.integers(0, 5, size=n)
+        pools.append(pl)
+        sizes = np.bincount(pl, minlength=5)
+        keep.append([int(g.integers(0, sz + 1)) for sz in sizes])
+    kept, score, koff, off, st = run_pools(sp, w, prefixes, confs, pools, 5, keep)
+    assert st == 0
+    cat = gc.concat_prefixes(prefixes)
+    n = sum(lens)
+    pool = torch.cat([torch.as_tensor(p, dtype=torch.uint8) for p in pools]).to(DEV)
+    keep_t = torch.tensor(keep, dtype=torch.int32, device=DEV).reshape(-1)
+    kept_off = torch.tensor(koff, dtype=torch.int32, device=DEV)
+    status = sp.new_status(DEV)
+    u = sp.sprint_key_norms(cat["K"], cat["off"], n, w.NL, w.Hkv, w.d, status=status)
+    kept2, score2 = sp.sprint_select_kept_pools(u, cat["off"], n, torch.cat(confs).to(DEV), pool,
+                                                5, keep_t, w.alpha, kept_off, koff[-1],
+                                                want_score=True, status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert np.array_equal(kept, kept2.cpu().numpy())
+    assert np.array_equal(score, score2.cpu().numpy())

@@ -242,6 +242,28 @@ def test_native_step_driver_4096_block_rows(sp):
     assert torch.equal(a.conf_blk, b.conf_blk)
 
 
+def test_overlapped_key_norms_match_one_call(sp):
+    """The default prefix pass (key norms on a side stream under the prefix
+    LM head, then the selection on them) and one sprint_score_prune call
+    after the LM head give the same scores, kept set and tokens."""
+    from kv_cache_pruning_step_b300 import BlockDecoder
+    w, pre, steps, _ = _decoder_and_steps("prefix-4k")
+    W = lm_head_weight(w, device=DEV)
+    mod = pre["modality"].cpu().numpy()
+    counts = [(int((mod == 0).sum()), int((mod == 1).sum()))]
+    res = []
+    for overlap in (True, False):
+        dec = BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
+                           r_text=w.r_text, r_img=w.r_img, alpha=w.alpha,
+                           modality_counts=counts, overlap_keynorm=overlap)
+        r = dec.decode(pre, lambda t: steps[t])
+        torch.cuda.synchronize()
+        assert dec.status.item() == 0
+        res.append((dec.score.clone(), dec.kept_idx.clone(), r.tokens.clone()))
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
+
+
 def test_native_step_driver_skips_steps_after_the_block_is_done(sp):
     """tau below every confidence: step 0 accepts all LB positions, and the
     kernels of steps 1..T-1 return without touching any output."""
