@@ -536,6 +536,20 @@ def run_ours(args):
     stage_launches = {k: len(v) for k, v in dec.timing.items()}
     stage_ms.update(timed_ms)  # the roofline kernel: measured inside the timed region
     dec.timing = None
+    # Confidence histograms, outside the timed region: every prefix c_i of
+    # the last block, and the block's c_n at every step of one stepwise
+    # decode of the same block (the unmask rule sees these).
+    blk_conf = []
+    dec.decode_stepwise(prefix, step_fn,
+                        on_step=lambda t, d: blk_conf.append(d.conf_blk.clone()))
+
+    def histo(x):
+        return [int(v) for v in torch.histc(x.float(), bins=10, min=0.0, max=1.0).tolist()]
+    blk_all = torch.cat(blk_conf)
+    conf_hist = {"bins": "10 equal bins over [0, 1]", "prefix_c": histo(dec.conf_prefix),
+                 "block_c_every_step": histo(blk_all),
+                 "block_c_above_tau": int((blk_all > w.tau).sum().item()),
+                 "block_c_max": float(blk_all.max().item())}
     assert dec.status.item() == 0, f"device status {dec.status.item()}"
 
     t_job = max_over_ranks(elapsed, world, dev)
@@ -688,6 +702,7 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}, one sequence set per GPU"},
         "decode_steps_per_block": n_steps / args.steps,
         "accepted_per_step_hist": {str(k): v for k, v in sorted(hist.items())},
+        "confidence_hist": conf_hist,
         "stages_ms": stage_ms, "stage_launches": stage_launches,
         "stages_ms_source": (f"lmhead_prefix: CUDA events inside the timed region; other stages: "
                              f"{breakdown_blocks} further blocks with events around every stage"),
@@ -696,9 +711,14 @@ def run_ours(args):
         "e2e": e2e, "full_retention_comparison": compare,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, cpu_inputs(pres, steps_h, W_h),
-                                           n_steps / args.steps, selection=args.selection,
-                                           r_global=args.r_global)
+        ci = cpu_inputs(pres, steps_h, W_h)
+        # one untimed pass first (thread pools, first touch of the widened
+        # inputs), as the reference arm's warm-up does
+        cpu_baseline(w, ci, n_steps / args.steps, selection=args.selection,
+                     r_global=args.r_global)
+        out["cpu_baseline"] = cpu_baseline(w, ci, n_steps / args.steps,
+                                           selection=args.selection, r_global=args.r_global)
+        out["cpu_baseline"]["warmup"] = 1
     if rank == 0:
         print(json.dumps(out))
     if world > 1:

@@ -44,8 +44,10 @@
 // full cache through the kept indices.  Then warps 0 and 11 each load half
 // of a prefix tile with 16-byte cp.async copies (a 256-byte head row per 16
 // lanes) into the same 128-byte-swizzled layout the TMA writes; each lane
-// waits for its own copies and fences them for the tensor cores (generic to
-// async proxy), and lane 0 of each warp arrives on the stage's full barrier.
+// waits for its own copies, fences them for the tensor cores (generic to
+// async proxy) and arrives on the stage's full barrier itself (64 arrivals:
+// every lane's release follows its own fence); the MMA issuers fence again
+// after their wait, before the tensor cores read the stage.
 // With three or more stages a warp does not wait for tile q's copies right
 // after issuing them: it arrives for tile q once it has issued the first
 // quarter of tile q+1 (the stage of q+1 frees when the PV of tile q-2 ends,
@@ -330,7 +332,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (threadIdx.x == 0) {
     tc::mbar_init(tc::smem_u32(q_full), 1);
     for (int i = 0; i < MAX_STAGES; ++i) {
-      tc::mbar_init(tc::smem_u32(kv_full + i), kIndexed ? 2 : 1);  // one per producer warp
+      tc::mbar_init(tc::smem_u32(kv_full + i), kIndexed ? 64 : 1);  // every producer lane
       tc::mbar_init(tc::smem_u32(kv_empty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -379,9 +381,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (kIndexed && (warp == 0 || warp == GATHER_WARP) && run) {
       // ------------------------------------------------ producers, indexed prefix
       // Warps 0 and GATHER_WARP each gather half of a prefix tile's rows
-      // (gw = 0: rows 0-63, gw = 1: rows 64-127) and each arrive once on
-      // the stage's full barrier (count 2); lane 0 of warp 0 also loads Q
-      // and the block's own key tiles by TMA.
+      // (gw = 0: rows 0-63, gw = 1: rows 64-127); every lane of both arrives
+      // on the stage's full barrier (count 64); lane 0 of warp 0 also loads
+      // Q and the block's own key tiles by TMA (its arrival carries the
+      // expected bytes).
       const int gw = warp == 0 ? 0 : 1;
       if (gw == 0 && lane == 0) {
         const uint32_t qb = tc::smem_u32(q_full);
@@ -424,8 +427,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (pend_stage < 0) return;
         if (all) cp_async_wait<0>(); else cp_async_wait<1>();
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(tc::smem_u32(kv_full + pend_stage));
+        tc::mbar_arrive(tc::smem_u32(kv_full + pend_stage));
         pend_stage = -1;
       };
       for (int t = 0; t < sg.ntile; ++t) {
@@ -485,8 +487,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
               tc::tma_load_3d(kdst + b * L::KBOX, &tm_kb, fb, b * 64, sg.g, z);
               tc::tma_load_3d(vdst + b * L::KBOX, &tm_vb, fb, b * 64, sg.g, z);
             }
-          } else if (gw == 1 && lane == 0) {
-            tc::mbar_arrive(fb);  // the second of the barrier's two arrivals
+          } else {
+            tc::mbar_arrive(fb);  // the other 63 of the barrier's 64 arrivals
           }
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (ph << stage);
@@ -559,6 +561,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           break;
         }
         tc::fence_after_sync();
+        if (kIndexed) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         const uint64_t kd = kd0 + (uint64_t)stage * kStageD;
         const uint32_t sd = tmem + h * TILE;
 #pragma unroll
@@ -597,6 +600,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             break;
           }
           tc::fence_after_sync();
+          if (kIndexed && half == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 #pragma unroll
           for (int kk = 0; kk < TILE / 32; ++kk) {  // 16 keys: 8 columns of P, 16 rows of V
             const int k = half * (TILE / 32) + kk;

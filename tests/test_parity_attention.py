@@ -138,3 +138,44 @@ def test_many_short_sequences_two_stage_ring(sp):
     picks = [0, 1, 57, 150, 299] + [s for s, n in enumerate(lens) if n == 0][:2]
     check(w, [prefixes[s] for s in picks], [steps[s] for s in picks], O[picks],
           what="many sequences")
+
+
+def _aligned_keys(Q, a, d):
+    """Keys k_i = a_i * dir_g with dir_g = q_g sqrt(d) / (|q_g|^2 log2 e): a
+    query equal to q_g scores key i at a_i in the kernel's log2 units."""
+    q = Q[:, 0].float()                                     # [NL][Hkv][d] (one row per head)
+    dirs = q * (d ** 0.5) / (q.pow(2).sum(-1, keepdim=True) * np.log2(np.e))
+    return (a.view(1, -1, 1, 1) * dirs.unsqueeze(1))       # [NL][n][Hkv][d]
+
+
+@pytest.mark.parametrize("pattern", ["ramp", "spikes", "descending"])
+def test_row_maxima_moving_within_tiles(sp, pattern):
+    """Scores that climb through a tile (the reference maximum moves in both
+    key halves of most tiles), isolated spikes in the first and second half
+    of tiles, and falling scores, for query rows that see them with either
+    sign.  The output must match the fp64 oracle whatever the order in
+    which the row maxima appear."""
+    NL, Hq, Hkv, d, LB, n = 1, 2, 2, 128, 32, 1000
+    w = small_workload(dtype="bf16", NL=NL, Hq=Hq, Hkv=Hkv, d=d, LB=LB, n=n, n_img=0, seed=77)
+    pre = prefix_inputs(w, device=DEV)
+    x = step_inputs(w, 0, 0, 1, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(78)
+    q = torch.randn((NL, 1, Hq, d), generator=g, device=DEV)
+    sign = torch.ones(LB, device=DEV)
+    sign[LB // 2:] = -1.0                                   # half the rows see -a
+    x["Q"] = (q * sign.view(1, LB, 1, 1)).to(torch.bfloat16).contiguous()
+    i = torch.arange(n, device=DEV, dtype=torch.float32)
+    if pattern == "ramp":
+        a = 0.6 * i                                         # +19 per 32-key chunk
+    elif pattern == "spikes":
+        a = 0.5 * torch.randn(n, generator=g, device=DEV)
+        for t0 in range(0, n, 128):
+            for off, hgt in ((40, 30.0), (70, 60.0), (100, 90.0)):
+                if t0 + off < n:
+                    a[t0 + off] = hgt + t0 / 10.0
+    else:
+        a = 40.0 - 0.04 * i
+    pre["K"] = _aligned_keys(x["Q"].float(), a, d).to(torch.bfloat16).contiguous()
+    x["Kb"] = (0.1 * torch.randn(x["Kb"].shape, generator=g, device=DEV)).to(torch.bfloat16)
+    O = run_attn(sp, w, [pre], [x])
+    check(w, [pre], [x], O, what=pattern)

@@ -140,3 +140,33 @@ def test_decoder_runs_the_prefix_attention_at_step_0(sp):
     want = orc.prefix_attention(pre["Qp"], pre["K"], pre["V"], rows=rows)
     got = gc.host(da.O_prefix.view(w.NL, 700, w.Hq, w.d))[:, rows]
     gc.assert_close(got, want, torch.bfloat16, "decoder O_prefix")
+
+
+@pytest.mark.parametrize("pattern", ["ramp", "spikes"])
+def test_row_maxima_moving_within_tiles(sp, pattern):
+    """Prefix self-attention with keys whose scores climb through every key
+    tile, or spike inside tiles, for every query (queries along one
+    direction, keys scaled along it): the output must match the fp64 oracle
+    whatever the order in which the row maxima appear."""
+    NL, Hq, Hkv, d, n = 1, 2, 2, 128, 700
+    g = generator(DEV, "prefix-attn-moving", 1)
+    dirs = torch.randn((NL, 1, Hkv, d), generator=g, device=DEV)
+    dirs = dirs / dirs.norm(dim=-1, keepdim=True)
+    scale = torch.linspace(0.5, 1.5, n, device=DEV).view(1, n, 1, 1)
+    Q = (dirs.repeat_interleave(Hq // Hkv, dim=2) * scale * 4.0).to(torch.bfloat16)
+    i = torch.arange(n, device=DEV, dtype=torch.float32)
+    if pattern == "ramp":
+        a = 0.08 * i
+    else:
+        a = 0.3 * torch.randn(n, generator=g, device=DEV)
+        for t0 in range(0, n, 128):
+            for off, hgt in ((40, 6.0), (100, 12.0)):
+                if t0 + off < n:
+                    a[t0 + off] = hgt + t0 / 64.0
+    K = (dirs * a.view(1, n, 1, 1) * (d ** 0.5)).to(torch.bfloat16)
+    V = torch.randn((NL, n, Hkv, d), generator=g, device=DEV).to(torch.bfloat16)
+    off = [0, n]
+    Op = _run(sp, [Q.reshape(-1), K.reshape(-1), V.reshape(-1)], off, NL, Hq, Hkv, d)
+    want = orc.prefix_attention(Q, K, V)
+    got = gc.host(Op.view(NL, n, Hq, d))
+    gc.assert_close(got, want, torch.bfloat16, pattern)
