@@ -680,9 +680,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         const float nm = -m_used;
         float lsum = 0.f;
-        // Unrolled by two, not four: at the 168-register cap of three warps
-        // per sub-partition the full unroll spilled registers.
-#pragma unroll 2
+        // Decode: unrolled by two, not four: at the 168-register cap of three
+        // warps per sub-partition the full unroll spilled registers and was
+        // slower.  Prefix mode keeps the full unroll, which measured faster
+        // there in spite of a small spill.
+#pragma unroll(kPrefix ? 4 : 2)
         for (int c = 0; c < TILE / 32; ++c) {
           float v[32];
           tc::tmem_ld32(s_addr + c * 32, v);
