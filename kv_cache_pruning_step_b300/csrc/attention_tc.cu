@@ -37,8 +37,12 @@
 //               max moves only when the tile max exceeds it by more than 2^8
 //               (O_h is then rescaled in TMEM); a second pass writes P =
 //               exp2(S * log2e/sqrt(d) - m_h) as bf16 pairs over the first 64
-//               columns of S_h, where the PV product reads it.  At the end of
-//               the segment each warpgroup writes its (O_h, m_h, l_h) partial.
+//               columns of S_h, where the PV product reads it.  P is handed
+//               to the PV issuer in quarters of 32 keys, each with its own
+//               barrier, so the products of a quarter run while the next is
+//               computed and little of the PV is left once the softmax ends.
+//               At the end of the segment each warpgroup writes its (O_h,
+//               m_h, l_h) partial.
 //
 // Indexed prefix (no compacted copy): the kept rows are gathered from the
 // full cache through the kept indices.  Then warps 0 and 11 each load half
@@ -306,8 +310,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   uint64_t *kv_full = bar + 1;                   // MAX_STAGES
   uint64_t *kv_empty = kv_full + MAX_STAGES;     // MAX_STAGES
   uint64_t *s_full = kv_empty + MAX_STAGES;      // 2
-  uint64_t *p_ready = s_full + 2;                // 4: [warpgroup][key half]
-  uint64_t *pv_done = p_ready + 4;               // 2
+  uint64_t *p_ready = s_full + 2;                // 8: [warpgroup][key quarter]
+  uint64_t *pv_done = p_ready + 8;               // 2
   uint64_t *o_full = pv_done + 2, *drain = o_full + 1;  // drain[2]: one per issuer
   uint64_t *never = drain + 2;  // no one arrives: the stall test waits on it
   uint64_t *ml_ready = never + 1;  // 2: prefix mode, a warpgroup's (m, l) are published
@@ -337,8 +341,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(tc::smem_u32(s_full + i), 1);
-      tc::mbar_init(tc::smem_u32(p_ready + 2 * i), 4);  // the 4 warps of warpgroup i,
-      tc::mbar_init(tc::smem_u32(p_ready + 2 * i + 1), 4);  // one per key half
+      for (int k4 = 0; k4 < 4; ++k4)  // the 4 warps of warpgroup i, one per key quarter
+        tc::mbar_init(tc::smem_u32(p_ready + 4 * i + k4), 4);
       tc::mbar_init(tc::smem_u32(pv_done + i), 1);
     }
     tc::mbar_init(tc::smem_u32(o_full), 1);
@@ -588,11 +592,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const uint64_t vd = vd0 + (uint64_t)stage * kStageD;
         const uint32_t pa = tmem + h * TILE;          // P[h]: 64 columns of bf16 pairs
         const uint32_t od = tmem + L::TMEM_O + h * D;
-        // P arrives in two halves of 64 keys: the first half's products run
-        // while the softmax still computes the second.
+        // P arrives in quarters of 32 keys: a quarter's products run while
+        // the softmax still computes the next.
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          if (!tc::mbar_wait(tc::smem_u32(p_ready + 2 * h + half), (q >> 1) & 1, pb.cap_ns,
+        for (int half = 0; half < 4; ++half) {  // quarters of 32 keys
+          if (!tc::mbar_wait(tc::smem_u32(p_ready + 4 * h + half), (q >> 1) & 1, pb.cap_ns,
                              abort_flag) ||
               (half == 0 &&
                !tc::mbar_wait(tc::smem_u32(kv_full + stage), ph, pb.cap_ns, abort_flag))) {
@@ -602,8 +606,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           tc::fence_after_sync();
           if (kIndexed && half == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 #pragma unroll
-          for (int kk = 0; kk < TILE / 32; ++kk) {  // 16 keys: 8 columns of P, 16 rows of V
-            const int k = half * (TILE / 32) + kk;
+          for (int kk = 0; kk < 2; ++kk) {  // 16 keys: 8 columns of P, 16 rows of V
+            const int k = half * 2 + kk;
             // A warpgroup's first tile of the segment (u < 2) starts its O.
             mma_bf16_ts(od, pa + 8 * k, vd + (16 * 128 >> 4) * k, idesc_pv,
                         (u >= 2 || k > 0) ? 1u : 0u);
@@ -699,11 +703,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             pk[u] = *reinterpret_cast<uint32_t *>(&h2);
           }
           tmem_st16(s_addr + c * 16, pk);
-          if (c == TILE / 64 - 1 || c == TILE / 32 - 1) {
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          {  // every 32-key quarter of P is handed over on its own
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(tc::smem_u32(p_ready + 2 * h + (c * 32 >= TILE / 2)));
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(p_ready + 4 * h + c));
           }
         }
         l_sum += lsum;
