@@ -264,6 +264,40 @@ def test_overlapped_key_norms_match_one_call(sp):
         assert torch.equal(a, b)
 
 
+def test_native_step_driver_captured_in_a_cuda_graph(sp):
+    """sprint_decode_steps captured into a CUDA graph from the caller's
+    stream, the attention combines on the library's side stream included,
+    and replayed: the same attention output, tokens and masked counts as
+    the direct call."""
+    w, pre, steps, make = _decoder_and_steps("prefix-4k")
+    dec = make()
+    r = dec.decode(pre, lambda t: steps[t])
+    torch.cuda.synchronize()
+    O_ref, tok_ref, m_ref = dec.O.clone(), r.tokens.clone(), dec.m_hist.clone()
+    xs = steps
+    args = dict(
+        Q=[x["Q"] for x in xs], Kb=[x["Kb"] for x in xs], Vb=[x["Vb"] for x in xs],
+        h=[x["h"] for x in xs], theta=[x.get("theta") for x in xs],
+        Kf=pre["K"], Vf=pre["V"], prefix_off=dec.prefix_off, max_rows=dec.max_rows,
+        total_rows=dec.total_rows, Kp=dec.Kp, Vp=dec.Vp, kept_off=dec.kept_off,
+        max_kept=dec.max_kept, total_kept=dec.total_kept, W=dec.W, T=dec.T, tau=dec.tau,
+        mode=dec.mode, O=dec.O, conf=dec.conf_blk, argmax=dec.argmax_blk, mask=dec.mask,
+        tokens=dec.tokens, m_hist=dec.m_hist, ws_attn=dec.ws_attn, ws_lm=dec.ws_lm_blk,
+        status=dec.status)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sp.sprint_decode_steps(**args)
+    dec.O.zero_()
+    dec.tokens.fill_(-7)
+    dec.m_hist.fill_(-7)
+    g.replay()
+    torch.cuda.synchronize()
+    assert dec.status.item() == 0
+    assert torch.equal(dec.O, O_ref)
+    assert torch.equal(dec.tokens, tok_ref)
+    assert torch.equal(dec.m_hist, m_ref)
+
+
 def test_native_step_driver_skips_steps_after_the_block_is_done(sp):
     """tau below every confidence: step 0 accepts all LB positions, and the
     kernels of steps 1..T-1 return without touching any output."""
