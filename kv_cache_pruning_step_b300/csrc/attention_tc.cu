@@ -7,12 +7,16 @@
 // Work decomposition (stream-K).  For sequence s the keys of one (layer l,
 // KV head g) pair are ceil(k_s / 128) prefix tiles of 128 keys plus
 // ceil(LB / 128) tiles of the block's own keys.  All tiles of all pairs form
-// one ordered list of T tiles; CTA c (of G = #SMs, one per SM) takes tiles
-// [c T / G, (c+1) T / G).  A CTA's range splits into segments at pair
-// boundaries; each segment writes two unnormalised partials (O rows, row
-// max, row sum; one per softmax warpgroup) into slots 2 * slot + {0, 1} with
-// slot = pair(x) + min(G, ceil((x+1) G / T)) - 1 (x = the segment's first
-// tile), which is unique over all segments and below #pairs + G.
+// one ordered list of T tiles, split over G CTAs (one per SM) in contiguous
+// ranges.  The split charges every pair start kPairCost tiles: tile x of
+// pair p sits at virtual position v(x) = x + kPairCost (p + 1) of VT = T +
+// kPairCost #pairs, and CTA c takes the tiles with v(x) in [c VT / G,
+// (c+1) VT / G), so a CTA whose range takes in a pair start gets fewer tiles.
+// A CTA's range splits into segments at pair boundaries; each segment writes
+// two unnormalised partials (O rows, row max, row sum; one per softmax
+// warpgroup) into slots 2 * slot + {0, 1} with slot = pair(x) + min(G,
+// ceil((v(x)+1) G / VT)) - 1 (x = the segment's first tile, the second term
+// its CTA), which is unique over all segments and below #pairs + G.
 // attn_tc_combine_kernel enumerates the segments of every pair the same way
 // and merges them in tile order.
 //
@@ -173,14 +177,44 @@ __device__ __forceinline__ int seq_of(const int *ts, int S, int x) {
   return lo;
 }
 
-__device__ __forceinline__ long long starts_le(long long x, int G, long long T) {
-  long long c = ((x + 1) * G + T - 1) / T;
+// Number of CTAs c in [0, G) whose virtual range starts at or below
+// virtual position v: floor(c VT / G) <= v.
+__device__ __forceinline__ long long starts_le(long long v, int G, long long VT) {
+  long long c = ((v + 1) * G + VT - 1) / VT;
   return c < G ? c : G;
+}
+
+// Cost-aware split.  Every pair start costs a CTA about kPairCost tiles'
+// time (its query load, the pipeline refill and the partials' write), so the
+// list is split over a virtual axis on which pair p takes kPairCost + n_p
+// positions: kPairCost for its start, then one per tile.  Tile x of pair p
+// sits at v(x) = x + kPairCost (p + 1); CTA c takes the virtual range
+// [c VT / G, (c+1) VT / G) and with it the tiles whose v(x) fall there.
+constexpr int kPairCost = 6;
+
+__device__ __forceinline__ long long virt_total(const Problem &pb, long long T) {
+  return T + (long long)kPairCost * pb.S * pb.NL * pb.Hkv;
+}
+
+// Number of tiles x with v(x) < v, for 0 <= v <= VT: the first real tile of
+// the CTA whose virtual range starts at v.
+__device__ __forceinline__ int real_of(const Problem &pb, const int *ts, const int *nt,
+                                       long long v) {
+  const long long per_seq = (long long)pb.NL * pb.Hkv;
+  int lo = 0, hi = pb.S - 1;  // the last sequence whose virtual start is <= v
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (ts[mid] + kPairCost * per_seq * mid <= v) lo = mid; else hi = mid - 1;
+  }
+  const long long y = v - (ts[lo] + kPairCost * per_seq * lo);
+  const long long span = nt[lo] + kPairCost;
+  const long long pis = y / span, rem = y - pis * span;
+  return (int)(ts[lo] + pis * nt[lo] + (rem > kPairCost ? rem - kPairCost : 0));
 }
 
 __device__ __forceinline__ Seg locate(const Problem &pb, const int *ts, const int *nt,
                                       const int *ks, const int *k0, int x, int end, int G,
-                                      int T) {
+                                      long long VT) {
   Seg sg;
   sg.s = seq_of(ts, pb.S, x);
   const int y = x - ts[sg.s];
@@ -194,7 +228,7 @@ __device__ __forceinline__ Seg locate(const Problem &pb, const int *ts, const in
   sg.ntile = min(end, pair_end) - x;
   sg.kv0 = k0[sg.s];
   sg.k_s = ks[sg.s];
-  sg.slot = sg.pair + (int)starts_le(x, G, T) - 1;
+  sg.slot = sg.pair + (int)starts_le(x + (long long)kPairCost * (sg.pair + 1), G, VT) - 1;
   return sg;
 }
 
@@ -365,8 +399,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   // Decode: a contiguous range of the tile list (stream-K).  Prefix mode:
   // units blockIdx.x, blockIdx.x + G, ... (whole key ranges).
   const int T = ts[pb.S];
-  const int x_begin = kPrefix ? (int)blockIdx.x : (int)((long long)blockIdx.x * T / G);
-  const int x_end = kPrefix ? T : (int)((long long)(blockIdx.x + 1) * T / G);
+  const long long VT = kPrefix ? T : virt_total(pb, T);
+  const int x_begin =
+      kPrefix ? (int)blockIdx.x : real_of(pb, ts, nt, (long long)blockIdx.x * VT / G);
+  const int x_end = kPrefix ? T : real_of(pb, ts, nt, (long long)(blockIdx.x + 1) * VT / G);
   const uint32_t sQ = tc::smem_u32(smem + L::OFF_Q);
   const uint32_t sKV = tc::smem_u32(smem + L::OFF_KV);
   const float qk_scale = kLog2e * rsqrtf((float)D);
@@ -378,7 +414,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   for (int x = x_begin; x < x_end; ++seg_no) {
     const Seg sg = kPrefix ? locate_prefix(pb, ts, nt, ks, k0, x)
-                           : locate(pb, ts, nt, ks, k0, x, x_end, G, T);
+                           : locate(pb, ts, nt, ks, k0, x, x_end, G, VT);
     x += kPrefix ? G : sg.ntile;
     const int np = (sg.k_s + TILE - 1) / TILE;  // prefix tiles of the pair
     const bool run = !*abort_flag;
@@ -838,16 +874,20 @@ attn_tc_combine_kernel(Problem pb, int G, __nv_bfloat16 *__restrict__ O, AttnRes
   const int per_seq = pb.NL * pb.Hkv;
   const int s = pair / per_seq, pis = pair % per_seq;
   const int l = pis / pb.Hkv, g = pis % pb.Hkv;
-  const long long T = ts[pb.S];
+  const long long VT = virt_total(pb, ts[pb.S]);
   const int p0 = ts[s] + pis * nt[s], p1 = p0 + nt[s];
-  // The CTAs whose tile ranges meet [p0, p1) are c_first..c_last, and CTA c
-  // wrote this pair's partials into slot pair + c.  When T < G some CTAs
-  // have empty ranges and hold no segment: they are skipped.
-  const int c_first = (int)starts_le(p0, G, T) - 1;
-  const int c_last = (int)starts_le(p1 - 1, G, T) - 1;
-  const bool dense = T >= G;
+  // The CTAs whose tile ranges meet [p0, p1) are c_first..c_last (found from
+  // the tiles' virtual positions), and CTA c wrote this pair's partials into
+  // slot pair + c.  A CTA between them whose virtual range is empty (VT < G)
+  // holds no segment and is skipped; one with a non-empty range there holds
+  // tiles of this pair, since the virtual positions between v(p0) and
+  // v(p1 - 1) are all tiles of it.
+  const long long vp = (long long)kPairCost * (pair + 1);
+  const int c_first = (int)starts_le(p0 + vp, G, VT) - 1;
+  const int c_last = (int)starts_le(p1 - 1 + vp, G, VT) - 1;
+  const bool dense = VT >= G;
   auto holds = [&](int c) {
-    return dense || (long long)c * T / G < (long long)(c + 1) * T / G;
+    return dense || (long long)c * VT / G < (long long)(c + 1) * VT / G;
   };
   // Pass 1: the largest row max over all partials (independent loads).
   float mx = -INFINITY;
