@@ -46,7 +46,15 @@
 //               barrier, so the products of a quarter run while the next is
 //               computed and little of the PV is left once the softmax ends.
 //               At the end of the segment each warpgroup writes its (O_h,
-//               m_h, l_h) partial.
+//               m_h, l_h) partial, O in column quads of 32-row runs so that
+//               every store of a warp is 512 contiguous bytes.
+//
+// Segments of a CTA follow each other without a CTA-wide barrier: the
+// producer loads the next segment's first K/V tile while the last tiles of
+// the current one are still being computed, and its query once the
+// segment's last QK has read Q (q_empty); each warpgroup writes its partial
+// as soon as its own last PV is done (o_full[h]) and goes on to the next
+// segment, whose first PV into its accumulator follows from the P hand-over.
 //
 // Indexed prefix (no compacted copy): the kept rows are gathered from the
 // full cache through the kept indices.  Then warps 0 and 11 each load half
@@ -79,6 +87,9 @@ namespace {
 
 constexpr int TILE = 128;       // keys per tile
 constexpr int MAX_STAGES = 4;   // K/V ring depth at most (as many as fit)
+// mbarriers (21 + 2 MAX_STAGES), the TMEM address and the abort flag share
+// a 256-byte block.
+static_assert((21 + 2 * MAX_STAGES) * 8 + 8 <= 256, "barrier block overflows");
 constexpr int ROWS = 128;       // query rows per MMA tile (LB x G <= 128)
 constexpr int THREADS = 352;
 // The indexed-prefix kernel adds a second gathering warp; 384 threads still
@@ -185,12 +196,13 @@ __device__ __forceinline__ long long starts_le(long long v, int G, long long VT)
 }
 
 // Cost-aware split.  Every pair start costs a CTA about kPairCost tiles'
-// time (its query load, the pipeline refill and the partials' write), so the
+// time (its query load behind the last QK of the previous pair, the first
+// tiles of a fresh softmax and the partials' write), so the
 // list is split over a virtual axis on which pair p takes kPairCost + n_p
 // positions: kPairCost for its start, then one per tile.  Tile x of pair p
 // sits at v(x) = x + kPairCost (p + 1); CTA c takes the virtual range
 // [c VT / G, (c+1) VT / G) and with it the tiles whose v(x) fall there.
-constexpr int kPairCost = 6;
+constexpr int kPairCost = 3;
 
 __device__ __forceinline__ long long virt_total(const Problem &pb, long long T) {
   return T + (long long)kPairCost * pb.S * pb.NL * pb.Hkv;
@@ -346,10 +358,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   uint64_t *s_full = kv_empty + MAX_STAGES;      // 2
   uint64_t *p_ready = s_full + 2;                // 8: [warpgroup][key quarter]
   uint64_t *pv_done = p_ready + 8;               // 2
-  uint64_t *o_full = pv_done + 2, *drain = o_full + 1;  // drain[2]: one per issuer
+  // o_full[h]: the segment's last PV of warpgroup h is done (prefix mode:
+  // o_full[0], every PV of the unit).  drain[2]: one per issuer.
+  uint64_t *o_full = pv_done + 2, *drain = o_full + 2;
   uint64_t *never = drain + 2;  // no one arrives: the stall test waits on it
   uint64_t *ml_ready = never + 1;  // 2: prefix mode, a warpgroup's (m, l) are published
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(ml_ready + 2);
+  uint64_t *q_empty = ml_ready + 2;  // decode: the segment's last QK has read Q
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(q_empty + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *ts = reinterpret_cast<int *>(smem + off_bar + 256);
   int *nt = ts + (pb.S + 1), *ks = nt + (pb.S + 1), *k0 = ks + (pb.S + 1);
@@ -380,6 +395,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       tc::mbar_init(tc::smem_u32(pv_done + i), 1);
     }
     tc::mbar_init(tc::smem_u32(o_full), 1);
+    tc::mbar_init(tc::smem_u32(o_full + 1), 1);
+    tc::mbar_init(tc::smem_u32(q_empty), 1);
     tc::mbar_init(tc::smem_u32(drain), 1);
     tc::mbar_init(tc::smem_u32(drain + 1), 1);
     tc::mbar_init(tc::smem_u32(never), 1);
@@ -409,6 +426,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   // Global tile counter (same in every role) and segment counter.
   uint32_t seg_no = 0, tile_no = 0;
+  uint32_t o_phase = 0;  // softmax, decode: segments in which this warpgroup had a tile
   // Producer bookkeeping for the final drain.
   uint32_t issued = 0, last_par = 0, q_issued = 0, q_par = 0;
 
@@ -426,15 +444,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       // Q and the block's own key tiles by TMA (its arrival carries the
       // expected bytes).
       const int gw = warp == 0 ? 0 : 1;
-      if (gw == 0 && lane == 0) {
+      // The query follows the segment's first tile (lane 0 of warp 0 only),
+      // once the previous segment's last QK has read Q.
+      auto load_q = [&]() {
+        if (gw != 0 || lane != 0) return true;
+        if (seg_no > 0 &&
+            !tc::mbar_wait(tc::smem_u32(q_empty), (seg_no - 1) & 1, pb.cap_ns, abort_flag))
+          return false;
         const uint32_t qb = tc::smem_u32(q_full);
         tc::mbar_arrive_expect_tx(qb, (uint32_t)((D / 64) * R * 128));
         const int qrow = (sg.s * pb.NL + sg.l) * pb.LB;
         for (int b = 0; b < D / 64; ++b)
           tc::tma_load_3d(sQ + b * L::QBOX, &tm_q, qb, b * 64, sg.g * GQ, qrow);
-      }
-      q_issued = 1;
-      q_par = seg_no & 1;
+        q_issued = 1;
+        q_par = seg_no & 1;
+        return true;
+      };
       // The sequence's full prefix: rows [pf0, pf1) of every layer.
       int pf0 = __ldg(pb.kvi.prefix_off + sg.s), pf1 = __ldg(pb.kvi.prefix_off + sg.s + 1);
       if (pf0 < 0 || pf1 < pf0 || pf1 > pb.kvi.total_prefix_rows) {
@@ -474,6 +499,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const uint32_t q = tile_no + t;
         const int stage = q % stages;
         const uint32_t ph = (q / stages) & 1;
+        if (t == 1 && !__all_sync(0xffffffffu, load_q())) break;
         if (!__all_sync(0xffffffffu, tc::mbar_wait(tc::smem_u32(kv_empty + stage), ph ^ 1,
                                                    pb.cap_ns, abort_flag)))
           break;
@@ -533,24 +559,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           issued |= 1u << stage;
           last_par = (last_par & ~(1u << stage)) | (ph << stage);
         }
+        if (t == 0 && sg.ntile == 1 && !__all_sync(0xffffffffu, load_q())) break;
       }
       arrive_pending(true);
     } else if (warp == 0 && lane == 0 && run) {
       // ------------------------------------------------ producer
-      const uint32_t qb = tc::smem_u32(q_full);
-      tc::mbar_arrive_expect_tx(qb, (uint32_t)((D / 64) * R * 128));
-      if (kPrefix) {  // 128 prefix positions of head g GQ + hh
-        const int qrow = pb.NL * sg.kv0 + sg.l * sg.k_s + sg.qt * TILE;
-        for (int b = 0; b < D / 64; ++b)
-          tc::tma_load_3d(sQ + b * L::QBOX, &tm_q, qb, b * 64, sg.g * GQ + sg.hh, qrow);
-      } else {
-        const int qrow = (sg.s * pb.NL + sg.l) * pb.LB;
-        for (int b = 0; b < D / 64; ++b)
-          tc::tma_load_3d(sQ + b * L::QBOX, &tm_q, qb, b * 64, sg.g * GQ, qrow);
-      }
-      q_issued = 1;
-      q_par = seg_no & 1;
+      // Decode: the segment's first K/V tile goes out before its query, so
+      // that it loads while the previous segment's last QK still reads Q.
+      auto load_q = [&]() {
+        if (!kPrefix && seg_no > 0 &&
+            !tc::mbar_wait(tc::smem_u32(q_empty), (seg_no - 1) & 1, pb.cap_ns, abort_flag))
+          return false;
+        const uint32_t qb = tc::smem_u32(q_full);
+        tc::mbar_arrive_expect_tx(qb, (uint32_t)((D / 64) * R * 128));
+        if (kPrefix) {  // 128 prefix positions of head g GQ + hh
+          const int qrow = pb.NL * sg.kv0 + sg.l * sg.k_s + sg.qt * TILE;
+          for (int b = 0; b < D / 64; ++b)
+            tc::tma_load_3d(sQ + b * L::QBOX, &tm_q, qb, b * 64, sg.g * GQ + sg.hh, qrow);
+        } else {
+          const int qrow = (sg.s * pb.NL + sg.l) * pb.LB;
+          for (int b = 0; b < D / 64; ++b)
+            tc::tma_load_3d(sQ + b * L::QBOX, &tm_q, qb, b * 64, sg.g * GQ, qrow);
+        }
+        q_issued = 1;
+        q_par = seg_no & 1;
+        return true;
+      };
+      if (kPrefix) load_q();  // never waits in prefix mode
       for (int t = 0; t < sg.ntile; ++t) {
+        if (!kPrefix && t == 1 && !load_q()) break;
         const uint32_t q = tile_no + t;
         const int stage = q % stages;
         const uint32_t ph = (q / stages) & 1;
@@ -575,6 +612,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         issued |= 1u << stage;
         last_par = (last_par & ~(1u << stage)) | (ph << stage);
+        if (!kPrefix && t == 0 && sg.ntile == 1) load_q();
       }
     } else if (warp == 1 && lane == 0 && run) {
       // ------------------------------------------------ QK issuer
@@ -593,9 +631,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const uint32_t q = tile_no + t;
         const int stage = q % stages, h = q & 1;
         const uint32_t ph = (q / stages) & 1;
-        // S[h] also holds P of tile q - 2: its PV must be done first.
+        // S[h] also holds P of tile q - 2, which may belong to the previous
+        // segment: its PV must be done first.
         if (!tc::mbar_wait(tc::smem_u32(kv_full + stage), ph, pb.cap_ns, abort_flag) ||
-            (t >= 2 && !tc::mbar_wait(tc::smem_u32(pv_done + h), ((q >> 1) & 1) ^ 1, pb.cap_ns,
+            (q >= 2 && !tc::mbar_wait(tc::smem_u32(pv_done + h), ((q >> 1) & 1) ^ 1, pb.cap_ns,
                                       abort_flag))) {
           ok = false;
           break;
@@ -612,6 +651,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         tc::mma_commit(tc::smem_u32(s_full + h));
       }
+      // Decode: Q is free for the next segment's query once these QKs are done.
+      if (!kPrefix && ok) tc::mma_commit(tc::smem_u32(q_empty));
     } else if (warp == 10 && lane == 0 && run) {
       // ------------------------------------------------ PV issuer
       // O[h] += P[h] V for every tile (h = q & 1); P is the A operand, read
@@ -652,8 +693,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!ok) break;
         tc::mma_commit(tc::smem_u32(pv_done + h));
         tc::mma_commit(tc::smem_u32(kv_empty + stage));
+        // Decode: warpgroup h's accumulator is final after its last tile of
+        // the segment (u = ntile - 1 or ntile - 2; one of each parity).
+        if (!kPrefix && u >= sg.ntile - 2) tc::mma_commit(tc::smem_u32(o_full + h));
       }
-      if (ok) tc::mma_commit(tc::smem_u32(o_full));
+      if (kPrefix && ok) tc::mma_commit(tc::smem_u32(o_full));
     } else if (warp >= 2 && warp < 10 && run) {
       // ------------------------------------------------ softmax, warpgroup h
       const int h = (warp - 2) >> 2;
@@ -802,21 +846,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         tc::fence_before_sync();
       } else if (!kPrefix && ok &&
-                 __all_sync(0xffffffffu, tc::mbar_wait(tc::smem_u32(o_full), seg_no & 1,
-                                                       pb.cap_ns, abort_flag))) {
+                 (!mine || __all_sync(0xffffffffu,
+                                      tc::mbar_wait(tc::smem_u32(o_full + h), o_phase++ & 1,
+                                                    pb.cap_ns, abort_flag)))) {
+        // o_full[h] completes once per segment in which warpgroup h has a
+        // tile, so its phase counts those segments.
         tc::fence_after_sync();
         const size_t part = (size_t)(2 * sg.slot + h) * ROWS + r;
         if (mine) {
-          float *dst = pb.ws_o + part * D;
+          // Partial O in [part][D/4 column quads][ROWS rows]: the warp's 32
+          // rows of one quad are 512 contiguous bytes, so every store below
+          // is coalesced (one row per thread, as tensor memory hands it out).
+          float4 *dst = reinterpret_cast<float4 *>(pb.ws_o) +
+                        (size_t)(2 * sg.slot + h) * (D / 4) * ROWS + r;
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             float o[32];
             tc::tmem_ld32(o_addr + c * 32, o);
             if (r < R) {
 #pragma unroll
-              for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4 *>(dst + c * 32 + j) =
-                    make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+              for (int j = 0; j < 8; ++j)
+                dst[(size_t)(c * 8 + j) * ROWS] =
+                    make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
             }
           }
         }
@@ -826,9 +877,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
     }
     tile_no += sg.ntile;
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
+    // Prefix mode: the next unit's query lands where the (m, l) of this one
+    // were exchanged, so every role finishes the unit first.  Decode roles
+    // run on into the next segment; their hand-overs are the barriers above
+    // (the K/V ring, q_empty, pv_done and o_full).
+    if (kPrefix) {
+      tc::fence_before_sync();
+      __syncthreads();
+      tc::fence_after_sync();
+    }
   }
 
   // Drain: no copy or MMA of this CTA may be in flight when it exits.  These
@@ -855,22 +912,30 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (warp == 1) tc::tmem_dealloc(tmem, 512);
 }
 
-// One warp per (pair, query row): merge both warpgroup partials of every
-// segment of the pair in tile order (max of the row maxima, then the
-// weighted sums).
+// One CTA per (pair, group of 32 query rows): merge both warpgroup partials
+// of every segment of the pair in tile order (max of the row maxima, then
+// the weighted sums).  Lane i of every warp takes row 32 group + i, and warp
+// w the column quads [w D/32, (w+1) D/32), so each load of a partial reads
+// the 512 contiguous bytes that one warp of the chunk kernel stored.  The
+// bf16 rows go out through shared memory, 16 bytes per thread and store.
 template <int D>
 __global__ void __launch_bounds__(256)
 attn_tc_combine_kernel(Problem pb, int G, __nv_bfloat16 *__restrict__ O, AttnResidual res) {
   if (gate_closed(pb.gate)) return;
+  constexpr int C4 = D / 4;       // float4 column quads of a row
+  constexpr int PER = C4 / 8;     // quads of one warp
+  constexpr int PITCH = D + 8;    // bf16 row pitch of the staging tile (16-byte multiple)
   __shared__ int ts[MAX_SEQ + 1], nt[MAX_SEQ + 1], ks[MAX_SEQ + 1], k0[MAX_SEQ + 1];
+  __shared__ __align__(16) __nv_bfloat16 tile[32 * PITCH];
   build_seq_tables(pb, ts, nt, ks, k0, nullptr);
   __syncthreads();
   const int GQ = pb.Hq / pb.Hkv, R = pb.LB * GQ;
-  const int lane = threadIdx.x & 31;
-  const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long pairs = (long long)pb.S * pb.NL * pb.Hkv;
-  if (w >= pairs * R) return;
-  const int pair = (int)(w / R), r = (int)(w % R);
+  const int groups = (R + 31) / 32;
+  const int pair = (int)(blockIdx.x / groups), rg = (int)(blockIdx.x % groups);
+  if (pair >= pb.S * pb.NL * pb.Hkv) return;  // whole CTA
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = rg * 32 + lane;
+  const bool live = r < R;
   const int per_seq = pb.NL * pb.Hkv;
   const int s = pair / per_seq, pis = pair % per_seq;
   const int l = pis / pb.Hkv, g = pis % pb.Hkv;
@@ -889,52 +954,103 @@ attn_tc_combine_kernel(Problem pb, int G, __nv_bfloat16 *__restrict__ O, AttnRes
   auto holds = [&](int c) {
     return dense || (long long)c * VT / G < (long long)(c + 1) * VT / G;
   };
-  // Pass 1: the largest row max over all partials (independent loads).
-  float mx = -INFINITY;
+  const float2 *ml_all = reinterpret_cast<const float2 *>(pb.ws_ml);
+  const float4 *o_all = reinterpret_cast<const float4 *>(pb.ws_o);
+  float acc[4 * PER];
+#pragma unroll
+  for (int q = 0; q < 4 * PER; ++q) acc[q] = 0.f;
+  float den = 0.f;
+  if (live) {
+    // Pass 1: the largest row max over all partials (independent loads).
+    float mx = -INFINITY;
 #pragma unroll 4
-  for (int c = c_first; c <= c_last; ++c) {
-    if (!holds(c)) continue;
-    const size_t part = (size_t)(2 * (pair + c)) * ROWS + r;
-    mx = fmaxf(mx, fmaxf(pb.ws_ml[part * 2], pb.ws_ml[(part + ROWS) * 2]));
-  }
-  // Pass 2: weighted sum of the partials in tile order.
-  float den = 0.f, acc[D / 32];
-#pragma unroll
-  for (int q = 0; q < D / 32; ++q) acc[q] = 0.f;
+    for (int c = c_first; c <= c_last; ++c) {
+      if (!holds(c)) continue;
+      const size_t part = (size_t)(2 * (pair + c)) * ROWS + r;
+      mx = fmaxf(mx, fmaxf(ml_all[part].x, ml_all[part + ROWS].x));
+    }
+    // Pass 2: weighted sum of the partials in tile order.
 #pragma unroll 2
-  for (int c = c_first; c <= c_last; ++c) {
-    if (!holds(c)) continue;
+    for (int c = c_first; c <= c_last; ++c) {
+      if (!holds(c)) continue;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const size_t part = (size_t)(2 * (pair + c) + h) * ROWS + r;
-      const float2 ml = *reinterpret_cast<const float2 *>(pb.ws_ml + part * 2);
-      const float *oc = pb.ws_o + part * D;
-      // A warpgroup that saw no key of the segment left m = -inf: weight 0.
-      const float wgt = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mx);
-      den = fmaf(wgt, ml.x == -INFINITY ? 0.f : ml.y, den);
+      for (int h = 0; h < 2; ++h) {
+        const size_t pidx = (size_t)(2 * (pair + c) + h);
+        const float2 ml = ml_all[pidx * ROWS + r];
+        // A warpgroup that saw no key of the segment left m = -inf: weight 0.
+        const bool none = ml.x == -INFINITY;
+        const float wgt = none ? 0.f : exp2f(ml.x - mx);
+        den = fmaf(wgt, none ? 0.f : ml.y, den);
+        const float4 *oc = o_all + (pidx * C4 + (size_t)warp * PER) * ROWS + r;
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        const float o = oc[lane + 32 * q];
-        acc[q] = fmaf(wgt, ml.x == -INFINITY ? 0.f : o, acc[q]);
+        for (int k = 0; k < PER; ++k) {
+          const float4 o = oc[(size_t)k * ROWS];
+          acc[4 * k + 0] = fmaf(wgt, none ? 0.f : o.x, acc[4 * k + 0]);
+          acc[4 * k + 1] = fmaf(wgt, none ? 0.f : o.y, acc[4 * k + 1]);
+          acc[4 * k + 2] = fmaf(wgt, none ? 0.f : o.z, acc[4 * k + 2]);
+          acc[4 * k + 3] = fmaf(wgt, none ? 0.f : o.w, acc[4 * k + 3]);
+        }
       }
     }
-  }
-  const int j = r / GQ, hh = r % GQ;
-  __nv_bfloat16 *dst =
-      O + (((size_t)(s * pb.NL + l) * pb.LB + j) * pb.Hq + (size_t)(g * GQ + hh)) * D;
-  const float inv = 1.0f / den;
-  // Residual epilogue on the last layer: h_out[s][j] = h_in[s][j] + O (heads
-  // concatenated), from O as stored (bf16).
-  const bool last = res.h_out && l == pb.NL - 1;
-  const size_t hat = (((size_t)s * pb.LB + j) * pb.Hq + (size_t)(g * GQ + hh)) * D;
+    const float inv = 1.0f / den;
 #pragma unroll
-  for (int q = 0; q < D / 32; ++q) {
-    const __nv_bfloat16 o = __float2bfloat16_rn(acc[q] * inv);
-    dst[lane + 32 * q] = o;
-    if (last)
-      static_cast<__nv_bfloat16 *>(res.h_out)[hat + lane + 32 * q] = __float2bfloat16_rn(
-          __bfloat162float(static_cast<const __nv_bfloat16 *>(res.h_in)[hat + lane + 32 * q]) +
-          __bfloat162float(o));
+    for (int k = 0; k < PER; ++k) {
+      __nv_bfloat162 a = __floats2bfloat162_rn(acc[4 * k] * inv, acc[4 * k + 1] * inv);
+      __nv_bfloat162 b = __floats2bfloat162_rn(acc[4 * k + 2] * inv, acc[4 * k + 3] * inv);
+      uint2 v;
+      v.x = *reinterpret_cast<uint32_t *>(&a);
+      v.y = *reinterpret_cast<uint32_t *>(&b);
+      *reinterpret_cast<uint2 *>(tile + lane * PITCH + (warp * PER + k) * 4) = v;
+    }
+  }
+  __syncthreads();
+  // Rows out: O[s][l][j][g GQ + hh][:] for row r = j GQ + hh, 16 bytes per
+  // thread.  Residual epilogue on the last layer: h_out[s][j] = h_in[s][j] +
+  // O (heads concatenated), from O as stored (bf16).
+  constexpr int V16 = D / 8;  // 16-byte pieces of a row
+  const bool last = res.h_out && l == pb.NL - 1;
+  const __nv_bfloat16 *h_in = static_cast<const __nv_bfloat16 *>(res.h_in);
+  __nv_bfloat16 *h_out = static_cast<__nv_bfloat16 *>(res.h_out);
+  // The caller's buffers need only bf16 alignment: 16-byte stores only when
+  // every one of them allows it (the same for the whole grid).
+  const bool vec = ((reinterpret_cast<uintptr_t>(O) |
+                     (last ? reinterpret_cast<uintptr_t>(h_in) | reinterpret_cast<uintptr_t>(h_out)
+                           : 0)) & 15) == 0;
+  for (int idx = threadIdx.x; idx < 32 * V16; idx += blockDim.x) {
+    const int rr = idx / V16, v = idx % V16, row = rg * 32 + rr;
+    if (row >= R) continue;
+    const int j = row / GQ, hh = row % GQ;
+    const uint4 val = *reinterpret_cast<const uint4 *>(tile + rr * PITCH + v * 8);
+    const __nv_bfloat16 *oi = reinterpret_cast<const __nv_bfloat16 *>(&val);
+    __nv_bfloat16 *dst =
+        O + (((size_t)(s * pb.NL + l) * pb.LB + j) * pb.Hq + (size_t)(g * GQ + hh)) * D + v * 8;
+    if (vec) {
+      *reinterpret_cast<uint4 *>(dst) = val;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dst[e] = oi[e];
+    }
+    if (last) {
+      const size_t hat = (((size_t)s * pb.LB + j) * pb.Hq + (size_t)(g * GQ + hh)) * D + v * 8;
+      uint4 hin, out;
+      __nv_bfloat16 *hi = reinterpret_cast<__nv_bfloat16 *>(&hin);
+      __nv_bfloat16 *ho = reinterpret_cast<__nv_bfloat16 *>(&out);
+      if (vec) {
+        hin = *reinterpret_cast<const uint4 *>(h_in + hat);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) hi[e] = h_in[hat + e];
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        ho[e] = __float2bfloat16_rn(__bfloat162float(hi[e]) + __bfloat162float(oi[e]));
+      if (vec) {
+        *reinterpret_cast<uint4 *>(h_out + hat) = out;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) h_out[hat + e] = ho[e];
+      }
+    }
   }
 }
 
@@ -1040,7 +1156,6 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
   else
     attn_tc_kernel<D, false, false><<<G, THREADS, smem, stream>>>(tq, tkp, tvp, tkb, tvb, pb);
   if (launch_status() != SPRINT_OK) return SPRINT_ERR_CUDA;
-  const long long warps = (long long)pairs * LB * GQ;
   cudaStream_t cs = stream;
   if (side.side) {  // the combine on the side stream, after the chunk kernel
     if (cudaEventRecord(side.fork, stream) != cudaSuccess ||
@@ -1048,7 +1163,7 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
       return SPRINT_ERR_CUDA;
     cs = side.side;
   }
-  attn_tc_combine_kernel<D><<<(int)((warps * 32 + 255) / 256), 256, 0, cs>>>(
+  attn_tc_combine_kernel<D><<<(int)(pairs * ((LB * GQ + 31) / 32)), 256, 0, cs>>>(
       pb, G, static_cast<__nv_bfloat16 *>(O), res);
   const int rc = launch_status();
   if (rc == SPRINT_OK && side.side && cudaEventRecord(side.join, side.side) != cudaSuccess)

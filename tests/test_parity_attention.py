@@ -62,6 +62,28 @@ def test_fuzz_ragged(sp, dtype, Hq, Hkv, d, LB):
     check(w, prefixes, steps, O, what=f"{dtype} {Hq}/{Hkv}/{d}/{LB}")
 
 
+@pytest.mark.parametrize("d,LB,Hq,Hkv", [(128, 32, 16, 4), (64, 7, 6, 2)])
+def test_output_buffer_with_bf16_alignment_only(sp, d, LB, Hq, Hkv):
+    """O may start at any bf16 element: the combine then stores element by
+    element, with the same bits as into a 16-byte aligned buffer."""
+    w = small_workload(dtype="bf16", NL=2, Hq=Hq, Hkv=Hkv, d=d, LB=LB, n=900, n_img=300, seed=23)
+    pre = prefix_inputs(w, device=DEV)
+    x = step_inputs(w, 0, 0, 1, device=DEV)
+    O = run_attn(sp, w, [pre], [x])
+    cat = gc.concat_prefixes([pre])
+    buf = torch.full((O.numel() + 1,), float("nan"), dtype=O.dtype, device=DEV)
+    O1 = buf[1:].view(O.shape)
+    assert O1.data_ptr() % 16 != 0
+    status = sp.new_status(DEV)
+    sp.sprint_block_attn(x["Q"][None].contiguous(), cat["K"], cat["V"], cat["off"], 900, 900,
+                         x["Kb"][None].contiguous(), x["Vb"][None].contiguous(), O=O1,
+                         status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert torch.equal(O1, O)
+    assert torch.isnan(buf[0])
+
+
 def test_identical_keys_average_values(sp):
     w = small_workload(dtype="f32", NL=1, Hq=4, Hkv=2, d=64, LB=8, n=50, n_img=0)
     pre = prefix_inputs(w, device=DEV)
