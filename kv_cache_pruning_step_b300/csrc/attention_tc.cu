@@ -140,33 +140,66 @@ struct Problem {
                                 // (layer, query head, 128-row query tile), whole key range)
 };
 
-// Per-sequence tables: ts[s] = first global tile of sequence s; nt[s] =
-// tiles per (layer, KV head) pair = ceil(k_s/64) + ceil(LB/64); ks[s] =
-// prefix keys (0 when the offsets are invalid); k0[s] = kv_off[s].
+// Per-sequence tables: ts[s] = first global unit of sequence s (decode: its
+// first tile); nt[s] = tiles per (layer, KV head) pair = ceil(k_s / TILE) +
+// ceil(LB / TILE) (prefix mode: ceil(k_s / TILE)); ks[s] = prefix keys (0
+// when the offsets are invalid); k0[s] = kv_off[s].
+//
+// kParallel (decode and the combine): one thread per sequence reads its
+// offsets, and warp 0 turns the per-sequence unit counts into ts by an
+// exclusive scan (each lane over a contiguous run of sequences); every
+// thread of the CTA calls it.  Otherwise thread 0 walks the sequences (the
+// prefix self-attention's units are long, and its registers are tight).
+template <bool kParallel>
 __device__ void build_seq_tables(const Problem &pb, int *ts, int *nt, int *ks, int *k0,
                                  int32_t *status) {
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    bool bad = false;
-    for (int s = 0; s < pb.S; ++s) {
-      int a = pb.kv_off[s], b = pb.kv_off[s + 1];
-      int k = b - a;
-      if (a < 0 || k < 0 || b > pb.total_kv_rows) { bad = true; k = 0; a = 0; }
-      ts[s] = acc;
-      ks[s] = k;
-      k0[s] = a;
-      if (pb.prefix) {
-        // units: (layer, KV head, query tile, head of the group); the key
-        // tiles of a unit are all ceil(k / TILE) prefix tiles
-        nt[s] = (k + TILE - 1) / TILE;
-        acc += pb.NL * pb.Hkv * (pb.Hq / pb.Hkv) * nt[s];
-      } else {
-        nt[s] = (k + TILE - 1) / TILE + (pb.LB + TILE - 1) / TILE;
-        acc += pb.NL * pb.Hkv * nt[s];
+  const int per_pair = pb.prefix ? pb.NL * pb.Hkv * (pb.Hq / pb.Hkv) : pb.NL * pb.Hkv;
+  // Prefix mode: units (layer, KV head, query tile, head of the group) of
+  // ceil(k / TILE) key tiles each; decode: the prefix tiles and the block's
+  // own key tiles of every (layer, KV head) pair.
+  auto seq = [&](int s, bool &bad) {
+    int a = pb.kv_off[s], b = pb.kv_off[s + 1];
+    int k = b - a;
+    if (a < 0 || k < 0 || b > pb.total_kv_rows) { bad = true; k = 0; a = 0; }
+    ks[s] = k;
+    k0[s] = a;
+    nt[s] = pb.prefix ? (k + TILE - 1) / TILE : (k + TILE - 1) / TILE + (pb.LB + TILE - 1) / TILE;
+  };
+  if (!kParallel) {
+    if (threadIdx.x == 0) {
+      int acc = 0;
+      bool bad = false;
+      for (int s = 0; s < pb.S; ++s) {
+        seq(s, bad);
+        ts[s] = acc;
+        acc += per_pair * nt[s];
       }
+      ts[pb.S] = acc;
+      if (bad && blockIdx.x == 0) report(status, SPRINT_STATUS_BAD_OFFSETS);
     }
-    ts[pb.S] = acc;
-    if (bad && blockIdx.x == 0) report(status, SPRINT_STATUS_BAD_OFFSETS);
+    return;
+  }
+  bool bad = false;
+  for (int s = threadIdx.x; s < pb.S; s += blockDim.x) seq(s, bad);
+  if (bad && blockIdx.x == 0) report(status, SPRINT_STATUS_BAD_OFFSETS);
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int run = (pb.S + 31) / 32, lo = min(pb.S, lane * run), hi = min(pb.S, lo + run);
+    int sum = 0;
+    for (int s = lo; s < hi; ++s) sum += per_pair * nt[s];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int acc = incl - sum;
+    for (int s = lo; s < hi; ++s) {
+      ts[s] = acc;
+      acc += per_pair * nt[s];
+    }
+    if (lane == 31) ts[pb.S] = incl;
   }
 }
 
@@ -381,7 +414,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   for (int i = threadIdx.x * 16; i < off_bar; i += (int)blockDim.x * 16)
     *reinterpret_cast<uint4 *>(smem + i) = make_uint4(0, 0, 0, 0);
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  build_seq_tables(pb, ts, nt, ks, k0, pb.status);
+  build_seq_tables<!kPrefix>(pb, ts, nt, ks, k0, pb.status);
   if (threadIdx.x == 0) {
     tc::mbar_init(tc::smem_u32(q_full), 1);
     for (int i = 0; i < MAX_STAGES; ++i) {
@@ -915,19 +948,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 // One CTA per (pair, group of 32 query rows): merge both warpgroup partials
 // of every segment of the pair in tile order (max of the row maxima, then
 // the weighted sums).  Lane i of every warp takes row 32 group + i, and warp
-// w the column quads [w D/32, (w+1) D/32), so each load of a partial reads
-// the 512 contiguous bytes that one warp of the chunk kernel stored.  The
-// bf16 rows go out through shared memory, 16 bytes per thread and store.
-template <int D>
-__global__ void __launch_bounds__(256)
+// w the column quads [w PER, (w+1) PER), so each load of a partial reads the
+// 512 contiguous bytes that one warp of the chunk kernel stored.  PER = 1
+// (D/4 warps) spreads few pairs over many warps; with many pairs, eight
+// warps of D/32 quads each keep more loads in flight per thread and read
+// the row maxima fewer times.  The bf16 rows go out through shared memory,
+// 16 bytes per thread and store.
+template <int D, int PER> constexpr int combine_threads() { return 32 * (D / 4) / PER; }
+
+template <int D, int PER>
+__global__ void __launch_bounds__(combine_threads<D, PER>())
 attn_tc_combine_kernel(Problem pb, int G, __nv_bfloat16 *__restrict__ O, AttnResidual res) {
   if (gate_closed(pb.gate)) return;
   constexpr int C4 = D / 4;       // float4 column quads of a row
-  constexpr int PER = C4 / 8;     // quads of one warp
   constexpr int PITCH = D + 8;    // bf16 row pitch of the staging tile (16-byte multiple)
   __shared__ int ts[MAX_SEQ + 1], nt[MAX_SEQ + 1], ks[MAX_SEQ + 1], k0[MAX_SEQ + 1];
   __shared__ __align__(16) __nv_bfloat16 tile[32 * PITCH];
-  build_seq_tables(pb, ts, nt, ks, k0, nullptr);
+  build_seq_tables<true>(pb, ts, nt, ks, k0, nullptr);
   __syncthreads();
   const int GQ = pb.Hq / pb.Hkv, R = pb.LB * GQ;
   const int groups = (R + 31) / 32;
@@ -1163,8 +1200,15 @@ int launch(const __nv_bfloat16 *Q, const __nv_bfloat16 *Kp, const __nv_bfloat16 
       return SPRINT_ERR_CUDA;
     cs = side.side;
   }
-  attn_tc_combine_kernel<D><<<(int)(pairs * ((LB * GQ + 31) / 32)), 256, 0, cs>>>(
-      pb, G, static_cast<__nv_bfloat16 *>(O), res);
+  // Few CTAs (a few sequences): one warp per column quad; many: eight warps.
+  const long long ctas = (long long)pairs * ((LB * GQ + 31) / 32);
+  constexpr int kWide = D / 32;
+  if (ctas >= 2 * (long long)G)
+    attn_tc_combine_kernel<D, kWide><<<(int)ctas, combine_threads<D, kWide>(), 0, cs>>>(
+        pb, G, static_cast<__nv_bfloat16 *>(O), res);
+  else
+    attn_tc_combine_kernel<D, 1><<<(int)ctas, combine_threads<D, 1>(), 0, cs>>>(
+        pb, G, static_cast<__nv_bfloat16 *>(O), res);
   const int rc = launch_status();
   if (rc == SPRINT_OK && side.side && cudaEventRecord(side.join, side.side) != cudaSuccess)
     return SPRINT_ERR_CUDA;
