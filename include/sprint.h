@@ -332,7 +332,8 @@ int sprint_compact_kv(const void *K, const void *V, int S,
  *   max_kv_rows  max_s k_s (host; sizes the launch)
  *   total_kv_rows kv_off[S] (host; bounds the reads)
  *   Kb, Vb       [S][NL][LB][Hkv][d] the block's own keys/values
- *   O            OUT [S][NL][LB][Hq][d] (dtype)
+ *   O            OUT [S][NL][LB][Hq][d] (dtype); element alignment suffices
+ *                (16-byte aligned O is written with 16-byte stores)
  *   ws           workspace of sprint_block_attn_workspace_bytes(...)
  *
  * d in {64, 128}; Hq % Hkv == 0; LB * Hq / Hkv <= 128 for bf16.
