@@ -762,14 +762,19 @@ def run_sequential(args):
                        indexed=args.prefix_layout == "indexed")
 
     def one_pass(cache):
-        n_steps, prev = 0, 0
+        # Blocks are enqueued without waiting: block b's step count is read
+        # after block b+1 is on the stream, so the GPU never waits for the
+        # host between blocks (the blocks still run in stream order).
+        n_steps, prev, pend = 0, 0, None
         for b in range(w.blocks):
             dec.set_prefix(counts[b])
-            res = dec.decode(pres[b], lambda t, s=steps[b]: s[t],
-                             conf_from=prev if cache and b > 0 else 0)
-            n_steps += res.steps
+            cur = dec.decode(pres[b], lambda t, s=steps[b]: s[t],
+                             conf_from=prev if cache and b > 0 else 0, wait=False)
+            if pend is not None:
+                n_steps += dec.finish(pend).steps
+            pend = cur
             prev = dec.total_rows
-        return n_steps
+        return n_steps + dec.finish(pend).steps
 
     for _ in range(args.warmup):
         one_pass(True)

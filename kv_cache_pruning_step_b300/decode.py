@@ -170,6 +170,13 @@ class BlockDecoder:
             self._cap[name] = t
         return t[:numel]
 
+    def _dev_ints(self, values):
+        """An int32 device tensor of host ints, copied from pinned memory on
+        the current stream without waiting for the GPU (a blocking copy
+        from pageable memory would wait for every block still in flight)."""
+        host = torch.tensor(values, dtype=torch.int32).pin_memory()
+        return host.to(self.dev, non_blocking=True)
+
     def set_prefix(self, modality_counts, pool_sizes=None):
         """(Re)target the decoder to prefixes with these (n_text, n_image)
         counts per sequence (the number of sequences is fixed).  Buffers
@@ -199,7 +206,7 @@ class BlockDecoder:
                          for ps in pool_sizes]
             self.n_pools = len(table[0])
             kept = [sum(row) for row in table]
-            self.keep = torch.tensor(table, dtype=torch.int32, device=self.dev).reshape(-1)
+            self.keep = self._dev_ints([c for row in table for c in row])
         self.prefix_off_host = [0]
         self.kept_off_host = [0]
         for n, k in zip(lens, kept):
@@ -209,9 +216,8 @@ class BlockDecoder:
         self.total_kept = self.kept_off_host[-1]
         self.max_rows = max(lens) if lens else 0
         self.max_kept = max(kept) if kept else 0
-        i32 = dict(dtype=torch.int32, device=self.dev)
-        self.prefix_off = torch.tensor(self.prefix_off_host, **i32)
-        self.kept_off = torch.tensor(self.kept_off_host, **i32)
+        self.prefix_off = self._dev_ints(self.prefix_off_host)
+        self.kept_off = self._dev_ints(self.kept_off_host)
         dt = self._dt = sp.BF16 if self.dtype == torch.bfloat16 else sp.F32
         u8 = torch.uint8
         # step-0 prefix pass

@@ -183,3 +183,48 @@ def test_sequential_prefix_confidence_cache_is_bit_exact(sp):
     assert cached.steps == fresh.steps and torch.equal(cached.tokens, fresh.tokens)
     # the cached decode ran step 0's block LM head within the prefix call
     assert cached.accepted_per_step == fresh.accepted_per_step
+
+
+def test_sequential_blocks_enqueued_without_waiting(sp):
+    """Consecutive blocks of one sequence enqueued with decode(wait=False)
+    (set_prefix between them copies its tables without waiting for the GPU)
+    decode exactly as the same blocks decoded one at a time."""
+    from kv_cache_pruning_step_b300 import BlockDecoder
+    w = WORKLOADS["sequential-64-blocks"]
+    W, _ = weights_of(w.name)
+    blocks = [30, 31, 32, 33]
+    pres = [prefix_inputs(w, seq=0, block=b, device=DEV) for b in blocks]
+    counts = [[(int((p["modality"] == 0).sum()), int((p["modality"] != 0).sum()))] for p in pres]
+    xss = [[step_inputs(w, 0, b, t, device=DEV) for t in range(w.T)] for b in blocks]
+
+    def steps_of(i):
+        xs = xss[i]
+        return lambda t: {"Q": xs[t]["Q"][None].contiguous(), "Kb": xs[t]["Kb"][None].contiguous(),
+                          "Vb": xs[t]["Vb"][None].contiguous(), "h": xs[t]["h"],
+                          "theta": xs[t]["theta"]}
+
+    def make():
+        return BlockDecoder(W, NL=w.NL, Hq=w.Hq, Hkv=w.Hkv, d=w.d, LB=w.LB, T=w.T, tau=w.tau,
+                            r_text=w.r_text, r_img=w.r_img, alpha=w.alpha,
+                            modality_counts=counts[-1])
+
+    def run(wait):
+        dec = make()
+        out, pend, prev = [], [], 0
+        for i in range(len(blocks)):
+            dec.set_prefix(counts[i])
+            r = dec.decode(pres[i], steps_of(i), conf_from=prev, wait=wait)
+            # the live token buffer is the next block's: copy it on the stream
+            out.append([r, dec.tokens.clone(), dec.conf_prefix.clone(), dec.kept_idx.clone()])
+            prev = dec.total_rows
+        res = [dec.finish(r) if not wait else r for r, *_ in out]
+        torch.cuda.synchronize()
+        assert dec.status.item() == 0
+        return [(r.steps, r.accepted_per_step, tok, conf, kept)
+                for r, (_, tok, conf, kept) in zip(res, out)]
+
+    a, b = run(True), run(False)
+    for i, (x, y) in enumerate(zip(a, b)):
+        assert x[0] == y[0] and x[1] == y[1], f"block {blocks[i]}"
+        for u, v in zip(x[2:], y[2:]):
+            assert torch.equal(u, v), f"block {blocks[i]}"
