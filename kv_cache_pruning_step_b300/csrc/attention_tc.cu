@@ -330,6 +330,28 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return r;
 }
 
+// Two f32 lanes in one 64-bit register pair (Blackwell's packed FP32 path:
+// one fma / add instruction for both lanes, each lane rounded as the scalar
+// instruction would round it).
+__device__ __forceinline__ uint64_t pack2(float x, float y) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float &x, float &y) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // Tensor-memory stores, each waited for in the same statement: tcgen05.st
 // reads its source registers asynchronously until tcgen05.wait::st, and the
 // compiler, seeing the registers as read by the store itself, may reuse
@@ -796,7 +818,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           }
         }
         const float nm = -m_used;
-        float lsum = 0.f;
+        // Exponent arguments s * log2e/sqrt(d) - m two keys per instruction
+        // (each lane one fma, as fmaf), and the row sum in two lanes (even
+        // and odd keys), added at the end of the tile.
+        const uint64_t scale2 = pack2(qk_scale, qk_scale), nm2 = pack2(nm, nm);
+        uint64_t lsum2 = pack2(0.f, 0.f);
         // Decode: unrolled by two, not four: at the 168-register cap of three
         // warps per sub-partition the full unroll spilled registers and was
         // slower.  Prefix mode keeps the full unroll, which measured faster
@@ -809,9 +835,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
             const int j = 2 * u;
-            const float p0 = c * 32 + j < nvalid ? fast_exp2(fmaf(v[j], qk_scale, nm)) : 0.f;
-            const float p1 = c * 32 + j + 1 < nvalid ? fast_exp2(fmaf(v[j + 1], qk_scale, nm)) : 0.f;
-            lsum += p0 + p1;
+            float x0, x1;
+            unpack2(fma2(pack2(v[j], v[j + 1]), scale2, nm2), x0, x1);
+            const float p0 = c * 32 + j < nvalid ? fast_exp2(x0) : 0.f;
+            const float p1 = c * 32 + j + 1 < nvalid ? fast_exp2(x1) : 0.f;
+            lsum2 = add2(lsum2, pack2(p0, p1));
             __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
             pk[u] = *reinterpret_cast<uint32_t *>(&h2);
           }
@@ -822,7 +850,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (lane == 0) tc::mbar_arrive(tc::smem_u32(p_ready + 4 * h + c));
           }
         }
-        l_sum += lsum;
+        float ls0, ls1;
+        unpack2(lsum2, ls0, ls1);
+        l_sum += ls0 + ls1;
       }
       if (kPrefix && ok &&
           __all_sync(0xffffffffu, tc::mbar_wait(tc::smem_u32(o_full), seg_no & 1, pb.cap_ns,
