@@ -71,6 +71,8 @@
 #include <cuda.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "attention.cuh"
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -827,29 +829,40 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // warps per sub-partition the full unroll spilled registers and was
         // slower.  Prefix mode keeps the full unroll, which measured faster
         // there in spite of a small spill.
+        // The same pass for a full tile (no key to mask, the common case;
+        // the branch is uniform over the CTA) and for a partial one.
+        auto exp_pass = [&](auto masked) {
 #pragma unroll(kPrefix ? 4 : 2)
-        for (int c = 0; c < TILE / 32; ++c) {
-          float v[32];
-          tc::tmem_ld32(s_addr + c * 32, v);
-          uint32_t pk[16];
+          for (int c = 0; c < TILE / 32; ++c) {
+            float v[32];
+            tc::tmem_ld32(s_addr + c * 32, v);
+            uint32_t pk[16];
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const int j = 2 * u;
-            float x0, x1;
-            unpack2(fma2(pack2(v[j], v[j + 1]), scale2, nm2), x0, x1);
-            const float p0 = c * 32 + j < nvalid ? fast_exp2(x0) : 0.f;
-            const float p1 = c * 32 + j + 1 < nvalid ? fast_exp2(x1) : 0.f;
-            lsum2 = add2(lsum2, pack2(p0, p1));
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-            pk[u] = *reinterpret_cast<uint32_t *>(&h2);
+            for (int u = 0; u < 16; ++u) {
+              const int j = 2 * u;
+              float x0, x1;
+              unpack2(fma2(pack2(v[j], v[j + 1]), scale2, nm2), x0, x1);
+              float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              if (decltype(masked)::value) {
+                if (c * 32 + j >= nvalid) p0 = 0.f;
+                if (c * 32 + j + 1 >= nvalid) p1 = 0.f;
+              }
+              lsum2 = add2(lsum2, pack2(p0, p1));
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+              pk[u] = *reinterpret_cast<uint32_t *>(&h2);
+            }
+            tmem_st16(s_addr + c * 16, pk);
+            {  // every 32-key quarter of P is handed over on its own
+              tc::fence_before_sync();
+              __syncwarp();
+              if (lane == 0) tc::mbar_arrive(tc::smem_u32(p_ready + 4 * h + c));
+            }
           }
-          tmem_st16(s_addr + c * 16, pk);
-          {  // every 32-key quarter of P is handed over on its own
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(tc::smem_u32(p_ready + 4 * h + c));
-          }
-        }
+        };
+        if (nvalid >= TILE)
+          exp_pass(std::false_type{});
+        else
+          exp_pass(std::true_type{});
         float ls0, ls1;
         unpack2(lsum2, ls0, ls1);
         l_sum += ls0 + ls1;
